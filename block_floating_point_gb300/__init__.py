@@ -1,0 +1,354 @@
+"""Python binding of the GB300 BFP MoE decode library (``include/bfpmoe.h``).
+
+Argument marshalling only: every step of the decode path runs in the native
+library ``_build/libbfpmoe.so`` (CUDA for sm_103a plus the host packer). There
+is no Python or CPU fallback; if the library is missing or cannot be loaded,
+every call raises.
+
+PyTorch supplies device memory and streams: device arguments are CUDA torch
+tensors (their ``data_ptr()`` is passed), the stream is the current torch
+stream unless one is given.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+
+from . import build as _build
+
+BFP_OK, BFP_EINVAL, BFP_ESHAPE, BFP_EALIGN, BFP_ENONFINITE, BFP_EWORKSPACE, BFP_ECUDA, BFP_ETIMEOUT = \
+    0, -1, -2, -3, -4, -5, -6, -7
+BFP4, BFP8 = 4, 8
+STATUS_NAMES = {0: "BFP_OK", -1: "BFP_EINVAL", -2: "BFP_ESHAPE", -3: "BFP_EALIGN", -4: "BFP_ENONFINITE",
+                -5: "BFP_EWORKSPACE", -6: "BFP_ECUDA", -7: "BFP_ETIMEOUT"}
+
+
+class BFPError(RuntimeError):
+    def __init__(self, code: int, fn: str, msg: str):
+        super().__init__(f"{fn}: {STATUS_NAMES.get(code, code)}: {msg}")
+        self.code = code
+
+
+class BfpMatrixC(ctypes.Structure):
+    _fields_ = [("fmt", ctypes.c_int32), ("reserved", ctypes.c_int32), ("n", ctypes.c_int64),
+                ("k", ctypes.c_int64), ("data", ctypes.c_void_p), ("bytes", ctypes.c_int64)]
+
+
+class MoeLayerC(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int32), ("n_experts", ctypes.c_int32), ("ffn", ctypes.c_int32),
+                ("top_k", ctypes.c_int32), ("shared_ffn", ctypes.c_int32), ("expert_fmt", ctypes.c_int32),
+                ("router", ctypes.c_void_p), ("router_bias", ctypes.c_void_p), ("shared_gate", ctypes.c_void_p),
+                ("experts_gate_up", ctypes.c_void_p), ("experts_down", ctypes.c_void_p),
+                ("gate_up_stride", ctypes.c_int64), ("down_stride", ctypes.c_int64),
+                ("shared_gate_up", ctypes.c_void_p), ("shared_down", ctypes.c_void_p)]
+
+
+# Every entry point declared in include/bfpmoe.h, with its ctypes signature.
+_P, _I, _I64, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+_MP = ctypes.POINTER(BfpMatrixC)
+_LP = ctypes.POINTER(MoeLayerC)
+SIGNATURES = {
+    "bfp_packed_size": [_I, _I64, _I64, ctypes.POINTER(_I64)],
+    "bfp_encode": [_I, _P, _I64, _I64, _P, _I64, _I],
+    "bfp_encode_gate_up": [_I, _P, _P, _I64, _I64, _P, _I64, _I],
+    "bfp_read_fields": [_MP, _P, _P],
+    "bfp_decode_host": [_MP, _P],
+    "bfp_unpack_device": [_MP, _P, _P],
+    "bfp_linear_workspace_size": [_MP, _I, ctypes.POINTER(_SZ)],
+    "bfp_linear": [_MP, _P, _I, _I64, _P, _P, _I64, _P, _SZ, _P],
+    "moe_workspace_size": [_LP, _I, ctypes.POINTER(_SZ)],
+    "bfp_workspace_init": [_P, _SZ, _P],
+    "moe_decode_layer": [_LP, _P, _I, _P, _P, _P, _P, _SZ, _P],
+    "moe_stack_workspace_size": [_LP, _I, _MP, _I, ctypes.POINTER(_SZ)],
+    "moe_stack_decode": [_LP, _I, _MP, _P, _I, _P, _P, _SZ, _P],
+    "bfp_workspace_status": [_P, ctypes.POINTER(_I), _P],
+    "bfp_set_wait_limit": [_I64],
+    "bfp_last_error": [],
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load():
+    """Load (building first if needed) the native library; raises if it cannot."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build()
+            lib = ctypes.CDLL(path)
+            for name, args in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.argtypes = args
+                fn.restype = ctypes.c_char_p if name == "bfp_last_error" else ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _check(rc: int, fn: str):
+    if rc != BFP_OK:
+        raise BFPError(rc, fn, load().bfp_last_error().decode())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+# ----------------------------------------------------------------------------- format
+def packed_size(fmt: int, n: int, k: int) -> int:
+    out = ctypes.c_int64()
+    _check(load().bfp_packed_size(fmt, n, k, ctypes.byref(out)), "bfp_packed_size")
+    return out.value
+
+
+def encode(fmt: int, w: np.ndarray, threads: int = 0, out: np.ndarray | None = None) -> np.ndarray:
+    """Host packer: fp32 [n, k] -> packed uint8 buffer (tile-record layout)."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    n, k = w.shape
+    size = packed_size(fmt, n, k)
+    if out is None:
+        out = np.empty(size, dtype=np.uint8)
+    assert out.nbytes >= size and out.flags.c_contiguous
+    _check(load().bfp_encode(fmt, w.ctypes.data, n, k, out.ctypes.data, out.nbytes, threads), "bfp_encode")
+    return out
+
+
+def encode_gate_up(fmt: int, gate: np.ndarray, up: np.ndarray, threads: int = 0,
+                   out: np.ndarray | None = None) -> np.ndarray:
+    """Host packer for an expert's gate and up [ffn, hidden] -> packed [2*ffn, hidden] (row groups interleaved)."""
+    gate = np.ascontiguousarray(gate, dtype=np.float32)
+    up = np.ascontiguousarray(up, dtype=np.float32)
+    ffn, hidden = gate.shape
+    assert up.shape == gate.shape
+    size = packed_size(fmt, 2 * ffn, hidden)
+    if out is None:
+        out = np.empty(size, dtype=np.uint8)
+    assert out.nbytes >= size
+    _check(load().bfp_encode_gate_up(fmt, gate.ctypes.data, up.ctypes.data, ffn, hidden, out.ctypes.data,
+                                     out.nbytes, threads), "bfp_encode_gate_up")
+    return out
+
+
+def _host_matrix(fmt, n, k, packed: np.ndarray) -> BfpMatrixC:
+    return BfpMatrixC(fmt, 0, n, k, packed.ctypes.data, packed_size(fmt, n, k))
+
+
+def read_fields(fmt: int, n: int, k: int, packed: np.ndarray):
+    """Logical (exps [n, k/16], codes [n, k]) of a packed host buffer."""
+    m = _host_matrix(fmt, n, k, packed)
+    exps = np.zeros((n, k // 16), dtype=np.uint8)
+    codes = np.zeros((n, k), dtype=np.uint8)
+    _check(load().bfp_read_fields(ctypes.byref(m), exps.ctypes.data, codes.ctypes.data), "bfp_read_fields")
+    return exps, codes
+
+
+def decode_host(fmt: int, n: int, k: int, packed: np.ndarray) -> np.ndarray:
+    m = _host_matrix(fmt, n, k, packed)
+    out = np.zeros((n, k), dtype=np.float32)
+    _check(load().bfp_decode_host(ctypes.byref(m), out.ctypes.data), "bfp_decode_host")
+    return out
+
+
+class DeviceMatrix:
+    """A packed BFP matrix resident in device memory (a torch uint8 CUDA tensor)."""
+
+    def __init__(self, fmt: int, n: int, k: int, data):
+        self.fmt, self.n, self.k, self.data = fmt, n, k, data
+        self.nbytes = packed_size(fmt, n, k)
+        assert data.numel() >= self.nbytes
+
+    @classmethod
+    def from_host(cls, fmt, n, k, packed: np.ndarray, device="cuda"):
+        import torch
+        t = torch.from_numpy(np.ascontiguousarray(packed)).to(device)
+        return cls(fmt, n, k, t)
+
+    def c(self) -> BfpMatrixC:
+        return BfpMatrixC(self.fmt, 0, self.n, self.k, self.data.data_ptr(), self.nbytes)
+
+
+def unpack_device(mat: DeviceMatrix, stream=None):
+    import torch
+    out = torch.empty((mat.n, mat.k), dtype=torch.float32, device=mat.data.device)
+    m = mat.c()
+    _check(load().bfp_unpack_device(ctypes.byref(m), _ptr(out), _stream(stream)), "bfp_unpack_device")
+    return out
+
+
+# ----------------------------------------------------------------------------- workspaces
+def workspace_init(ws, stream=None):
+    _check(load().bfp_workspace_init(_ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "bfp_workspace_init")
+
+
+def workspace_status(ws, stream=None) -> int:
+    st = ctypes.c_int()
+    _check(load().bfp_workspace_status(_ptr(ws), ctypes.byref(st), _stream(stream)), "bfp_workspace_status")
+    return st.value
+
+
+def set_wait_limit(iterations: int):
+    _check(load().bfp_set_wait_limit(iterations), "bfp_set_wait_limit")
+
+
+def _alloc_ws(nbytes: int, device, stream=None):
+    import torch
+    ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+    workspace_init(ws, stream)
+    return ws
+
+
+# ----------------------------------------------------------------------------- dense linear
+def linear_workspace_size(mat: DeviceMatrix, m: int) -> int:
+    out = ctypes.c_size_t()
+    c = mat.c()
+    _check(load().bfp_linear_workspace_size(ctypes.byref(c), m, ctypes.byref(out)), "bfp_linear_workspace_size")
+    return out.value
+
+
+def linear_workspace(mat: DeviceMatrix, m: int, stream=None):
+    return _alloc_ws(linear_workspace_size(mat, m), mat.data.device, stream)
+
+
+def linear(mat: DeviceMatrix, x, ws, y=None, y_bf16=None, stream=None):
+    """y = x W^T for bf16 x [m, k] (CUDA tensor); fills y (fp32 [m, n]) and/or y_bf16 (bf16 [m, n])."""
+    import torch
+    m = x.shape[0]
+    if y is None and y_bf16 is None:
+        y = torch.empty((m, mat.n), dtype=torch.float32, device=x.device)
+    ldy = (y if y is not None else y_bf16).stride(0)
+    c = mat.c()
+    _check(load().bfp_linear(ctypes.byref(c), _ptr(x), m, x.stride(0), _ptr(y), _ptr(y_bf16), ldy, _ptr(ws),
+                             ws.numel(), _stream(stream)), "bfp_linear")
+    return y if y is not None else y_bf16
+
+
+# ----------------------------------------------------------------------------- MoE layer
+class MoELayer:
+    """Device-resident weights of one MoE decode layer (all BFP experts packed, bf16 router/gate)."""
+
+    def __init__(self, hidden, n_experts, ffn, top_k, shared_ffn, expert_fmt, router, shared_gate,
+                 experts_gate_up, experts_down, shared_gate_up, shared_down, router_bias=None):
+        self.hidden, self.n_experts, self.ffn, self.top_k, self.shared_ffn = hidden, n_experts, ffn, top_k, shared_ffn
+        self.expert_fmt = expert_fmt
+        self.router, self.shared_gate, self.router_bias = router, shared_gate, router_bias
+        self.experts_gate_up, self.experts_down = experts_gate_up, experts_down
+        self.shared_gate_up, self.shared_down = shared_gate_up, shared_down
+        self.gate_up_bytes = packed_size(expert_fmt, 2 * ffn, hidden)
+        self.down_bytes = packed_size(expert_fmt, hidden, ffn)
+
+    def c(self) -> MoeLayerC:
+        return MoeLayerC(self.hidden, self.n_experts, self.ffn, self.top_k, self.shared_ffn, self.expert_fmt,
+                         self.router.data_ptr(), None if self.router_bias is None else self.router_bias.data_ptr(),
+                         self.shared_gate.data_ptr(), self.experts_gate_up.data_ptr(), self.experts_down.data_ptr(),
+                         self.gate_up_bytes, self.down_bytes, self.shared_gate_up.data_ptr(),
+                         self.shared_down.data_ptr())
+
+    def weight_bytes(self, n_routed: int) -> int:
+        """BFP bytes one step streams for n_routed distinct routed experts plus the shared expert."""
+        sh = packed_size(self.expert_fmt, 2 * self.shared_ffn, self.hidden) + \
+            packed_size(self.expert_fmt, self.hidden, self.shared_ffn)
+        return n_routed * (self.gate_up_bytes + self.down_bytes) + sh
+
+    @classmethod
+    def from_source(cls, hidden, n_experts, ffn, top_k, shared_ffn, expert_fmt, router_bf16: np.ndarray,
+                    shared_gate_bf16: np.ndarray, expert_source, shared_source, router_bias=None, device="cuda",
+                    threads: int = 0):
+        """Pack fp32 weights on the host (bfp_encode / bfp_encode_gate_up) and upload them.
+
+        expert_source(e) -> (gate [ffn, hidden], up [ffn, hidden], down [hidden, ffn]) fp32;
+        shared_source() -> the same for the shared expert.
+        """
+        import torch
+        gub = packed_size(expert_fmt, 2 * ffn, hidden)
+        dnb = packed_size(expert_fmt, hidden, ffn)
+        host_gu = np.empty(n_experts * gub, dtype=np.uint8)
+        host_dn = np.empty(n_experts * dnb, dtype=np.uint8)
+        for e in range(n_experts):
+            g, u, d = expert_source(e)
+            encode_gate_up(expert_fmt, g, u, threads, out=host_gu[e * gub:(e + 1) * gub])
+            encode(expert_fmt, d, threads, out=host_dn[e * dnb:(e + 1) * dnb])
+        g, u, d = shared_source()
+        sgu = encode_gate_up(expert_fmt, g, u, threads)
+        sdn = encode(expert_fmt, d, threads)
+        dev = torch.device(device)
+
+        def up_(a):
+            return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+        rb = None if router_bias is None else up_(np.asarray(router_bias, dtype=np.float32))
+        return cls(hidden, n_experts, ffn, top_k, shared_ffn, expert_fmt,
+                   up_(np.asarray(router_bf16, dtype=np.uint16).view(np.int16)),
+                   up_(np.asarray(shared_gate_bf16, dtype=np.uint16).view(np.int16)),
+                   up_(host_gu), up_(host_dn), up_(sgu), up_(sdn), router_bias=rb)
+
+
+def moe_workspace_size(layer: MoELayer, m: int) -> int:
+    out = ctypes.c_size_t()
+    c = layer.c()
+    _check(load().moe_workspace_size(ctypes.byref(c), m, ctypes.byref(out)), "moe_workspace_size")
+    return out.value
+
+
+def moe_workspace(layer: MoELayer, m: int, stream=None):
+    return _alloc_ws(moe_workspace_size(layer, m), layer.router.device, stream)
+
+
+def moe_decode_layer(layer: MoELayer, x, ws, y=None, topk_idx=None, topk_w=None, stream=None):
+    """One MoE decode layer on bf16 x [m, hidden]; returns y fp32 [m, hidden] (and fills topk_idx/topk_w)."""
+    import torch
+    m = x.shape[0]
+    if y is None:
+        y = torch.empty((m, layer.hidden), dtype=torch.float32, device=x.device)
+    c = layer.c()
+    _check(load().moe_decode_layer(ctypes.byref(c), _ptr(x), m, _ptr(y), _ptr(topk_idx), _ptr(topk_w), _ptr(ws),
+                                   ws.numel(), _stream(stream)), "moe_decode_layer")
+    return y
+
+
+def _layers_array(layers):
+    arr = (MoeLayerC * len(layers))()
+    for i, l in enumerate(layers):
+        arr[i] = l.c()
+    return arr
+
+
+def moe_stack_workspace_size(layers, lm_head: DeviceMatrix, m: int) -> int:
+    out = ctypes.c_size_t()
+    arr = _layers_array(layers)
+    c = lm_head.c()
+    _check(load().moe_stack_workspace_size(arr, len(layers), ctypes.byref(c), m, ctypes.byref(out)),
+           "moe_stack_workspace_size")
+    return out.value
+
+
+def moe_stack_workspace(layers, lm_head: DeviceMatrix, m: int, stream=None):
+    return _alloc_ws(moe_stack_workspace_size(layers, lm_head, m), lm_head.data.device, stream)
+
+
+def moe_stack_decode(layers, lm_head: DeviceMatrix, h, ws, logits=None, stream=None):
+    """Decode stack: h (bf16 [m, hidden], updated in place) through every layer, then LM-head logits fp32."""
+    import torch
+    m = h.shape[0]
+    if logits is None:
+        logits = torch.empty((m, lm_head.n), dtype=torch.float32, device=h.device)
+    arr = _layers_array(layers)
+    c = lm_head.c()
+    _check(load().moe_stack_decode(arr, len(layers), ctypes.byref(c), _ptr(h), m, _ptr(logits), _ptr(ws),
+                                   ws.numel(), _stream(stream)), "moe_stack_decode")
+    return logits

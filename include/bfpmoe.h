@@ -1,0 +1,236 @@
+/*
+ * bfpmoe.h — C-ABI of the GB300 block-floating-point MoE decode library.
+ *
+ * Operation sources on the block_floating_point pages ("P1" Qwen3.6-35B-A3B
+ * TT-Mixed-BFP4-BFP8-P150 card, "P3" qwen3.6-a3b-blackhole tt-kernel bundle,
+ * "P4" Qwen3.8-27B s27v6 card, "P5" Qwen3.8-27B gptq-ctx2 card):
+ *   BFP4 experts, BFP8 dense projections and LM head, bf16 router and norms
+ *     (P1, "Precision as served");
+ *   16-value blocks (P5, "What changed in this release");
+ *   round-to-nearest conversion (P1, "Verification", checkpoint bullet);
+ *   MoE decode through device top-k routing and batched expert streams, one
+ *     gate/up + down expert program for several rows (P1, "Fused decode kernels");
+ *   256 experts, top-8 plus a shared expert (P3, opening paragraph);
+ *   several users as the rows of one pass that streams every weight once
+ *     (P4, "Multi-user decode").
+ *
+ * Conventions for every function:
+ *   - returns an int status: BFP_OK (0) or a negative BFP_E* code; never
+ *     throws, never exits; bfp_last_error() gives a message (thread-local);
+ *   - the caller owns and allocates every buffer (host or device); the
+ *     library allocates no device memory;
+ *   - device work is enqueued on the caller's stream and is asynchronous;
+ *     only bfp_workspace_status() synchronises (the stream it is given);
+ *   - device pointers must be 16-byte aligned (BFP_EALIGN otherwise);
+ *   - invalid shapes give BFP_ESHAPE, null/inconsistent arguments BFP_EINVAL,
+ *     CUDA launch errors BFP_ECUDA (with the CUDA message in bfp_last_error).
+ *
+ * BFP value of a code (sign bit s above an mb-bit magnitude m, mb = 3 for
+ * BFP4 and 7 for BFP8) under its block's exponent byte E:
+ *     v = (-1)^s * m * 2^(E - 127 - (mb - 1)).
+ * E is the largest fp32 exponent field in the block (0 for an all-zero
+ * block); m is round-to-nearest-even, saturating at 2^mb - 1; zero, -0 and
+ * fp32 subnormals encode as +0; NaN/Inf are rejected (BFP_ENONFINITE).
+ *
+ * Packed layout of a matrix W [n x k] (k % 16 == 0), "tile-record" layout:
+ *   16 rows form a row group (NG = ceil(n/16)); along k, CB blocks of 16
+ *   values form a chunk (CB = 4 for BFP4, 2 for BFP8; KC = ceil(k/16/CB)).
+ *   The buffer is NG*KC records, record (rg, c) at byte (rg*KC + c)*REC,
+ *   REC = 576 (BFP4) or 544 (BFP8). A record is
+ *     bytes [0, 512):   codes, 16 bytes per lane l = 4*g + t (g = 0..7, t = 0..3)
+ *     bytes [512, REC): exponents, byte 512 + (g*CB + b)*2 + h = E of row
+ *                       16*rg + g + 8*h, block CB*c + b.
+ *   Lane l's 16 bytes are 4 little-endian 32-bit words holding the codes of
+ *   rows g and g+8 at the columns {2t, 2t+1, 2t+8, 2t+9} of each block:
+ *     BFP4: word b covers block CB*c + b; "pair" p = 0..3 is
+ *           (row g, cols 2t|2t+1), (row g+8, 2t|2t+1), (row g, 2t+8|2t+9),
+ *           (row g+8, 2t+8|2t+9). The first value of pair p keeps its
+ *           magnitude in bits 4p..4p+2 and its sign in bit (15+4p) mod 32;
+ *           the second value its magnitude in bits (16+4p..18+4p) mod 32 and
+ *           its sign in bit (31+4p) mod 32.
+ *     BFP8: words 2b and 2b+1 cover block CB*c + b; word 2b holds pairs
+ *           (row g, 2t|2t+1) and (row g+8, 2t|2t+1), word 2b+1 holds
+ *           (row g, 2t+8|2t+9) and (row g+8, 2t+8|2t+9); pair q = 0, 1 of a
+ *           word keeps its first magnitude in bits 8q..8q+6, sign in bit
+ *           (15+8q) mod 32, second magnitude in bits (16+8q..22+8q) mod 32,
+ *           sign in bit (31+8q) mod 32.
+ *   Rows >= n and blocks >= k/16 are zero (code 0, exponent 0). Every byte
+ *   carries information: 0.5625 (BFP4) / 1.0625 (BFP8) bytes per value when
+ *   n % 16 == 0 and k % (16*CB) == 0. A warp streams 512 contiguous code
+ *   bytes per record, and a rotation plus one mask of a word yields two
+ *   fp16 lanes (sign << 15 | magnitude), ready for a tensor-core fragment.
+ */
+#ifndef BFPMOE_H
+#define BFPMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without including the CUDA headers; NULL is the legacy default stream. */
+typedef struct CUstream_st *bfp_stream_t;
+
+enum {
+    BFP_OK = 0,
+    BFP_EINVAL = -1,     /* null pointer, bad enum, inconsistent sizes */
+    BFP_ESHAPE = -2,     /* shape outside the supported range */
+    BFP_EALIGN = -3,     /* pointer or stride not 16-byte aligned */
+    BFP_ENONFINITE = -4, /* NaN or Inf given to the encoder */
+    BFP_EWORKSPACE = -5, /* workspace too small or null */
+    BFP_ECUDA = -6,      /* CUDA error (launch, attribute, device query) */
+    BFP_ETIMEOUT = -7    /* a device-side wait ran out; reported by bfp_workspace_status */
+};
+
+enum { BFP_FMT_BFP4 = 4, BFP_FMT_BFP8 = 8 };
+
+/* A packed BFP matrix (host or device memory, as each function states). */
+typedef struct {
+    int32_t fmt;      /* BFP_FMT_BFP4 or BFP_FMT_BFP8 */
+    int32_t reserved; /* must be 0 */
+    int64_t n, k;     /* logical rows and columns; k % 16 == 0 */
+    const void *data; /* packed tile-record layout (above), 16-byte aligned */
+    int64_t bytes;    /* size of data; must equal bfp_packed_size(fmt, n, k) */
+} bfp_matrix;
+
+/* Packed size in bytes of an [n x k] matrix (layout above). n >= 1, k >= 16, k % 16 == 0. */
+int bfp_packed_size(int fmt, int64_t n, int64_t k, int64_t *bytes);
+
+/*
+ * Host packer. Encodes a row-major fp32 matrix w [n x k] (host memory) into
+ * out (host memory, out_bytes >= bfp_packed_size). Round to nearest, ties to
+ * even, 16-value blocks along k (P1 "Verification": CPU round-to-nearest
+ * conversion; P5: 16-value blocks). nthreads <= 0 picks the host core count.
+ * Returns BFP_ENONFINITE (and writes nothing useful) if w holds NaN/Inf.
+ */
+int bfp_encode(int fmt, const float *w, int64_t n, int64_t k, void *out, int64_t out_bytes, int nthreads);
+
+/*
+ * Host packer for one expert's gate and up projections, both [ffn x hidden]
+ * row-major fp32 (host). Produces the packed [2*ffn x hidden] matrix whose
+ * row group 2i holds gate rows 16i..16i+15 and row group 2i+1 holds up rows
+ * 16i..16i+15, so that one contiguous span carries both halves of an
+ * f-tile (P1 "Fused decode kernels": one gate/up + down expert program).
+ * ffn % 16 == 0.
+ */
+int bfp_encode_gate_up(int fmt, const float *gate, const float *up, int64_t ffn, int64_t hidden, void *out,
+                       int64_t out_bytes, int nthreads);
+
+/*
+ * Host reader of a packed matrix (w->data in host memory): the logical
+ * fields, exps [n x k/16] and codes [n x k] (one code per byte, sign << mb |
+ * magnitude). Test aid for bit-exact comparisons.
+ */
+int bfp_read_fields(const bfp_matrix *w, uint8_t *exps, uint8_t *codes);
+
+/* Host decode of a packed matrix (host memory) to row-major fp32 [n x k]; exact. */
+int bfp_decode_host(const bfp_matrix *w, float *out);
+
+/*
+ * Device decode of a packed matrix (device memory) to row-major fp32
+ * [n x k] (device memory), through the same fragment unpack and tensor-core
+ * instruction the kernels use (each block multiplied by unit columns).
+ * Test aid for the bit-exact unpack check.
+ */
+int bfp_unpack_device(const bfp_matrix *w, float *out, bfp_stream_t stream);
+
+/*
+ * Workspace for bfp_linear with m rows: *bytes of device memory that must be
+ * zeroed once (bfp_workspace_init) before first use; every successful call
+ * leaves it zeroed again. One workspace may serve calls in stream order only.
+ */
+int bfp_linear_workspace_size(const bfp_matrix *w, int m, size_t *bytes);
+
+/*
+ * Dense BFP decode projection (P1 "Precision as served": dense projections and
+ * LM head in BFP8; P4 "Multi-user decode": all rows in one weight pass):
+ *     y[r][o] = sum_j x[r][j] * W[o][j],   r < m, o < n,
+ * x bf16 [m x k] (device, row stride ldx elements, ldx % 8 == 0), fp32
+ * accumulation. y (nullable) receives fp32 [m x n], y_bf16 (nullable) the
+ * round-to-nearest-even bf16 of the same fp32 values; both row stride ldy
+ * elements. At least one output must be given. 1 <= m <= 16. W in device
+ * memory. ws: bfp_linear_workspace_size bytes (device).
+ */
+int bfp_linear(const bfp_matrix *w, const uint16_t *x, int m, int64_t ldx, float *y, uint16_t *y_bf16, int64_t ldy,
+               void *ws, size_t ws_bytes, bfp_stream_t stream);
+
+/*
+ * One MoE decode layer's weights (all device memory).
+ * Shapes: hidden % 16 == 0, ffn % 16 == 0, shared_ffn % 16 == 0,
+ * 1 <= top_k <= 8, top_k <= n_experts <= 256.
+ */
+typedef struct {
+    int32_t hidden, n_experts, ffn, top_k, shared_ffn;
+    int32_t expert_fmt;            /* BFP_FMT_BFP4 (as served) or BFP_FMT_BFP8 */
+    const uint16_t *router;        /* [n_experts x hidden] bf16, row-major */
+    const float *router_bias;      /* nullable [n_experts] fp32, added to the logits before softmax and top-k */
+    const uint16_t *shared_gate;   /* [hidden] bf16: the shared expert is scaled by sigmoid(shared_gate . x) */
+    const void *experts_gate_up;   /* n_experts packed [2*ffn x hidden] matrices (bfp_encode_gate_up) */
+    const void *experts_down;      /* n_experts packed [hidden x ffn] matrices (bfp_encode) */
+    int64_t gate_up_stride;        /* bytes between consecutive experts' gate/up; >= packed size, % 16 == 0 */
+    int64_t down_stride;           /* bytes between consecutive experts' down; >= packed size, % 16 == 0 */
+    const void *shared_gate_up;    /* packed [2*shared_ffn x hidden] */
+    const void *shared_down;       /* packed [hidden x shared_ffn] */
+} bfp_moe_layer;
+
+/* Device workspace for moe_decode_layer with m rows (zeroed once, left zeroed). */
+int moe_workspace_size(const bfp_moe_layer *layer, int m, size_t *bytes);
+
+/* Zeroes a workspace (any of this library's) on the stream; also clears its status word. */
+int bfp_workspace_init(void *ws, size_t ws_bytes, bfp_stream_t stream);
+
+/*
+ * One MoE decode layer for m rows (1..16) of bf16 input x [m x hidden]
+ * (device, row-major, contiguous). Per row r:
+ *     l = router . x_r (+ router_bias)   fp32 logits
+ *     p = softmax(l); S = the top_k largest l (ties: lower index), in
+ *     descending order; w_s = p_s / sum_S p
+ *     y_r = sum_s w_s * D_s(silu(G_s x_r) * (U_s x_r)) + sigmoid(g . x_r) * shared(x_r)
+ * with silu(a) = a * sigmoid(a), fp32 accumulation, fp32 intermediates.
+ * The union of the experts the rows select is streamed from HBM once
+ * (P1 "Fused decode kernels": device top-k routing and batched expert
+ * streams). Outputs (device): y fp32 [m x hidden]; topk_idx int32 [m x top_k]
+ * and topk_w fp32 [m x top_k] (both nullable) in slot order.
+ * One persistent cooperative launch; its cross-block waits are bounded and
+ * report BFP_ETIMEOUT through bfp_workspace_status.
+ */
+int moe_decode_layer(const bfp_moe_layer *layer, const uint16_t *x, int m, float *y, int32_t *topk_idx,
+                     float *topk_w, void *ws, size_t ws_bytes, bfp_stream_t stream);
+
+/*
+ * Decode stack: for each of n_layers layers,
+ *     h <- bf16( h + MoE_l( bf16(RMSNorm(h)) ) ),  RMSNorm(h) = h / sqrt(mean(h^2) + 1e-6)
+ * (unit weight, fp32), then logits = LMhead( bf16(RMSNorm(h)) ) in fp32
+ * [m x lm_head->n] (P1 "Fused decode kernels": one-launch RMSNorm, packed LM
+ * head). h: bf16 [m x hidden] device, updated in place. lm_head: BFP matrix
+ * [vocab x hidden] in device memory. ws: moe_stack_workspace_size bytes.
+ */
+int moe_stack_workspace_size(const bfp_moe_layer *layers, int n_layers, const bfp_matrix *lm_head, int m,
+                             size_t *bytes);
+int moe_stack_decode(const bfp_moe_layer *layers, int n_layers, const bfp_matrix *lm_head, uint16_t *h, int m,
+                     float *logits, void *ws, size_t ws_bytes, bfp_stream_t stream);
+
+/*
+ * Synchronises the stream and reads the workspace's status word: *status =
+ * BFP_OK or the first device-side error (BFP_ETIMEOUT). The word stays set
+ * until bfp_workspace_init.
+ */
+int bfp_workspace_status(const void *ws, int *status, bfp_stream_t stream);
+
+/*
+ * Test hook for the bounded waits: sets the iteration limit of every
+ * cross-block wait in later launches from this thread (0 = the default
+ * limit, about a second). A limit of 1 makes waits that are not already
+ * satisfied give up at once and report BFP_ETIMEOUT.
+ */
+int bfp_set_wait_limit(int64_t iterations);
+
+/* Message for the last non-OK status returned on this thread. */
+const char *bfp_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BFPMOE_H */

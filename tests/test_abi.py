@@ -1,0 +1,163 @@
+"""C-ABI library on the CPU: loads, exports every symbol of include/bfpmoe.h, and
+its host packer agrees bit for bit with the oracle's encoding.
+
+The packed layout is read back two independent ways: by the library's own
+``bfp_read_fields`` and by a NumPy statement of the layout text in the header
+(``layout_fields`` below), so a packer bug that the library's reader mirrored
+would still show.
+"""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import block_floating_point_gb300 as bfp
+import oracle
+import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def header_functions():
+    txt = open(os.path.join(ROOT, "include", "bfpmoe.h")).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:int|const char \*)\s*\*?\s*(\w+)\s*\(", txt, flags=re.M)))
+
+
+def test_library_exports_every_header_symbol():
+    lib = bfp.load()
+    names = header_functions()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in bfp.SIGNATURES, n
+    assert set(bfp.SIGNATURES) == set(names)
+
+
+def layout_fields(fmt, n, k, packed):
+    """NumPy reading of the tile-record layout exactly as include/bfpmoe.h states it."""
+    cb = 4 if fmt == 4 else 2
+    mb = 3 if fmt == 4 else 7
+    rec = 512 + 16 * cb
+    ng = (n + 15) // 16
+    kb = k // 16
+    kc = (kb + cb - 1) // cb
+    codes = np.zeros((ng * 16, kc * cb * 16), dtype=np.uint8)
+    exps = np.zeros((ng * 16, kc * cb), dtype=np.uint8)
+    buf = np.asarray(packed, dtype=np.uint8)[: ng * kc * rec].reshape(ng, kc, rec)
+    words = buf[:, :, :512].copy().view("<u4").reshape(ng, kc, 32, 4)
+    ex = buf[:, :, 512:].reshape(ng, kc, 8, cb, 2)
+    for g in range(8):
+        for b in range(cb):
+            for h in range(2):
+                exps[np.arange(ng)[:, None] * 16 + g + 8 * h, np.arange(kc)[None, :] * cb + b] = ex[:, :, g, b, h]
+
+    def bits(w, pos, cnt):
+        pos %= 32
+        return (w >> np.uint32(pos)) & np.uint32((1 << cnt) - 1) if pos + cnt <= 32 else None
+
+    for lane in range(32):
+        g, t = lane >> 2, lane & 3
+        for b in range(cb):
+            blk = np.arange(kc)[None, :] * cb + b
+            rows0 = np.arange(ng)[:, None] * 16 + g
+            if fmt == 4:
+                w = words[:, :, lane, b]
+                pairs = [(rows0, 2 * t), (rows0 + 8, 2 * t), (rows0, 2 * t + 8), (rows0 + 8, 2 * t + 8)]
+                for p, (rr, col) in enumerate(pairs):
+                    for second in (0, 1):
+                        mpos = (16 * second + 4 * p) % 32
+                        spos = (15 + 16 * second + 4 * p) % 32
+                        m = bits(w, mpos, 3)
+                        s = bits(w, spos, 1)
+                        codes[rr, blk * 16 + col + second] = (s << np.uint32(mb)) | m
+            else:
+                for half in range(2):
+                    w = words[:, :, lane, 2 * b + half]
+                    for q, rr in enumerate((rows0, rows0 + 8)):
+                        col = 2 * t + 8 * half
+                        for second in (0, 1):
+                            mpos = (16 * second + 8 * q) % 32
+                            spos = (15 + 16 * second + 8 * q) % 32
+                            m = bits(w, mpos, 7)
+                            s = bits(w, spos, 1)
+                            codes[rr, blk * 16 + col + second] = (s << np.uint32(mb)) | m
+    return exps[:n, :kb], codes[:n, :k]
+
+
+SHAPES = [(16, 64), (16, 16), (37, 96), (5, 208), (64, 512), (130, 2048)]
+
+
+@pytest.mark.parametrize("fmt", [4, 8])
+@pytest.mark.parametrize("n,k", SHAPES)
+def test_host_packer_matches_oracle(fmt, n, k):
+    w = synth.normal(11, 7000 + n * 31 + k, (n, k), std=0.02)
+    if n > 5:  # adversarial rows: zeros, a huge dynamic range, exact ties, saturation
+        w[1, :] = 0.0
+        w[2, :16] = np.float32(2.0) ** -np.arange(16, dtype=np.float32)
+        w[3, :16] = [1.5, 1.25, 1.75, 0.625, -0.375, 1.9999999, -1.9999999, 0.0625] * 2
+    packed = bfp.encode(fmt, w)
+    assert packed.nbytes == bfp.packed_size(fmt, n, k)
+    e_or, c_or = oracle.encode(fmt, w)
+    e_lib, c_lib = bfp.read_fields(fmt, n, k, packed)
+    assert np.array_equal(e_lib, e_or) and np.array_equal(c_lib, c_or)
+    e_lay, c_lay = layout_fields(fmt, n, k, packed)
+    assert np.array_equal(e_lay, e_or) and np.array_equal(c_lay, c_or)
+    assert np.array_equal(bfp.decode_host(fmt, n, k, packed), oracle.decode(fmt, e_or, c_or))
+
+
+@pytest.mark.parametrize("fmt", [4, 8])
+def test_packed_size_is_the_storage_cost(fmt):
+    per_value = oracle.storage_bytes_per_value(fmt)
+    for n, k in [(16, 64), (8192, 2048), (512, 2048), (2048, 512), (151936, 2048)]:
+        assert bfp.packed_size(fmt, n, k) == int(per_value * n * k)
+    # ragged shapes pad to whole records
+    assert bfp.packed_size(fmt, 17, 16) == 2 * (512 + 16 * (4 if fmt == 4 else 2))
+
+
+def test_gate_up_interleaves_row_groups():
+    ffn, hidden = 48, 64
+    g = synth.normal(5, 1, (ffn, hidden), std=0.02)
+    u = synth.normal(5, 2, (ffn, hidden), std=0.02)
+    packed = bfp.encode_gate_up(4, g, u)
+    e, c = bfp.read_fields(4, 2 * ffn, hidden, packed)
+    ge, gc = oracle.encode(4, g)
+    ue, uc = oracle.encode(4, u)
+    for i in range(ffn // 16):
+        assert np.array_equal(c[32 * i:32 * i + 16], gc[16 * i:16 * i + 16])
+        assert np.array_equal(c[32 * i + 16:32 * i + 32], uc[16 * i:16 * i + 16])
+        assert np.array_equal(e[32 * i:32 * i + 16], ge[16 * i:16 * i + 16])
+        assert np.array_equal(e[32 * i + 16:32 * i + 32], ue[16 * i:16 * i + 16])
+
+
+def test_error_codes():
+    with pytest.raises(bfp.BFPError) as ei:
+        bfp.packed_size(4, 16, 24)
+    assert ei.value.code == bfp.BFP_ESHAPE
+    with pytest.raises(bfp.BFPError) as ei:
+        bfp.packed_size(5, 16, 32)
+    assert ei.value.code == bfp.BFP_EINVAL
+    w = np.zeros((16, 32), dtype=np.float32)
+    w[3, 7] = np.nan
+    with pytest.raises(bfp.BFPError) as ei:
+        bfp.encode(8, w)
+    assert ei.value.code == bfp.BFP_ENONFINITE
+    w[3, 7] = np.inf
+    with pytest.raises(bfp.BFPError) as ei:
+        bfp.encode(4, w)
+    assert ei.value.code == bfp.BFP_ENONFINITE
+    with pytest.raises(bfp.BFPError) as ei:
+        bfp.encode_gate_up(4, np.zeros((8, 32), np.float32), np.zeros((8, 32), np.float32))
+    assert ei.value.code == bfp.BFP_ESHAPE
+    with pytest.raises(bfp.BFPError) as ei:
+        bfp.set_wait_limit(-1)
+    assert ei.value.code == bfp.BFP_EINVAL
+    bfp.set_wait_limit(0)
+
+
+def test_packer_threads_do_not_change_bytes():
+    w = synth.normal(3, 3, (256, 512), std=0.02)
+    a = bfp.encode(4, w, threads=1)
+    b = bfp.encode(4, w, threads=7)
+    assert np.array_equal(a, b)
