@@ -146,6 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1) bfp_linear_kernel(const LinearArg
                 flags[0] = 1;
             }
         }
+        __syncwarp();
     } else {
         // ----------------------------------------------------------- consumers
         build_act_frags<NW * kWarp>(a.x, a.ldx, a.m, a.k, a.kbp, NGRP, a.norm != 0, a.eps, frag, shift, inv, tid, warp, lane);
@@ -174,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1) bfp_linear_kernel(const LinearArg
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[slot]);
+            if (lane == 0 && !bad) mbar_arrive(&empty[slot]);  // a slot whose data never came is kept
             pos += len;
             ++u;
             if (c0 + len < a.kc && pos < e) continue;  // row group continues in the next slot
@@ -403,7 +404,7 @@ int linear_launch_ex(const bfp_matrix *w, const uint16_t *x, int m, int64_t ldx,
     a.slot_recs = p.slot_recs;
     a.slot_bytes = p.slot_bytes;
     a.frag_bytes = p.frag_bytes;
-    a.wait = wait_cfg();
+    a.wait = WaitCfg{kDefaultWaitIters, kDefaultWaitNanos};  // only this CTA's own copies are waited on
     if (g.fmt == BFP_FMT_BFP4)
         return p.ngrp == 1 ? launch_linear_t<4, 1>(a, p, st) : launch_linear_t<4, 2>(a, p, st);
     return p.ngrp == 1 ? launch_linear_t<8, 1>(a, p, st) : launch_linear_t<8, 2>(a, p, st);

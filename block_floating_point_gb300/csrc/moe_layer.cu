@@ -68,7 +68,8 @@ struct MoeArgs {
     int rec, kc_h, kbp_h, kc_f, kbp_f, kc_fs, kbp_fs;
     int nft, nft_s, ng_d, r2, noct, Fmax;
     int nslot, slot_bytes, frag_bytes, scr_bytes;
-    WaitCfg wait;
+    WaitCfg wait;       // cross-block waits (router counter, expert counters)
+    WaitCfg wait_data;  // this CTA's own bulk copies and slot hand-backs
 };
 
 // Shared-memory bookkeeping of one CTA.
@@ -133,25 +134,27 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
 
     if (warp == NW) {
         // ==================================================================== producer
+        // Lane 0 issues every copy; the whole warp meets the consumers at the
+        // routing hand-off (named barrier 2) at one convergent point.
+        int64_t u = 0;
+        bool bad = false;
+        auto issue = [&](int nspan, const uint8_t *const *src, const uint32_t *bytes) -> bool {
+            const int slot = (int)(u % a.nslot);
+            const int64_t use = u / a.nslot;
+            if (use > 0 && !mbar_wait(&empty[slot], (uint32_t)((use - 1) & 1), a.wait_data, vflags)) return false;
+            if (vflags[0]) return false;
+            uint32_t total = 0;
+            for (int i = 0; i < nspan; ++i) total += bytes[i];
+            mbar_arrive_expect_tx(&full[slot], total);
+            uint8_t *dst = ring + (size_t)slot * a.slot_bytes;
+            for (int i = 0; i < nspan; ++i) {
+                bulk_g2s(dst, src[i], bytes[i], &full[slot]);
+                dst += bytes[i];
+            }
+            ++u;
+            return true;
+        };
         if (lane == 0) {
-            int64_t u = 0;
-            bool bad = false;
-            auto issue = [&](int nspan, const uint8_t *const *src, const uint32_t *bytes) -> bool {
-                const int slot = (int)(u % a.nslot);
-                const int64_t use = u / a.nslot;
-                if (use > 0 && !mbar_wait(&empty[slot], (uint32_t)((use - 1) & 1), a.wait, vflags)) return false;
-                if (vflags[0]) return false;
-                uint32_t total = 0;
-                for (int i = 0; i < nspan; ++i) total += bytes[i];
-                mbar_arrive_expect_tx(&full[slot], total);
-                uint8_t *dst = ring + (size_t)slot * a.slot_bytes;
-                for (int i = 0; i < nspan; ++i) {
-                    bulk_g2s(dst, src[i], bytes[i], &full[slot]);
-                    dst += bytes[i];
-                }
-                ++u;
-                return true;
-            };
             // 1. router rows
             if (rr1 > rr0) {
                 const uint8_t *src[2];
@@ -174,8 +177,11 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
                 const uint32_t bytes[1] = {(uint32_t)(2 * gb_h)};
                 bad = !issue(1, src, bytes);
             }
-            // 3. wait for the consumers' routing decision
-            bar_sync(2, kThreads);
+        }
+        // 3. wait for the consumers' routing decision
+        __syncwarp();
+        bar_sync(2, kThreads);
+        if (lane == 0) {
             const int nU = ms->nU;
             if (vflags[0]) bad = true;
             // 4. routed gate/up f-tiles
@@ -203,6 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
                 const uint32_t bytes[1] = {(uint32_t)(nrg * gb_f)};
                 bad = !issue(1, src, bytes);
             }
+            // No copy may still be landing in shared memory when the CTA exits.
             WaitCfg drain{int64_t(1) << 40, 1000000000ull};
             for (int64_t sl = 0; sl < min64(u, a.nslot); ++sl) {
                 const int64_t last_use = (u - 1 - sl) / a.nslot;
@@ -212,9 +219,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
                 raise_status(a.status, kStatusTimeout);
                 vflags[0] = 1;
             }
-        } else {
-            bar_sync(2, kThreads);  // keep the whole producer warp in the hand-off barrier count
         }
+        __syncwarp();
     } else {
         // =================================================================== consumers
         bool dispatched = false;
@@ -230,12 +236,16 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
         };
         auto wait_slot = [&](int64_t uu) -> int {
             const int slot = (int)(uu % a.nslot);
-            if (!bad) bad = !__all_sync(0xffffffffu, mbar_wait(&full[slot], (uint32_t)((uu / a.nslot) & 1), a.wait, nullptr));
+            if (!bad)
+                bad = !__all_sync(0xffffffffu,
+                                  mbar_wait(&full[slot], (uint32_t)((uu / a.nslot) & 1), a.wait_data, nullptr));
             return slot;
         };
+        // A warp whose data never arrived keeps the slot, so the producer cannot
+        // start a second copy into memory that a first copy may still be filling.
         auto release_slot = [&](int slot) {
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[slot]);
+            if (lane == 0 && !bad) mbar_arrive(&empty[slot]);
         };
 
         // ---- activation fragments (MoE input: x, or bf16(RMSNorm(h)) in stack mode)
@@ -785,6 +795,7 @@ static int moe_launch(const bfp_moe_layer *L, const uint16_t *x, int m, int norm
     a.frag_bytes = p.frag_bytes;
     a.scr_bytes = p.scr_bytes;
     a.wait = wait_cfg();
+    a.wait_data = WaitCfg{kDefaultWaitIters, kDefaultWaitNanos};
     if (L->expert_fmt == BFP_FMT_BFP4)
         return p.ngrp == 1 ? launch_moe_t<4, 1>(a, p, st) : launch_moe_t<4, 2>(a, p, st);
     return p.ngrp == 1 ? launch_moe_t<8, 1>(a, p, st) : launch_moe_t<8, 2>(a, p, st);

@@ -1,0 +1,92 @@
+"""GPU parity of the BFP unpack and the dense BFP linear against the oracle (C-ABI calls)."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from harness import assert_close, bf16_tensor
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+bfp = None
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    global bfp
+    import block_floating_point_gb300 as m
+    assert torch.cuda.is_available(), "GPU tests need CUDA"
+    m.load()
+    bfp = m
+    yield
+
+
+def adversarial(w):
+    n = w.shape[0]
+    if n > 6:
+        w[1, :] = 0.0
+        w[2, :] = np.float32(1e-37) * np.sign(w[2, :])     # block exponents near the bottom: subnormal decodes
+        w[3, :16] = [1.5, 1.25, 1.75, 0.625, -0.375, 1.9999999, -1.9999999, 0.0625] * 2  # ties, saturation
+        w[4, :] *= np.float32(1e30)                          # large exponents
+        w[5, ::17] = 0.0
+    return w
+
+
+@pytest.mark.parametrize("fmt", [4, 8])
+@pytest.mark.parametrize("n,k", [(16, 64), (37, 96), (5, 208), (130, 2048), (512, 2048)])
+def test_unpack_device_bit_exact(fmt, n, k):
+    w = adversarial(synth.normal(21, 100 + n + k, (n, k), std=0.02))
+    e, c = oracle.encode(fmt, w)
+    ref = oracle.decode(fmt, e, c)
+    mat = bfp.DeviceMatrix.from_host(fmt, n, k, bfp.encode(fmt, w))
+    got = bfp.unpack_device(mat).cpu().numpy()
+    torch.cuda.synchronize()
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+LINEAR_CASES = [
+    (8, 8192, 2048, 1), (8, 8192, 2048, 8), (8, 8192, 2048, 16),   # dense BFP8 projection y[M x 8192] = x W^T
+    (4, 512, 2048, 1), (4, 512, 2048, 16),
+    (8, 37, 96, 3), (4, 37, 96, 9), (8, 130, 2048, 16), (4, 16, 16, 1), (8, 2000, 1024, 5),
+]
+
+
+@pytest.mark.parametrize("fmt,n,k,m", LINEAR_CASES)
+def test_linear_matches_oracle(fmt, n, k, m):
+    w = adversarial(synth.normal(31, 200 + n + k, (n, k), std=0.02))
+    if n > 6:
+        w[2, :] = synth.normal(31, 9, (k,), std=0.02)  # keep rows' outputs in a normal range
+        w[4, :] = synth.normal(31, 10, (k,), std=0.02)
+    x = np.stack([synth.activation_row(31, 1000 + r, k, False) for r in range(m)])
+    e, c = oracle.encode(fmt, w)
+    y_ref, yb_ref = oracle.linear(fmt, e, c, x)
+    mat = bfp.DeviceMatrix.from_host(fmt, n, k, bfp.encode(fmt, w))
+    ws = bfp.linear_workspace(mat, m)
+    xt = bf16_tensor(x)
+    y = torch.empty((m, n), dtype=torch.float32, device="cuda")
+    yb = torch.empty((m, n), dtype=torch.int16, device="cuda")
+    bfp.linear(mat, xt, ws, y=y, y_bf16=yb)
+    got = y.cpu().numpy()
+    gotb = yb.cpu().numpy().view(np.uint16)
+    assert bfp.workspace_status(ws) == bfp.BFP_OK
+    assert_close(got, y_ref, f"linear fmt={fmt} {n}x{k} m={m}")
+    assert np.array_equal(gotb, synth.to_bf16_bits(got))  # bf16 output is the RNE of the kernel's own fp32
+    # and within one bf16 step of the oracle's bf16 output
+    diff = np.abs(gotb.astype(np.int32) - yb_ref.astype(np.int32))
+    assert np.all((diff <= 1) | (np.sign(got) != np.sign(y_ref)) | (np.abs(y_ref) < 1e-30))
+    # repeated calls are bit-identical (fixed-order reduction, workspace left clean)
+    y2 = bfp.linear(mat, xt, ws)
+    assert torch.equal(y, y2)
+
+
+def test_linear_rejects_bad_arguments():
+    mat = bfp.DeviceMatrix.from_host(8, 64, 64, bfp.encode(8, synth.normal(1, 1, (64, 64), std=0.02)))
+    ws = bfp.linear_workspace(mat, 1)
+    x = torch.zeros((17, 64), dtype=torch.int16, device="cuda")
+    with pytest.raises(bfp.BFPError) as ei:
+        bfp.linear(mat, x, ws)
+    assert ei.value.code == bfp.BFP_ESHAPE
+    with pytest.raises(bfp.BFPError) as ei:
+        bfp.linear(mat, x[:2], ws[:64])
+    assert ei.value.code == bfp.BFP_EWORKSPACE

@@ -1,0 +1,140 @@
+"""GPU parity of the fused MoE decode layer against the oracle (C-ABI calls).
+
+Expert selection (top-k indices, slot order) must match bit for bit; routing
+weights and outputs within 1e-3 * (|oracle| + rms(oracle)). Inputs are redrawn
+per row until the k-th / (k+1)-th router-logit gap is at least 1e-3.
+"""
+import numpy as np
+import pytest
+
+import synth
+from harness import LayerCase, assert_close, bf16_tensor
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+bfp = None
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    global bfp
+    import block_floating_point_gb300 as m
+    assert torch.cuda.is_available(), "GPU tests need CUDA"
+    m.load()
+    bfp = m
+    yield
+
+
+def run_layer(layer, x, m):
+    ws = bfp.moe_workspace(layer, m)
+    xt = bf16_tensor(x)
+    idx = torch.empty((m, layer.top_k), dtype=torch.int32, device="cuda")
+    w = torch.empty((m, layer.top_k), dtype=torch.float32, device="cuda")
+    y = bfp.moe_decode_layer(layer, xt, ws, topk_idx=idx, topk_w=w)
+    torch.cuda.synchronize()
+    assert bfp.workspace_status(ws) == bfp.BFP_OK
+    return y, idx, w, ws, xt
+
+
+def check(case, layer, m, rms_norm, row_seed0=0):
+    x, _ = case.inputs(m, rms_norm, row_seed0)
+    y, idx, w, ws, xt = run_layer(layer, x, m)
+    y_ref, idx_ref, w_ref = case.oracle_layer(x)
+    assert np.array_equal(idx.cpu().numpy(), idx_ref), "expert selection differs"
+    assert_close(w.cpu().numpy(), w_ref, "routing weights")
+    assert_close(y.cpu().numpy(), y_ref, "layer output")
+    # a second launch on the same workspace gives the same bits (self-cleaning counters, fixed-order combine)
+    idx2 = torch.empty_like(idx)
+    y2 = bfp.moe_decode_layer(layer, xt, ws, topk_idx=idx2)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y2) and torch.equal(idx, idx2)
+    return x
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    case = LayerCase(synth.TINY, seed=101)
+    return case, case.device_layer()
+
+
+@pytest.fixture(scope="module")
+def full():
+    case = LayerCase(synth.FULL, seed=202)
+    return case, case.device_layer()
+
+
+@pytest.mark.parametrize("m", [1, 2, 5, 16])
+def test_tiny_layer(tiny, m):
+    case, layer = tiny
+    check(case, layer, m, rms_norm=False, row_seed0=10 * m)
+
+
+def test_tiny_layer_bfp8_experts():
+    case = LayerCase(synth.TINY, seed=103, fmt=8)
+    check(case, case.device_layer(), 3, rms_norm=False)
+
+
+def test_full_layer_m1(full):
+    case, layer = full
+    check(case, layer, 1, rms_norm=True, row_seed0=0)
+
+
+def test_full_layer_m16(full):
+    case, layer = full
+    check(case, layer, 16, rms_norm=True, row_seed0=100)
+
+
+def test_full_layer_m8(full):
+    case, layer = full
+    check(case, layer, 8, rms_norm=True, row_seed0=300)
+
+
+def test_full_layer_hot_routing_m16():
+    case = LayerCase(synth.FULL, seed=303, hot=True)
+    layer = case.device_layer()
+    x = check(case, layer, 16, rms_norm=True, row_seed0=500)
+    # the bias concentrates the rows on few experts
+    idx = case.oracle_layer(x)[1]
+    assert len(np.unique(idx)) < 40
+
+
+def test_odd_shapes():
+    spec = synth.MoESpec(hidden=208, n_experts=37, ffn=48, top_k=3, shared_ffn=80)
+    case = LayerCase(spec, seed=404)
+    check(case, case.device_layer(), 7, rms_norm=False)
+
+
+def test_bounded_wait_reports_timeout_and_recovers(tiny):
+    """A cross-block wait that cannot be satisfied in one poll gives BFP_ETIMEOUT, not a hang;
+    after re-initialising the workspace the layer runs correctly again."""
+    case, layer = tiny
+    x, _ = case.inputs(4, False, 900)
+    ws = bfp.moe_workspace(layer, 4)
+    xt = bf16_tensor(x)
+    bfp.set_wait_limit(1)
+    try:
+        seen = set()
+        for _ in range(5):
+            bfp.moe_decode_layer(layer, xt, ws)
+            seen.add(bfp.workspace_status(ws))
+    finally:
+        bfp.set_wait_limit(0)
+    assert bfp.BFP_ETIMEOUT in seen
+    bfp.workspace_init(ws)
+    y = bfp.moe_decode_layer(layer, xt, ws)
+    torch.cuda.synchronize()
+    assert bfp.workspace_status(ws) == bfp.BFP_OK
+    assert_close(y.cpu().numpy(), case.oracle_layer(x)[0], "after recovery")
+
+
+def test_rejects_bad_arguments(tiny):
+    case, layer = tiny
+    ws = bfp.moe_workspace(layer, 1)
+    x = torch.zeros((17, case.spec.hidden), dtype=torch.int16, device="cuda")
+    with pytest.raises(bfp.BFPError) as ei:
+        bfp.moe_decode_layer(layer, x, ws)
+    assert ei.value.code == bfp.BFP_ESHAPE
+    with pytest.raises(bfp.BFPError) as ei:
+        bfp.moe_decode_layer(layer, x[:1], ws[:256])
+    assert ei.value.code == bfp.BFP_EWORKSPACE
