@@ -72,9 +72,11 @@ def test_linear_matches_oracle(fmt, n, k, m):
     assert bfp.workspace_status(ws) == bfp.BFP_OK
     assert_close(got, y_ref, f"linear fmt={fmt} {n}x{k} m={m}")
     assert np.array_equal(gotb, synth.to_bf16_bits(got))  # bf16 output is the RNE of the kernel's own fp32
-    # and within one bf16 step of the oracle's bf16 output
+    # and, away from cancellation (|y| >= rms/10), within one bf16 step of the oracle's bf16 output
+    rms = np.sqrt(np.mean(y_ref.astype(np.float64) ** 2, axis=1, keepdims=True))
+    big = np.abs(y_ref) >= 0.1 * rms
     diff = np.abs(gotb.astype(np.int32) - yb_ref.astype(np.int32))
-    assert np.all((diff <= 1) | (np.sign(got) != np.sign(y_ref)) | (np.abs(y_ref) < 1e-30))
+    assert np.all(diff[big] <= 1)
     # repeated calls are bit-identical (fixed-order reduction, workspace left clean)
     y2 = bfp.linear(mat, xt, ws)
     assert torch.equal(y, y2)
