@@ -1,0 +1,490 @@
+#!/usr/bin/env python
+"""Benchmark of the BFP MoE decode layer on GB300.
+
+Metric: MoE decode layer us and effective weight GB/s (BFP weight bytes the
+step actually streams / device time; % of ~8 TB/s HBM). The headline
+workload is the full-size layer at M=16 rows (hidden 2048, 256 experts of
+width 512, top-8, shared expert of width 512, BFP4 experts, bf16 router):
+each step streams the union of the experts the 16 rows select (~100) plus the
+shared expert, ~180 MB, more than the 129 MB L2, and steps rotate over
+several independently drawn layer instances. Secondary lines (same run): the
+same layer at M=1, the hot-expert routing variant at M=16, and the dense BFP8
+projection [8192 x 2048] at M=1/16; those steps are smaller than L2, so each
+one is timed alone after a 256 MB L2-flushing write.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--quick]
+
+Under torchrun (N > 1) every rank runs its own replica of the workload (the
+layer does not need a second GPU); value = all ranks' bytes / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE decode layer µs & effective weight GB/s (% of ~8 TB/s HBM) at M=1/16"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the M=16 layer kernel, from one ncu
+# capture (profiles/moe_layer_m16.md), valid while the kernel sources hash to src_sha.
+NCU_TRAFFIC = {"moe_layer_m16": {"bytes_per_launch": None, "src_sha": None}}
+
+
+def kernel_src_sha() -> str:
+    h = hashlib.sha256()
+    for f in ("moe_layer.cu", "bfp_tiles.cuh", "bfp_device.cuh", "bfp_launch.h"):
+        with open(os.path.join(ROOT, "block_floating_point_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--instances", type=int, default=3)
+    ap.add_argument("--seed", type=int, default=20261202)
+    ap.add_argument("--quick", action="store_true", help="headline line only (no secondary workloads, no oracle)")
+    ap.add_argument("--no-graph", action="store_true")
+    return ap.parse_args()
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+    FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_id: str):
+        self.samples = []
+        self.window = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", gpu_id, "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.th = threading.Thread(target=self._read, daemon=True)
+        self.th.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [s.strip() for s in line.split(",")]))
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = self.samples
+        if self.window:
+            inside = [s for s in rows if self.window[0] - 0.15 <= s[0] <= self.window[1] + 0.15]
+            rows = inside or rows
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for _, v in rows:
+            try:
+                sm.append(float(v[1]))
+                mx.append(float(v[2]))
+            except Exception:
+                continue
+            for n, val in zip(names, v[5:9]):
+                if val.lower() not in ("not active", "0x0000000000000000", "[n/a]", "n/a"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- workload
+def build_instances(n, seed, device):
+    import block_floating_point_gb300 as bfp
+    import synth
+    spec = synth.FULL
+    layers = []
+    for i in range(n):
+        lw = synth.LayerWeights(spec, seed, layer=0, instance=i)
+
+        def src(e, lw=lw):
+            key = synth.SHARED_EXPERT if e == "shared" else e
+            return lw.gate(key), lw.up(key), lw.down(key)
+        layers.append(bfp.MoELayer.from_source(spec.hidden, spec.n_experts, spec.ffn, spec.top_k, spec.shared_ffn,
+                                               bfp.BFP4, lw.router_bf16(), lw.shared_gate_bf16(), src,
+                                               lambda src=src: src("shared"), device=device))
+    return spec, layers
+
+
+def make_x(spec, seed, m, instance, device):
+    import torch
+    import synth
+    x = np.stack([synth.activation_row(seed, 1000 * instance + r, spec.hidden, True, instance=instance)
+                  for r in range(m)])
+    return x, torch.from_numpy(x.view(np.int16)).to(device)
+
+
+def union_bytes(layer, idx):
+    return layer.weight_bytes(len(np.unique(idx)))
+
+
+def other_bytes(layer, m):
+    """bf16 router + shared gate read, bf16 x in, fp32 y out (the kernel's non-BFP traffic)."""
+    return layer.n_experts * layer.hidden * 2 + layer.hidden * 2 + m * layer.hidden * (2 + 4)
+
+
+def timed_graph(step, k, warmup, use_graph, group=99):
+    """Run warmup then exactly k steps; returns device ms for the k steps (CUDA events on the launch stream)."""
+    import torch
+    stream = torch.cuda.current_stream()
+    graphs = []
+    if use_graph:
+        try:
+            for size in sorted({min(group, k), k % group} - {0}, reverse=True):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    for i in range(size):
+                        step(i)
+                graphs.append((size, g))
+        except Exception as exc:  # capture unsupported: eager launches
+            print(f"# graph capture failed ({exc}); timing eager launches", file=sys.stderr)
+            graphs = []
+            torch.cuda.synchronize()
+
+    def run(n):
+        if graphs:
+            full = dict(graphs)
+            big = graphs[0][0]
+            for _ in range(n // big):
+                full[big].replay()
+            rem = n % big
+            if rem:
+                if rem in full:
+                    full[rem].replay()
+                else:
+                    for i in range(rem):
+                        step(i)
+        else:
+            for i in range(n):
+                step(i)
+
+    run(warmup)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    run(k)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
+
+
+def timed_flushed(step, k, warmup, flush_buf, batch=32):
+    """Each step timed alone (events around its launch) after a write of flush_buf (> L2); launches are queued
+    behind a device sleep so the host never starves the device between the events. Returns (sum ms, per-step ms)."""
+    import torch
+    stream = torch.cuda.current_stream()
+    for i in range(warmup):
+        flush_buf.zero_()
+        step(i)
+    torch.cuda.synchronize()
+    times = []
+    done = 0
+    while done < k:
+        n = min(batch, k - done)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        torch.cuda._sleep(int(4e6))
+        for j in range(n):
+            flush_buf.zero_()
+            evs[j][0].record(stream)
+            step(done + j)
+            evs[j][1].record(stream)
+        torch.cuda.synchronize()
+        times += [a.elapsed_time(b) for a, b in evs]
+        done += n
+    return float(np.sum(times)), times
+
+
+# --------------------------------------------------------------------------- reference arm (the oracle)
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    import synth
+    spec = synth.FULL
+    lw = synth.LayerWeights(spec, args.seed, 0, 0)
+
+    def src(e):
+        key = synth.SHARED_EXPERT if e == "shared" else e
+        return lw.gate(key), lw.up(key), lw.down(key)
+    router, sgate = lw.router_bf16(), lw.shared_gate_bf16()
+    cache = oracle.ExpertCache(4, src)
+    rows = [synth.activation_row(args.seed, r, spec.hidden, True) for r in range(16)]
+    per_expert = 1769472
+    # setup (not timed): the oracle's own encoding of every expert the sample rows select
+    for x in rows:
+        idx, _ = oracle.route_row(oracle.router_logits(router, x[None])[0], spec.top_k)
+        for e in idx:
+            cache(int(e))
+    cache("shared")
+    times = []
+    for s in range(args.warmup + args.steps):
+        x = rows[s % 16][None]
+        t = time.perf_counter()
+        oracle.moe_layer(x, router, sgate, cache, spec.top_k)
+        if s >= args.warmup:
+            times.append(time.perf_counter() - t)
+    sec = float(np.mean(times))
+    bytes_row = (spec.top_k + 1) * per_expert
+    val = bytes_row / sec / 1e9
+    out = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "MoE decode layer, full size (H=2048, 256 experts F=512, top-8, shared F=512, BFP4); "
+                               "oracle step = one row of the M=16 workload", "rows_per_step": 1},
+        "cpu_baseline": {"value": val, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": "one row of the M=16 decode step per step (its 8 experts + shared), single thread"},
+        "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def cpu_baseline_sample(args, spec, x_np):
+    """The oracle as it stands, single-threaded, on one full M=16 step of instance 0 (encoding excluded)."""
+    import oracle
+    import synth
+    lw = synth.LayerWeights(spec, args.seed, 0, 0)
+
+    def src(e):
+        key = synth.SHARED_EXPERT if e == "shared" else e
+        return lw.gate(key), lw.up(key), lw.down(key)
+    router, sgate = lw.router_bf16(), lw.shared_gate_bf16()
+    cache = oracle.ExpertCache(4, src)
+    logits = oracle.router_logits(router, x_np)
+    sel = set()
+    for r in range(x_np.shape[0]):
+        idx, _ = oracle.route_row(logits[r], spec.top_k)
+        sel.update(int(e) for e in idx)
+    for e in sel:
+        cache(e)
+    cache("shared")
+    t = time.perf_counter()
+    oracle.moe_layer(x_np, router, sgate, cache, spec.top_k)
+    sec = time.perf_counter() - t
+    return (len(sel) + 1) * 1769472 / sec / 1e9, sec
+
+
+# --------------------------------------------------------------------------- our arm
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    import torch
+    import torch.distributed as dist
+    import block_floating_point_gb300 as bfp
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
+    bfp.load()
+    peak, peak_kind = measured_peak()
+
+    spec, layers = build_instances(args.instances, args.seed + 7919 * rank, device)
+    R = len(layers)
+    M = 16
+    xs, xts, ys, idxs = [], [], [], []
+    ws = bfp.moe_workspace(layers[0], M)
+    for i, L in enumerate(layers):
+        x, xt = make_x(spec, args.seed + rank, M, i, device)
+        xs.append(x)
+        xts.append(xt)
+        ys.append(torch.empty((M, spec.hidden), dtype=torch.float32, device=device))
+        idx = torch.empty((M, spec.top_k), dtype=torch.int32, device=device)
+        bfp.moe_decode_layer(L, xt, ws, y=ys[i], topk_idx=idx)
+        idxs.append(idx)
+    torch.cuda.synchronize()
+    assert bfp.workspace_status(ws) == bfp.BFP_OK
+    step_bytes = [union_bytes(L, idxs[i].cpu().numpy()) for i, L in enumerate(layers)]
+    n_union = [len(np.unique(idxs[i].cpu().numpy())) for i in range(R)]
+    avg_bytes = float(np.mean([step_bytes[i % R] for i in range(args.steps)]))
+    avg_other = float(other_bytes(layers[0], M))
+
+    def step16(i):
+        j = i % R
+        bfp.moe_decode_layer(layers[j], xts[j], ws, y=ys[j])
+
+    gpu_id = "0"
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+    except Exception:
+        gpu_id = str(local)
+    sampler = ClockSampler(gpu_id)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    ms = timed_graph(step16, args.steps, args.warmup, not args.no_graph)
+    t1 = time.time()
+    sampler.mark(t0, t1)
+    if world > 1:
+        tt = torch.tensor([ms], device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+        dist.barrier()
+    clocks = sampler.stop()
+    assert bfp.workspace_status(ws) == bfp.BFP_OK
+    us_layer = ms * 1e3 / args.steps
+    gbs = avg_bytes * args.steps * world / (ms * 1e-3) / 1e9
+    kernel_gbs = (avg_bytes + avg_other) / (us_layer * 1e-6) / 1e9
+    sha = kernel_src_sha()
+    tr = NCU_TRAFFIC["moe_layer_m16"]
+    traffic = tr["bytes_per_launch"] if tr["src_sha"] == sha else None
+
+    # ---- e2e through the public API with host buffers (pinned x in, y out, synchronised every step)
+    xh = [torch.from_numpy(x.view(np.int16)).pin_memory() for x in xs]
+    yh = torch.empty((M, spec.hidden), dtype=torch.float32).pin_memory()
+    xd = torch.empty((M, spec.hidden), dtype=torch.int16, device=device)
+    yd = torch.empty((M, spec.hidden), dtype=torch.float32, device=device)
+    ke = max(1, min(args.steps, 300))
+    for i in range(3):
+        xd.copy_(xh[i % R], non_blocking=True)
+        bfp.moe_decode_layer(layers[i % R], xd, ws, y=yd)
+        yh.copy_(yd, non_blocking=True)
+        torch.cuda.synchronize()
+    t = time.perf_counter()
+    for i in range(ke):
+        xd.copy_(xh[i % R], non_blocking=True)
+        bfp.moe_decode_layer(layers[i % R], xd, ws, y=yd)
+        yh.copy_(yd, non_blocking=True)
+        torch.cuda.synchronize()
+    e2e_sec = (time.perf_counter() - t) / ke
+    e2e_bytes = float(np.mean([step_bytes[i % R] for i in range(ke)]))
+
+    out = {
+        "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": us_layer / 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bfp4 weights x bf16 activations, fp16 tensor-core products, fp32 accumulate",
+        "data": "synthetic (seeded N(0,0.02) weights encoded to BFP4, RMS-normalised N(0,1) bf16 rows)",
+        "config": {"workload": "MoE decode layer M=16 (H=2048, 256 experts F=512, top-8, shared F=512, BFP4 "
+                               "experts, bf16 router)", "rows": M, "instances": R,
+                   "union_experts_per_step": n_union, "us_per_layer": us_layer,
+                   "bfp_bytes_per_step": avg_bytes, "pct_of_8tbs": 100 * gbs / world / NOMINAL_HBM_GBS,
+                   "pct_of_measured_copy": 100 * gbs / world / peak,
+                   "gbs_incl_bf16_router_gate": (avg_bytes + layers[0].n_experts * layers[0].hidden * 2
+                                                 + layers[0].hidden * 2) * args.steps * world / (ms * 1e-3) / 1e9,
+                   "l2": "inputs larger than L2: each step streams ~180 MB of experts (> 129 MB L2), "
+                         f"rotating over {R} independently drawn layer instances",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": kernel_gbs, "peak": peak, "unit": "GB/s",
+                     "frac": kernel_gbs / peak, "traffic": traffic,
+                     "kernel": "moe_layer_kernel<4,2> (one launch per step)",
+                     "algorithmic_bytes_per_launch": avg_bytes + avg_other, "peak_source": peak_kind},
+        "e2e": {"value": e2e_bytes / e2e_sec / 1e9, "unit": "GB/s", "h2d_bytes_per_step": M * spec.hidden * 2,
+                "d2h_bytes_per_step": M * spec.hidden * 4, "us_per_step": e2e_sec * 1e6,
+                "note": "public Python API over the C-ABI; pinned host x -> device, layer, y -> host, sync each step"},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+
+    if not args.quick:
+        sec = {}
+        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+        ksec = max(20, min(200, args.steps))
+        # M=1 on the same instances, each step alone after an L2 flush
+        ws1 = bfp.moe_workspace(layers[0], 1)
+        x1 = [xt[:1].contiguous() for xt in xts]
+        y1 = torch.empty((1, spec.hidden), dtype=torch.float32, device=device)
+        b1 = []
+        for i, L in enumerate(layers):
+            idx = torch.empty((1, spec.top_k), dtype=torch.int32, device=device)
+            bfp.moe_decode_layer(L, x1[i], ws1, y=y1, topk_idx=idx)
+            b1.append(union_bytes(L, idx.cpu().numpy()))
+        tot, _ = timed_flushed(lambda i: bfp.moe_decode_layer(layers[i % R], x1[i % R], ws1, y=y1), ksec, 5, flush)
+        us1 = tot * 1e3 / ksec
+        g1 = float(np.mean([b1[i % R] for i in range(ksec)])) / (us1 * 1e-6) / 1e9
+        sec["m1"] = {"us_per_layer": us1, "gbs": g1, "pct_of_8tbs": 100 * g1 / NOMINAL_HBM_GBS,
+                     "pct_of_measured_copy": 100 * g1 / peak, "bfp_bytes_per_step": float(np.mean(b1)),
+                     "timing": "each step alone after a 256 MB L2 flush, CUDA events"}
+        # hot-expert routing at M=16 (logit bias +2.0 on 8 fixed experts), same weights
+        import synth
+        bias = torch.from_numpy(synth.hot_bias(spec.n_experts, args.seed)).to(device)
+        hot = [bfp.MoELayer(L.hidden, L.n_experts, L.ffn, L.top_k, L.shared_ffn, L.expert_fmt, L.router,
+                            L.shared_gate, L.experts_gate_up, L.experts_down, L.shared_gate_up, L.shared_down,
+                            router_bias=bias) for L in layers]
+        bh, nh = [], []
+        for i, L in enumerate(hot):
+            idx = torch.empty((M, spec.top_k), dtype=torch.int32, device=device)
+            bfp.moe_decode_layer(L, xts[i], ws, y=ys[i], topk_idx=idx)
+            bh.append(union_bytes(L, idx.cpu().numpy()))
+            nh.append(len(np.unique(idx.cpu().numpy())))
+        tot, _ = timed_flushed(lambda i: bfp.moe_decode_layer(hot[i % R], xts[i % R], ws, y=ys[i % R]), ksec, 5,
+                               flush)
+        ush = tot * 1e3 / ksec
+        gh = float(np.mean([bh[i % R] for i in range(ksec)])) / (ush * 1e-6) / 1e9
+        sec["m16_hot"] = {"us_per_layer": ush, "gbs": gh, "pct_of_8tbs": 100 * gh / NOMINAL_HBM_GBS,
+                          "union_experts_per_step": nh, "timing": "each step alone after a 256 MB L2 flush"}
+        # dense BFP8 projection [8192 x 2048], M = 1 / 8 / 16
+        w = synth.normal(args.seed, synth.stream_id(synth.KIND_DENSE), (8192, 2048), std=0.02)
+        mat = bfp.DeviceMatrix.from_host(8, 8192, 2048, bfp.encode(8, w), device=device)
+        for m in (1, 8, 16):
+            xd_ = torch.from_numpy(np.stack([synth.activation_row(args.seed, 50000 + r, 2048, False)
+                                             for r in range(m)]).view(np.int16)).to(device)
+            wsl = bfp.linear_workspace(mat, m)
+            yl = torch.empty((m, 8192), dtype=torch.int16, device=device)
+            tot, _ = timed_flushed(lambda i: bfp.linear(mat, xd_, wsl, y_bf16=yl), ksec, 5, flush)
+            usd = tot * 1e3 / ksec
+            gd = mat.nbytes / (usd * 1e-6) / 1e9
+            sec[f"dense_bfp8_m{m}"] = {"us": usd, "gbs": gd, "pct_of_8tbs": 100 * gd / NOMINAL_HBM_GBS,
+                                      "bytes": mat.nbytes}
+        out["secondary"] = sec
+        if rank == 0 and world == 1:
+            v, s_ = cpu_baseline_sample(args, spec, xs[0])
+            out["cpu_baseline"] = {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                   "sample": f"one full M=16 step of instance 0 (16 rows), {s_:.2f} s, single "
+                                             "thread, expert encoding excluded"}
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -280,10 +280,16 @@ class MoELayer:
         dnb = packed_size(expert_fmt, hidden, ffn)
         host_gu = np.empty(n_experts * gub, dtype=np.uint8)
         host_dn = np.empty(n_experts * dnb, dtype=np.uint8)
-        for e in range(n_experts):
+        def pack(e):
             g, u, d = expert_source(e)
             encode_gate_up(expert_fmt, g, u, threads, out=host_gu[e * gub:(e + 1) * gub])
             encode(expert_fmt, d, threads, out=host_dn[e * dnb:(e + 1) * dnb])
+
+        # experts are independent: pack several at once (the C calls release the GIL)
+        import concurrent.futures as cf
+        workers = max(1, min(8, (os.cpu_count() or 1) // 2))
+        with cf.ThreadPoolExecutor(max_workers=workers) as ex:
+            list(ex.map(pack, range(n_experts)))
         g, u, d = shared_source()
         sgu = encode_gate_up(expert_fmt, g, u, threads)
         sdn = encode(expert_fmt, d, threads)

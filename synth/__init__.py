@@ -32,7 +32,7 @@ def build(force: bool = False) -> str:
     src = os.path.join(_HERE, "gen.c")
     if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(src):
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", src, "-o", tmp, "-lm"])
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fno-fast-math", "-fPIC", "-shared", "-pthread", src, "-o", tmp, "-lm"])
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 

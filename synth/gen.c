@@ -12,8 +12,8 @@
  * Every value is a pure function of (seed, stream, index), so any slice of
  * any matrix can be regenerated alone and threads can split a range freely.
  *
- * Normal deviates use the Box-Muller transform on the four 32-bit words of
- * one Philox block: (w0, w1) -> two deviates, (w2, w3) -> two deviates.
+ * Normal deviates use the Box-Muller transform (in fp32) on the four 32-bit
+ * words of one Philox block: (w0, w1) -> two deviates, (w2, w3) -> two deviates.
  */
 #include <math.h>
 #include <pthread.h>
@@ -48,18 +48,19 @@ static void philox_block(uint64_t seed, uint64_t stream, uint64_t block, uint32_
     philox4x32_10(ctr, key, out);
 }
 
-/* (0, 1): never 0, so log() is finite. */
-static double u01_open(uint32_t w) { return ((double)w + 0.5) * (1.0 / 4294967296.0); }
+/* (0, 1): never 0, so log() is finite. 24 significant bits, as an fp32 deviate needs. */
+static float u01_open(uint32_t w) { return ((float)(w >> 8) + 0.5f) * (1.0f / 16777216.0f); }
 
 static void normal_block(uint64_t seed, uint64_t stream, uint64_t block, double z[4]) {
     uint32_t w[4];
     philox_block(seed, stream, block, w);
-    const double two_pi = 6.283185307179586476925286766559;
+    const float two_pi = 6.28318530717958647692f;
     for (int p = 0; p < 2; ++p) {
-        double u1 = u01_open(w[2 * p]), u2 = u01_open(w[2 * p + 1]);
-        double r = sqrt(-2.0 * log(u1));
-        z[2 * p] = r * cos(two_pi * u2);
-        z[2 * p + 1] = r * sin(two_pi * u2);
+        float u1 = u01_open(w[2 * p]), u2 = u01_open(w[2 * p + 1]);
+        float r = sqrtf(-2.0f * logf(u1));
+        float a = two_pi * u2;
+        z[2 * p] = (double)(r * cosf(a));
+        z[2 * p + 1] = (double)(r * sinf(a));
     }
 }
 
