@@ -62,6 +62,7 @@ SIGNATURES = {
     "moe_workspace_size": [_LP, _I, ctypes.POINTER(_SZ)],
     "bfp_workspace_init": [_P, _SZ, _P],
     "moe_decode_layer": [_LP, _P, _I, _P, _P, _P, _P, _SZ, _P],
+    "moe_decode_layer_static": [_LP, _P, _I, _P, _P, _P, _P],
     "moe_stack_workspace_size": [_LP, _I, _MP, _I, ctypes.POINTER(_SZ)],
     "moe_stack_decode": [_LP, _I, _MP, _P, _I, _P, _P, _SZ, _P],
     "bfp_workspace_status": [_P, ctypes.POINTER(_I), _P],
@@ -324,6 +325,23 @@ def moe_decode_layer(layer: MoELayer, x, ws, y=None, topk_idx=None, topk_w=None,
     c = layer.c()
     _check(load().moe_decode_layer(ctypes.byref(c), _ptr(x), m, _ptr(y), _ptr(topk_idx), _ptr(topk_w), _ptr(ws),
                                    ws.numel(), _stream(stream)), "moe_decode_layer")
+    return y
+
+
+def moe_decode_layer_static(layer: MoELayer, x, y=None, topk_idx=None, topk_w=None, stream=None):
+    """moe_decode_layer without a workspace, for callers that cannot allocate device memory.
+
+    Uses the library's built-in 2 MiB device scratch array (shared by every
+    call on a device; overlapping calls race). The first call on a device
+    sets the array up synchronously, so make it before any stream capture.
+    """
+    import torch
+    m = x.shape[0]
+    if y is None:
+        y = torch.empty((m, layer.hidden), dtype=torch.float32, device=x.device)
+    c = layer.c()
+    _check(load().moe_decode_layer_static(ctypes.byref(c), _ptr(x), m, _ptr(y), _ptr(topk_idx), _ptr(topk_w),
+                                          _stream(stream)), "moe_decode_layer_static")
     return y
 
 

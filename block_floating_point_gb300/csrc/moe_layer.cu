@@ -31,6 +31,8 @@
 // Every expert's weights are read from HBM once per step however many rows
 // chose it. All cross-CTA waits are bounded and report BFP_ETIMEOUT.
 #include <algorithm>
+#include <mutex>
+#include <string>
 #include <vector>
 
 #include "bfp_launch.h"
@@ -882,3 +884,61 @@ int moe_stack_decode(const bfp_moe_layer *layers, int n_layers, const bfp_matrix
 }
 
 }  // extern "C"
+
+// ----------------------------------------------------------------------------
+// moe_decode_layer_static: the same layer for callers that cannot allocate
+// device memory. Its scratch is one file-scope device array of a fixed size,
+// shared by every call on a device and kept for the life of the process.
+// ----------------------------------------------------------------------------
+namespace bfp {
+
+constexpr size_t kStaticScratchBytes = size_t(2) << 20;  // 2 MiB: a full-size layer at 16 rows needs ~1.5 MiB
+static __device__ __align__(256) uint8_t g_moe_static_scratch[kStaticScratchBytes];
+
+// Device address of the scratch array on the current device. The array's name
+// in host code is only a host-side stand-in, so the address comes from
+// cudaGetSymbolAddress, once per device, with that device current; the array
+// is zeroed at the same time. Both steps are synchronous: the first call on a
+// device must not happen inside a stream capture.
+static int static_scratch(void **out) {
+    static std::mutex mu;
+    static std::vector<void *> addr;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> lk(mu);
+    if ((int)addr.size() <= dev) addr.resize(dev + 1, nullptr);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_moe_static_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+        e = cudaMemset(p, 0, kStaticScratchBytes);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(static scratch)");
+        addr[dev] = p;
+    }
+    *out = addr[dev];
+    return BFP_OK;
+}
+
+}  // namespace bfp
+
+extern "C" int moe_decode_layer_static(const bfp_moe_layer *layer, const uint16_t *x, int m, float *y,
+                                       int32_t *topk_idx, float *topk_w, bfp_stream_t stream) {
+    if (!y) return fail(BFP_EINVAL, "null y");
+    MoePlan p;
+    int rc = plan_moe(layer, m, &p);
+    if (rc) return rc;
+    if (p.ws_bytes > kStaticScratchBytes)
+        return fail(BFP_EWORKSPACE, "this layer needs " + std::to_string(p.ws_bytes) +
+                                        " bytes of scratch; the built-in scratch holds " +
+                                        std::to_string(kStaticScratchBytes) +
+                                        " (use moe_decode_layer with a caller-allocated workspace)");
+    void *ws = nullptr;
+    rc = static_scratch(&ws);
+    if (rc) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // The status word and the cross-block counters must start at zero: clear them on the stream.
+    cudaError_t e = cudaMemsetAsync(ws, 0, p.off_logits, st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(static scratch counters)");
+    return moe_launch(layer, x, m, 0, y, nullptr, topk_idx, topk_w, ws, kStaticScratchBytes, st);
+}

@@ -18,7 +18,8 @@
  *   - returns an int status: BFP_OK (0) or a negative BFP_E* code; never
  *     throws, never exits; bfp_last_error() gives a message (thread-local);
  *   - the caller owns and allocates every buffer (host or device); the
- *     library allocates no device memory;
+ *     library allocates no device memory while it runs (its one built-in
+ *     array, see moe_decode_layer_static, comes with the loaded module);
  *   - device work is enqueued on the caller's stream and is asynchronous;
  *     only bfp_workspace_status() synchronises (the stream it is given);
  *   - device pointers must be 16-byte aligned (BFP_EALIGN otherwise);
@@ -198,6 +199,36 @@ int bfp_workspace_init(void *ws, size_t ws_bytes, bfp_stream_t stream);
  */
 int moe_decode_layer(const bfp_moe_layer *layer, const uint16_t *x, int m, float *y, int32_t *topk_idx,
                      float *topk_w, void *ws, size_t ws_bytes, bfp_stream_t stream);
+
+/*
+ * moe_decode_layer without a workspace argument, for callers that cannot
+ * allocate device memory: for example code embedded in a host runtime whose
+ * device memory is all owned by that runtime's own allocator, or a
+ * latency-critical path that must not call cudaMalloc because it can
+ * synchronise the device. The block_floating_point pages have no counterpart;
+ * this is a convenience of this library.
+ *   - Computes exactly what moe_decode_layer computes; x, y, topk_idx, topk_w
+ *     as there (caller-owned device memory).
+ *   - Scratch: one built-in device array of 2 MiB (2,097,152 bytes), allocated
+ *     when the library is loaded and held by every GPU that loads it until the
+ *     process exits. A layer needing more (moe_workspace_size > 2 MiB) is
+ *     rejected with BFP_EWORKSPACE; the full-size layer (hidden 2048, 256
+ *     experts, ffn 512, top-8) at 16 rows needs about 1.5 MiB.
+ *   - The first call on a device looks up the array's device address and
+ *     zeroes it, synchronously: make that first call before any stream
+ *     capture. Each call then clears the array's counters on its stream.
+ *   - Each device has its own copy of the array, and every call on that
+ *     device shares it; it keeps the last call's contents. Calls on one
+ *     device that can overlap on the GPU (on streams with no ordering
+ *     between them) race on it and give wrong results: keep them in one
+ *     stream order.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *   - A device-side wait that times out cannot be reported (there is no
+ *     caller-visible workspace status word); use moe_decode_layer when the
+ *     status matters.
+ */
+int moe_decode_layer_static(const bfp_moe_layer *layer, const uint16_t *x, int m, float *y, int32_t *topk_idx,
+                            float *topk_w, bfp_stream_t stream);
 
 /*
  * Decode stack: for each of n_layers layers,
