@@ -331,7 +331,7 @@ def moe_decode_layer(layer: MoELayer, x, ws, y=None, topk_idx=None, topk_w=None,
 def moe_decode_layer_static(layer: MoELayer, x, y=None, topk_idx=None, topk_w=None, stream=None):
     """moe_decode_layer without a workspace, for callers that cannot allocate device memory.
 
-    Uses the library's built-in 2 MiB device scratch array (shared by every
+    Uses the library's built-in 1.5 MiB device scratch array (shared by every
     call on a device; overlapping calls race). The first call on a device
     sets the array up synchronously, so make it before any stream capture.
     """

@@ -82,6 +82,10 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// Orders this thread's view of global memory (generic proxy) before its later bulk copies
+// (async proxy) read it: data other blocks wrote and this thread acquired.
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
 // ------------------------------------------------------ cross-block counters
 __device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p) {
     uint32_t v;
@@ -169,10 +173,20 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
-// Power-of-two exponent that brings max|v| into [2^14, 2^15) (0 for an all-zero row).
+// Power-of-two exponent that brings max|v| into [2^14, 2^15) (0 for an all-zero row),
+// clamped to 126 so that 2^shift is an fp32 normal (rows below 2^-112 stay tiny, still exact).
 __device__ __forceinline__ int frag_shift(float maxabs) {
     uint32_t e = (__float_as_uint(maxabs) >> 23) & 0xFFu;
-    return maxabs > 0.f ? 141 - (int)e : 0;
+    const int s = maxabs > 0.f ? 141 - (int)e : 0;
+    return s > 126 ? 126 : s;
+}
+
+// 2^e as fp32 for e in [-126, 127].
+__device__ __forceinline__ float pow2f(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
+// x * 2^e for |e| <= 252 in two exact power-of-two steps (exact unless the result leaves the normal range).
+__device__ __forceinline__ float mul_pow2(float x, int e) {
+    const int e1 = e / 2;
+    return (x * pow2f(e1)) * pow2f(e - e1);
 }
 
 // Pack two fp32 values already scaled into fp16 range as an fp16x2 word (low = first).
@@ -181,10 +195,19 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// Fragment-layout address (in 32-bit words) of pair j (cols 2j, 2j+1) of block b of row r:
-//   frag[grp = r>>3][b][lane = 4*(r&7) + (j&3)][reg = j>>2], with kbp blocks per row group.
+// Activation-fragment layout: for activation group grp (8 rows) and block b, 64 words (256 B)
+// holding the mma.sync B fragment of every lane: lane 4g + t owns words {2s, 2s+1} with
+// s = (4g + t) ^ frag_swz(b), i.e. row 8*grp + g, cols (2t, 2t+1) and (2t+8, 2t+9) of the block.
+// The XOR swizzle permutes lanes within a block (so a warp's fragment read stays one
+// conflict-free 256-byte access) and spreads a warp's writes of one row across banks.
+__device__ __forceinline__ int frag_swz(int b) { return (b & 7) << 2; }
+// Index (in uint2 units) of lane `lane`'s fragment of block b in group grp.
+__device__ __forceinline__ int frag_idx(int grp, int b, int lane, int kbp) {
+    return (grp * kbp + b) * kWarp + (lane ^ frag_swz(b));
+}
+// Word address of pair j (cols 2j, 2j+1) of block b of row r.
 __device__ __forceinline__ int frag_word(int r, int b, int j, int kbp) {
-    return ((((r >> 3) * kbp + b) * kWarp + 4 * (r & 7) + (j & 3)) << 1) + (j >> 2);
+    return (frag_idx(r >> 3, b, 4 * (r & 7) + (j & 3), kbp) << 1) + (j >> 2);
 }
 
 // Deterministic warp sum / max (butterfly; every lane gets the same value).

@@ -118,6 +118,16 @@ __global__ void __launch_bounds__(kThreads, 1) bfp_linear_kernel(const LinearArg
         if (lane == 0) {
             int64_t u = 0;
             bool bad = false;
+            // the activation rows first, 8 rows per slot (the fragments are built from them)
+            for (int r0 = 0; r0 < a.m; r0 += 8) {
+                const int slot = (int)(u % a.nslot);
+                const int nr = min(8, a.m - r0);
+                mbar_arrive_expect_tx(&full[slot], (uint32_t)nr * a.k * 2);
+                for (int r = 0; r < nr; ++r)  // one copy per row: rows are ldx apart in global memory
+                    bulk_g2s(ring + (size_t)slot * a.slot_bytes + (size_t)r * a.k * 2, a.x + (int64_t)(r0 + r) * a.ldx,
+                             (uint32_t)a.k * 2, &full[slot]);
+                ++u;
+            }
             for (int64_t pos = s; pos < e;) {
                 const int64_t rg = pos / a.kc;
                 const int c0 = (int)(pos - rg * a.kc);
@@ -149,7 +159,20 @@ __global__ void __launch_bounds__(kThreads, 1) bfp_linear_kernel(const LinearArg
         __syncwarp();
     } else {
         // ----------------------------------------------------------- consumers
-        build_act_frags<NW * kWarp>(a.x, a.ldx, a.m, a.k, a.kbp, NGRP, a.norm != 0, a.eps, frag, shift, inv, tid, warp, lane);
+        bool bad = false;
+        int64_t u = 0;
+        {
+            // activation rows staged by the producer in slots 0 .. nx-1
+            const int nx = (a.m + 7) / 8;
+            for (int i = 0; i < nx; ++i)
+                if (!bad) bad = !__all_sync(0xffffffffu, mbar_wait(&full[i], 0u, a.wait, nullptr));
+            build_act_frags<NW * kWarp>(reinterpret_cast<const uint16_t *>(ring), a.k, 8, a.slot_bytes / 2, a.m, a.k,
+                                        a.kbp, NGRP, a.norm != 0, a.eps, frag, shift, inv, tid, warp, lane);
+            __syncwarp();
+            for (int i = 0; i < nx; ++i)
+                if (lane == 0 && !bad) mbar_arrive(&empty[i]);
+            u = nx;
+        }
         const uint2 *frag2 = reinterpret_cast<const uint2 *>(frag);
         const uint32_t gmask = a.m > 8 ? 3u : 1u;
         float acc[1][NGRP][4];
@@ -157,8 +180,6 @@ __global__ void __launch_bounds__(kThreads, 1) bfp_linear_kernel(const LinearArg
         for (int g = 0; g < NGRP; ++g)
 #pragma unroll
             for (int i = 0; i < 4; ++i) acc[0][g][i] = 0.f;
-        bool bad = false;
-        int64_t u = 0;
         const int64_t rg_first = s / a.kc;
         for (int64_t pos = s; pos < e;) {
             const int64_t rg = pos / a.kc;
@@ -205,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1) bfp_linear_kernel(const LinearArg
                 const int grp = tid >> 7, i = (tid >> 5) & 3, ln = tid & 31;
                 nrow = rg * 16 + acc_wrow(ln, i);
                 r = acc_xrow(ln, grp, i);
-                if (r < a.m) v = scalbnf(v, 24 - (MB - 1) - shift[r]);
+                if (r < a.m) v = mul_pow2(v, 24 - (MB - 1) - shift[r]);
             }
             auto store = [&](float val) {
                 if (have && r < a.m && nrow < a.n) {
@@ -219,16 +240,15 @@ __global__ void __launch_bounds__(kThreads, 1) bfp_linear_kernel(const LinearArg
             } else {
                 const int slotp = 2 * c + (rg == rg_first ? 0 : 1);
                 if (have) a.part[(size_t)slotp * TILE + tid] = v;
-                __threadfence();
                 bar_sync(1, NW * kWarp);
                 const int cf = cta_of(rg * a.kc, R, a.ncta), cl = cta_of((rg + 1) * a.kc - 1, R, a.ncta);
                 if (tid == 0) {
+                    __threadfence();  // every thread's partial store, ordered by the barrier, before the count
                     const uint32_t old = atom_add_acq_rel(&a.cnt[rg], 1u);
                     flags[1] = (old == (uint32_t)(cl - cf)) ? 1 : 0;
                 }
                 bar_sync(1, NW * kWarp);
                 if (flags[1]) {
-                    __threadfence();
                     float sum = 0.f;
                     if (have) {
                         for (int cc = cf; cc <= cl; ++cc) {
@@ -331,8 +351,9 @@ static int plan_linear(const Geometry &g, int m, LinearPlan *p) {
     const int64_t per_cta = (R + p->ncta - 1) / p->ncta;
     int recs = (int)std::min<int64_t>(std::min<int64_t>(g.kc, std::max<int64_t>(1, 36864 / g.rec)), per_cta);
     if (recs < 1) recs = 1;
+    const size_t xrows = (size_t)std::min(m, 8) * g.k * 2;  // staged activation rows per slot
     for (;;) {
-        const size_t slot = (size_t)recs * g.rec;
+        const size_t slot = align_up(std::max((size_t)recs * g.rec, xrows), 16);
         const size_t avail = di.smem_optin > (int)fixed ? di.smem_optin - fixed : 0;
         int nslot = (int)std::min<size_t>(8, avail / slot);
         if (nslot >= 2) {

@@ -12,6 +12,7 @@
 #pragma once
 
 #include "bfp_device.cuh"
+#include "bfp_trace.h"
 
 namespace bfp {
 namespace dev {
@@ -48,8 +49,8 @@ __device__ __forceinline__ void mma_records(const uint8_t *const recs[NREC], con
 #pragma unroll
         for (int grp = 0; grp < NGRP; ++grp) {
             if (grp_mask & (1u << grp)) {
-                bx[grp] = frag[(grp * kbp + kb0 + b) * kWarp + lane];
-                if constexpr (HILO) bl[grp] = frag_lo[(grp * kbp + kb0 + b) * kWarp + lane];
+                bx[grp] = frag[frag_idx(grp, kb0 + b, lane, kbp)];
+                if constexpr (HILO) bl[grp] = frag_lo[frag_idx(grp, kb0 + b, lane, kbp)];
             }
         }
 #pragma unroll
@@ -96,56 +97,72 @@ __device__ __forceinline__ int acc_xrow(int lane, int grp, int i) { return 8 * g
 // each row scaled by the power of two shift[r] that puts its max |value| in
 // [2^14, 2^15) and rounded to fp16 (exact for every bf16 value above
 // 2^-14 of the row maximum). Rows >= m and blocks >= k/16 are zero.
+// Row r of x is at x + (r / rpp) * part + (r % rpp) * ldx (elements): x may be one strided array
+// (rpp >= m) or, when staged in shared memory, several slots of rpp rows each.
+// One warp per row: the row is read once (16-byte vectors, k % 8 == 0, 16-byte aligned rows),
+// its max (and sum of squares) reduced, then the lane's own values written as fragment words.
 // Called by the NC consumer threads only (named barrier 1).
 template <int NC>
-__device__ __noinline__ void build_act_frags(const uint16_t *x, int64_t ldx, int m, int k, int kbp, int ngrp, bool norm, float eps,
-                                uint32_t *frag, int *shift, float *inv_out, int tid, int warp, int lane) {
+__device__ __noinline__ void build_act_frags(const uint16_t *x, int64_t ldx, int rpp, int64_t part, int m, int k,
+                                             int kbp, int ngrp, bool norm, float eps, uint32_t *frag, int *shift,
+                                             float *inv_out, int tid, int warp, int lane) {
+    constexpr int B = 8;  // 16-byte vectors per lane held at once (k <= 8 * 8 * 32 = 2048 in one pass)
     const int nvec = ngrp * kbp * kWarp * 2 / 4;
     for (int i = tid; i < nvec; i += NC) reinterpret_cast<uint4 *>(frag)[i] = make_uint4(0, 0, 0, 0);
+    bar_sync(1, NC);
+    const int nv = k / 8;  // uint4 per row
     for (int r = warp; r < m; r += NC / kWarp) {
-        const uint16_t *xr = x + (int64_t)r * ldx;
+        const uint4 *xr = reinterpret_cast<const uint4 *>(x + (r / rpp) * part + (int64_t)(r % rpp) * ldx);
+        // statistics over the whole row
+        float ss = 0.f, mx = 0.f;
+        for (int base = 0; base < nv; base += B * kWarp) {
+#pragma unroll
+            for (int q = 0; q < B; ++q) {
+                const int i = base + q * kWarp + lane;
+                if (i < nv) {
+                    const uint4 v = xr[i];
+                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const float lo = bf16_bits_to_f32(w[h] & 0xFFFFu), hi = bf16_bits_to_f32(w[h] >> 16);
+                        ss = fmaf(lo, lo, ss);
+                        ss = fmaf(hi, hi, ss);
+                        mx = fmaxf(mx, fmaxf(fabsf(lo), fabsf(hi)));
+                    }
+                }
+            }
+        }
+        ss = warp_sum(ss);
+        mx = warp_max(mx);
         float inv = 1.f;
         if (norm) {
-            float ss = 0.f;
-            for (int j = lane; j < k; j += kWarp) {
-                float v = bf16_bits_to_f32(xr[j]);
-                ss = fmaf(v, v, ss);
-            }
-            ss = warp_sum(ss);
             inv = 1.0f / sqrtf(ss / (float)k + eps);
+            mx = __bfloat162float(__float2bfloat16_rn(mx * inv));  // rounding is monotonic
         }
-        float mx = 0.f;
-        for (int j = lane; j < k; j += kWarp) {
-            float v = bf16_bits_to_f32(xr[j]);
-            if (norm) v = __bfloat162float(__float2bfloat16_rn(v * inv));
-            mx = fmaxf(mx, fabsf(v));
-        }
-        mx = warp_max(mx);
+        const int sh = frag_shift(mx);
         if (lane == 0) {
-            shift[r] = frag_shift(mx);
+            shift[r] = sh;
             if (inv_out) inv_out[r] = inv;
         }
-    }
-    bar_sync(1, NC);
-    const int kb = k / 16;
-    const int total = m * kb * 8;
-    for (int idx = tid; idx < total; idx += NC) {
-        const int r = idx / (kb * 8);
-        const int rem = idx - r * kb * 8;
-        const int b = rem >> 3, j = rem & 7;
-        const uint32_t two = *reinterpret_cast<const uint32_t *>(x + (int64_t)r * ldx + 16 * b + 2 * j);
-        float v0 = bf16_bits_to_f32(two & 0xFFFFu), v1 = bf16_bits_to_f32(two >> 16);
-        if (norm) {
-            const float inv = inv_out[r];
-            v0 = __bfloat162float(__float2bfloat16_rn(v0 * inv));
-            v1 = __bfloat162float(__float2bfloat16_rn(v1 * inv));
+        const float sc = pow2f(sh);
+        // fragment words: vector i holds cols 8i..8i+7 = block i/2, half i&1 (pairs 4(i&1) + t)
+        for (int i = lane; i < nv; i += kWarp) {
+            const uint4 v = xr[i];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            const int b = i >> 1, hh = i & 1;
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                float lo = bf16_bits_to_f32(w[t] & 0xFFFFu), hi = bf16_bits_to_f32(w[t] >> 16);
+                if (norm) {
+                    lo = __bfloat162float(__float2bfloat16_rn(lo * inv));
+                    hi = __bfloat162float(__float2bfloat16_rn(hi * inv));
+                }
+                frag[frag_word(r, b, 4 * hh + t, kbp)] = pack_half2(lo * sc, hi * sc);
+            }
         }
-        const int sh = shift[r];
-        frag[frag_word(r, b, j, kbp)] = pack_half2(scalbnf(v0, sh), scalbnf(v1, sh));
     }
     bar_sync(1, NC);
 }
-
 
 }  // namespace dev
 }  // namespace bfp

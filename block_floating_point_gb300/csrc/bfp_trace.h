@@ -1,0 +1,21 @@
+// Optional per-CTA timestamps (%globaltimer, ns) for studying where a kernel's
+// time goes. Compiled in only with -DBFP_TRACE; the library as built by
+// build.py has none of it, and BFP_TRACE_AT expands to nothing.
+#pragma once
+
+#ifdef BFP_TRACE
+#define BFP_TRACE_SLOTS 64
+// One copy per translation unit, set through that unit's bfp_debug_set_trace
+// (trace builds only); one row of slots per CTA.
+static __device__ unsigned long long *g_bfp_trace = nullptr;
+#define BFP_TRACE_AT(slot)                                                                                  \
+    do {                                                                                                    \
+        if (g_bfp_trace != nullptr && (threadIdx.x == 0 || threadIdx.x == 256))                             \
+            g_bfp_trace[(size_t)blockIdx.x * BFP_TRACE_SLOTS + (slot) + (threadIdx.x == 256 ? 32 : 0)] =    \
+                bfp::dev::global_ns();                                                                      \
+    } while (0)
+#else
+#define BFP_TRACE_AT(slot) \
+    do {                   \
+    } while (0)
+#endif

@@ -37,6 +37,7 @@
 
 #include "bfp_launch.h"
 #include "bfp_tiles.cuh"
+#include "bfp_trace.h"
 
 namespace bfp {
 
@@ -65,7 +66,8 @@ struct MoeArgs {
     uint16_t *h_out;
     int32_t *topk_idx;
     float *topk_w;
-    uint32_t *status, *ctrl, *done1, *rgcnt;
+    uint32_t *status, *ctrl;  // ctrl: [0] router, [1] exit, [2] phase-1, [3] phase-2 barrier counters
+    uint32_t *hmax;  // [M][K+1] max |h| bits per (row, slot), raised in phase 1
     float *logits, *hbuf, *part;
     int rec, kc_h, kbp_h, kc_f, kbp_f, kc_fs, kbp_fs;
     int nft, nft_s, ng_d, r2, noct, Fmax;
@@ -76,6 +78,7 @@ struct MoeArgs {
 
 // Shared-memory bookkeeping of one CTA.
 struct MoeMisc {
+    uint64_t cbar;  // consumers' own bulk copies (logits, h rows)
     int shift_x[kMaxRows];
     float inv[kMaxRows];
     int shift_h[kMaxRows];
@@ -88,12 +91,43 @@ struct MoeMisc {
     int16_t pos[kMaxExperts];
     int16_t ulist[kMaxExperts + 1];
     int8_t uslot[kMaxExperts + 1][kMaxRows];
-    uint32_t maxbits[kMaxRows];
+    uint32_t maxbits[2][kMaxRows];  // per-unit max |h| per row (double-buffered like the scratch)
+    int8_t colrow[kMaxRows];        // phase 2: fragment column -> row of the current expert
     int nU;
     int flags[4];  // [0] abort
 };
 
 __host__ __device__ inline int router_row_start(int c, int rows, int ncta) { return (int)((int64_t)c * rows / ncta); }
+
+// Phase-2 unit cost in MMAs per block: an expert used by <= 4 rows carries the hi and lo halves of
+// its rows' h in one 8-column MMA; <= 8 rows need two MMAs (hi, lo); more rows two groups of two.
+__device__ __forceinline__ int p2_cost(uint32_t rowmask) {
+    const int n = __popc(rowmask);
+    return n <= 4 ? 1 : (n <= 8 ? 2 : 4);
+}
+// First phase-2 unit (q = j * noct + oct, j = 0..nU) whose cumulative-cost start is >= X.
+__device__ int p2_first_unit(const uint32_t *umask, int nU, int noct, int64_t X) {
+    int64_t base = 0;
+    for (int j = 0; j <= nU; ++j) {
+        const int cj = p2_cost(umask[j]);
+        const int64_t span = (int64_t)noct * cj;
+        if (X <= base) return j * noct;
+        if (X < base + span) {
+            const int o = (int)((X - base + cj - 1) / cj);
+            if (o < noct) return j * noct + o;
+        }
+        base += span;
+    }
+    return (nU + 1) * noct;
+}
+// CTA c's phase-2 units [q0, q1): an equal share of the total cost.
+__device__ __forceinline__ void p2_range(const uint32_t *umask, int nU, int noct, int c, int ncta, int64_t *q0,
+                                         int64_t *q1) {
+    int64_t total = 0;
+    for (int j = 0; j <= nU; ++j) total += (int64_t)noct * p2_cost(umask[j]);
+    *q0 = p2_first_unit(umask, nU, noct, total * c / ncta);
+    *q1 = p2_first_unit(umask, nU, noct, total * (c + 1) / ncta);
+}
 
 // Ordered 32-bit key of a float: larger float <=> larger unsigned key.
 __device__ __forceinline__ uint32_t order_key(float v) {
@@ -119,7 +153,9 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x;
-    const int E1 = a.E + 1;  // router rows + the shared-gate row
+    const int E1 = a.E + 1;
+#define STAMP(i) BFP_TRACE_AT(i)
+    STAMP(0);  // router rows + the shared-gate row
     const int rr0 = router_row_start(c, E1, a.ncta), rr1 = router_row_start(c + 1, E1, a.ncta);
     const int64_t gb_h = (int64_t)a.kc_h * a.rec;  // bytes of one gate/up row group
     const int nft_total_pre = a.nft_s;              // phase-1 units known before routing
@@ -130,9 +166,12 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
             mbar_init(&empty[i], NW);
         }
         for (int i = 0; i < 4; ++i) ms->flags[i] = 0;
+        ms->nU = 0;  // read by the producer even when the consumers abort before routing
+        mbar_init(&ms->cbar, 1);
         mbar_fence_init();
     }
     __syncthreads();
+    STAMP(13);
 
     if (warp == NW) {
         // ==================================================================== producer
@@ -157,6 +196,12 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
             return true;
         };
         if (lane == 0) {
+            // 0. the activation rows, 8 rows per slot (bulk copies: the fragments are built from them)
+            for (int r0 = 0; !bad && r0 < a.M; r0 += 8) {
+                const uint8_t *src[1] = {reinterpret_cast<const uint8_t *>(a.x + (int64_t)r0 * a.H)};
+                const uint32_t bytes[1] = {(uint32_t)min(8, a.M - r0) * a.H * 2};
+                bad = !issue(1, src, bytes);
+            }
             // 1. router rows
             if (rr1 > rr0) {
                 const uint8_t *src[2];
@@ -180,12 +225,13 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
                 bad = !issue(1, src, bytes);
             }
         }
+        STAMP(1);  // producer: pre-routing copies issued
         // 3. wait for the consumers' routing decision
         __syncwarp();
         bar_sync(2, kThreads);
-        if (lane == 0) {
-            const int nU = ms->nU;
-            if (vflags[0]) bad = true;
+        if (lane == 0 && !vflags[0] && !bad) {
+            // routing tables are valid only when the consumers finished the dispatch (no abort)
+            const int nU = min(max(ms->nU, 0), min(a.E, a.M * a.K));
             // 4. routed gate/up f-tiles
             const int p1 = a.nft_s + nU * a.nft;
             int g = c;
@@ -198,8 +244,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
                 bad = !issue(1, src, bytes);
             }
             // 5. down-projection units
-            const int64_t p2 = (int64_t)(nU + 1) * a.noct;
-            const int64_t q0 = (int64_t)c * p2 / a.ncta, q1 = (int64_t)(c + 1) * p2 / a.ncta;
+            int64_t q0, q1;
+            p2_range(ms->umask, nU, a.noct, c, a.ncta, &q0, &q1);
             for (int64_t q = q0; !bad && q < q1; ++q) {
                 const int j = (int)(q / a.noct), oct = (int)(q % a.noct);
                 const bool sh = j == nU;
@@ -211,7 +257,10 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
                 const uint32_t bytes[1] = {(uint32_t)(nrg * gb_f)};
                 bad = !issue(1, src, bytes);
             }
-            // No copy may still be landing in shared memory when the CTA exits.
+            STAMP(3);  // producer: every copy issued
+        }
+        if (lane == 0) {
+            // No copy may still be landing in shared memory when the CTA exits (every path).
             WaitCfg drain{int64_t(1) << 40, 1000000000ull};
             for (int64_t sl = 0; sl < min64(u, a.nslot); ++sl) {
                 const int64_t last_use = (u - 1 - sl) / a.nslot;
@@ -250,14 +299,64 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
             if (lane == 0 && !bad) mbar_arrive(&empty[slot]);
         };
 
-        // ---- activation fragments (MoE input: x, or bf16(RMSNorm(h)) in stack mode)
-        build_act_frags<NC>(a.x, a.H, a.M, a.H, a.kbp_h, NGRP, a.norm != 0, a.eps, frag, ms->shift_x, ms->inv, tid, warp,
-                        lane);
+        // Bulk copies issued by the consumers themselves (data other CTAs wrote, already acquired):
+        // thread 0 issues, every consumer thread waits; one phase of ms->cbar per call.
+        uint32_t cphase = 0;
+        auto stage_wait = [&]() {
+            if (!bad)
+                bad = !__all_sync(0xffffffffu, mbar_wait(&ms->cbar, cphase & 1u, a.wait_data, nullptr));
+            ++cphase;
+        };
+
+        // ---- activation fragments (MoE input: x, or bf16(RMSNorm(h)) in stack mode), from the rows
+        //      the producer staged in the first slots (units 0 .. nx-1 are slots 0 .. nx-1)
+        {
+            const int nx = (a.M + 7) / 8;
+            for (int i = 0; i < nx; ++i) wait_slot(u + i);
+            const uint16_t *xs = reinterpret_cast<const uint16_t *>(ring);
+            build_act_frags<NC>(xs, a.H, 8, a.slot_bytes / 2, a.M, a.H, a.kbp_h, NGRP, a.norm != 0, a.eps, frag,
+                                ms->shift_x, ms->inv, tid, warp, lane);
+            for (int i = 0; i < nx; ++i) release_slot((int)((u + i) % a.nslot));
+            u += nx;
+        }
+        STAMP(1);  // activation fragments built
 
         // ---- phase-1 unit: one f-tile (16 ffn rows) of gate and up; h = silu(gate) * up for the
         //      rows in rowmask, slot table row jrow. Returns false on abort (same answer in all warps).
+        // One CTA barrier per unit: the reduction scratch and the per-row max |h| are double-
+        // buffered; a unit's row maxima go to the workspace at the next unit's barrier (or at
+        // flush_pending). Cross-CTA ordering of h comes from the grid barrier after phase 1.
+        int p1n = 0;  // phase-1 units done by this CTA (selects the buffers)
+        int pending_jrow = -1, pending_buf = 0;
+        uint32_t pending_mask = 0;
+        if (tid < 2 * kMaxRows) (&ms->maxbits[0][0])[tid] = 0u;
+        auto signal_pending = [&]() {
+            if (pending_jrow >= 0 && tid < a.M && ((pending_mask >> tid) & 1u)) {
+                atomicMax(&a.hmax[tid * (a.K + 1) + ms->uslot[pending_jrow][tid]], ms->maxbits[pending_buf][tid]);
+                ms->maxbits[pending_buf][tid] = 0u;
+            }
+            pending_jrow = -1;
+        };
+        auto flush_pending = [&]() {
+            bar_sync(1, NC);
+            signal_pending();
+        };
+        // Grid barrier over the consumer threads of every CTA, on a workspace counter.
+        // Returns false on abort (same answer in every consumer thread of the CTA).
+        auto grid_barrier = [&](uint32_t *counter) -> bool {
+            bar_sync(1, NC);
+            bool ok = true;
+            if (tid == 0) {
+                __threadfence();
+                red_release_add(counter, 1u);
+                ok = wait_counter(counter, (uint32_t)a.ncta, a.wait);
+            }
+            return !bar_or(1, NC, !ok || bad);
+        };
         auto run_phase1 = [&](int eid, int ft, uint32_t rowmask, int jrow) -> bool {
+            if (p1n == 2) STAMP(21);  // third phase-1 unit: start
             const int slot = wait_slot(u);
+            if (p1n == 2) STAMP(22);  // ... its data landed
             const uint8_t *slotp = ring + (size_t)slot * a.slot_bytes;
             const uint32_t gm = (((rowmask & 0xFFu) ? 1u : 0u) | ((rowmask & 0xFF00u) ? 2u : 0u)) & ngrp_rows;
             float acc[2][NGRP][4];
@@ -275,8 +374,11 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
             }
             release_slot(slot);
             ++u;
+            if (p1n == 2) STAMP(23);  // ... MMAs done (warp 0)
             constexpr int TILE = NGRP * 128;
-            float *mine = scr + warp * 2 * TILE;
+            float *buf = scr + (p1n & 1) * (NW * 2 * TILE);
+            ++p1n;
+            float *mine = buf + warp * 2 * TILE;
 #pragma unroll
             for (int r = 0; r < 2; ++r)
 #pragma unroll
@@ -284,73 +386,91 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
 #pragma unroll
                     for (int i = 0; i < 4; ++i) mine[r * TILE + (g * 4 + i) * kWarp + lane] = acc[r][g][i];
             if (bar_or(1, NC, bad)) return false;
+            if (p1n == 3) STAMP(24);  // ... every warp's MMAs done
+            signal_pending();
             if (tid < TILE) {
                 float va = 0.f, vb = 0.f;
                 for (int w = 0; w < NW; ++w) {
-                    va += scr[w * 2 * TILE + tid];
-                    vb += scr[w * 2 * TILE + TILE + tid];
+                    va += buf[w * 2 * TILE + tid];
+                    vb += buf[w * 2 * TILE + TILE + tid];
                 }
                 const int grp = tid >> 7, i = (tid >> 5) & 3, ln = tid & 31;
                 const int r = acc_xrow(ln, grp, i);
                 const int f = ft * 16 + acc_wrow(ln, i);
                 if (r < a.M && ((rowmask >> r) & 1u)) {
                     const int sh = 24 - (MB - 1) - ms->shift_x[r];
-                    const float ga = scalbnf(va, sh), ub = scalbnf(vb, sh);
+                    const float ga = mul_pow2(va, sh), ub = mul_pow2(vb, sh);
                     const float hv = ga / (1.0f + expf(-ga)) * ub;  // silu(gate) * up
                     const int s = ms->uslot[jrow][r];
                     a.hbuf[((int64_t)r * (a.K + 1) + s) * a.Fmax + f] = hv;
+                    atomicMax(&ms->maxbits[(p1n - 1) & 1][r], __float_as_uint(fabsf(hv)));
                 }
             }
-            __threadfence();
-            bar_sync(1, NC);
-            if (tid == 0) red_release_add(&a.done1[eid], 1u);
+            if (p1n == 3) STAMP(25);  // ... reduction + h stores issued
+            pending_jrow = jrow;
+            pending_mask = rowmask;
+            pending_buf = (p1n - 1) & 1;
             return true;
         };
 
-        // ---- 1. router rows
+        // ---- 1. router rows: logits from the bf16 router rows (shared memory) and the activation
+        //      fragments (shared memory); x' = x * 2^shift exactly, so l = 2^-shift * sum w * x'.
+        //      Work item = (router row i, activation group grp, block segment seg); lane 4g+t reads its
+        //      own fragment words (rows 8grp+g, cols 2t|2t+1 and 2t+8|2t+9 of each block): no bank
+        //      conflicts; the four lanes of a row add up with two shuffles; segments are summed in order.
         if (rr1 > rr0) {
             const int slot = wait_slot(u);
+            STAMP(2);  // router rows landed
             const uint16_t *wr = reinterpret_cast<const uint16_t *>(ring + (size_t)slot * a.slot_bytes);
             const int nrows = rr1 - rr0;
+            const int kb = a.H / 16;
+            const int ngrp = (a.M + 7) / 8;
+            const int nseg = max(1, NW / (nrows * ngrp));
+            float *rpart = scr;  // [nrows][ngrp][nseg][8]
             if (!bad) {
-                for (int p = warp; p < nrows * a.M; p += NW) {
-                    const int i = p / a.M, r = p % a.M;
-                    const uint16_t *xr = a.x + (int64_t)r * a.H;
+                const int g = lane >> 2, t = lane & 3;
+                for (int it = warp; it < nrows * ngrp * nseg; it += NW) {
+                    const int i = it / (ngrp * nseg), grp = (it / nseg) % ngrp, seg = it % nseg;
                     const uint16_t *w = wr + (int64_t)i * a.H;
-                    const float inv = ms->inv[r];
+                    const int b0 = seg * kb / nseg, b1 = (seg + 1) * kb / nseg;
                     float acc = 0.f;
-                    for (int j = lane * 8; j < a.H; j += 8 * kWarp) {
-                        const uint4 wv = *reinterpret_cast<const uint4 *>(w + j);
-                        const uint4 xv = *reinterpret_cast<const uint4 *>(xr + j);
-                        const uint32_t wa[4] = {wv.x, wv.y, wv.z, wv.w}, xa[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            float x0 = bf16_bits_to_f32(xa[q] & 0xFFFFu), x1 = bf16_bits_to_f32(xa[q] >> 16);
-                            if (a.norm) {
-                                x0 = __bfloat162float(__float2bfloat16_rn(x0 * inv));
-                                x1 = __bfloat162float(__float2bfloat16_rn(x1 * inv));
-                            }
-                            acc = fmaf(bf16_bits_to_f32(wa[q] & 0xFFFFu), x0, acc);
-                            acc = fmaf(bf16_bits_to_f32(wa[q] >> 16), x1, acc);
-                        }
+                    for (int b = b0; b < b1; ++b) {
+                        const uint2 xf = frag2[frag_idx(grp, b, lane, a.kbp_h)];
+                        const uint32_t w0 = *reinterpret_cast<const uint32_t *>(w + 16 * b + 2 * t);
+                        const uint32_t w1 = *reinterpret_cast<const uint32_t *>(w + 16 * b + 2 * t + 8);
+                        const float2 x0 = __half22float2(*reinterpret_cast<const __half2 *>(&xf.x));
+                        const float2 x1 = __half22float2(*reinterpret_cast<const __half2 *>(&xf.y));
+                        acc = fmaf(bf16_bits_to_f32(w0 & 0xFFFFu), x0.x, acc);
+                        acc = fmaf(bf16_bits_to_f32(w0 >> 16), x0.y, acc);
+                        acc = fmaf(bf16_bits_to_f32(w1 & 0xFFFFu), x1.x, acc);
+                        acc = fmaf(bf16_bits_to_f32(w1 >> 16), x1.y, acc);
                     }
-                    acc = warp_sum(acc);
-                    if (lane == 0) {
-                        const int row = rr0 + i;
-                        if (row < a.E && a.rbias) acc += a.rbias[row];
-                        a.logits[(int64_t)r * E1 + row] = acc;
-                    }
+                    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+                    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+                    if (t == 0) rpart[((i * ngrp + grp) * nseg + seg) * 8 + g] = acc;
                 }
+            }
+            bar_sync(1, NC);
+            for (int idx = tid; !bad && idx < nrows * a.M; idx += NC) {
+                const int i = idx / a.M, r = idx % a.M;
+                float acc = 0.f;
+                for (int seg = 0; seg < nseg; ++seg) acc += rpart[((i * ngrp + (r >> 3)) * nseg + seg) * 8 + (r & 7)];
+                const int row = rr0 + i;
+                float l = acc * pow2f(-ms->shift_x[r]);
+                if (row < a.E && a.rbias) l += a.rbias[row];
+                a.logits[(int64_t)r * E1 + row] = l;
             }
             release_slot(slot);
             ++u;
         }
-        __threadfence();
         if (bar_or(1, NC, bad)) {
             abort_all();
             goto done;
         }
-        if (tid == 0) red_release_add(&a.ctrl[0], 1u);
+        if (tid == 0) {
+            __threadfence();
+            red_release_add(&a.ctrl[0], 1u);
+        }
 
         // ---- 2. shared-expert gate/up f-tiles (all rows use the shared expert)
         for (int g = c; g < a.nft_s; g += a.ncta) {
@@ -365,6 +485,10 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
             }
         }
 
+        STAMP(3);  // router logits published
+        flush_pending();
+        STAMP(4);  // shared-expert f-tiles done
+
         // ---- 3. routing: wait for every CTA's router rows, then top-k and the expert union
         {
             bool ok = true;
@@ -373,9 +497,16 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
                 abort_all();
                 goto done;
             }
-            float *lg = scr;  // M x E1 logits (the phase-1 scratch is free here)
-            for (int i = tid; i < a.M * E1; i += NC) lg[i] = __ldcg(&a.logits[i]);
-            bar_sync(1, NC);
+            STAMP(5);  // every CTA's router rows published
+            float *lg = scr;  // M x E1 logits (the phase-1 scratch is free here), one bulk copy
+            if (tid == 0) {
+                const uint32_t bytes = (uint32_t)align_up((size_t)a.M * E1 * 4, 16);  // stays inside the workspace
+                fence_proxy_async_global();
+                mbar_arrive_expect_tx(&ms->cbar, bytes);
+                bulk_g2s(lg, a.logits, bytes, &ms->cbar);
+            }
+            stage_wait();
+            STAMP(26);  // logits in shared memory
             for (int r = warp; r < a.M; r += NW) {
                 float v[8];
                 float p[8];
@@ -427,6 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
                     ms->gate_w[r] = 1.0f / (1.0f + expf(-lg[r * E1 + a.E]));
                 }
             }
+            STAMP(27);  // top-k of warp 0's rows done
             if (tid < kMaxExperts / 32) ms->bitmap[tid] = 0u;
             for (int i = tid; i <= kMaxExperts; i += NC) ms->umask[i] = 0u;
             bar_sync(1, NC);
@@ -471,6 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
             if (tid == 0) ms->umask[nU] = (1u << a.M) - 1u;
             bar_sync(1, NC);
         }
+        STAMP(6);  // top-k + union done
         bar_arrive(2, kThreads);
         dispatched = true;
 
@@ -488,71 +621,100 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
                     goto done;
                 }
             }
+            flush_pending();
+            STAMP(8);  // routed f-tiles done
+            if (!grid_barrier(&a.ctrl[2])) {  // every CTA's h and row maxima written
+                abort_all();
+                goto done;
+            }
+            STAMP(9);  // phase-1 grid barrier passed
         }
 
-        // ---- 5. down projection + combine
+        // ---- 5. down projection + combine. Per expert, the rows that chose it become the
+        //      columns 0..n-1 of its h fragments (routing weight folded in, fp16 hi + lo parts):
+        //      n <= 4: hi in columns c, lo in columns c + 4 of one 8-column MMA (summed at the end);
+        //      n <= 8: hi and lo fragments, two MMAs; more rows: two column groups.
         {
             const int nU = ms->nU;
-            const int64_t p2 = (int64_t)(nU + 1) * a.noct;
-            const int64_t q0 = (int64_t)c * p2 / a.ncta, q1 = (int64_t)(c + 1) * p2 / a.ncta;
+            int64_t q0, q1;
+            p2_range(ms->umask, nU, a.noct, c, a.ncta, &q0, &q1);
             int cur = -1;
+            int nr = 0;
+            bool packed = false;
+            uint32_t gm2 = 1;
             uint32_t *hfrag = frag;  // x fragments are dead once phase 1 is done
             for (int64_t q = q0; q < q1; ++q) {
                 const int j = (int)(q / a.noct), oct = (int)(q % a.noct);
                 const bool sh = j == nU;
-                const int eid = sh ? a.E : ms->ulist[j];
                 const int Fe = sh ? a.Fs : a.F;
                 const int kc = sh ? a.kc_fs : a.kc_f, kbp = sh ? a.kbp_fs : a.kbp_f;
                 const uint32_t rowmask = ms->umask[j];
                 if (j != cur) {
-                    // h of this expert complete? (all its f-tiles, from whichever CTAs ran them)
-                    bool ok = true;
-                    if (tid == 0) ok = wait_counter(&a.done1[eid], (uint32_t)(sh ? a.nft_s : a.nft), a.wait);
-                    if (bar_or(1, NC, !ok)) {
+                    // every warp is done with the previous expert's fragments
+                    if (bar_or(1, NC, bad)) {
                         abort_all();
                         goto done;
                     }
+                    nr = __popc(rowmask);
+                    packed = nr <= 4;
+                    gm2 = nr > 8 ? 3u : 1u;
+                    // routing weight folded into h; per-row power-of-two scale into fp16 range from the
+                    // phase-1 maximum (weights are positive, so max |w h| = w max |h|, rounding included)
                     if (tid < a.M) {
-                        ms->maxbits[tid] = 0u;
-                        ms->hw[tid] = ((rowmask >> tid) & 1u) ? (sh ? ms->gate_w[tid] : ms->tk_w[tid][ms->uslot[j][tid]]) : 0.f;
+                        const bool use = (rowmask >> tid) & 1u;
+                        const float w = use ? (sh ? ms->gate_w[tid] : ms->tk_w[tid][ms->uslot[j][tid]]) : 0.f;
+                        ms->hw[tid] = w;
+                        const uint32_t hm = use ? __ldcg(&a.hmax[tid * (a.K + 1) + ms->uslot[j][tid]]) : 0u;
+                        ms->shift_h[tid] = frag_shift(w * __uint_as_float(hm));
+                        if (use) ms->colrow[__popc(rowmask & ((1u << tid) - 1u))] = (int8_t)tid;
                     }
                     const int words = 2 * NGRP * kbp * kWarp * 2;
                     for (int i = tid; i < words / 4; i += NC) reinterpret_cast<uint4 *>(hfrag)[i] = make_uint4(0, 0, 0, 0);
                     bar_sync(1, NC);
-                    // routing weight folded into h; per-row power-of-two scale into fp16 range
-                    for (int i = tid; i < a.M * Fe; i += NC) {
-                        const int r = i / Fe, f = i % Fe;
-                        if ((rowmask >> r) & 1u) {
-                            const float v = __ldcg(&a.hbuf[((int64_t)r * (a.K + 1) + ms->uslot[j][r]) * a.Fmax + f]) * ms->hw[r];
-                            atomicMax(&ms->maxbits[r], __float_as_uint(fabsf(v)));
+                    // h rows of this expert (one bulk copy per row) into the scratch: row at column c
+                    float *hs = scr;
+                    if (tid == 0) {
+                        fence_proxy_async_global();
+                        mbar_arrive_expect_tx(&ms->cbar, (uint32_t)nr * Fe * 4);
+                        for (int r = 0; r < a.M; ++r)
+                            if ((rowmask >> r) & 1u)
+                                bulk_g2s(hs + __popc(rowmask & ((1u << r) - 1u)) * Fe,
+                                         a.hbuf + ((int64_t)r * (a.K + 1) + ms->uslot[j][r]) * a.Fmax,
+                                         (uint32_t)Fe * 4, &ms->cbar);
+                    }
+                    stage_wait();
+                    // one item = 4 consecutive h values (cols 4qq..4qq+3 of block b) of a column
+                    {
+                        const int fb = Fe / 16;
+                        const int lo_off = NGRP * kbp * kWarp * 2;  // words
+                        for (int it = tid; it < nr * fb * 4; it += NC) {
+                            const int col = it / (fb * 4), rem = it - col * fb * 4, b = rem >> 2, qq = rem & 3;
+                            const int r = ms->colrow[col];
+                            const float4 v4 = *reinterpret_cast<const float4 *>(hs + col * Fe + 4 * rem);
+                            const float w = ms->hw[r];
+                            const float sc = pow2f(ms->shift_h[r]);
+                            const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+                            for (int pr = 0; pr < 2; ++pr) {
+                                const float v0 = vv[2 * pr] * w * sc, v1 = vv[2 * pr + 1] * w * sc;
+                                const __half h0 = __float2half_rn(v0), h1 = __float2half_rn(v1);
+                                const float r0 = v0 - __half2float(h0), r1 = v1 - __half2float(h1);
+                                __half2 hh = __halves2half2(h0, h1);
+                                hfrag[frag_word(col, b, 2 * qq + pr, kbp)] = *reinterpret_cast<uint32_t *>(&hh);
+                                if (packed)
+                                    hfrag[frag_word(col + 4, b, 2 * qq + pr, kbp)] = pack_half2(r0, r1);
+                                else
+                                    hfrag[lo_off + frag_word(col, b, 2 * qq + pr, kbp)] = pack_half2(r0, r1);
+                            }
                         }
                     }
                     bar_sync(1, NC);
-                    if (tid < a.M) ms->shift_h[tid] = frag_shift(__uint_as_float(ms->maxbits[tid]));
-                    bar_sync(1, NC);
-                    const int fb = Fe / 16;
-                    const int lo_off = NGRP * kbp * kWarp * 2;  // words
-                    for (int i = tid; i < a.M * fb * 8; i += NC) {
-                        const int r = i / (fb * 8), rem = i % (fb * 8), b = rem >> 3, jj = rem & 7;
-                        if (!((rowmask >> r) & 1u)) continue;
-                        const float *hp = a.hbuf + ((int64_t)r * (a.K + 1) + ms->uslot[j][r]) * a.Fmax + 16 * b + 2 * jj;
-                        const float w = ms->hw[r];
-                        const int shh = ms->shift_h[r];
-                        const float v0 = scalbnf(__ldcg(hp) * w, shh), v1 = scalbnf(__ldcg(hp + 1) * w, shh);
-                        const __half h0 = __float2half_rn(v0), h1 = __float2half_rn(v1);
-                        const float r0 = v0 - __half2float(h0), r1 = v1 - __half2float(h1);
-                        const int wi = frag_word(r, b, jj, kbp);
-                        __half2 hh = __halves2half2(h0, h1);
-                        hfrag[wi] = *reinterpret_cast<uint32_t *>(&hh);
-                        hfrag[lo_off + wi] = pack_half2(r0, r1);
-                    }
-                    bar_sync(1, NC);
+                    if (cur < 0) STAMP(10);  // first expert's h fragments ready
                     cur = j;
                 }
                 const int slot = wait_slot(u);
                 const uint8_t *slotp = ring + (size_t)slot * a.slot_bytes;
                 const int rg0 = oct * a.r2, nrg = min(a.r2, a.ng_d - rg0);
-                const uint32_t gm = (((rowmask & 0xFFu) ? 1u : 0u) | ((rowmask & 0xFF00u) ? 2u : 0u)) & ngrp_rows;
                 float acc[1][NGRP][4];
 #pragma unroll
                 for (int g = 0; g < NGRP; ++g)
@@ -563,65 +725,86 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
                     const uint8_t *rb = slotp + (size_t)warp * kc * a.rec;
                     const uint2 *hi2 = reinterpret_cast<const uint2 *>(hfrag);
                     const uint2 *lo2 = hi2 + NGRP * kbp * kWarp;
-                    for (int ch = 0; ch < kc; ++ch) {
-                        const uint8_t *recs[1] = {rb + (size_t)ch * a.rec};
-                        mma_records<FMT, NGRP, 1, true>(recs, hi2, lo2, kbp, ch * CB, lane, gm, acc);
+                    if (packed) {
+                        for (int ch = 0; ch < kc; ++ch) {
+                            const uint8_t *recs[1] = {rb + (size_t)ch * a.rec};
+                            mma_records<FMT, NGRP, 1, false>(recs, hi2, nullptr, kbp, ch * CB, lane, 1u, acc);
+                        }
+                    } else {
+                        for (int ch = 0; ch < kc; ++ch) {
+                            const uint8_t *recs[1] = {rb + (size_t)ch * a.rec};
+                            mma_records<FMT, NGRP, 1, true>(recs, hi2, lo2, kbp, ch * CB, lane, gm2, acc);
+                        }
                     }
                 }
                 release_slot(slot);
                 ++u;
                 if (!bad && mine) {
                     const int rg = rg0 + warp;
+                    if (packed) {  // column c + 4 holds the lo half of column c: lanes t and t ^ 2
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) acc[0][0][i] += __shfl_xor_sync(0xffffffffu, acc[0][0][i], 2);
+                    }
 #pragma unroll
                     for (int g = 0; g < NGRP; ++g)
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
-                            const int r = acc_xrow(lane, g, i);
-                            if (r < a.M && ((rowmask >> r) & 1u)) {
+                            const int col = acc_xrow(lane, g, i);
+                            if (col < nr && (!packed || col < 4)) {
+                                const int r = ms->colrow[col];
                                 const int s = ms->uslot[j][r];
                                 const int n = rg * 16 + acc_wrow(lane, i);
                                 a.part[((int64_t)r * (a.K + 1) + s) * a.H + n] =
-                                    scalbnf(acc[0][g][i], 24 - (MB - 1) - ms->shift_h[r]);
+                                    mul_pow2(acc[0][g][i], 24 - (MB - 1) - ms->shift_h[r]);
                             }
                         }
-                    __threadfence();
-                    __syncwarp();
-                    uint32_t old = 0;
-                    if (lane == 0) old = atom_add_acq_rel(&a.rgcnt[rg], 1u);
-                    old = __shfl_sync(0xffffffffu, old, 0);
-                    if (old == (uint32_t)nU) {  // last of the nU + 1 experts for this row group
-                        __threadfence();
-                        for (int i = lane; i < a.M * 16; i += kWarp) {
-                            const int r = i >> 4, n = rg * 16 + (i & 15);
-                            float sum = 0.f;
-                            for (int s = 0; s <= a.K; ++s) sum += __ldcg(&a.part[((int64_t)r * (a.K + 1) + s) * a.H + n]);
-                            if (a.y) a.y[(int64_t)r * a.H + n] = sum;
-                            if (a.h_out) {
-                                const float hin = bf16_bits_to_f32(a.x[(int64_t)r * a.H + n]);
-                                a.h_out[(int64_t)r * a.H + n] = f32_to_bf16_bits(hin + sum);
-                            }
-                        }
-                        if (lane == 0) atomicExch(&a.rgcnt[rg], 0u);
-                    }
                 }
-                if (bar_or(1, NC, bad)) {
-                    abort_all();
-                    goto done;
+            }
+            STAMP(11);  // down projections done
+            if (!grid_barrier(&a.ctrl[3])) {  // every (row, slot) partial written
+                abort_all();
+                goto done;
+            }
+            STAMP(12);
+            // ---- 6. combine: y_r = sum over slots (in slot order) + shared, for this CTA's row groups
+            const int g0 = (int)((int64_t)c * a.ng_d / a.ncta), g1 = (int)((int64_t)(c + 1) * a.ng_d / a.ncta);
+            for (int i = tid; i < (g1 - g0) * a.M * 16; i += NC) {
+                const int rgl = i / (a.M * 16), rem = i - rgl * a.M * 16;
+                const int r = rem >> 4, n = (g0 + rgl) * 16 + (rem & 15);
+                float pv[kMaxTopK + 1];
+#pragma unroll
+                for (int s2 = 0; s2 <= kMaxTopK; ++s2)
+                    pv[s2] = s2 <= a.K ? __ldcg(&a.part[((int64_t)r * (a.K + 1) + s2) * a.H + n]) : 0.f;
+                float sum = 0.f;
+#pragma unroll
+                for (int s2 = 0; s2 <= kMaxTopK; ++s2)
+                    if (s2 <= a.K) sum += pv[s2];
+                if (a.y) a.y[(int64_t)r * a.H + n] = sum;
+                if (a.h_out) {
+                    const float hin = bf16_bits_to_f32(a.x[(int64_t)r * a.H + n]);
+                    a.h_out[(int64_t)r * a.H + n] = f32_to_bf16_bits(hin + sum);
                 }
             }
         }
     done:
         if (!dispatched) bar_arrive(2, kThreads);
+        if (tid == 0 && cphase > 0) {  // no copy of ours may still be landing when the CTA exits
+            WaitCfg drain{int64_t(1) << 40, 1000000000ull};
+            mbar_wait(&ms->cbar, (cphase - 1) & 1u, drain, nullptr);
+        }
     }
     __syncthreads();
+    STAMP(30);
+#undef STAMP
     // ---- the last CTA out resets the cross-block counters for the next launch
     if (tid == 0) {
         __threadfence();
         const uint32_t old = atom_add_acq_rel(&a.ctrl[1], 1u);
         if (old == (uint32_t)(a.ncta - 1)) {
-            for (int i = 0; i <= a.E; ++i) a.done1[i] = 0u;
-            for (int i = 0; i < a.ng_d; ++i) a.rgcnt[i] = 0u;
+            for (int i = 0; i < a.M * (a.K + 1); ++i) a.hmax[i] = 0u;
             a.ctrl[0] = 0u;
+            a.ctrl[2] = 0u;
+            a.ctrl[3] = 0u;
             __threadfence();
             atomicExch(&a.ctrl[1], 0u);
         }
@@ -635,7 +818,7 @@ struct MoePlan {
     Geometry gu, dn, sgu, sdn;
     int ngrp, ncta, nslot, slot_bytes, frag_bytes, scr_bytes, r2, noct, Fmax;
     size_t smem;
-    size_t off_ctrl, off_done1, off_rgcnt, off_logits, off_hbuf, off_part, ws_bytes;
+    size_t off_ctrl, off_hmax, off_logits, off_hbuf, off_part, ws_bytes;
 };
 
 static int validate_layer(const bfp_moe_layer *L, int m) {
@@ -678,8 +861,9 @@ static int plan_moe(const bfp_moe_layer *L, int m, MoePlan *p) {
     p->Fmax = std::max(L->ffn, L->shared_ffn);
     p->frag_bytes = (int)std::max<int64_t>((int64_t)p->ngrp * kbp_h * 256,
                                            (int64_t)2 * p->ngrp * std::max(kbp_f, kbp_fs) * 256);
-    p->scr_bytes = (int)align_up(std::max<size_t>((size_t)kConsumerWarps * 2 * p->ngrp * 128 * 4,
-                                                  (size_t)m * (L->n_experts + 1) * 4),
+    p->scr_bytes = (int)align_up(std::max<size_t>(std::max<size_t>((size_t)2 * kConsumerWarps * 2 * p->ngrp * 128 * 4,
+                                                                    (size_t)m * (L->n_experts + 1) * 4 + 16),
+                                                  (size_t)m * p->Fmax * 4),
                                  128);
     const int64_t gbh = p->gu.group_bytes();
     const int64_t gbf = std::max(p->dn.group_bytes(), p->sdn.group_bytes());
@@ -692,6 +876,7 @@ static int plan_moe(const bfp_moe_layer *L, int m, MoePlan *p) {
     const int rows_per_cta = (L->n_experts + 1 + p->ncta - 1) / p->ncta;
     int64_t slot = std::max<int64_t>(2 * gbh, (int64_t)p->r2 * gbf);
     slot = std::max<int64_t>(slot, (int64_t)rows_per_cta * L->hidden * 2);
+    slot = std::max<int64_t>(slot, (int64_t)std::min(m, 8) * L->hidden * 2);  // staged activation rows
     slot = (int64_t)align_up((size_t)slot, 128);
     const size_t fixed = align_up(align_up((size_t)p->frag_bytes + p->scr_bytes + sizeof(MoeMisc), 16) + 16 * 8, 128);
     if ((int64_t)di.smem_optin < (int64_t)fixed + 2 * slot) return fail(BFP_ESHAPE, "layer too large for shared memory");
@@ -702,10 +887,8 @@ static int plan_moe(const bfp_moe_layer *L, int m, MoePlan *p) {
     size_t o = kWsHeader;
     p->off_ctrl = o;
     o += 16;
-    p->off_done1 = o;
-    o = align_up(o + 4 * (size_t)(L->n_experts + 1), 16);
-    p->off_rgcnt = o;
-    o = align_up(o + 4 * (size_t)p->dn.ng, 256);
+    p->off_hmax = o;
+    o = align_up(o + 4 * (size_t)m * (L->top_k + 1), 256);
     p->off_logits = o;
     o = align_up(o + 4 * (size_t)m * (L->n_experts + 1), 256);
     p->off_hbuf = o;
@@ -735,6 +918,12 @@ static int launch_moe_t(const MoeArgs &a, const MoePlan &p, cudaStream_t st) {
     if (e != cudaSuccess) return cuda_fail(e, "launch moe_layer (cooperative)");
     return BFP_OK;
 }
+
+#ifdef BFP_TRACE
+extern "C" int bfp_debug_set_trace(void *buf) {
+    return (int)cudaMemcpyToSymbol(g_bfp_trace, &buf, sizeof(buf));
+}
+#endif
 
 static int moe_launch(const bfp_moe_layer *L, const uint16_t *x, int m, int norm, float *y, uint16_t *h_out,
                       int32_t *topk_idx, float *topk_w, void *ws, size_t ws_bytes, cudaStream_t st) {
@@ -774,8 +963,7 @@ static int moe_launch(const bfp_moe_layer *L, const uint16_t *x, int m, int norm
     a.topk_w = topk_w;
     a.status = reinterpret_cast<uint32_t *>(w);
     a.ctrl = reinterpret_cast<uint32_t *>(w + p.off_ctrl);
-    a.done1 = reinterpret_cast<uint32_t *>(w + p.off_done1);
-    a.rgcnt = reinterpret_cast<uint32_t *>(w + p.off_rgcnt);
+    a.hmax = reinterpret_cast<uint32_t *>(w + p.off_hmax);
     a.logits = reinterpret_cast<float *>(w + p.off_logits);
     a.hbuf = reinterpret_cast<float *>(w + p.off_hbuf);
     a.part = reinterpret_cast<float *>(w + p.off_part);
@@ -892,7 +1080,7 @@ int moe_stack_decode(const bfp_moe_layer *layers, int n_layers, const bfp_matrix
 // ----------------------------------------------------------------------------
 namespace bfp {
 
-constexpr size_t kStaticScratchBytes = size_t(2) << 20;  // 2 MiB: a full-size layer at 16 rows needs ~1.5 MiB
+constexpr size_t kStaticScratchBytes = size_t(3) << 19;  // 1.5 MiB: a full-size layer at 16 rows needs 1,492,224 B
 static __device__ __align__(256) uint8_t g_moe_static_scratch[kStaticScratchBytes];
 
 // Device address of the scratch array on the current device. The array's name

@@ -209,11 +209,11 @@ int moe_decode_layer(const bfp_moe_layer *layer, const uint16_t *x, int m, float
  * this is a convenience of this library.
  *   - Computes exactly what moe_decode_layer computes; x, y, topk_idx, topk_w
  *     as there (caller-owned device memory).
- *   - Scratch: one built-in device array of 2 MiB (2,097,152 bytes), allocated
- *     when the library is loaded and held by every GPU that loads it until the
- *     process exits. A layer needing more (moe_workspace_size > 2 MiB) is
- *     rejected with BFP_EWORKSPACE; the full-size layer (hidden 2048, 256
- *     experts, ffn 512, top-8) at 16 rows needs about 1.5 MiB.
+ *   - Scratch: one built-in device array of 1.5 MiB (1,572,864 bytes),
+ *     allocated when the library is loaded and held by every GPU that loads
+ *     it until the process exits. A layer needing more (moe_workspace_size >
+ *     1.5 MiB) is rejected with BFP_EWORKSPACE; the full-size layer (hidden
+ *     2048, 256 experts, ffn 512, top-8) at 16 rows needs 1,492,224 bytes.
  *   - The first call on a device looks up the array's device address and
  *     zeroes it, synchronously: make that first call before any stream
  *     capture. Each call then clears the array's counters on its stream.
