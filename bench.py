@@ -129,6 +129,25 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# --------------------------------------------------------------------------- ranks
+def reduce_over_ranks(value: float, op: str, device=None) -> float:
+    """max or sum of a per-rank scalar over the process group (identity without one)."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def aggregate_throughput(bytes_per_step: float, steps: int, ms: float, device=None):
+    """Whole-job GB/s: every rank's streamed bytes over the slowest rank's time. Returns (GB/s, max ms)."""
+    ms_max = reduce_over_ranks(ms, "max", device)
+    total = reduce_over_ranks(bytes_per_step * steps, "sum", device)
+    return total / (ms_max * 1e-3) / 1e9, ms_max
+
+
 # --------------------------------------------------------------------------- workload
 def build_instances(n, seed, device):
     import block_floating_point_gb300 as bfp
@@ -363,15 +382,12 @@ def main():
     ms = timed_graph(step16, args.steps, args.warmup, not args.no_graph)
     t1 = time.time()
     sampler.mark(t0, t1)
+    gbs, ms = aggregate_throughput(avg_bytes, args.steps, ms, device)
     if world > 1:
-        tt = torch.tensor([ms], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
         dist.barrier()
     clocks = sampler.stop()
     assert bfp.workspace_status(ws) == bfp.BFP_OK
     us_layer = ms * 1e3 / args.steps
-    gbs = avg_bytes * args.steps * world / (ms * 1e-3) / 1e9
     kernel_gbs = (avg_bytes + avg_other) / (us_layer * 1e-6) / 1e9
     sha = kernel_src_sha()
     tr = NCU_TRAFFIC["moe_layer_m16"]
