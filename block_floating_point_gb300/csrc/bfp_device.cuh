@@ -20,6 +20,7 @@ namespace dev {
 constexpr int kWarp = 32;
 constexpr uint32_t kMaskBfp4 = 0x80078007u;
 constexpr uint32_t kMaskBfp8 = 0x807F807Fu;
+constexpr int kRecCodes = 512;  // code bytes at the start of every tile record (exponents follow)
 constexpr int kStatusTimeout = 7;  // stored as -BFP_ETIMEOUT in the status word
 
 struct WaitCfg {

@@ -79,7 +79,8 @@ __device__ __forceinline__ int cta_of(int64_t q, int64_t R, int ncta) {
     return c;
 }
 
-constexpr int kLinMisc = 256;  // shift[16], inv[16], flags
+constexpr int kLinEsc = 256;                                                 // offset of the per-warp scale scratch
+constexpr int kLinMisc = kLinEsc + kConsumerWarps * rec_scale_floats<4, 1>() * 4;  // shift[16], inv[16], flags, scales
 
 template <int FMT, int NGRP>
 __global__ void __launch_bounds__(kThreads, 1) bfp_linear_kernel(const LinearArgs a) {
@@ -93,6 +94,8 @@ __global__ void __launch_bounds__(kThreads, 1) bfp_linear_kernel(const LinearArg
     int *shift = reinterpret_cast<int *>(scr + NW * TILE);
     float *inv = reinterpret_cast<float *>(shift + 16);
     volatile int *flags = reinterpret_cast<volatile int *>(inv + 16);
+    float *esc = reinterpret_cast<float *>(smem + a.frag_bytes + NW * TILE * 4 + kLinEsc) +
+                 (threadIdx.x >> 5) * rec_scale_floats<4, 1>();  // this warp's scale scratch
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + a.frag_bytes + NW * TILE * 4 + kLinMisc);
     uint64_t *empty = full + a.nslot;
     uint8_t *ring = smem + align_up(a.frag_bytes + NW * TILE * 4 + kLinMisc + 16 * a.nslot, 128);
@@ -174,7 +177,6 @@ __global__ void __launch_bounds__(kThreads, 1) bfp_linear_kernel(const LinearArg
             u = nx;
         }
         const uint2 *frag2 = reinterpret_cast<const uint2 *>(frag);
-        const uint32_t gmask = a.m > 8 ? 3u : 1u;
         float acc[1][NGRP][4];
 #pragma unroll
         for (int g = 0; g < NGRP; ++g)
@@ -192,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1) bfp_linear_kernel(const LinearArg
                 const uint8_t *base = ring + (size_t)slot * a.slot_bytes;
                 for (int i = warp; i < len; i += NW) {
                     const uint8_t *recs[1] = {base + (size_t)i * a.rec};
-                    mma_records<FMT, NGRP, 1, false>(recs, frag2, nullptr, a.kbp, (c0 + i) * CB, lane, gmask, acc);
+                    mma_records<FMT, NGRP, 1, false>(recs, frag2, nullptr, a.kbp, (c0 + i) * CB, lane, esc, acc);
                 }
             }
             __syncwarp();

@@ -17,71 +17,105 @@
 namespace bfp {
 namespace dev {
 
-// acc[r][grp][i] += sum over the record's blocks of 2^(E-127) * (A_r . B_grp)
+// Exponent bytes of one record (16 rows x CB blocks), and how many of a call's bytes each lane converts.
+template <int FMT>
+__host__ __device__ constexpr int rec_exp_bytes() { return FMT == 4 ? 64 : 32; }
+// Scratch floats one warp needs for mma_records<FMT, *, NREC, *>.
+template <int FMT, int NREC>
+__host__ __device__ constexpr int rec_scale_floats() { return NREC * rec_exp_bytes<FMT>(); }
+
+// acc[r][grp][i] += sum over the record's blocks of 2^(E-127) * (A_r . B_grp), grp < NG
 //   recs[r]:  record r in shared memory (NREC records share the activation fragments)
-//   frag:     activation fragments, [grp][block][lane] uint2; frag_lo (HILO) a second,
-//             low-order part added into the same tile before scaling
-//   kb0:      index of the record's first block in the fragment arrays
-//   grp_mask: bit g set = compute activation group g (8 rows each)
-template <int FMT, int NGRP, int NREC, bool HILO>
+//   frag:     activation fragments of the first group computed: [grp][block][lane] uint2, groups
+//             kbp blocks apart; frag_lo (HILO) a second, low-order part added into the same
+//             tile before scaling, same layout
+//   kb0:      index of the record's first block in the fragment arrays (a multiple of the
+//             record's block count)
+//   esc:      this warp's scratch of rec_scale_floats<FMT, NREC>() floats (16-byte aligned)
+// Branch-free: the group count is a template parameter, so the compiler can interleave the
+// independent tiles of a record. The four lanes of a row pair (lane >> 2 equal) need the same
+// block scales, so the warp first turns the records' exponent bytes into fp32 scales once, each
+// lane its share, through esc: the integer work per scale is done once instead of four times.
+template <int FMT, int NG, int NREC, bool HILO>
 __device__ __forceinline__ void mma_records(const uint8_t *const recs[NREC], const uint2 *frag, const uint2 *frag_lo,
-                                            int kbp, int kb0, int lane, uint32_t grp_mask,
-                                            float acc[NREC][NGRP][4]) {
+                                            int kbp, int kb0, int lane, float *esc, float acc[NREC][NG][4]) {
+    constexpr int EB = rec_exp_bytes<FMT>();
+    constexpr int CB = FMT == 4 ? 4 : 2;
+    constexpr int BPL = NREC * EB / kWarp;  // exponent bytes converted per lane
+    static_assert(BPL == 1 || BPL == 2 || BPL == 4, "unsupported record count");
     const int g = lane >> 2;
     uint4 wq[NREC];
-    uint32_t e0[NREC], e1[NREC];
+#pragma unroll
+    for (int r = 0; r < NREC; ++r) wq[r] = *reinterpret_cast<const uint4 *>(recs[r] + 16 * lane);
+    {
+        const int byte0 = lane * BPL;  // byte of the call's exponents, records in order
+        const uint8_t *rp = recs[0];
+#pragma unroll
+        for (int r = 1; r < NREC; ++r)
+            if (byte0 >= r * EB) rp = recs[r];
+        const uint8_t *src = rp + kRecCodes + byte0 % EB;
+        __syncwarp();  // every lane is done reading the previous call's scales
+        if constexpr (BPL == 4) {
+            const uint32_t w = *reinterpret_cast<const uint32_t *>(src);
+            *reinterpret_cast<float4 *>(esc + byte0) =
+                make_float4(exp_scale(w, 0), exp_scale(w, 1), exp_scale(w, 2), exp_scale(w, 3));
+        } else if constexpr (BPL == 2) {
+            const uint32_t w = *reinterpret_cast<const uint16_t *>(src);
+            *reinterpret_cast<float2 *>(esc + byte0) = make_float2(exp_scale(w, 0), exp_scale(w, 1));
+        } else {
+            esc[byte0] = exp_scale(*src, 0);
+        }
+        __syncwarp();
+    }
+    // this lane's scales: record r, block b -> sc[r][2b] (row g), sc[r][2b + 1] (row g + 8)
+    float sc[NREC][2 * CB];
 #pragma unroll
     for (int r = 0; r < NREC; ++r) {
-        wq[r] = *reinterpret_cast<const uint4 *>(recs[r] + 16 * lane);
-        if constexpr (FMT == 4) {
-            const uint2 eq = *reinterpret_cast<const uint2 *>(recs[r] + 512 + 8 * g);
-            e0[r] = eq.x;
-            e1[r] = eq.y;
-        } else {
-            e0[r] = *reinterpret_cast<const uint32_t *>(recs[r] + 512 + 4 * g);
-            e1[r] = 0;
+#pragma unroll
+        for (int q = 0; q < CB / 2; ++q) {
+            const float4 f = *reinterpret_cast<const float4 *>(esc + r * EB + 2 * CB * g + 4 * q);
+            sc[r][4 * q] = f.x;
+            sc[r][4 * q + 1] = f.y;
+            sc[r][4 * q + 2] = f.z;
+            sc[r][4 * q + 3] = f.w;
         }
     }
-    constexpr int CB = FMT == 4 ? 4 : 2;
+    // fragment of block kb0 + b for this lane: lane ^ frag_swz(kb0 + b), and since kb0 is a
+    // multiple of CB, (kb0 + b) & 7 = (kb0 & 7) | b
+    const int l0 = lane ^ ((kb0 & 7) << 2);
+    const uint2 *fh = frag + (int64_t)kb0 * kWarp;
+    const uint2 *fl = HILO ? frag_lo + (int64_t)kb0 * kWarp : nullptr;
 #pragma unroll
     for (int b = 0; b < CB; ++b) {
-        uint2 bx[NGRP], bl[NGRP];
+        const int li = b * kWarp + (l0 ^ (b << 2));
+        uint2 bx[NG], bl[NG];
 #pragma unroll
-        for (int grp = 0; grp < NGRP; ++grp) {
-            if (grp_mask & (1u << grp)) {
-                bx[grp] = frag[frag_idx(grp, kb0 + b, lane, kbp)];
-                if constexpr (HILO) bl[grp] = frag_lo[frag_idx(grp, kb0 + b, lane, kbp)];
-            }
+        for (int grp = 0; grp < NG; ++grp) {
+            bx[grp] = fh[(int64_t)grp * kbp * kWarp + li];
+            if constexpr (HILO) bl[grp] = fl[(int64_t)grp * kbp * kWarp + li];
         }
 #pragma unroll
         for (int r = 0; r < NREC; ++r) {
             uint32_t a[4];
-            float s0, s1;
             if constexpr (FMT == 4) {
                 const uint32_t wsel = b == 0 ? wq[r].x : b == 1 ? wq[r].y : b == 2 ? wq[r].z : wq[r].w;
                 unpack_bfp4(wsel, a);
-                const uint32_t ew = b < 2 ? e0[r] : e1[r];
-                s0 = exp_scale(ew, 2 * (b & 1));
-                s1 = exp_scale(ew, 2 * (b & 1) + 1);
             } else {
                 if (b == 0)
                     unpack_bfp8(wq[r].x, wq[r].y, a);
                 else
                     unpack_bfp8(wq[r].z, wq[r].w, a);
-                s0 = exp_scale(e0[r], 2 * b);
-                s1 = exp_scale(e0[r], 2 * b + 1);
             }
+            const float s0 = sc[r][2 * b], s1 = sc[r][2 * b + 1];
 #pragma unroll
-            for (int grp = 0; grp < NGRP; ++grp) {
-                if (grp_mask & (1u << grp)) {
-                    float c[4] = {0.f, 0.f, 0.f, 0.f};
-                    mma16816(c, a, bx[grp].x, bx[grp].y);
-                    if constexpr (HILO) mma16816(c, a, bl[grp].x, bl[grp].y);
-                    acc[r][grp][0] = fmaf(s0, c[0], acc[r][grp][0]);
-                    acc[r][grp][1] = fmaf(s0, c[1], acc[r][grp][1]);
-                    acc[r][grp][2] = fmaf(s1, c[2], acc[r][grp][2]);
-                    acc[r][grp][3] = fmaf(s1, c[3], acc[r][grp][3]);
-                }
+            for (int grp = 0; grp < NG; ++grp) {
+                float c[4] = {0.f, 0.f, 0.f, 0.f};
+                mma16816(c, a, bx[grp].x, bx[grp].y);
+                if constexpr (HILO) mma16816(c, a, bl[grp].x, bl[grp].y);
+                acc[r][grp][0] = fmaf(s0, c[0], acc[r][grp][0]);
+                acc[r][grp][1] = fmaf(s0, c[1], acc[r][grp][1]);
+                acc[r][grp][2] = fmaf(s1, c[2], acc[r][grp][2]);
+                acc[r][grp][3] = fmaf(s1, c[3], acc[r][grp][3]);
             }
         }
     }

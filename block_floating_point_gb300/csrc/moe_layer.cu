@@ -78,6 +78,7 @@ struct MoeArgs {
 
 // Shared-memory bookkeeping of one CTA.
 struct MoeMisc {
+    alignas(16) float esc[kConsumerWarps][rec_scale_floats<4, 2>()];  // per-warp block scales (mma_records)
     uint64_t cbar;  // consumers' own bulk copies (logits, h rows)
     int shift_x[kMaxRows];
     float inv[kMaxRows];
@@ -367,9 +368,29 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
 #pragma unroll
                     for (int i = 0; i < 4; ++i) acc[r][g][i] = 0.f;
             if (!bad) {
-                for (int ch = warp; ch < a.kc_h; ch += NW) {
-                    const uint8_t *recs[2] = {slotp + (size_t)ch * a.rec, slotp + gb_h + (size_t)ch * a.rec};
-                    mma_records<FMT, NGRP, 2, false>(recs, frag2, nullptr, a.kbp_h, ch * CB, lane, gm, acc);
+                bool both = false;
+                if constexpr (NGRP == 2) both = gm == 3u;
+                if (both) {
+                    for (int ch = warp; ch < a.kc_h; ch += NW) {
+                        const uint8_t *recs[2] = {slotp + (size_t)ch * a.rec, slotp + gb_h + (size_t)ch * a.rec};
+                        mma_records<FMT, NGRP, 2, false>(recs, frag2, nullptr, a.kbp_h, ch * CB, lane, ms->esc[warp],
+                                                         acc);
+                    }
+                } else {
+                    // one activation group holds every row of this unit: compute only that one
+                    const int gsel = gm == 2u ? 1 : 0;
+                    const uint2 *fg = frag2 + (int64_t)gsel * a.kbp_h * kWarp;
+                    float a1[2][1][4] = {};
+                    for (int ch = warp; ch < a.kc_h; ch += NW) {
+                        const uint8_t *recs[2] = {slotp + (size_t)ch * a.rec, slotp + gb_h + (size_t)ch * a.rec};
+                        mma_records<FMT, 1, 2, false>(recs, fg, nullptr, a.kbp_h, ch * CB, lane, ms->esc[warp], a1);
+                    }
+#pragma unroll
+                    for (int r = 0; r < 2; ++r)
+#pragma unroll
+                        for (int g = 0; g < NGRP; ++g)
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) acc[r][g][i] = g == gsel ? a1[r][0][i] : 0.f;
                 }
             }
             release_slot(slot);
@@ -725,16 +746,29 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
                     const uint8_t *rb = slotp + (size_t)warp * kc * a.rec;
                     const uint2 *hi2 = reinterpret_cast<const uint2 *>(hfrag);
                     const uint2 *lo2 = hi2 + NGRP * kbp * kWarp;
-                    if (packed) {
+                    bool both = false;
+                    if constexpr (NGRP == 2) both = !packed && gm2 == 3u;
+                    if (both) {
                         for (int ch = 0; ch < kc; ++ch) {
                             const uint8_t *recs[1] = {rb + (size_t)ch * a.rec};
-                            mma_records<FMT, NGRP, 1, false>(recs, hi2, nullptr, kbp, ch * CB, lane, 1u, acc);
+                            mma_records<FMT, NGRP, 1, true>(recs, hi2, lo2, kbp, ch * CB, lane, ms->esc[warp], acc);
                         }
                     } else {
-                        for (int ch = 0; ch < kc; ++ch) {
-                            const uint8_t *recs[1] = {rb + (size_t)ch * a.rec};
-                            mma_records<FMT, NGRP, 1, true>(recs, hi2, lo2, kbp, ch * CB, lane, gm2, acc);
+                        // columns of group 0 only: hi and lo packed side by side (<= 4 rows) or hi + lo parts
+                        float a1[1][1][4] = {};
+                        if (packed) {
+                            for (int ch = 0; ch < kc; ++ch) {
+                                const uint8_t *recs[1] = {rb + (size_t)ch * a.rec};
+                                mma_records<FMT, 1, 1, false>(recs, hi2, nullptr, kbp, ch * CB, lane, ms->esc[warp], a1);
+                            }
+                        } else {
+                            for (int ch = 0; ch < kc; ++ch) {
+                                const uint8_t *recs[1] = {rb + (size_t)ch * a.rec};
+                                mma_records<FMT, 1, 1, true>(recs, hi2, lo2, kbp, ch * CB, lane, ms->esc[warp], a1);
+                            }
                         }
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) acc[0][0][i] = a1[0][0][i];
                     }
                 }
                 release_slot(slot);
