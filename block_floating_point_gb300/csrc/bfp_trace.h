@@ -11,7 +11,7 @@ static __device__ unsigned long long *g_bfp_trace = nullptr;
 #define BFP_TRACE_AT(slot)                                                                                  \
     do {                                                                                                    \
         if (g_bfp_trace != nullptr && (threadIdx.x == 0 || threadIdx.x == 256))                             \
-            g_bfp_trace[(size_t)blockIdx.x * BFP_TRACE_SLOTS + (slot) + (threadIdx.x == 256 ? 32 : 0)] =    \
+            g_bfp_trace[(size_t)blockIdx.x * BFP_TRACE_SLOTS + (slot) + (threadIdx.x == 256 ? 48 : 0)] =    \
                 bfp::dev::global_ns();                                                                      \
     } while (0)
 #else

@@ -94,6 +94,8 @@ struct MoeMisc {
     int8_t uslot[kMaxExperts + 1][kMaxRows];
     uint32_t maxbits[2][kMaxRows];  // per-unit max |h| per row (double-buffered like the scratch)
     int8_t colrow[kMaxRows];        // phase 2: fragment column -> row of the current expert
+    int32_t p2cum[kMaxExperts + 2];  // phase-2 unit cost before each expert of the union (and the total)
+    int64_t p2q[2];                  // this CTA's phase-2 units [p2q[0], p2q[1])
     int nU;
     int flags[4];  // [0] abort
 };
@@ -106,34 +108,49 @@ __device__ __forceinline__ int p2_cost(uint32_t rowmask) {
     const int n = __popc(rowmask);
     return n <= 4 ? 1 : (n <= 8 ? 2 : 4);
 }
-// First phase-2 unit (q = j * noct + oct, j = 0..nU) whose cumulative-cost start is >= X.
-__device__ int p2_first_unit(const uint32_t *umask, int nU, int noct, int64_t X) {
-    int64_t base = 0;
-    for (int j = 0; j <= nU; ++j) {
-        const int cj = p2_cost(umask[j]);
-        const int64_t span = (int64_t)noct * cj;
-        if (X <= base) return j * noct;
-        if (X < base + span) {
-            const int o = (int)((X - base + cj - 1) / cj);
-            if (o < noct) return j * noct + o;
-        }
-        base += span;
+// First phase-2 unit (q = j * noct + o, j = 0..nU) whose cost start cum[j] + o * cost_j is >= X,
+// given cum[j] = the cost of all units of experts before j (cum[0] = 0, cum[nU + 1] = total).
+__device__ __forceinline__ int64_t p2_first_unit(const int32_t *cum, const uint32_t *umask, int nU, int noct,
+                                                 int64_t X) {
+    if (X <= 0) return 0;
+    int lo = 0, hi = nU;  // last j with cum[j] < X: cum[0] = 0 < X
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (cum[mid] < X)
+            lo = mid;
+        else
+            hi = mid - 1;
     }
-    return (nU + 1) * noct;
-}
-// CTA c's phase-2 units [q0, q1): an equal share of the total cost.
-__device__ __forceinline__ void p2_range(const uint32_t *umask, int nU, int noct, int c, int ncta, int64_t *q0,
-                                         int64_t *q1) {
-    int64_t total = 0;
-    for (int j = 0; j <= nU; ++j) total += (int64_t)noct * p2_cost(umask[j]);
-    *q0 = p2_first_unit(umask, nU, noct, total * c / ncta);
-    *q1 = p2_first_unit(umask, nU, noct, total * (c + 1) / ncta);
+    const int cj = p2_cost(umask[lo]);
+    const int64_t o = (X - cum[lo] + cj - 1) / cj;
+    return o < noct ? (int64_t)lo * noct + o : (int64_t)(lo + 1) * noct;
 }
 
 // Ordered 32-bit key of a float: larger float <=> larger unsigned key.
 __device__ __forceinline__ uint32_t order_key(float v) {
     uint32_t u = __float_as_uint(v);
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+// Inverse of order_key.
+__device__ __forceinline__ float key_value(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+// Compare-exchange on (key, index) pairs: larger key first, lower index first among equal keys.
+__device__ __forceinline__ void cmp_xchg(uint32_t &ka, int &qa, uint32_t &kb, int &qb) {
+    const bool sw = kb > ka || (kb == ka && qb < qa);
+    const uint32_t k0 = sw ? kb : ka, k1 = sw ? ka : kb;
+    const int q0 = sw ? qb : qa, q1 = sw ? qa : qb;
+    ka = k0;
+    kb = k1;
+    qa = q0;
+    qb = q1;
+}
+// Sorts 8 (key, index) pairs in registers (Batcher's odd-even merge network, 19 comparators).
+__device__ __forceinline__ void sort8_desc(uint32_t k[8], int q[8]) {
+    constexpr int net[19][2] = {{0, 1}, {2, 3}, {4, 5}, {6, 7}, {0, 2}, {1, 3}, {4, 6}, {5, 7}, {1, 2}, {5, 6},
+                                {0, 4}, {1, 5}, {2, 6}, {3, 7}, {2, 4}, {3, 5}, {1, 2}, {3, 4}, {5, 6}};
+#pragma unroll
+    for (int i = 0; i < 19; ++i) cmp_xchg(k[net[i][0]], q[net[i][0]], k[net[i][1]], q[net[i][1]]);
 }
 
 template <int FMT, int NGRP>
@@ -245,8 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
                 bad = !issue(1, src, bytes);
             }
             // 5. down-projection units
-            int64_t q0, q1;
-            p2_range(ms->umask, nU, a.noct, c, a.ncta, &q0, &q1);
+            const int64_t q0 = ms->p2q[0], q1 = ms->p2q[1];
             for (int64_t q = q0; !bad && q < q1; ++q) {
                 const int j = (int)(q / a.noct), oct = (int)(q % a.noct);
                 const bool sh = j == nU;
@@ -528,53 +544,56 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
             }
             stage_wait();
             STAMP(26);  // logits in shared memory
-            for (int r = warp; r < a.M; r += NW) {
-                float v[8];
-                float p[8];
+            // Top-k per row. Warp w takes rows w and w + NW in one loop (two independent chains per
+            // round). Lane l holds experts 8l .. 8l+7 and first sorts them (key descending, index
+            // ascending among equal keys); each round the lanes offer their heads, the largest key wins
+            // and among equal keys the lowest lane, i.e. the lowest expert index (ties go to the lower
+            // index), and the winner records its expert and logit and drops its head.
+            // Slot 0 is the row maximum, so p_s = exp(l_s - l_0) and w_s = p_s / sum of p.
+            {
+                constexpr int RPW = kMaxRows / NW;
+                uint32_t key[RPW][8];
+                int qi[RPW][8];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const int e = lane + 32 * q;
-                    v[q] = e < a.E ? lg[r * E1 + e] : -INFINITY;
-                }
-                float mx = -INFINITY;
-#pragma unroll
-                for (int q = 0; q < 8; ++q) mx = fmaxf(mx, v[q]);
-                mx = warp_max(mx);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) p[q] = (lane + 32 * q < a.E) ? expf(v[q] - mx) : 0.f;
-                uint32_t taken = 0;
-                float psum = 0.f;
-                for (int s = 0; s < a.K; ++s) {
-                    int bq = -1;
-                    float bv = 0.f;
+                for (int j = 0; j < RPW; ++j) {
+                    const int r = warp + NW * j;
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
-                        const bool ok2 = lane + 32 * q < a.E && !((taken >> q) & 1u);
-                        if (ok2 && (bq < 0 || v[q] > bv)) {
-                            bq = q;
-                            bv = v[q];
-                        }
+                        const int e = 8 * lane + q;
+                        key[j][q] = r < a.M && e < a.E ? order_key(lg[r * E1 + e]) : 0u;  // 0: below any key
+                        qi[j][q] = q;
                     }
-                    const uint32_t key = bq >= 0 ? order_key(bv) : 0u;
-                    const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
-                    const uint32_t cand = (bq >= 0 && key == kmax) ? (uint32_t)(lane + 32 * bq) : 0xFFFFFFFFu;
-                    const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
-                    const int owner = (int)(win & 31u), wq = (int)(win >> 5);
-                    float pw = 0.f;
-                    if (lane == owner) {
-                        taken |= 1u << wq;
+                    sort8_desc(key[j], qi[j]);
+                }
+                for (int s = 0; s < a.K; ++s) {
 #pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            if (q == wq) pw = p[q];
-                    }
-                    pw = __shfl_sync(0xffffffffu, pw, owner);
-                    psum += pw;
-                    if (lane == 0) {
-                        ms->tk_idx[r][s] = (int32_t)win;
-                        ms->tk_w[r][s] = pw;
+                    for (int j = 0; j < RPW; ++j) {
+                        const uint32_t kmax = __reduce_max_sync(0xffffffffu, key[j][0]);
+                        const uint32_t bal = __ballot_sync(0xffffffffu, kmax != 0u && key[j][0] == kmax);
+                        const bool win = bal != 0u && lane == __ffs(bal) - 1;
+                        if (win) {
+                            const int r = warp + NW * j;
+                            ms->tk_idx[r][s] = 8 * lane + qi[j][0];
+                            ms->tk_w[r][s] = key_value(key[j][0]);  // the logit until the weights below
+                        }
+#pragma unroll
+                        for (int q = 0; q < 7; ++q) {
+                            key[j][q] = win ? key[j][q + 1] : key[j][q];
+                            qi[j][q] = win ? qi[j][q + 1] : qi[j][q];
+                        }
+                        key[j][7] = win ? 0u : key[j][7];
                     }
                 }
-                if (lane == 0) {
+                __syncwarp();
+                const int r = warp + NW * lane;
+                if (lane < RPW && r < a.M) {
+                    const float mx = ms->tk_w[r][0];
+                    float psum = 0.f;
+                    for (int s = 0; s < a.K; ++s) {
+                        const float p = expf(ms->tk_w[r][s] - mx);
+                        ms->tk_w[r][s] = p;
+                        psum += p;
+                    }
                     for (int s = 0; s < a.K; ++s) ms->tk_w[r][s] = ms->tk_w[r][s] / psum;
                     ms->gate_w[r] = 1.0f / (1.0f + expf(-lg[r * E1 + a.E]));
                 }
@@ -623,6 +642,30 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
             if (tid < a.M) ms->uslot[nU][tid] = (int8_t)a.K;
             if (tid == 0) ms->umask[nU] = (1u << a.M) - 1u;
             bar_sync(1, NC);
+            // phase-2 shares: exclusive prefix of the unit costs over the union (warp scan), then this
+            // CTA's range [first unit starting at >= total*c/ncta, ... >= total*(c+1)/ncta)
+            if (warp == 0) {
+                int carry = 0;
+                for (int j0 = 0; j0 <= nU; j0 += kWarp) {
+                    const int j = j0 + lane;
+                    const int cj = j <= nU ? a.noct * p2_cost(ms->umask[j]) : 0;
+                    int incl = cj;
+#pragma unroll
+                    for (int o = 1; o < kWarp; o <<= 1) {
+                        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+                        if (lane >= o) incl += t;
+                    }
+                    if (j <= nU) ms->p2cum[j] = carry + incl - cj;
+                    carry += __shfl_sync(0xffffffffu, incl, kWarp - 1);
+                }
+                if (lane == 0) ms->p2cum[nU + 1] = carry;
+                __syncwarp();
+                if (lane < 2) {
+                    const int64_t X = (int64_t)ms->p2cum[nU + 1] * (c + lane) / a.ncta;
+                    ms->p2q[lane] = p2_first_unit(ms->p2cum, ms->umask, nU, a.noct, X);
+                }
+            }
+            bar_sync(1, NC);
         }
         STAMP(6);  // top-k + union done
         bar_arrive(2, kThreads);
@@ -657,9 +700,9 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
         //      n <= 8: hi and lo fragments, two MMAs; more rows: two column groups.
         {
             const int nU = ms->nU;
-            int64_t q0, q1;
-            p2_range(ms->umask, nU, a.noct, c, a.ncta, &q0, &q1);
+            const int64_t q0 = ms->p2q[0], q1 = ms->p2q[1];
             int cur = -1;
+            int p2n = 0;  // phase-2 units done by this CTA (trace stamps)
             int nr = 0;
             bool packed = false;
             uint32_t gm2 = 1;
@@ -676,6 +719,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
                         abort_all();
                         goto done;
                     }
+                    if (cur < 0) STAMP(14);  // first expert: setup start
                     nr = __popc(rowmask);
                     packed = nr <= 4;
                     gm2 = nr > 8 ? 3u : 1u;
@@ -692,6 +736,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
                     const int words = 2 * NGRP * kbp * kWarp * 2;
                     for (int i = tid; i < words / 4; i += NC) reinterpret_cast<uint4 *>(hfrag)[i] = make_uint4(0, 0, 0, 0);
                     bar_sync(1, NC);
+                    if (cur < 0) STAMP(15);  // ... fragments zeroed
                     // h rows of this expert (one bulk copy per row) into the scratch: row at column c
                     float *hs = scr;
                     if (tid == 0) {
@@ -702,8 +747,10 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
                                 bulk_g2s(hs + __popc(rowmask & ((1u << r) - 1u)) * Fe,
                                          a.hbuf + ((int64_t)r * (a.K + 1) + ms->uslot[j][r]) * a.Fmax,
                                          (uint32_t)Fe * 4, &ms->cbar);
+                        if (cur < 0) STAMP(20);  // ... h copies issued
                     }
                     stage_wait();
+                    if (cur < 0) STAMP(7);  // first expert's h rows landed
                     // one item = 4 consecutive h values (cols 4qq..4qq+3 of block b) of a column
                     {
                         const int fb = Fe / 16;
@@ -733,7 +780,10 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
                     if (cur < 0) STAMP(10);  // first expert's h fragments ready
                     cur = j;
                 }
+                if (p2n == 0) STAMP(16);  // first phase-2 unit: start
                 const int slot = wait_slot(u);
+                if (p2n == 0) STAMP(17);  // ... its data landed
+                if (p2n == 1) STAMP(28);  // second unit: data landed
                 const uint8_t *slotp = ring + (size_t)slot * a.slot_bytes;
                 const int rg0 = oct * a.r2, nrg = min(a.r2, a.ng_d - rg0);
                 float acc[1][NGRP][4];
@@ -773,6 +823,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
                 }
                 release_slot(slot);
                 ++u;
+                if (p2n == 0) STAMP(18);  // ... warp 0's MMAs done
+                if (p2n == 1) STAMP(29);
                 if (!bad && mine) {
                     const int rg = rg0 + warp;
                     if (packed) {  // column c + 4 holds the lo half of column c: lanes t and t ^ 2
@@ -793,6 +845,9 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
                             }
                         }
                 }
+                if (p2n == 0) STAMP(19);  // ... partial outputs stored
+                if (p2n == 1) STAMP(31);
+                ++p2n;
             }
             STAMP(11);  // down projections done
             if (!grid_barrier(&a.ctrl[3])) {  // every (row, slot) partial written
