@@ -86,6 +86,11 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
 // Orders this thread's view of global memory (generic proxy) before its later bulk copies
 // (async proxy) read it: data other blocks wrote and this thread acquired.
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+// Orders this thread's earlier shared-memory accesses (generic proxy) before its later bulk copies
+// into shared memory (async proxy): needed before a copy overwrites memory the CTA has read.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 
 // ------------------------------------------------------ cross-block counters
 __device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p) {

@@ -14,7 +14,18 @@ static __device__ unsigned long long *g_bfp_trace = nullptr;
             g_bfp_trace[(size_t)blockIdx.x * BFP_TRACE_SLOTS + (slot) + (threadIdx.x == 256 ? 48 : 0)] =    \
                 bfp::dev::global_ns();                                                                      \
     } while (0)
+// Stores a value (a duration accumulated in registers, a count) into a slot of thread 0's row.
+#define BFP_TRACE_SET(slot, v)                                                                              \
+    do {                                                                                                    \
+        if (g_bfp_trace != nullptr && threadIdx.x == 0)                                                     \
+            g_bfp_trace[(size_t)blockIdx.x * BFP_TRACE_SLOTS + (slot)] = (v);                               \
+    } while (0)
+#define BFP_TRACE_NOW() bfp::dev::global_ns()
 #else
+#define BFP_TRACE_SET(slot, v) \
+    do {                       \
+    } while (0)
+#define BFP_TRACE_NOW() 0ull
 #define BFP_TRACE_AT(slot) \
     do {                   \
     } while (0)

@@ -48,6 +48,8 @@ int linear_launch_ex(const bfp_matrix *w, const uint16_t *x, int m, int64_t ldx,
 int linear_ws_body_bytes(const bfp_matrix *w, int m, size_t *bytes);
 
 constexpr int kMaxRows = 16;
+constexpr int kMoeWarps = 8;                 // warps of the layer kernel (no producer warp)
+constexpr int kMoeThreads = kMoeWarps * 32;
 constexpr int kMaxTopK = 8;
 constexpr int kMaxExperts = 256;
 
@@ -71,15 +73,17 @@ struct MoeArgs {
     float *logits, *hbuf, *part;
     int rec, kc_h, kbp_h, kc_f, kbp_f, kc_fs, kbp_fs;
     int nft, nft_s, ng_d, r2, noct, Fmax;
-    int nslot, slot_bytes, frag_bytes, scr_bytes;
+    int nsw, ch1, slot_bytes, frag_bytes, scr_bytes;  // per-warp slots, phase-1 chunk records, slot bytes
+    int stage_off, stage_r;  // preamble stage: ring offset of the activation rows; router rows after stage_r bytes
     WaitCfg wait;       // cross-block waits (router counter, expert counters)
     WaitCfg wait_data;  // this CTA's own bulk copies and slot hand-backs
 };
 
 // Shared-memory bookkeeping of one CTA.
 struct MoeMisc {
-    alignas(16) float esc[kConsumerWarps][rec_scale_floats<4, 2>()];  // per-warp block scales (mma_records)
-    uint64_t cbar;  // consumers' own bulk copies (logits, h rows)
+    alignas(16) float esc[kMoeWarps][rec_scale_floats<4, 2>()];  // per-warp block scales (mma_records)
+    uint64_t cbar;        // consumers' own bulk copies (logits, h rows)
+    uint64_t stage_full;  // the preamble stage (activation rows, router rows) landed
     int shift_x[kMaxRows];
     float inv[kMaxRows];
     int shift_h[kMaxRows];
@@ -126,6 +130,25 @@ __device__ __forceinline__ int64_t p2_first_unit(const int32_t *cum, const uint3
     return o < noct ? (int64_t)lo * noct + o : (int64_t)(lo + 1) * noct;
 }
 
+// Phase-1 unit g of the list [shared-expert f-tiles, routed f-tiles of union expert 0, 1, ...]:
+// slot-table row (kMaxExperts for the shared expert) and f-tile.
+struct P1Tile {
+    int jrow, ft;
+    bool sh;
+};
+__device__ __forceinline__ P1Tile p1_tile(int g, int nft_s, int nft) {
+    P1Tile t;
+    t.sh = g < nft_s;
+    t.jrow = t.sh ? kMaxExperts : (g - nft_s) / nft;
+    t.ft = t.sh ? g : (g - nft_s) % nft;
+    return t;
+}
+// Number of phase-1 units i = w, w + NW, ... of CTA c (unit i is g = c + i * ncta) with g < total.
+__device__ __forceinline__ int p1_warp_units(int total, int c, int ncta, int w, int nw) {
+    const int nc = c < total ? (total - c + ncta - 1) / ncta : 0;
+    return w < nc ? (nc - w + nw - 1) / nw : 0;
+}
+
 // Ordered 32-bit key of a float: larger float <=> larger unsigned key.
 __device__ __forceinline__ uint32_t order_key(float v) {
     uint32_t u = __float_as_uint(v);
@@ -153,147 +176,64 @@ __device__ __forceinline__ void sort8_desc(uint32_t k[8], int q[8]) {
     for (int i = 0; i < 19; ++i) cmp_xchg(k[net[i][0]], q[net[i][0]], k[net[i][1]], q[net[i][1]]);
 }
 
+// Per-warp streams. Warp w has nsw slots of its own in the ring; its k-th item lands in slot
+// k mod nsw, and the warp itself issues item k + nsw (lane 0, one or two bulk copies) as soon as it is
+// done with item k. Its items, in order:
+//   phase 1: the CTA's units i = w, w + NW, ... (unit i is list entry g = c + i * ncta, see p1_tile),
+//            each in chunks of ch1 records of its gate row group followed by the same records of its
+//            up row group;
+//   phase 2: for each down-projection unit q of the CTA's range that has a row group oct * r2 + w,
+//            that row group in chunks of 2 * ch1 records.
+// No warp waits for another inside a phase: a warp accumulates whole f-tiles (phase 1) or whole row
+// groups (phase 2) over all of k and writes its own results.
 template <int FMT, int NGRP>
-__global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a) {
+__global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
-    constexpr int NW = kConsumerWarps;
-    constexpr int NC = NW * kWarp;  // consumer threads
+    constexpr int NW = kMoeWarps;
+    constexpr int NC = NW * kWarp;  // threads
     constexpr int MB = FMT == 4 ? 3 : 7;
     constexpr int CB = FMT == 4 ? 4 : 2;
     uint32_t *frag = reinterpret_cast<uint32_t *>(smem);
     float *scr = reinterpret_cast<float *>(smem + a.frag_bytes);
     MoeMisc *ms = reinterpret_cast<MoeMisc *>(smem + a.frag_bytes + a.scr_bytes);
     const size_t bar_off = align_up(a.frag_bytes + a.scr_bytes + sizeof(MoeMisc), 16);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + bar_off);
-    uint64_t *empty = full + a.nslot;
-    uint8_t *ring = smem + align_up(bar_off + 16 * a.nslot, 128);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + bar_off);  // [NW][nsw]
+    uint8_t *ring = smem + align_up(bar_off + 8 * NW * a.nsw, 128);
+    uint8_t *stage = ring + a.stage_off;  // preamble only: activation rows, then router rows
     volatile int *vflags = ms->flags;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x;
     const int E1 = a.E + 1;
 #define STAMP(i) BFP_TRACE_AT(i)
-    STAMP(0);  // router rows + the shared-gate row
+    STAMP(0);
     const int rr0 = router_row_start(c, E1, a.ncta), rr1 = router_row_start(c + 1, E1, a.ncta);
     const int64_t gb_h = (int64_t)a.kc_h * a.rec;  // bytes of one gate/up row group
-    const int nft_total_pre = a.nft_s;              // phase-1 units known before routing
+    const int ch1 = a.ch1, ch2 = 2 * a.ch1;
 
     if (tid == 0) {
-        for (int i = 0; i < a.nslot; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], NW);
-        }
+        for (int i = 0; i < NW * a.nsw; ++i) mbar_init(&full[i], 1);
         for (int i = 0; i < 4; ++i) ms->flags[i] = 0;
-        ms->nU = 0;  // read by the producer even when the consumers abort before routing
+        ms->nU = 0;
         mbar_init(&ms->cbar, 1);
+        mbar_init(&ms->stage_full, 1);
         mbar_fence_init();
     }
     __syncthreads();
     STAMP(13);
-
-    if (warp == NW) {
-        // ==================================================================== producer
-        // Lane 0 issues every copy; the whole warp meets the consumers at the
-        // routing hand-off (named barrier 2) at one convergent point.
-        int64_t u = 0;
+    if (tid == 0) {
+        // preamble stage: activation rows, this CTA's router rows and (last CTA) the shared-gate row
+        const uint32_t xb = (uint32_t)a.M * a.H * 2;
+        const int re = min(rr1, a.E);
+        const uint32_t rb = re > rr0 ? (uint32_t)(re - rr0) * a.H * 2 : 0u;
+        const uint32_t gsb = rr1 > a.E ? (uint32_t)a.H * 2 : 0u;
+        mbar_arrive_expect_tx(&ms->stage_full, xb + rb + gsb);
+        bulk_g2s(stage, a.x, xb, &ms->stage_full);
+        if (rb) bulk_g2s(stage + a.stage_r, a.router + (int64_t)rr0 * a.H, rb, &ms->stage_full);
+        if (gsb) bulk_g2s(stage + a.stage_r + rb, a.sgate, gsb, &ms->stage_full);
+    }
+    {
         bool bad = false;
-        auto issue = [&](int nspan, const uint8_t *const *src, const uint32_t *bytes) -> bool {
-            const int slot = (int)(u % a.nslot);
-            const int64_t use = u / a.nslot;
-            if (use > 0 && !mbar_wait(&empty[slot], (uint32_t)((use - 1) & 1), a.wait_data, vflags)) return false;
-            if (vflags[0]) return false;
-            uint32_t total = 0;
-            for (int i = 0; i < nspan; ++i) total += bytes[i];
-            mbar_arrive_expect_tx(&full[slot], total);
-            uint8_t *dst = ring + (size_t)slot * a.slot_bytes;
-            for (int i = 0; i < nspan; ++i) {
-                bulk_g2s(dst, src[i], bytes[i], &full[slot]);
-                dst += bytes[i];
-            }
-            ++u;
-            return true;
-        };
-        if (lane == 0) {
-            // 0. the activation rows, 8 rows per slot (bulk copies: the fragments are built from them)
-            for (int r0 = 0; !bad && r0 < a.M; r0 += 8) {
-                const uint8_t *src[1] = {reinterpret_cast<const uint8_t *>(a.x + (int64_t)r0 * a.H)};
-                const uint32_t bytes[1] = {(uint32_t)min(8, a.M - r0) * a.H * 2};
-                bad = !issue(1, src, bytes);
-            }
-            // 1. router rows
-            if (rr1 > rr0) {
-                const uint8_t *src[2];
-                uint32_t bytes[2];
-                int ns = 0;
-                const int re = min(rr1, a.E);
-                if (re > rr0) {
-                    src[ns] = reinterpret_cast<const uint8_t *>(a.router + (int64_t)rr0 * a.H);
-                    bytes[ns++] = (uint32_t)(re - rr0) * a.H * 2;
-                }
-                if (rr1 > a.E) {
-                    src[ns] = reinterpret_cast<const uint8_t *>(a.sgate);
-                    bytes[ns++] = (uint32_t)a.H * 2;
-                }
-                bad = !issue(ns, src, bytes);
-            }
-            // 2. shared-expert gate/up f-tiles
-            for (int g = c; !bad && g < nft_total_pre; g += a.ncta) {
-                const uint8_t *src[1] = {a.sgu + (int64_t)2 * g * gb_h};
-                const uint32_t bytes[1] = {(uint32_t)(2 * gb_h)};
-                bad = !issue(1, src, bytes);
-            }
-        }
-        STAMP(1);  // producer: pre-routing copies issued
-        // 3. wait for the consumers' routing decision
-        __syncwarp();
-        bar_sync(2, kThreads);
-        if (lane == 0 && !vflags[0] && !bad) {
-            // routing tables are valid only when the consumers finished the dispatch (no abort)
-            const int nU = min(max(ms->nU, 0), min(a.E, a.M * a.K));
-            // 4. routed gate/up f-tiles
-            const int p1 = a.nft_s + nU * a.nft;
-            int g = c;
-            while (g < a.nft_s) g += a.ncta;
-            for (; !bad && g < p1; g += a.ncta) {
-                const int i = g - a.nft_s;
-                const int e = ms->ulist[i / a.nft], ft = i % a.nft;
-                const uint8_t *src[1] = {a.gu + (int64_t)e * a.gu_stride + (int64_t)2 * ft * gb_h};
-                const uint32_t bytes[1] = {(uint32_t)(2 * gb_h)};
-                bad = !issue(1, src, bytes);
-            }
-            // 5. down-projection units
-            const int64_t q0 = ms->p2q[0], q1 = ms->p2q[1];
-            for (int64_t q = q0; !bad && q < q1; ++q) {
-                const int j = (int)(q / a.noct), oct = (int)(q % a.noct);
-                const bool sh = j == nU;
-                const int kc = sh ? a.kc_fs : a.kc_f;
-                const int64_t gb_f = (int64_t)kc * a.rec;
-                const int rg0 = oct * a.r2, nrg = min(a.r2, a.ng_d - rg0);
-                const uint8_t *base = sh ? a.sdn : a.dn + (int64_t)ms->ulist[j] * a.dn_stride;
-                const uint8_t *src[1] = {base + rg0 * gb_f};
-                const uint32_t bytes[1] = {(uint32_t)(nrg * gb_f)};
-                bad = !issue(1, src, bytes);
-            }
-            STAMP(3);  // producer: every copy issued
-        }
-        if (lane == 0) {
-            // No copy may still be landing in shared memory when the CTA exits (every path).
-            WaitCfg drain{int64_t(1) << 40, 1000000000ull};
-            for (int64_t sl = 0; sl < min64(u, a.nslot); ++sl) {
-                const int64_t last_use = (u - 1 - sl) / a.nslot;
-                mbar_wait(&full[sl], (uint32_t)(last_use & 1), drain, nullptr);
-            }
-            if (bad && !vflags[0]) {
-                raise_status(a.status, kStatusTimeout);
-                vflags[0] = 1;
-            }
-        }
-        __syncwarp();
-    } else {
-        // =================================================================== consumers
-        bool dispatched = false;
-        bool bad = false;
-        int64_t u = 0;
         const uint2 *frag2 = reinterpret_cast<const uint2 *>(frag);
         const int ngrp_rows = a.M > 8 ? 3 : 1;
         auto abort_all = [&]() {
@@ -302,18 +242,121 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
                 raise_status(a.status, kStatusTimeout);
             }
         };
-        auto wait_slot = [&](int64_t uu) -> int {
-            const int slot = (int)(uu % a.nslot);
-            if (!bad)
-                bad = !__all_sync(0xffffffffu,
-                                  mbar_wait(&full[slot], (uint32_t)((uu / a.nslot) & 1), a.wait_data, nullptr));
-            return slot;
+        // A warp that gives up marks the CTA aborted; the other warps' waits see the flag and stop, and
+        // the CTA-wide checks turn it into an exit.
+        auto abort_warp = [&]() {
+            bad = true;
+            if (lane == 0) {
+                vflags[0] = 1;
+                raise_status(a.status, kStatusTimeout);
+            }
         };
-        // A warp whose data never arrived keeps the slot, so the producer cannot
-        // start a second copy into memory that a first copy may still be filling.
-        auto release_slot = [&](int slot) {
+        auto check_abort = [&]() {
+            if (!bad && vflags[0]) bad = true;
+        };
+        // ---- this warp's stream of weight chunks (see the comment above the kernel). The cursor is
+        //      warp-uniform (every lane computes it); lane 0 issues. The stream is a sequence of
+        //      segments (a phase-1 unit: gate and up row groups; a phase-2 row group), each issued in
+        //      chunks of s_ch records.
+        int cu = 0, cu_slot = 0;                 // items consumed, slot of the next one
+        uint32_t cu_par = 0;                     // parity of that slot's next fill
+        int iss = 0, is_slot = 0;                // items issued, slot of the next one
+        const uint8_t *sa = nullptr, *sb = nullptr;  // segment sources: gate (or row group), up (or none)
+        int s_left = 0;                          // records of the segment not yet issued
+        int s_ch = 0;                            // records per chunk
+        uint32_t s_b = 0;                        // bytes of a full chunk of one source
+        bool s_live = false;
+        int u1 = 0, n1u = 0, g1 = 0;             // phase 1: units started, this warp's units, next unit's entry
+        int q2 = 0, q2end = 0, j2 = 0, oct2 = 0; // phase 2: next unit (and its expert, octet), range end
+        int nUl = 0;
+        uint8_t *const my_slots = ring + (size_t)warp * a.nsw * a.slot_bytes;
+        uint64_t *const my_full = full + warp * a.nsw;
+        // Next segment of the stream: a phase-1 unit (gate and up row groups of an f-tile), then the
+        // phase-2 row groups oct * r2 + warp of the CTA's units. Once per segment (not per chunk).
+        auto next_segment = [&]() {
+            s_live = true;
+            if (u1 < n1u) {
+                const P1Tile pt = p1_tile(g1, a.nft_s, a.nft);
+                const uint8_t *base = pt.sh ? a.sgu : a.gu + (int64_t)ms->ulist[pt.jrow] * a.gu_stride;
+                sa = base + (int64_t)(2 * pt.ft) * gb_h;
+                sb = sa + gb_h;
+                s_left = a.kc_h;
+                s_ch = ch1;
+                ++u1;
+                g1 += NW * a.ncta;
+                return;
+            }
+            // units whose octet has no row group for this warp are skipped (only an expert's last octet)
+            while (q2 < q2end && warp >= min(a.r2, a.ng_d - oct2 * a.r2)) {
+                ++q2;
+                if (++oct2 == a.noct) {
+                    oct2 = 0;
+                    ++j2;
+                }
+            }
+            if (q2 >= q2end) {
+                s_live = false;
+                return;
+            }
+            const bool sh = j2 == nUl;
+            s_left = sh ? a.kc_fs : a.kc_f;
+            const uint8_t *base = sh ? a.sdn : a.dn + (int64_t)ms->ulist[j2] * a.dn_stride;
+            sa = base + (int64_t)(oct2 * a.r2 + warp) * s_left * a.rec;
+            sb = nullptr;
+            s_ch = ch2;
+            ++q2;
+            if (++oct2 == a.noct) {
+                oct2 = 0;
+                ++j2;
+            }
+        };
+        // Issues the stream's next chunk (if any) into slot is_slot; warp-uniform.
+        auto issue_next = [&]() {
+            if (s_left <= 0) {
+                next_segment();
+                if (!s_live) return;
+                s_b = (uint32_t)s_ch * a.rec;
+            }
+            const uint32_t b = s_left >= s_ch ? s_b : (uint32_t)s_left * a.rec;
+            if (lane == 0) {
+                uint8_t *dst = my_slots + (size_t)is_slot * a.slot_bytes;
+                uint64_t *fb = my_full + is_slot;
+                fence_proxy_async_shared();  // this warp's reads of the slot come first
+                mbar_arrive_expect_tx(fb, sb ? 2 * b : b);
+                bulk_g2s(dst, sa, b, fb);
+                if (sb) bulk_g2s(dst + b, sb, b, fb);
+            }
+            sa += b;
+            if (sb) sb += b;
+            s_left -= s_ch;
+            ++iss;
+            if (++is_slot == a.nsw) is_slot = 0;
+        };
+        // trace builds: per-phase durations of warp 0 accumulated in registers: [0] phase-1 data waits,
+        // [1] phase-1 MMA sections, [2] phase-2 data waits, [3] phase-1 refills, [4] phase-1 chunks
+        unsigned long long tacc[10] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0};  // [5..9]: phase-2 MMA, refills, setups, units, experts
+        int tslot = 0;
+        // Waits for the next item; a warp whose data never came stops issuing and keeps its copies
+        // in the drain at exit.
+        auto take_item = [&]() -> const uint8_t * {
+            check_abort();
+            [[maybe_unused]] const unsigned long long tw0 = BFP_TRACE_NOW();
+            if (!bad && !__all_sync(0xffffffffu, mbar_wait(my_full + cu_slot, cu_par, a.wait_data, vflags)))
+                abort_warp();
+            tacc[tslot] += BFP_TRACE_NOW() - tw0;
+            return my_slots + (size_t)cu_slot * a.slot_bytes;
+        };
+        // Done with the item: refill its slot with the item nsw further on. After an abort the
+        // item counts as unconsumed, so the drain at exit waits for its copy.
+        auto give_item = [&]() {
             __syncwarp();
-            if (lane == 0 && !bad) mbar_arrive(&empty[slot]);
+            if (bad) return;
+            issue_next();
+            ++cu;
+            if (++cu_slot == a.nsw) {
+                cu_slot = 0;
+                cu_par ^= 1u;
+            }
         };
 
         // Bulk copies issued by the consumers themselves (data other CTAs wrote, already acquired):
@@ -323,40 +366,6 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
             if (!bad)
                 bad = !__all_sync(0xffffffffu, mbar_wait(&ms->cbar, cphase & 1u, a.wait_data, nullptr));
             ++cphase;
-        };
-
-        // ---- activation fragments (MoE input: x, or bf16(RMSNorm(h)) in stack mode), from the rows
-        //      the producer staged in the first slots (units 0 .. nx-1 are slots 0 .. nx-1)
-        {
-            const int nx = (a.M + 7) / 8;
-            for (int i = 0; i < nx; ++i) wait_slot(u + i);
-            const uint16_t *xs = reinterpret_cast<const uint16_t *>(ring);
-            build_act_frags<NC>(xs, a.H, 8, a.slot_bytes / 2, a.M, a.H, a.kbp_h, NGRP, a.norm != 0, a.eps, frag,
-                                ms->shift_x, ms->inv, tid, warp, lane);
-            for (int i = 0; i < nx; ++i) release_slot((int)((u + i) % a.nslot));
-            u += nx;
-        }
-        STAMP(1);  // activation fragments built
-
-        // ---- phase-1 unit: one f-tile (16 ffn rows) of gate and up; h = silu(gate) * up for the
-        //      rows in rowmask, slot table row jrow. Returns false on abort (same answer in all warps).
-        // One CTA barrier per unit: the reduction scratch and the per-row max |h| are double-
-        // buffered; a unit's row maxima go to the workspace at the next unit's barrier (or at
-        // flush_pending). Cross-CTA ordering of h comes from the grid barrier after phase 1.
-        int p1n = 0;  // phase-1 units done by this CTA (selects the buffers)
-        int pending_jrow = -1, pending_buf = 0;
-        uint32_t pending_mask = 0;
-        if (tid < 2 * kMaxRows) (&ms->maxbits[0][0])[tid] = 0u;
-        auto signal_pending = [&]() {
-            if (pending_jrow >= 0 && tid < a.M && ((pending_mask >> tid) & 1u)) {
-                atomicMax(&a.hmax[tid * (a.K + 1) + ms->uslot[pending_jrow][tid]], ms->maxbits[pending_buf][tid]);
-                ms->maxbits[pending_buf][tid] = 0u;
-            }
-            pending_jrow = -1;
-        };
-        auto flush_pending = [&]() {
-            bar_sync(1, NC);
-            signal_pending();
         };
         // Grid barrier over the consumer threads of every CTA, on a workspace counter.
         // Returns false on abort (same answer in every consumer thread of the CTA).
@@ -370,84 +379,104 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
             }
             return !bar_or(1, NC, !ok || bad);
         };
-        auto run_phase1 = [&](int eid, int ft, uint32_t rowmask, int jrow) -> bool {
-            if (p1n == 2) STAMP(21);  // third phase-1 unit: start
-            const int slot = wait_slot(u);
-            if (p1n == 2) STAMP(22);  // ... its data landed
-            const uint8_t *slotp = ring + (size_t)slot * a.slot_bytes;
+
+        // ---- activation fragments (MoE input: x, or bf16(RMSNorm(h)) in stack mode), from the rows
+        //      the producer staged
+        if (!__all_sync(0xffffffffu, mbar_wait(&ms->stage_full, 0u, a.wait_data, nullptr))) bad = true;
+        STAMP(2);  // stage landed
+        build_act_frags<NC>(reinterpret_cast<const uint16_t *>(stage), a.H, kMaxRows, 0, a.M, a.H, a.kbp_h, NGRP,
+                            a.norm != 0, a.eps, frag, ms->shift_x, ms->inv, tid, warp, lane);
+        STAMP(1);  // activation fragments built
+
+        // ---- phase-1 unit (run by one warp): f-tile of gate and up over all of k; h = silu(gate) * up
+        //      for the rows in the unit's row mask, to the workspace; row maxima of |h| to hmax.
+        auto run_p1_unit = [&](int g) {
+            const P1Tile pt = p1_tile(g, a.nft_s, a.nft);
+            const uint32_t rowmask = ms->umask[pt.jrow];
             const uint32_t gm = (((rowmask & 0xFFu) ? 1u : 0u) | ((rowmask & 0xFF00u) ? 2u : 0u)) & ngrp_rows;
+            bool both = false;
+            if constexpr (NGRP == 2) both = gm == 3u;
+            const int gsel = gm == 2u ? 1 : 0;  // the one activation group holding every row otherwise
+            const uint2 *fg = frag2 + (int64_t)gsel * a.kbp_h * kWarp;
             float acc[2][NGRP][4];
 #pragma unroll
             for (int r = 0; r < 2; ++r)
 #pragma unroll
-                for (int g = 0; g < NGRP; ++g)
+                for (int gg = 0; gg < NGRP; ++gg)
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) acc[r][g][i] = 0.f;
-            if (!bad) {
-                bool both = false;
-                if constexpr (NGRP == 2) both = gm == 3u;
-                if (both) {
-                    for (int ch = warp; ch < a.kc_h; ch += NW) {
-                        const uint8_t *recs[2] = {slotp + (size_t)ch * a.rec, slotp + gb_h + (size_t)ch * a.rec};
-                        mma_records<FMT, NGRP, 2, false>(recs, frag2, nullptr, a.kbp_h, ch * CB, lane, ms->esc[warp],
-                                                         acc);
-                    }
-                } else {
-                    // one activation group holds every row of this unit: compute only that one
-                    const int gsel = gm == 2u ? 1 : 0;
-                    const uint2 *fg = frag2 + (int64_t)gsel * a.kbp_h * kWarp;
-                    float a1[2][1][4] = {};
-                    for (int ch = warp; ch < a.kc_h; ch += NW) {
-                        const uint8_t *recs[2] = {slotp + (size_t)ch * a.rec, slotp + gb_h + (size_t)ch * a.rec};
-                        mma_records<FMT, 1, 2, false>(recs, fg, nullptr, a.kbp_h, ch * CB, lane, ms->esc[warp], a1);
-                    }
-#pragma unroll
-                    for (int r = 0; r < 2; ++r)
-#pragma unroll
-                        for (int g = 0; g < NGRP; ++g)
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) acc[r][g][i] = g == gsel ? a1[r][0][i] : 0.f;
+                    for (int i = 0; i < 4; ++i) acc[r][gg][i] = 0.f;
+            float a1[2][1][4] = {};
+            // each chunk: n gate records, then n up records; one loop per group count, so that each
+            // keeps only its own accumulators live
+            if (both) {
+                for (int k0 = 0; k0 < a.kc_h; k0 += ch1) {
+                    const int n = min(ch1, a.kc_h - k0);
+                    const uint8_t *sp = take_item();
+                    if (!bad)
+                        for (int ch = 0; ch < n; ++ch) {
+                            const uint8_t *recs[2] = {sp + (size_t)ch * a.rec, sp + (size_t)(n + ch) * a.rec};
+                            mma_records<FMT, NGRP, 2, false>(recs, frag2, nullptr, a.kbp_h, (k0 + ch) * CB, lane,
+                                                             ms->esc[warp], acc);
+                        }
+                    give_item();
+                }
+            } else {
+                for (int k0 = 0; k0 < a.kc_h; k0 += ch1) {
+                    const int n = min(ch1, a.kc_h - k0);
+                    const uint8_t *sp = take_item();
+                    [[maybe_unused]] const unsigned long long tm0 = BFP_TRACE_NOW();
+                    if (!bad)
+                        for (int ch = 0; ch < n; ++ch) {
+                            const uint8_t *recs[2] = {sp + (size_t)ch * a.rec, sp + (size_t)(n + ch) * a.rec};
+                            mma_records<FMT, 1, 2, false>(recs, fg, nullptr, a.kbp_h, (k0 + ch) * CB, lane,
+                                                          ms->esc[warp], a1);
+                        }
+                    __syncwarp();
+                    tacc[1] += BFP_TRACE_NOW() - tm0;
+                    tacc[4] += 1;
+                    [[maybe_unused]] const unsigned long long tg0 = BFP_TRACE_NOW();
+                    give_item();
+                    tacc[3] += BFP_TRACE_NOW() - tg0;
                 }
             }
-            release_slot(slot);
-            ++u;
-            if (p1n == 2) STAMP(23);  // ... MMAs done (warp 0)
-            constexpr int TILE = NGRP * 128;
-            float *buf = scr + (p1n & 1) * (NW * 2 * TILE);
-            ++p1n;
-            float *mine = buf + warp * 2 * TILE;
+            if (bad) return;
 #pragma unroll
-            for (int r = 0; r < 2; ++r)
+            for (int gg = 0; gg < NGRP; ++gg) {
+                if (!both && gg > 0) continue;
+                const int grp = both ? gg : gsel;
+                uint32_t me = 0u, mo = 0u;  // max |h| of rows 8 grp + 2 (lane & 3) and the next one
 #pragma unroll
-                for (int g = 0; g < NGRP; ++g)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) mine[r * TILE + (g * 4 + i) * kWarp + lane] = acc[r][g][i];
-            if (bar_or(1, NC, bad)) return false;
-            if (p1n == 3) STAMP(24);  // ... every warp's MMAs done
-            signal_pending();
-            if (tid < TILE) {
-                float va = 0.f, vb = 0.f;
-                for (int w = 0; w < NW; ++w) {
-                    va += buf[w * 2 * TILE + tid];
-                    vb += buf[w * 2 * TILE + TILE + tid];
+                for (int i = 0; i < 4; ++i) {
+                    const float va = both ? acc[0][gg][i] : a1[0][0][i];
+                    const float vb = both ? acc[1][gg][i] : a1[1][0][i];
+                    const int r = acc_xrow(lane, grp, i);
+                    if (r < a.M && ((rowmask >> r) & 1u)) {
+                        const int sh = 24 - (MB - 1) - ms->shift_x[r];
+                        const float ga = mul_pow2(va, sh), ub = mul_pow2(vb, sh);
+                        const float hv = ga / (1.0f + expf(-ga)) * ub;  // silu(gate) * up
+                        const int f = pt.ft * 16 + acc_wrow(lane, i);
+                        a.hbuf[((int64_t)r * (a.K + 1) + ms->uslot[pt.jrow][r]) * a.Fmax + f] = hv;
+                        const uint32_t hb = __float_as_uint(fabsf(hv));
+                        if (i & 1)
+                            mo = max(mo, hb);
+                        else
+                            me = max(me, hb);
+                    }
                 }
-                const int grp = tid >> 7, i = (tid >> 5) & 3, ln = tid & 31;
-                const int r = acc_xrow(ln, grp, i);
-                const int f = ft * 16 + acc_wrow(ln, i);
-                if (r < a.M && ((rowmask >> r) & 1u)) {
-                    const int sh = 24 - (MB - 1) - ms->shift_x[r];
-                    const float ga = mul_pow2(va, sh), ub = mul_pow2(vb, sh);
-                    const float hv = ga / (1.0f + expf(-ga)) * ub;  // silu(gate) * up
-                    const int s = ms->uslot[jrow][r];
-                    a.hbuf[((int64_t)r * (a.K + 1) + s) * a.Fmax + f] = hv;
-                    atomicMax(&ms->maxbits[(p1n - 1) & 1][r], __float_as_uint(fabsf(hv)));
+                // the eight lanes with equal lane & 3 hold the same two rows
+#pragma unroll
+                for (int o = 4; o < kWarp; o <<= 1) {
+                    me = max(me, __shfl_xor_sync(0xffffffffu, me, o));
+                    mo = max(mo, __shfl_xor_sync(0xffffffffu, mo, o));
+                }
+                if (lane < 4) {
+                    const int re = 8 * grp + 2 * lane, ro = re + 1;
+                    if (re < a.M && ((rowmask >> re) & 1u))
+                        atomicMax(&a.hmax[re * (a.K + 1) + ms->uslot[pt.jrow][re]], me);
+                    if (ro < a.M && ((rowmask >> ro) & 1u))
+                        atomicMax(&a.hmax[ro * (a.K + 1) + ms->uslot[pt.jrow][ro]], mo);
                 }
             }
-            if (p1n == 3) STAMP(25);  // ... reduction + h stores issued
-            pending_jrow = jrow;
-            pending_mask = rowmask;
-            pending_buf = (p1n - 1) & 1;
-            return true;
         };
 
         // ---- 1. router rows: logits from the bf16 router rows (shared memory) and the activation
@@ -456,9 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
         //      own fragment words (rows 8grp+g, cols 2t|2t+1 and 2t+8|2t+9 of each block): no bank
         //      conflicts; the four lanes of a row add up with two shuffles; segments are summed in order.
         if (rr1 > rr0) {
-            const int slot = wait_slot(u);
-            STAMP(2);  // router rows landed
-            const uint16_t *wr = reinterpret_cast<const uint16_t *>(ring + (size_t)slot * a.slot_bytes);
+            const uint16_t *wr = reinterpret_cast<const uint16_t *>(stage + a.stage_r);
             const int nrows = rr1 - rr0;
             const int kb = a.H / 16;
             const int ngrp = (a.M + 7) / 8;
@@ -497,8 +524,6 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
                 if (row < a.E && a.rbias) l += a.rbias[row];
                 a.logits[(int64_t)r * E1 + row] = l;
             }
-            release_slot(slot);
-            ++u;
         }
         if (bar_or(1, NC, bad)) {
             abort_all();
@@ -509,22 +534,6 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
             red_release_add(&a.ctrl[0], 1u);
         }
 
-        // ---- 2. shared-expert gate/up f-tiles (all rows use the shared expert)
-        for (int g = c; g < a.nft_s; g += a.ncta) {
-            if (tid == 0) {
-                ms->umask[kMaxExperts] = (a.M >= 32 ? 0xFFFFFFFFu : ((1u << a.M) - 1u));
-                for (int r = 0; r < a.M; ++r) ms->uslot[kMaxExperts][r] = (int8_t)a.K;
-            }
-            bar_sync(1, NC);
-            if (!run_phase1(a.E, g, ms->umask[kMaxExperts], kMaxExperts)) {
-                abort_all();
-                goto done;
-            }
-        }
-
-        STAMP(3);  // router logits published
-        flush_pending();
-        STAMP(4);  // shared-expert f-tiles done
 
         // ---- 3. routing: wait for every CTA's router rows, then top-k and the expert union
         {
@@ -551,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
             // index), and the winner records its expert and logit and drops its head.
             // Slot 0 is the row maximum, so p_s = exp(l_s - l_0) and w_s = p_s / sum of p.
             {
-                constexpr int RPW = kMaxRows / NW;
+                constexpr int RPW = (kMaxRows + NW - 1) / NW;
                 uint32_t key[RPW][8];
                 int qi[RPW][8];
 #pragma unroll
@@ -639,8 +648,14 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
                 atomicOr(&ms->umask[j], 1u << r);
                 ms->uslot[j][r] = (int8_t)s;
             }
-            if (tid < a.M) ms->uslot[nU][tid] = (int8_t)a.K;
-            if (tid == 0) ms->umask[nU] = (1u << a.M) - 1u;
+            if (tid < a.M) {
+                ms->uslot[nU][tid] = (int8_t)a.K;
+                ms->uslot[kMaxExperts][tid] = (int8_t)a.K;
+            }
+            if (tid == 0) {
+                ms->umask[nU] = (1u << a.M) - 1u;
+                ms->umask[kMaxExperts] = (1u << a.M) - 1u;
+            }
             bar_sync(1, NC);
             // phase-2 shares: exclusive prefix of the unit costs over the union (warp scan), then this
             // CTA's range [first unit starting at >= total*c/ncta, ... >= total*(c+1)/ncta)
@@ -668,25 +683,27 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
             bar_sync(1, NC);
         }
         STAMP(6);  // top-k + union done
-        bar_arrive(2, kThreads);
-        dispatched = true;
+        // this warp's stream: its units and the CTA's phase-2 range are known now; fill its slots
+        // (every warp is past its reads of the stage, which the first slots may overlap)
+        nUl = ms->nU;
+        n1u = p1_warp_units(a.nft_s + nUl * a.nft, c, a.ncta, warp, NW);
+        g1 = c + warp * a.ncta;
+        q2end = (int)ms->p2q[1];
+        q2 = (int)ms->p2q[0];
+        j2 = q2 / a.noct;
+        oct2 = q2 % a.noct;
+        for (int i = 0; i < a.nsw; ++i) issue_next();
 
-        // ---- 4. routed gate/up f-tiles
+        // ---- 4. phase 1: this warp's units of the CTA's list [shared-expert f-tiles, routed f-tiles]
         {
-            const int nU = ms->nU;
-            const int p1 = a.nft_s + nU * a.nft;
-            int g = c;
-            while (g < a.nft_s) g += a.ncta;
-            for (; g < p1; g += a.ncta) {
-                const int i = g - a.nft_s;
-                const int j = i / a.nft, ft = i % a.nft;
-                if (!run_phase1(ms->ulist[j], ft, ms->umask[j], j)) {
-                    abort_all();
-                    goto done;
-                }
+            const int p1_total = a.nft_s + ms->nU * a.nft;
+            const int nmine = p1_warp_units(p1_total, c, a.ncta, warp, NW);
+            for (int k = 0; k < nmine; ++k) {
+                if (k == 1) STAMP(21);  // warp 0: second unit start
+                run_p1_unit(c + (warp + NW * k) * a.ncta);
             }
-            flush_pending();
-            STAMP(8);  // routed f-tiles done
+            STAMP(8);  // warp 0: phase-1 units done
+            tslot = 2;
             if (!grid_barrier(&a.ctrl[2])) {  // every CTA's h and row maxima written
                 abort_all();
                 goto done;
@@ -713,6 +730,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
                 const int Fe = sh ? a.Fs : a.F;
                 const int kc = sh ? a.kc_fs : a.kc_f, kbp = sh ? a.kbp_fs : a.kbp_f;
                 const uint32_t rowmask = ms->umask[j];
+                [[maybe_unused]] const unsigned long long tsu0 = BFP_TRACE_NOW();
+                const bool new_expert = j != cur;
                 if (j != cur) {
                     // every warp is done with the previous expert's fragments
                     if (bar_or(1, NC, bad)) {
@@ -780,49 +799,88 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
                     if (cur < 0) STAMP(10);  // first expert's h fragments ready
                     cur = j;
                 }
-                if (p2n == 0) STAMP(16);  // first phase-2 unit: start
-                const int slot = wait_slot(u);
-                if (p2n == 0) STAMP(17);  // ... its data landed
-                if (p2n == 1) STAMP(28);  // second unit: data landed
-                const uint8_t *slotp = ring + (size_t)slot * a.slot_bytes;
+                if (new_expert) {
+                    tacc[7] += BFP_TRACE_NOW() - tsu0;
+                    tacc[9] += 1;
+                }
+                tacc[8] += 1;
                 const int rg0 = oct * a.r2, nrg = min(a.r2, a.ng_d - rg0);
+                const bool mine = warp < nrg;
+                if (p2n == 0) STAMP(16);  // first phase-2 unit: start
                 float acc[1][NGRP][4];
 #pragma unroll
                 for (int g = 0; g < NGRP; ++g)
 #pragma unroll
                     for (int i = 0; i < 4; ++i) acc[0][g][i] = 0.f;
-                const bool mine = warp < nrg;
-                if (!bad && mine) {
-                    const uint8_t *rb = slotp + (size_t)warp * kc * a.rec;
+                if (mine) {
+                    // this warp's row group rg0 + warp of the unit, in chunks of ch2 records
                     const uint2 *hi2 = reinterpret_cast<const uint2 *>(hfrag);
                     const uint2 *lo2 = hi2 + NGRP * kbp * kWarp;
                     bool both = false;
                     if constexpr (NGRP == 2) both = !packed && gm2 == 3u;
+                    float a1[1][1][4] = {};
+                    // one chunk loop per path (the path is fixed per expert)
                     if (both) {
-                        for (int ch = 0; ch < kc; ++ch) {
-                            const uint8_t *recs[1] = {rb + (size_t)ch * a.rec};
-                            mma_records<FMT, NGRP, 1, true>(recs, hi2, lo2, kbp, ch * CB, lane, ms->esc[warp], acc);
+                        for (int k0 = 0; k0 < kc; k0 += ch2) {
+                            const int n = min(ch2, kc - k0);
+                            const uint8_t *rb = take_item();
+                            if (p2n == 0) STAMP(17);  // ... its first data landed (warp 0)
+                            [[maybe_unused]] const unsigned long long tm0 = BFP_TRACE_NOW();
+                            if (!bad)
+                                for (int ch = 0; ch < n; ++ch) {
+                                    const uint8_t *recs[1] = {rb + (size_t)ch * a.rec};
+                                    mma_records<FMT, NGRP, 1, true>(recs, hi2, lo2, kbp, (k0 + ch) * CB, lane,
+                                                                    ms->esc[warp], acc);
+                                }
+                            __syncwarp();
+                            tacc[5] += BFP_TRACE_NOW() - tm0;
+                            [[maybe_unused]] const unsigned long long tg0 = BFP_TRACE_NOW();
+                            give_item();
+                            tacc[6] += BFP_TRACE_NOW() - tg0;
+                        }
+                    } else if (packed) {
+                        // columns of group 0 only: hi in columns c, lo in columns c + 4
+                        for (int k0 = 0; k0 < kc; k0 += ch2) {
+                            const int n = min(ch2, kc - k0);
+                            const uint8_t *rb = take_item();
+                            if (p2n == 0) STAMP(17);
+                            [[maybe_unused]] const unsigned long long tm0 = BFP_TRACE_NOW();
+                            if (!bad)
+                                for (int ch = 0; ch < n; ++ch) {
+                                    const uint8_t *recs[1] = {rb + (size_t)ch * a.rec};
+                                    mma_records<FMT, 1, 1, false>(recs, hi2, nullptr, kbp, (k0 + ch) * CB, lane,
+                                                                  ms->esc[warp], a1);
+                                }
+                            __syncwarp();
+                            tacc[5] += BFP_TRACE_NOW() - tm0;
+                            [[maybe_unused]] const unsigned long long tg0 = BFP_TRACE_NOW();
+                            give_item();
+                            tacc[6] += BFP_TRACE_NOW() - tg0;
                         }
                     } else {
-                        // columns of group 0 only: hi and lo packed side by side (<= 4 rows) or hi + lo parts
-                        float a1[1][1][4] = {};
-                        if (packed) {
-                            for (int ch = 0; ch < kc; ++ch) {
-                                const uint8_t *recs[1] = {rb + (size_t)ch * a.rec};
-                                mma_records<FMT, 1, 1, false>(recs, hi2, nullptr, kbp, ch * CB, lane, ms->esc[warp], a1);
-                            }
-                        } else {
-                            for (int ch = 0; ch < kc; ++ch) {
-                                const uint8_t *recs[1] = {rb + (size_t)ch * a.rec};
-                                mma_records<FMT, 1, 1, true>(recs, hi2, lo2, kbp, ch * CB, lane, ms->esc[warp], a1);
-                            }
+                        for (int k0 = 0; k0 < kc; k0 += ch2) {
+                            const int n = min(ch2, kc - k0);
+                            const uint8_t *rb = take_item();
+                            if (p2n == 0) STAMP(17);
+                            [[maybe_unused]] const unsigned long long tm0 = BFP_TRACE_NOW();
+                            if (!bad)
+                                for (int ch = 0; ch < n; ++ch) {
+                                    const uint8_t *recs[1] = {rb + (size_t)ch * a.rec};
+                                    mma_records<FMT, 1, 1, true>(recs, hi2, lo2, kbp, (k0 + ch) * CB, lane,
+                                                                 ms->esc[warp], a1);
+                                }
+                            __syncwarp();
+                            tacc[5] += BFP_TRACE_NOW() - tm0;
+                            [[maybe_unused]] const unsigned long long tg0 = BFP_TRACE_NOW();
+                            give_item();
+                            tacc[6] += BFP_TRACE_NOW() - tg0;
                         }
+                    }
+                    if (!both) {
 #pragma unroll
                         for (int i = 0; i < 4; ++i) acc[0][0][i] = a1[0][0][i];
                     }
                 }
-                release_slot(slot);
-                ++u;
                 if (p2n == 0) STAMP(18);  // ... warp 0's MMAs done
                 if (p2n == 1) STAMP(29);
                 if (!bad && mine) {
@@ -850,6 +908,16 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
                 ++p2n;
             }
             STAMP(11);  // down projections done
+            BFP_TRACE_SET(40, tacc[0]);
+            BFP_TRACE_SET(41, tacc[1]);
+            BFP_TRACE_SET(42, tacc[2]);
+            BFP_TRACE_SET(44, tacc[3]);
+            BFP_TRACE_SET(43, tacc[4] * 1000);
+            BFP_TRACE_SET(45, tacc[5]);
+            BFP_TRACE_SET(46, tacc[6]);
+            BFP_TRACE_SET(47, tacc[7]);
+            BFP_TRACE_SET(35, tacc[8] * 1000);
+            BFP_TRACE_SET(36, tacc[9] * 1000);
             if (!grid_barrier(&a.ctrl[3])) {  // every (row, slot) partial written
                 abort_all();
                 goto done;
@@ -876,10 +944,23 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
             }
         }
     done:
-        if (!dispatched) bar_arrive(2, kThreads);
-        if (tid == 0 && cphase > 0) {  // no copy of ours may still be landing when the CTA exits
+        // No copy may still be landing in shared memory when the CTA exits (every path): this warp's
+        // issued but unconsumed items, the stage, the consumers' own copies.
+        {
             WaitCfg drain{int64_t(1) << 40, 1000000000ull};
-            mbar_wait(&ms->cbar, (cphase - 1) & 1u, drain, nullptr);
+            int sl = cu_slot;
+            uint32_t par = cu_par;
+            for (int k = cu; k < iss; ++k) {
+                if (lane == 0) mbar_wait(my_full + sl, par, drain, nullptr);
+                if (++sl == a.nsw) {
+                    sl = 0;
+                    par ^= 1u;
+                }
+            }
+            if (tid == 0) {
+                mbar_wait(&ms->stage_full, 0u, drain, nullptr);
+                if (cphase > 0) mbar_wait(&ms->cbar, (cphase - 1) & 1u, drain, nullptr);
+            }
         }
     }
     __syncthreads();
@@ -905,7 +986,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const MoeArgs a)
 // ----------------------------------------------------------------------------
 struct MoePlan {
     Geometry gu, dn, sgu, sdn;
-    int ngrp, ncta, nslot, slot_bytes, frag_bytes, scr_bytes, r2, noct, Fmax;
+    int ngrp, ncta, nsw, ch1, slot_bytes, frag_bytes, scr_bytes, r2, noct, Fmax, stage_off, stage_r;
     size_t smem;
     size_t off_ctrl, off_hmax, off_logits, off_hbuf, off_part, ws_bytes;
 };
@@ -950,28 +1031,35 @@ static int plan_moe(const bfp_moe_layer *L, int m, MoePlan *p) {
     p->Fmax = std::max(L->ffn, L->shared_ffn);
     p->frag_bytes = (int)std::max<int64_t>((int64_t)p->ngrp * kbp_h * 256,
                                            (int64_t)2 * p->ngrp * std::max(kbp_f, kbp_fs) * 256);
-    p->scr_bytes = (int)align_up(std::max<size_t>(std::max<size_t>((size_t)2 * kConsumerWarps * 2 * p->ngrp * 128 * 4,
-                                                                    (size_t)m * (L->n_experts + 1) * 4 + 16),
-                                                  (size_t)m * p->Fmax * 4),
-                                 128);
-    const int64_t gbh = p->gu.group_bytes();
-    const int64_t gbf = std::max(p->dn.group_bytes(), p->sdn.group_bytes());
-    p->r2 = (int)std::max<int64_t>(1, std::min<int64_t>(std::min<int64_t>(kConsumerWarps, 2 * gbh / gbf), p->dn.ng));
-    p->noct = (int)((p->dn.ng + p->r2 - 1) / p->r2);
     const int nft = L->ffn / 16, nft_s = L->shared_ffn / 16;
     // grid: enough CTAs for the phase-1 units of the worst-case union, at most one per SM
     const int64_t worst_units = nft_s + (int64_t)std::min(L->n_experts, m * L->top_k) * nft;
     p->ncta = (int)std::max<int64_t>(1, std::min<int64_t>(di.sms, worst_units));
-    const int rows_per_cta = (L->n_experts + 1 + p->ncta - 1) / p->ncta;
-    int64_t slot = std::max<int64_t>(2 * gbh, (int64_t)p->r2 * gbf);
-    slot = std::max<int64_t>(slot, (int64_t)rows_per_cta * L->hidden * 2);
-    slot = std::max<int64_t>(slot, (int64_t)std::min(m, 8) * L->hidden * 2);  // staged activation rows
-    slot = (int64_t)align_up((size_t)slot, 128);
-    const size_t fixed = align_up(align_up((size_t)p->frag_bytes + p->scr_bytes + sizeof(MoeMisc), 16) + 16 * 8, 128);
-    if ((int64_t)di.smem_optin < (int64_t)fixed + 2 * slot) return fail(BFP_ESHAPE, "layer too large for shared memory");
-    p->nslot = (int)std::min<int64_t>(8, ((int64_t)di.smem_optin - (int64_t)fixed) / slot);
-    p->slot_bytes = (int)slot;
-    p->smem = fixed + (size_t)p->nslot * slot;
+    const int rows_per_cta = (L->n_experts + 1 + p->ncta - 1) / p->ncta;  // router rows (+ gate row) per CTA
+    // scratch: logits of every row, the h rows of one phase-2 expert, router partial sums
+    p->scr_bytes = (int)align_up(std::max<size_t>(std::max<size_t>((size_t)m * (L->n_experts + 1) * 4 + 16,
+                                                                    (size_t)m * p->Fmax * 4),
+                                                  (size_t)std::max(kMoeWarps, 2 * rows_per_cta) * 8 * 4),
+                                 128);
+    // phase 2: units of up to one row group per consumer warp
+    p->r2 = (int)std::min<int64_t>(kMoeWarps, p->dn.ng);
+    p->noct = (int)((p->dn.ng + p->r2 - 1) / p->r2);
+    // per-warp slots: a phase-1 chunk is ch1 records of a gate row group and the same of its up row
+    // group, a phase-2 chunk 2 * ch1 records of one row group
+    p->ch1 = (int)std::min<int64_t>(4, p->gu.kc);
+    p->slot_bytes = 2 * p->ch1 * p->gu.rec;
+    // the preamble stage (activation rows, then the CTA's router rows) takes the ring's last bytes
+    p->stage_r = (int)align_up((size_t)m * L->hidden * 2, 16);
+    const size_t stage_bytes = align_up((size_t)p->stage_r + (size_t)rows_per_cta * L->hidden * 2, 128);
+    const size_t base = align_up((size_t)p->frag_bytes + p->scr_bytes + sizeof(MoeMisc), 16);
+    const int64_t avail = (int64_t)di.smem_optin - (int64_t)base - 128;
+    const int64_t per_slot_row = (int64_t)kMoeWarps * (p->slot_bytes + 8);  // one slot per warp + barrier
+    p->nsw = (int)std::min<int64_t>(8, avail / per_slot_row);
+    if (p->nsw < 2) return fail(BFP_ESHAPE, "layer too large for shared memory");
+    const size_t ring = (size_t)kMoeWarps * p->nsw * p->slot_bytes;
+    if (ring < stage_bytes) return fail(BFP_ESHAPE, "activation rows do not fit in shared memory");
+    p->stage_off = (int)(ring - stage_bytes);
+    p->smem = align_up(base + 8 * (size_t)kMoeWarps * p->nsw, 128) + ring;
     // workspace
     size_t o = kWsHeader;
     p->off_ctrl = o;
@@ -995,7 +1083,7 @@ static int launch_moe_t(const MoeArgs &a, const MoePlan &p, cudaStream_t st) {
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(moe_layer)");
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.ncta);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(kMoeThreads);
     cfg.dynamicSmemBytes = p.smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -1069,8 +1157,11 @@ static int moe_launch(const bfp_moe_layer *L, const uint16_t *x, int m, int norm
     a.r2 = p.r2;
     a.noct = p.noct;
     a.Fmax = p.Fmax;
-    a.nslot = p.nslot;
+    a.nsw = p.nsw;
+    a.ch1 = p.ch1;
     a.slot_bytes = p.slot_bytes;
+    a.stage_off = p.stage_off;
+    a.stage_r = p.stage_r;
     a.frag_bytes = p.frag_bytes;
     a.scr_bytes = p.scr_bytes;
     a.wait = wait_cfg();
