@@ -144,7 +144,8 @@ __global__ void __launch_bounds__(kThreads, 1) bfp_linear_kernel(const LinearArg
                 if (flags[0]) break;
                 const uint32_t bytes = (uint32_t)len * a.rec;
                 mbar_arrive_expect_tx(&full[slot], bytes);
-                bulk_g2s(ring + (size_t)slot * a.slot_bytes, a.w + (rg * a.kc + c0) * a.rec, bytes, &full[slot]);
+                bulk_g2s_hint(ring + (size_t)slot * a.slot_bytes, a.w + (rg * a.kc + c0) * a.rec, bytes, &full[slot],
+                              l2_evict_first());  // the weights are read once per launch
                 pos += len;
                 ++u;
             }

@@ -126,27 +126,38 @@ __device__ __forceinline__ void mma_records(const uint8_t *const recs[NREC], con
 __device__ __forceinline__ int acc_wrow(int lane, int i) { return (lane >> 2) + 8 * (i >> 1); }
 __device__ __forceinline__ int acc_xrow(int lane, int grp, int i) { return 8 * grp + 2 * (lane & 3) + (i & 1); }
 
-// Activation fragments for rows r < m of bf16 x (row stride ldx, k columns):
+// Activation fragments for rows r < m of bf16 x (row stride ldx, k columns, k % 16 == 0):
 // optional RMS normalisation t = bf16(x / sqrt(mean(x^2) + eps)) (fp32), then
 // each row scaled by the power of two shift[r] that puts its max |value| in
 // [2^14, 2^15) and rounded to fp16 (exact for every bf16 value above
 // 2^-14 of the row maximum). Rows >= m and blocks >= k/16 are zero.
 // Row r of x is at x + (r / rpp) * part + (r % rpp) * ldx (elements): x may be one strided array
 // (rpp >= m) or, when staged in shared memory, several slots of rpp rows each.
-// One warp per row: the row is read once (16-byte vectors, k % 8 == 0, 16-byte aligned rows),
-// its max (and sum of squares) reduced, then the lane's own values written as fragment words.
-// Called by the NC consumer threads only (named barrier 1).
+// One warp per row: the row's statistics from 16-byte vectors, then lane (bb, t) = (lane >> 2,
+// lane & 3) assembles whole fragments (cols 2t|2t+1 and 2t+8|2t+9 of blocks bb, bb + 8, ...) and
+// stores each with one 8-byte store; the XOR swizzle spreads a warp's stores over the banks.
+// Only the padding (rows >= m, blocks >= k/16) is zeroed. Called by the NC threads of the
+// caller's named barrier 1.
 template <int NC>
 __device__ __noinline__ void build_act_frags(const uint16_t *x, int64_t ldx, int rpp, int64_t part, int m, int k,
                                              int kbp, int ngrp, bool norm, float eps, uint32_t *frag, int *shift,
                                              float *inv_out, int tid, int warp, int lane) {
     constexpr int B = 8;  // 16-byte vectors per lane held at once (k <= 8 * 8 * 32 = 2048 in one pass)
-    const int nvec = ngrp * kbp * kWarp * 2 / 4;
-    for (int i = tid; i < nvec; i += NC) reinterpret_cast<uint4 *>(frag)[i] = make_uint4(0, 0, 0, 0);
-    bar_sync(1, NC);
+    const int kb = k / 16;
+    uint2 *f2 = reinterpret_cast<uint2 *>(frag);
+    if (m < 8 * ngrp || kb < kbp) {
+        // fragments that no row writes: rows m .. 8 ngrp - 1, blocks kb .. kbp - 1
+        for (int i = tid; i < ngrp * kbp * kWarp; i += NC) {
+            const int gb = i / kWarp, sl = i % kWarp, b = gb % kbp, grp = gb / kbp;
+            const int r = 8 * grp + ((sl ^ frag_swz(b)) >> 2);
+            if (r >= m || b >= kb) f2[i] = make_uint2(0u, 0u);
+        }
+    }
     const int nv = k / 8;  // uint4 per row
+    const int bb = lane >> 2, t = lane & 3;
     for (int r = warp; r < m; r += NC / kWarp) {
-        const uint4 *xr = reinterpret_cast<const uint4 *>(x + (r / rpp) * part + (int64_t)(r % rpp) * ldx);
+        const uint16_t *xrow = x + (r / rpp) * part + (int64_t)(r % rpp) * ldx;
+        const uint4 *xr = reinterpret_cast<const uint4 *>(xrow);
         // statistics over the whole row
         float ss = 0.f, mx = 0.f;
         for (int base = 0; base < nv; base += B * kWarp) {
@@ -179,20 +190,20 @@ __device__ __noinline__ void build_act_frags(const uint16_t *x, int64_t ldx, int
             if (inv_out) inv_out[r] = inv;
         }
         const float sc = pow2f(sh);
-        // fragment words: vector i holds cols 8i..8i+7 = block i/2, half i&1 (pairs 4(i&1) + t)
-        for (int i = lane; i < nv; i += kWarp) {
-            const uint4 v = xr[i];
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-            const int b = i >> 1, hh = i & 1;
+        // fragments: lane (bb, t) takes blocks b = bb, bb + 8, ...; fragment word j holds cols
+        // 2t + 8j, 2t + 8j + 1 of the block
+        const int grp = r >> 3, g = r & 7;
+        uint2 *fr = f2 + (int64_t)grp * kbp * kWarp + ((4 * g + t) ^ (bb << 2));  // (b & 7) == bb
+        for (int b = bb; b < kb; b += 8) {
+            const uint32_t w0 = *reinterpret_cast<const uint32_t *>(xrow + 16 * b + 2 * t);
+            const uint32_t w1 = *reinterpret_cast<const uint32_t *>(xrow + 16 * b + 2 * t + 8);
+            float v[4] = {bf16_bits_to_f32(w0 & 0xFFFFu), bf16_bits_to_f32(w0 >> 16), bf16_bits_to_f32(w1 & 0xFFFFu),
+                          bf16_bits_to_f32(w1 >> 16)};
+            if (norm) {
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                float lo = bf16_bits_to_f32(w[t] & 0xFFFFu), hi = bf16_bits_to_f32(w[t] >> 16);
-                if (norm) {
-                    lo = __bfloat162float(__float2bfloat16_rn(lo * inv));
-                    hi = __bfloat162float(__float2bfloat16_rn(hi * inv));
-                }
-                frag[frag_word(r, b, 4 * hh + t, kbp)] = pack_half2(lo * sc, hi * sc);
+                for (int e = 0; e < 4; ++e) v[e] = __bfloat162float(__float2bfloat16_rn(v[e] * inv));
             }
+            fr[(int64_t)b * kWarp] = make_uint2(pack_half2(v[0] * sc, v[1] * sc), pack_half2(v[2] * sc, v[3] * sc));
         }
     }
     bar_sync(1, NC);

@@ -321,10 +321,11 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
             if (lane == 0) {
                 uint8_t *dst = my_slots + (size_t)is_slot * a.slot_bytes;
                 uint64_t *fb = my_full + is_slot;
-                fence_proxy_async_shared();  // this warp's reads of the slot come first
+                const uint64_t pol = l2_evict_first();  // weights are read once per launch
+                fence_proxy_async_shared();              // this warp's reads of the slot come first
                 mbar_arrive_expect_tx(fb, sb ? 2 * b : b);
-                bulk_g2s(dst, sa, b, fb);
-                if (sb) bulk_g2s(dst + b, sb, b, fb);
+                bulk_g2s_hint(dst, sa, b, fb, pol);
+                if (sb) bulk_g2s_hint(dst + b, sb, b, fb, pol);
             }
             sa += b;
             if (sb) sb += b;
