@@ -20,7 +20,7 @@ static __device__ unsigned long long *g_bfp_trace = nullptr;
         if (g_bfp_trace != nullptr && threadIdx.x == 0)                                                     \
             g_bfp_trace[(size_t)blockIdx.x * BFP_TRACE_SLOTS + (slot)] = (v);                               \
     } while (0)
-#define BFP_TRACE_NOW() bfp::dev::global_ns()
+#define BFP_TRACE_NOW() ((unsigned long long)clock64())  // SM cycles (cheap), for durations
 #else
 #define BFP_TRACE_SET(slot, v) \
     do {                       \

@@ -48,7 +48,7 @@ int linear_launch_ex(const bfp_matrix *w, const uint16_t *x, int m, int64_t ldx,
 int linear_ws_body_bytes(const bfp_matrix *w, int m, size_t *bytes);
 
 constexpr int kMaxRows = 16;
-constexpr int kMoeWarps = 8;                 // warps of the layer kernel (no producer warp)
+constexpr int kMoeWarps = 16;                // warps of the layer kernel (no producer warp)
 constexpr int kMoeThreads = kMoeWarps * 32;
 constexpr int kMaxTopK = 8;
 constexpr int kMaxExperts = 256;
@@ -82,7 +82,6 @@ struct MoeArgs {
 // Shared-memory bookkeeping of one CTA.
 struct MoeMisc {
     alignas(16) float esc[kMoeWarps][rec_scale_floats<4, 2>()];  // per-warp block scales (mma_records)
-    uint64_t cbar;        // consumers' own bulk copies (logits, h rows)
     uint64_t stage_full;  // the preamble stage (activation rows, router rows) landed
     int shift_x[kMaxRows];
     float inv[kMaxRows];
@@ -215,7 +214,6 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
         for (int i = 0; i < NW * a.nsw; ++i) mbar_init(&full[i], 1);
         for (int i = 0; i < 4; ++i) ms->flags[i] = 0;
         ms->nU = 0;
-        mbar_init(&ms->cbar, 1);
         mbar_init(&ms->stage_full, 1);
         mbar_fence_init();
     }
@@ -335,7 +333,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
         };
         // trace builds: per-phase durations of warp 0 accumulated in registers: [0] phase-1 data waits,
         // [1] phase-1 MMA sections, [2] phase-2 data waits, [3] phase-1 refills, [4] phase-1 chunks
-        unsigned long long tacc[10] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0};  // [5..9]: phase-2 MMA, refills, setups, units, experts
+        unsigned long long tacc[13] = {};  // [10] phase-1 epilogues, [11] phase-1 unit starts, [12] phase-2 epilogues  // [5..9]: phase-2 MMA, refills, setups, units, experts
         int tslot = 0;
         // Waits for the next item; a warp whose data never came stops issuing and keeps its copies
         // in the drain at exit.
@@ -360,14 +358,6 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
             }
         };
 
-        // Bulk copies issued by the consumers themselves (data other CTAs wrote, already acquired):
-        // thread 0 issues, every consumer thread waits; one phase of ms->cbar per call.
-        uint32_t cphase = 0;
-        auto stage_wait = [&]() {
-            if (!bad)
-                bad = !__all_sync(0xffffffffu, mbar_wait(&ms->cbar, cphase & 1u, a.wait_data, nullptr));
-            ++cphase;
-        };
         // Grid barrier over the consumer threads of every CTA, on a workspace counter.
         // Returns false on abort (same answer in every consumer thread of the CTA).
         auto grid_barrier = [&](uint32_t *counter) -> bool {
@@ -392,6 +382,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
         // ---- phase-1 unit (run by one warp): f-tile of gate and up over all of k; h = silu(gate) * up
         //      for the rows in the unit's row mask, to the workspace; row maxima of |h| to hmax.
         auto run_p1_unit = [&](int g) {
+            [[maybe_unused]] const unsigned long long tu0 = BFP_TRACE_NOW();
             const P1Tile pt = p1_tile(g, a.nft_s, a.nft);
             const uint32_t rowmask = ms->umask[pt.jrow];
             const uint32_t gm = (((rowmask & 0xFFu) ? 1u : 0u) | ((rowmask & 0xFF00u) ? 2u : 0u)) & ngrp_rows;
@@ -407,6 +398,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
 #pragma unroll
                     for (int i = 0; i < 4; ++i) acc[r][gg][i] = 0.f;
             float a1[2][1][4] = {};
+            tacc[11] += BFP_TRACE_NOW() - tu0;
             // each chunk: n gate records, then n up records; one loop per group count, so that each
             // keeps only its own accumulators live
             if (both) {
@@ -441,6 +433,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
                 }
             }
             if (bad) return;
+            [[maybe_unused]] const unsigned long long te0 = BFP_TRACE_NOW();
 #pragma unroll
             for (int gg = 0; gg < NGRP; ++gg) {
                 if (!both && gg > 0) continue;
@@ -478,6 +471,8 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
                         atomicMax(&a.hmax[ro * (a.K + 1) + ms->uslot[pt.jrow][ro]], mo);
                 }
             }
+            __syncwarp();
+            tacc[10] += BFP_TRACE_NOW() - te0;
         };
 
         // ---- 1. router rows: logits from the bf16 router rows (shared memory) and the activation
@@ -545,15 +540,9 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
                 goto done;
             }
             STAMP(5);  // every CTA's router rows published
-            float *lg = scr;  // M x E1 logits (the phase-1 scratch is free here), one bulk copy
-            if (tid == 0) {
-                const uint32_t bytes = (uint32_t)align_up((size_t)a.M * E1 * 4, 16);  // stays inside the workspace
-                fence_proxy_async_global();
-                mbar_arrive_expect_tx(&ms->cbar, bytes);
-                bulk_g2s(lg, a.logits, bytes, &ms->cbar);
-            }
-            stage_wait();
-            STAMP(26);  // logits in shared memory
+            // the logits of every row, written by every CTA before the router counter (read from L2)
+            const float *lg = a.logits;
+            STAMP(26);
             // Top-k per row. Warp w takes rows w and w + NW in one loop (two independent chains per
             // round). Lane l holds experts 8l .. 8l+7 and first sorts them (key descending, index
             // ascending among equal keys); each round the lanes offer their heads, the largest key wins
@@ -570,7 +559,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
                         const int e = 8 * lane + q;
-                        key[j][q] = r < a.M && e < a.E ? order_key(lg[r * E1 + e]) : 0u;  // 0: below any key
+                        key[j][q] = r < a.M && e < a.E ? order_key(__ldcg(lg + r * E1 + e)) : 0u;  // 0: below any
                         qi[j][q] = q;
                     }
                     sort8_desc(key[j], qi[j]);
@@ -605,7 +594,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
                         psum += p;
                     }
                     for (int s = 0; s < a.K; ++s) ms->tk_w[r][s] = ms->tk_w[r][s] / psum;
-                    ms->gate_w[r] = 1.0f / (1.0f + expf(-lg[r * E1 + a.E]));
+                    ms->gate_w[r] = 1.0f / (1.0f + expf(-__ldcg(lg + r * E1 + a.E)));
                 }
             }
             STAMP(27);  // top-k of warp 0's rows done
@@ -757,28 +746,17 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
                     for (int i = tid; i < words / 4; i += NC) reinterpret_cast<uint4 *>(hfrag)[i] = make_uint4(0, 0, 0, 0);
                     bar_sync(1, NC);
                     if (cur < 0) STAMP(15);  // ... fragments zeroed
-                    // h rows of this expert (one bulk copy per row) into the scratch: row at column c
-                    float *hs = scr;
-                    if (tid == 0) {
-                        fence_proxy_async_global();
-                        mbar_arrive_expect_tx(&ms->cbar, (uint32_t)nr * Fe * 4);
-                        for (int r = 0; r < a.M; ++r)
-                            if ((rowmask >> r) & 1u)
-                                bulk_g2s(hs + __popc(rowmask & ((1u << r) - 1u)) * Fe,
-                                         a.hbuf + ((int64_t)r * (a.K + 1) + ms->uslot[j][r]) * a.Fmax,
-                                         (uint32_t)Fe * 4, &ms->cbar);
-                        if (cur < 0) STAMP(20);  // ... h copies issued
-                    }
-                    stage_wait();
-                    if (cur < 0) STAMP(7);  // first expert's h rows landed
-                    // one item = 4 consecutive h values (cols 4qq..4qq+3 of block b) of a column
+                    // one item = 4 consecutive h values (cols 4qq..4qq+3 of block b) of a column, read
+                    // from the workspace (written by every CTA before the phase-1 grid barrier; L2)
                     {
                         const int fb = Fe / 16;
                         const int lo_off = NGRP * kbp * kWarp * 2;  // words
                         for (int it = tid; it < nr * fb * 4; it += NC) {
                             const int col = it / (fb * 4), rem = it - col * fb * 4, b = rem >> 2, qq = rem & 3;
                             const int r = ms->colrow[col];
-                            const float4 v4 = *reinterpret_cast<const float4 *>(hs + col * Fe + 4 * rem);
+                            const float4 v4 = __ldcg(
+                                reinterpret_cast<const float4 *>(a.hbuf + ((int64_t)r * (a.K + 1) + ms->uslot[j][r]) * a.Fmax) +
+                                rem);
                             const float w = ms->hw[r];
                             const float sc = pow2f(ms->shift_h[r]);
                             const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
@@ -884,6 +862,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
                 }
                 if (p2n == 0) STAMP(18);  // ... warp 0's MMAs done
                 if (p2n == 1) STAMP(29);
+                [[maybe_unused]] const unsigned long long tp0 = BFP_TRACE_NOW();
                 if (!bad && mine) {
                     const int rg = rg0 + warp;
                     if (packed) {  // column c + 4 holds the lo half of column c: lanes t and t ^ 2
@@ -904,6 +883,8 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
                             }
                         }
                 }
+                __syncwarp();
+                tacc[12] += BFP_TRACE_NOW() - tp0;
                 if (p2n == 0) STAMP(19);  // ... partial outputs stored
                 if (p2n == 1) STAMP(31);
                 ++p2n;
@@ -919,6 +900,9 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
             BFP_TRACE_SET(47, tacc[7]);
             BFP_TRACE_SET(35, tacc[8] * 1000);
             BFP_TRACE_SET(36, tacc[9] * 1000);
+            BFP_TRACE_SET(37, tacc[10]);
+            BFP_TRACE_SET(38, tacc[11]);
+            BFP_TRACE_SET(39, tacc[12]);
             if (!grid_barrier(&a.ctrl[3])) {  // every (row, slot) partial written
                 abort_all();
                 goto done;
@@ -960,7 +944,6 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
             }
             if (tid == 0) {
                 mbar_wait(&ms->stage_full, 0u, drain, nullptr);
-                if (cphase > 0) mbar_wait(&ms->cbar, (cphase - 1) & 1u, drain, nullptr);
             }
         }
     }
@@ -1037,11 +1020,8 @@ static int plan_moe(const bfp_moe_layer *L, int m, MoePlan *p) {
     const int64_t worst_units = nft_s + (int64_t)std::min(L->n_experts, m * L->top_k) * nft;
     p->ncta = (int)std::max<int64_t>(1, std::min<int64_t>(di.sms, worst_units));
     const int rows_per_cta = (L->n_experts + 1 + p->ncta - 1) / p->ncta;  // router rows (+ gate row) per CTA
-    // scratch: logits of every row, the h rows of one phase-2 expert, router partial sums
-    p->scr_bytes = (int)align_up(std::max<size_t>(std::max<size_t>((size_t)m * (L->n_experts + 1) * 4 + 16,
-                                                                    (size_t)m * p->Fmax * 4),
-                                                  (size_t)std::max(kMoeWarps, 2 * rows_per_cta) * 8 * 4),
-                                 128);
+    // scratch: the router partial sums
+    p->scr_bytes = (int)align_up((size_t)std::max(kMoeWarps, 2 * rows_per_cta) * 8 * 4, 128);
     // phase 2: units of up to one row group per consumer warp
     p->r2 = (int)std::min<int64_t>(kMoeWarps, p->dn.ng);
     p->noct = (int)((p->dn.ng + p->r2 - 1) / p->r2);
