@@ -97,6 +97,7 @@ struct MoeMisc {
     int8_t uslot[kMaxExperts + 1][kMaxRows];
     uint32_t maxbits[2][kMaxRows];  // per-unit max |h| per row (double-buffered like the scratch)
     int8_t colrow[kMaxRows];        // phase 2: fragment column -> row of the current expert
+    int32_t p1cnt[kMoeWarps];         // phase 1, units split over warps: parts finished per unit
     int32_t p2cum[kMaxExperts + 2];  // phase-2 unit cost before each expert of the union (and the total)
     int64_t p2q[2];                  // this CTA's phase-2 units [p2q[0], p2q[1])
     int nU;
@@ -142,12 +143,6 @@ __device__ __forceinline__ P1Tile p1_tile(int g, int nft_s, int nft) {
     t.ft = t.sh ? g : (g - nft_s) % nft;
     return t;
 }
-// Number of phase-1 units i = w, w + NW, ... of CTA c (unit i is g = c + i * ncta) with g < total.
-__device__ __forceinline__ int p1_warp_units(int total, int c, int ncta, int w, int nw) {
-    const int nc = c < total ? (total - c + ncta - 1) / ncta : 0;
-    return w < nc ? (nc - w + nw - 1) / nw : 0;
-}
-
 // Ordered 32-bit key of a float: larger float <=> larger unsigned key.
 __device__ __forceinline__ uint32_t order_key(float v) {
     uint32_t u = __float_as_uint(v);
@@ -213,6 +208,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
     if (tid == 0) {
         for (int i = 0; i < NW * a.nsw; ++i) mbar_init(&full[i], 1);
         for (int i = 0; i < 4; ++i) ms->flags[i] = 0;
+        for (int i = 0; i < NW; ++i) ms->p1cnt[i] = 0;
         ms->nU = 0;
         mbar_init(&ms->stage_full, 1);
         mbar_fence_init();
@@ -264,7 +260,11 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
         int s_ch = 0;                            // records per chunk
         uint32_t s_b = 0;                        // bytes of a full chunk of one source
         bool s_live = false;
-        int u1 = 0, n1u = 0, g1 = 0;             // phase 1: units started, this warp's units, next unit's entry
+        // phase 1: this CTA's units are split into p1_S parts each (p1_S > 1 only with one activation
+        // group and fewer units than warps: the parts keep every warp busy); item it = unit it / p1_S,
+        // part it % p1_S (chunks [part * nch / p1_S, (part + 1) * nch / p1_S) of the unit)
+        int p1_S = 1, p1_items = 0, p1_nch = 1;
+        int p1_it = 0;                           // next item this warp issues
         int q2 = 0, q2end = 0, j2 = 0, oct2 = 0; // phase 2: next unit (and its expert, octet), range end
         int nUl = 0;
         uint8_t *const my_slots = ring + (size_t)warp * a.nsw * a.slot_bytes;
@@ -273,15 +273,16 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
         // phase-2 row groups oct * r2 + warp of the CTA's units. Once per segment (not per chunk).
         auto next_segment = [&]() {
             s_live = true;
-            if (u1 < n1u) {
-                const P1Tile pt = p1_tile(g1, a.nft_s, a.nft);
+            if (p1_it < p1_items) {
+                const int i = p1_it / p1_S, part = p1_it % p1_S;
+                const P1Tile pt = p1_tile(c + i * a.ncta, a.nft_s, a.nft);
                 const uint8_t *base = pt.sh ? a.sgu : a.gu + (int64_t)ms->ulist[pt.jrow] * a.gu_stride;
-                sa = base + (int64_t)(2 * pt.ft) * gb_h;
+                const int r0 = part * p1_nch / p1_S * ch1, r1 = min((part + 1) * p1_nch / p1_S * ch1, a.kc_h);
+                sa = base + (int64_t)(2 * pt.ft) * gb_h + (int64_t)r0 * a.rec;
                 sb = sa + gb_h;
-                s_left = a.kc_h;
+                s_left = r1 - r0;
                 s_ch = ch1;
-                ++u1;
-                g1 += NW * a.ncta;
+                p1_it += NW;
                 return;
             }
             // units whose octet has no row group for this warp are skipped (only an expert's last octet)
@@ -381,9 +382,11 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
 
         // ---- phase-1 unit (run by one warp): f-tile of gate and up over all of k; h = silu(gate) * up
         //      for the rows in the unit's row mask, to the workspace; row maxima of |h| to hmax.
-        auto run_p1_unit = [&](int g) {
+        auto run_p1_item = [&](int it) {
             [[maybe_unused]] const unsigned long long tu0 = BFP_TRACE_NOW();
-            const P1Tile pt = p1_tile(g, a.nft_s, a.nft);
+            const int ui = it / p1_S, part = it % p1_S;
+            const int r0 = part * p1_nch / p1_S * ch1, r1 = min((part + 1) * p1_nch / p1_S * ch1, a.kc_h);
+            const P1Tile pt = p1_tile(c + ui * a.ncta, a.nft_s, a.nft);
             const uint32_t rowmask = ms->umask[pt.jrow];
             const uint32_t gm = (((rowmask & 0xFFu) ? 1u : 0u) | ((rowmask & 0xFF00u) ? 2u : 0u)) & ngrp_rows;
             bool both = false;
@@ -402,8 +405,8 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
             // each chunk: n gate records, then n up records; one loop per group count, so that each
             // keeps only its own accumulators live
             if (both) {
-                for (int k0 = 0; k0 < a.kc_h; k0 += ch1) {
-                    const int n = min(ch1, a.kc_h - k0);
+                for (int k0 = r0; k0 < r1; k0 += ch1) {
+                    const int n = min(ch1, r1 - k0);
                     const uint8_t *sp = take_item();
                     if (!bad)
                         for (int ch = 0; ch < n; ++ch) {
@@ -414,8 +417,8 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
                     give_item();
                 }
             } else {
-                for (int k0 = 0; k0 < a.kc_h; k0 += ch1) {
-                    const int n = min(ch1, a.kc_h - k0);
+                for (int k0 = r0; k0 < r1; k0 += ch1) {
+                    const int n = min(ch1, r1 - k0);
                     const uint8_t *sp = take_item();
                     [[maybe_unused]] const unsigned long long tm0 = BFP_TRACE_NOW();
                     if (!bad)
@@ -433,6 +436,33 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
                 }
             }
             if (bad) return;
+            if constexpr (NGRP == 1) {
+                if (p1_S > 1) {
+                    // split unit: store this part's tile; the last part to finish adds the parts in
+                    // order (it < NW items, each with its scratch tile) and writes the unit's results
+                    float *mine = scr + (size_t)it * 256;
+#pragma unroll
+                    for (int r = 0; r < 2; ++r)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) mine[(r * 4 + i) * kWarp + lane] = a1[r][0][i];
+                    __syncwarp();
+                    int last = 0;
+                    if (lane == 0) {
+                        __threadfence_block();
+                        last = atomicAdd(&ms->p1cnt[ui], 1) == p1_S - 1;
+                    }
+                    if (!__shfl_sync(0xffffffffu, last, 0)) return;
+                    __threadfence_block();
+#pragma unroll
+                    for (int r = 0; r < 2; ++r)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            float v = 0.f;
+                            for (int q = 0; q < p1_S; ++q) v += scr[(size_t)(ui * p1_S + q) * 256 + (r * 4 + i) * kWarp + lane];
+                            a1[r][0][i] = v;
+                        }
+                }
+            }
             [[maybe_unused]] const unsigned long long te0 = BFP_TRACE_NOW();
 #pragma unroll
             for (int gg = 0; gg < NGRP; ++gg) {
@@ -676,8 +706,16 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
         // this warp's stream: its units and the CTA's phase-2 range are known now; fill its slots
         // (every warp is past its reads of the stage, which the first slots may overlap)
         nUl = ms->nU;
-        n1u = p1_warp_units(a.nft_s + nUl * a.nft, c, a.ncta, warp, NW);
-        g1 = c + warp * a.ncta;
+        {
+            const int p1_total = a.nft_s + nUl * a.nft;
+            const int nc = c < p1_total ? (p1_total - c + a.ncta - 1) / a.ncta : 0;  // this CTA's units
+            p1_nch = (a.kc_h + ch1 - 1) / ch1;
+            if constexpr (NGRP == 1) {
+                while (nc > 0 && nc * p1_S * 2 <= NW && p1_S * 2 <= p1_nch) p1_S *= 2;
+            }
+            p1_items = nc * p1_S;
+            p1_it = warp;
+        }
         q2end = (int)ms->p2q[1];
         q2 = (int)ms->p2q[0];
         j2 = q2 / a.noct;
@@ -686,11 +724,9 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
 
         // ---- 4. phase 1: this warp's units of the CTA's list [shared-expert f-tiles, routed f-tiles]
         {
-            const int p1_total = a.nft_s + ms->nU * a.nft;
-            const int nmine = p1_warp_units(p1_total, c, a.ncta, warp, NW);
-            for (int k = 0; k < nmine; ++k) {
-                if (k == 1) STAMP(21);  // warp 0: second unit start
-                run_p1_unit(c + (warp + NW * k) * a.ncta);
+            for (int it = warp; it < p1_items; it += NW) {
+                if (it == warp + NW) STAMP(21);  // warp 0: second item start
+                run_p1_item(it);
             }
             STAMP(8);  // warp 0: phase-1 units done
             tslot = 2;
@@ -1020,8 +1056,11 @@ static int plan_moe(const bfp_moe_layer *L, int m, MoePlan *p) {
     const int64_t worst_units = nft_s + (int64_t)std::min(L->n_experts, m * L->top_k) * nft;
     p->ncta = (int)std::max<int64_t>(1, std::min<int64_t>(di.sms, worst_units));
     const int rows_per_cta = (L->n_experts + 1 + p->ncta - 1) / p->ncta;  // router rows (+ gate row) per CTA
-    // scratch: the router partial sums
-    p->scr_bytes = (int)align_up((size_t)std::max(kMoeWarps, 2 * rows_per_cta) * 8 * 4, 128);
+    // scratch: the router partial sums, then (one activation group) the tiles of phase-1 units
+    // split over warps: one 256-float tile per warp
+    p->scr_bytes = (int)align_up(std::max<size_t>((size_t)std::max(kMoeWarps, 2 * rows_per_cta) * 8 * 4,
+                                                  p->ngrp == 1 ? (size_t)kMoeWarps * 256 * 4 : 0),
+                                 128);
     // phase 2: units of up to one row group per consumer warp
     p->r2 = (int)std::min<int64_t>(kMoeWarps, p->dn.ng);
     p->noct = (int)((p->dn.ng + p->r2 - 1) / p->r2);
