@@ -6,14 +6,16 @@
 // weights (Qwen3.8-27B s27v6 card, "Multi-user decode").
 //
 // GB300 design: the weight stream is the whole cost (1.0625 or 0.5625 bytes
-// per weight, read once). A persistent grid of one 288-thread CTA per SM walks
-// an equal share of the matrix's tile records (stream-K: shares may start and
-// end inside a row group). One producer warp streams the share into a ring of
-// shared-memory slots with 1D bulk copies (cp.async.bulk, the TMA engine)
-// completing on mbarriers; eight consumer warps unpack each 16-value block
-// into an fp16 A fragment and run one mma.sync k16 step per block. A row group
-// split between CTAs is finished by whichever CTA arrives last (fixed-order
-// sum of the partials, so results do not depend on timing).
+// per weight, read once). A grid of one 512-thread CTA per SM gives every CTA
+// the same number of whole 16-row groups. Each row group is cut into S parts
+// along k (S > 1 only when the CTA has fewer row groups than warps), and each
+// of the 16 warps takes whole parts: it streams the part's tile records
+// through two shared-memory slots of its own with 1D bulk copies (the TMA
+// engine; lane 0 refills a slot as soon as the warp is done with it),
+// unpacks each 16-value block into an fp16 A fragment and runs one mma.sync
+// k16 step per block. The parts of a split row group meet in shared memory:
+// the last one to finish adds them in order (results do not depend on
+// timing) and writes the outputs. Nothing crosses CTAs.
 #include <algorithm>
 #include <mutex>
 #include <vector>
@@ -53,10 +55,13 @@ int device_info(DeviceInfo *out) {
 // ----------------------------------------------------------------------------
 // bfp_linear kernel
 // ----------------------------------------------------------------------------
+constexpr int kLinWarps = 16;
+constexpr int kLinThreads = kLinWarps * 32;
+
 struct LinearArgs {
     const uint8_t *w;
-    int64_t n, ng;
-    int k, kc, kbp, rec;
+    int64_t n;
+    int ng, k, kc, kbp, rec;
     const uint16_t *x;
     int64_t ldx;
     int m, norm;
@@ -64,207 +69,189 @@ struct LinearArgs {
     float *y;
     uint16_t *yb;
     int64_t ldy;
-    uint32_t *status, *cnt;
-    float *part;
-    int ncta, nslot, slot_recs, slot_bytes, frag_bytes;
+    uint32_t *status;
+    int ncta, S, chw, nsw, slot_bytes, frag_bytes, scr_bytes, stage_off;
     WaitCfg wait;
 };
 
-// CTA c's share of the record line [0, R): [floor(cR/ncta), floor((c+1)R/ncta)).
-__device__ __forceinline__ int64_t share_start(int64_t c, int64_t R, int ncta) { return c * R / ncta; }
-__device__ __forceinline__ int cta_of(int64_t q, int64_t R, int ncta) {
-    int c = (int)(q * ncta / R);
-    while (c + 1 < ncta && share_start(c + 1, R, ncta) <= q) ++c;
-    while (c > 0 && share_start(c, R, ncta) > q) --c;
-    return c;
-}
-
-constexpr int kLinEsc = 256;                                                 // offset of the per-warp scale scratch
-constexpr int kLinMisc = kLinEsc + kConsumerWarps * rec_scale_floats<4, 1>() * 4;  // shift[16], inv[16], flags, scales
+// Shared-memory bookkeeping of one CTA.
+struct LinMisc {
+    alignas(16) float esc[kLinWarps][rec_scale_floats<4, 1>()];  // per-warp block scales (mma_records)
+    uint64_t stage_full;                                          // the activation rows landed
+    int shift[16];
+    float inv[16];
+    int cnt[kLinWarps];  // parts finished per row group of a split
+    int flags[4];        // [0] abort
+};
 
 template <int FMT, int NGRP>
-__global__ void __launch_bounds__(kThreads, 1) bfp_linear_kernel(const LinearArgs a) {
+__global__ void __launch_bounds__(kLinThreads, 1) bfp_linear_kernel(const LinearArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
-    constexpr int NW = kConsumerWarps;
-    constexpr int TILE = NGRP * 128;  // accumulator values per 16-row group
+    constexpr int NW = kLinWarps;
+    constexpr int NC = NW * kWarp;
+    constexpr int TILE = NGRP * 128;  // accumulator values of one 16-row group
     constexpr int MB = FMT == 4 ? 3 : 7;
     constexpr int CB = FMT == 4 ? 4 : 2;
     uint32_t *frag = reinterpret_cast<uint32_t *>(smem);
     float *scr = reinterpret_cast<float *>(smem + a.frag_bytes);
-    int *shift = reinterpret_cast<int *>(scr + NW * TILE);
-    float *inv = reinterpret_cast<float *>(shift + 16);
-    volatile int *flags = reinterpret_cast<volatile int *>(inv + 16);
-    float *esc = reinterpret_cast<float *>(smem + a.frag_bytes + NW * TILE * 4 + kLinEsc) +
-                 (threadIdx.x >> 5) * rec_scale_floats<4, 1>();  // this warp's scale scratch
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + a.frag_bytes + NW * TILE * 4 + kLinMisc);
-    uint64_t *empty = full + a.nslot;
-    uint8_t *ring = smem + align_up(a.frag_bytes + NW * TILE * 4 + kLinMisc + 16 * a.nslot, 128);
+    LinMisc *lm = reinterpret_cast<LinMisc *>(smem + a.frag_bytes + a.scr_bytes);
+    const size_t bar_off = align_up(a.frag_bytes + a.scr_bytes + sizeof(LinMisc), 16);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + bar_off);  // [NW][nsw]
+    uint8_t *ring = smem + align_up(bar_off + 8 * NW * a.nsw, 128);
+    uint8_t *stage = ring + a.stage_off;  // the activation rows, before the streams start
+    volatile int *flags = lm->flags;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x;
-    const int64_t R = a.ng * a.kc;
-    const int64_t s = share_start(c, R, a.ncta), e = share_start(c + 1, R, a.ncta);
+    const int rg0 = (int)((int64_t)c * a.ng / a.ncta), rg1 = (int)((int64_t)(c + 1) * a.ng / a.ncta);
+    const int S = a.S, items = (rg1 - rg0) * S;
 
     if (tid == 0) {
-        for (int i = 0; i < a.nslot; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], NW);
-        }
-        flags[0] = 0;
-        flags[1] = 0;
+        for (int i = 0; i < NW * a.nsw; ++i) mbar_init(&full[i], 1);
+        mbar_init(&lm->stage_full, 1);
+        for (int i = 0; i < NW; ++i) lm->cnt[i] = 0;
+        for (int i = 0; i < 4; ++i) lm->flags[i] = 0;
         mbar_fence_init();
     }
     __syncthreads();
+    if (tid == 0) {  // the activation rows, one copy per row (rows are ldx apart in global memory)
+        mbar_arrive_expect_tx(&lm->stage_full, (uint32_t)a.m * a.k * 2);
+        for (int r = 0; r < a.m; ++r)
+            bulk_g2s(stage + (size_t)r * a.k * 2, a.x + (int64_t)r * a.ldx, (uint32_t)a.k * 2, &lm->stage_full);
+    }
+    bool bad = !__all_sync(0xffffffffu, mbar_wait(&lm->stage_full, 0u, a.wait, nullptr));
+    build_act_frags<NC>(reinterpret_cast<const uint16_t *>(stage), a.k, 16, 0, a.m, a.k, a.kbp, NGRP, a.norm != 0,
+                        a.eps, frag, lm->shift, lm->inv, tid, warp, lane);
+    // every warp is past its reads of the stage (the barrier ending build_act_frags)
 
-    if (warp == NW) {
-        // ------------------------------------------------------------ producer
+    // ---- this warp's stream: items it = warp, warp + NW, ...; item it = part it % S of row group
+    //      rg0 + it / S, i.e. records [part * kc / S, (part + 1) * kc / S) of the group, in chunks
+    //      of chw records through the warp's nsw slots (lane 0 issues, every lane keeps the cursor)
+    uint8_t *const my_slots = ring + (size_t)warp * a.nsw * a.slot_bytes;
+    uint64_t *const my_full = full + warp * a.nsw;
+    int iss = 0, is_slot = 0, cu = 0, cu_slot = 0;
+    uint32_t cu_par = 0;
+    int it_iss = warp;  // next item to issue
+    const uint8_t *src = nullptr;
+    int s_left = 0;
+    auto issue_next = [&]() {
+        if (bad) return;
+        if (s_left <= 0) {
+            if (it_iss >= items) return;
+            const int rg = rg0 + it_iss / S, part = it_iss % S;
+            const int r0 = part * a.kc / S, r1 = (part + 1) * a.kc / S;
+            src = a.w + ((int64_t)rg * a.kc + r0) * a.rec;
+            s_left = r1 - r0;
+            it_iss += NW;
+        }
+        const uint32_t b = (uint32_t)min(a.chw, s_left) * a.rec;
         if (lane == 0) {
-            int64_t u = 0;
-            bool bad = false;
-            // the activation rows first, 8 rows per slot (the fragments are built from them)
-            for (int r0 = 0; r0 < a.m; r0 += 8) {
-                const int slot = (int)(u % a.nslot);
-                const int nr = min(8, a.m - r0);
-                mbar_arrive_expect_tx(&full[slot], (uint32_t)nr * a.k * 2);
-                for (int r = 0; r < nr; ++r)  // one copy per row: rows are ldx apart in global memory
-                    bulk_g2s(ring + (size_t)slot * a.slot_bytes + (size_t)r * a.k * 2, a.x + (int64_t)(r0 + r) * a.ldx,
-                             (uint32_t)a.k * 2, &full[slot]);
-                ++u;
-            }
-            for (int64_t pos = s; pos < e;) {
-                const int64_t rg = pos / a.kc;
-                const int c0 = (int)(pos - rg * a.kc);
-                const int len = (int)min64(min64(e - pos, a.kc - c0), a.slot_recs);
-                const int slot = (int)(u % a.nslot);
-                const int64_t use = u / a.nslot;
-                if (use > 0 && !mbar_wait(&empty[slot], (uint32_t)((use - 1) & 1), a.wait, flags)) {
-                    bad = true;
-                    break;
-                }
-                if (flags[0]) break;
-                const uint32_t bytes = (uint32_t)len * a.rec;
-                mbar_arrive_expect_tx(&full[slot], bytes);
-                bulk_g2s_hint(ring + (size_t)slot * a.slot_bytes, a.w + (rg * a.kc + c0) * a.rec, bytes, &full[slot],
-                              l2_evict_first());  // the weights are read once per launch
-                pos += len;
-                ++u;
-            }
-            // No copy may still be landing in shared memory when the CTA exits.
-            WaitCfg drain{int64_t(1) << 40, 1000000000ull};
-            for (int64_t sl = 0; sl < min64(u, a.nslot); ++sl) {
-                const int64_t last_use = (u - 1 - sl) / a.nslot;
-                mbar_wait(&full[sl], (uint32_t)(last_use & 1), drain, nullptr);
-            }
-            if (bad) {
-                raise_status(a.status, kStatusTimeout);
+            uint64_t *fb = my_full + is_slot;
+            const uint64_t pol = l2_evict_first();  // the weights are read once per launch
+            fence_proxy_async_shared();              // this warp's reads of the slot come first
+            mbar_arrive_expect_tx(fb, b);
+            bulk_g2s_hint(my_slots + (size_t)is_slot * a.slot_bytes, src, b, fb, pol);
+        }
+        src += b;
+        s_left -= a.chw;
+        ++iss;
+        if (++is_slot == a.nsw) is_slot = 0;
+    };
+    auto take_item = [&]() -> const uint8_t * {
+        if (!bad && flags[0]) bad = true;
+        if (!bad && !__all_sync(0xffffffffu, mbar_wait(my_full + cu_slot, cu_par, a.wait, flags))) {
+            bad = true;
+            if (lane == 0) {
                 flags[0] = 1;
+                raise_status(a.status, kStatusTimeout);
             }
         }
+        return my_slots + (size_t)cu_slot * a.slot_bytes;
+    };
+    auto give_item = [&]() {  // a slot whose data never came is kept (the drain below waits for it)
         __syncwarp();
-    } else {
-        // ----------------------------------------------------------- consumers
-        bool bad = false;
-        int64_t u = 0;
-        {
-            // activation rows staged by the producer in slots 0 .. nx-1
-            const int nx = (a.m + 7) / 8;
-            for (int i = 0; i < nx; ++i)
-                if (!bad) bad = !__all_sync(0xffffffffu, mbar_wait(&full[i], 0u, a.wait, nullptr));
-            build_act_frags<NW * kWarp>(reinterpret_cast<const uint16_t *>(ring), a.k, 8, a.slot_bytes / 2, a.m, a.k,
-                                        a.kbp, NGRP, a.norm != 0, a.eps, frag, shift, inv, tid, warp, lane);
-            __syncwarp();
-            for (int i = 0; i < nx; ++i)
-                if (lane == 0 && !bad) mbar_arrive(&empty[i]);
-            u = nx;
+        if (bad) return;
+        issue_next();
+        ++cu;
+        if (++cu_slot == a.nsw) {
+            cu_slot = 0;
+            cu_par ^= 1u;
         }
-        const uint2 *frag2 = reinterpret_cast<const uint2 *>(frag);
+    };
+    for (int i = 0; i < a.nsw; ++i) issue_next();
+
+    const uint2 *frag2 = reinterpret_cast<const uint2 *>(frag);
+    for (int it = warp; it < items; it += NW) {
+        const int rg = rg0 + it / S, part = it % S;
+        const int r0 = part * a.kc / S, r1 = (part + 1) * a.kc / S;
         float acc[1][NGRP][4];
 #pragma unroll
         for (int g = 0; g < NGRP; ++g)
 #pragma unroll
             for (int i = 0; i < 4; ++i) acc[0][g][i] = 0.f;
-        const int64_t rg_first = s / a.kc;
-        for (int64_t pos = s; pos < e;) {
-            const int64_t rg = pos / a.kc;
-            const int c0 = (int)(pos - rg * a.kc);
-            const int len = (int)min64(min64(e - pos, a.kc - c0), a.slot_recs);
-            const int slot = (int)(u % a.nslot);
-            const int64_t use = u / a.nslot;
-            if (!bad) bad = !__all_sync(0xffffffffu, mbar_wait(&full[slot], (uint32_t)(use & 1), a.wait, nullptr));
-            if (!bad) {
-                const uint8_t *base = ring + (size_t)slot * a.slot_bytes;
-                for (int i = warp; i < len; i += NW) {
-                    const uint8_t *recs[1] = {base + (size_t)i * a.rec};
-                    mma_records<FMT, NGRP, 1, false>(recs, frag2, nullptr, a.kbp, (c0 + i) * CB, lane, esc, acc);
+        for (int k0 = r0; k0 < r1; k0 += a.chw) {
+            const int n = min(a.chw, r1 - k0);
+            const uint8_t *sp = take_item();
+            if (!bad)
+                for (int ch = 0; ch < n; ++ch) {
+                    const uint8_t *recs[1] = {sp + (size_t)ch * a.rec};
+                    mma_records<FMT, NGRP, 1, false>(recs, frag2, nullptr, a.kbp, (k0 + ch) * CB, lane, lm->esc[warp],
+                                                     acc);
                 }
-            }
+            give_item();
+        }
+        if (bad) continue;
+        if (S > 1) {
+            // part of a split row group: store the tile; the last part to finish adds the parts in
+            // order (items < NW then: one scratch tile per item) and writes the outputs
+            float *mine = scr + (size_t)it * TILE;
+#pragma unroll
+            for (int g = 0; g < NGRP; ++g)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) mine[(g * 4 + i) * kWarp + lane] = acc[0][g][i];
             __syncwarp();
-            if (lane == 0 && !bad) mbar_arrive(&empty[slot]);  // a slot whose data never came is kept
-            pos += len;
-            ++u;
-            if (c0 + len < a.kc && pos < e) continue;  // row group continues in the next slot
-            // ---- end of this CTA's part of row group rg: reduce over warps
-            float *mine = scr + warp * TILE;
+            int last = 0;
+            if (lane == 0) {
+                __threadfence_block();
+                last = atomicAdd(&lm->cnt[it / S], 1) == S - 1;
+            }
+            if (!__shfl_sync(0xffffffffu, last, 0)) continue;
+            __threadfence_block();
 #pragma unroll
             for (int g = 0; g < NGRP; ++g)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    mine[(g * 4 + i) * kWarp + lane] = acc[0][g][i];
-                    acc[0][g][i] = 0.f;
+                    float v = 0.f;
+                    for (int q = 0; q < S; ++q) v += scr[(size_t)((it / S) * S + q) * TILE + (g * 4 + i) * kWarp + lane];
+                    acc[0][g][i] = v;
                 }
-            if (bar_or(1, NW * kWarp, bad)) {
-                if (tid == 0) {
-                    flags[0] = 1;
-                    raise_status(a.status, kStatusTimeout);
+        }
+#pragma unroll
+        for (int g = 0; g < NGRP; ++g)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int r = acc_xrow(lane, g, i);
+                const int64_t nrow = (int64_t)rg * 16 + acc_wrow(lane, i);
+                if (r < a.m && nrow < a.n) {
+                    const float v = mul_pow2(acc[0][g][i], 24 - (MB - 1) - lm->shift[r]);
+                    if (a.y) a.y[(int64_t)r * a.ldy + nrow] = v;
+                    if (a.yb) a.yb[(int64_t)r * a.ldy + nrow] = f32_to_bf16_bits(v);
                 }
-                break;
             }
-            const bool partial = rg * a.kc < s || (rg + 1) * a.kc > e;
-            float v = 0.f;
-            int r = 0;
-            int64_t nrow = 0;
-            const bool have = tid < TILE;
-            if (have) {
-                for (int w = 0; w < NW; ++w) v += scr[w * TILE + tid];
-                const int grp = tid >> 7, i = (tid >> 5) & 3, ln = tid & 31;
-                nrow = rg * 16 + acc_wrow(ln, i);
-                r = acc_xrow(ln, grp, i);
-                if (r < a.m) v = mul_pow2(v, 24 - (MB - 1) - shift[r]);
-            }
-            auto store = [&](float val) {
-                if (have && r < a.m && nrow < a.n) {
-                    if (a.y) a.y[(int64_t)r * a.ldy + nrow] = val;
-                    if (a.yb) a.yb[(int64_t)r * a.ldy + nrow] = f32_to_bf16_bits(val);
-                }
-            };
-            if (!partial) {
-                store(v);
-                bar_sync(1, NW * kWarp);
-            } else {
-                const int slotp = 2 * c + (rg == rg_first ? 0 : 1);
-                if (have) a.part[(size_t)slotp * TILE + tid] = v;
-                bar_sync(1, NW * kWarp);
-                const int cf = cta_of(rg * a.kc, R, a.ncta), cl = cta_of((rg + 1) * a.kc - 1, R, a.ncta);
-                if (tid == 0) {
-                    __threadfence();  // every thread's partial store, ordered by the barrier, before the count
-                    const uint32_t old = atom_add_acq_rel(&a.cnt[rg], 1u);
-                    flags[1] = (old == (uint32_t)(cl - cf)) ? 1 : 0;
-                }
-                bar_sync(1, NW * kWarp);
-                if (flags[1]) {
-                    float sum = 0.f;
-                    if (have) {
-                        for (int cc = cf; cc <= cl; ++cc) {
-                            const int sp = 2 * cc + (rg == share_start(cc, R, a.ncta) / a.kc ? 0 : 1);
-                            sum += __ldcg(&a.part[(size_t)sp * TILE + tid]);
-                        }
-                    }
-                    store(sum);
-                    if (tid == 0) atomicExch(&a.cnt[rg], 0u);
-                }
-                bar_sync(1, NW * kWarp);
+    }
+    // No copy may still be landing in shared memory when the CTA exits (every path).
+    {
+        WaitCfg drain{int64_t(1) << 40, 1000000000ull};
+        int sl = cu_slot;
+        uint32_t par = cu_par;
+        for (int k = cu; k < iss; ++k) {
+            if (lane == 0) mbar_wait(my_full + sl, par, drain, nullptr);
+            if (++sl == a.nsw) {
+                sl = 0;
+                par ^= 1u;
             }
         }
+        if (tid == 0) mbar_wait(&lm->stage_full, 0u, drain, nullptr);
     }
     __syncthreads();
 }
@@ -335,9 +322,9 @@ __global__ void bfp_unpack_kernel(const uint8_t *w, int64_t n, int k, int kc, in
 // Host side
 // ----------------------------------------------------------------------------
 struct LinearPlan {
-    int ngrp, ncta, nslot, slot_recs, slot_bytes, frag_bytes;
+    int ngrp, ncta, S, chw, nsw, slot_bytes, frag_bytes, scr_bytes, stage_off;
     size_t smem;
-    size_t ws_cnt_off, ws_part_off, ws_bytes;
+    size_t ws_bytes;  // workspace after its header (none: nothing crosses CTAs)
 };
 
 static int plan_linear(const Geometry &g, int m, LinearPlan *p) {
@@ -347,31 +334,30 @@ static int plan_linear(const Geometry &g, int m, LinearPlan *p) {
     p->ngrp = m > 8 ? 2 : 1;
     const int kbp = (int)(g.kc * g.cb);
     p->frag_bytes = p->ngrp * kbp * 32 * 8;
-    const size_t fixed =
-        align_up((size_t)p->frag_bytes + kConsumerWarps * p->ngrp * 128 * 4 + kLinMisc + 16 * 8, 128);
-    const int64_t R = g.ng * g.kc;
-    p->ncta = (int)std::min<int64_t>(di.sms, R);
-    const int64_t per_cta = (R + p->ncta - 1) / p->ncta;
-    int recs = (int)std::min<int64_t>(std::min<int64_t>(g.kc, std::max<int64_t>(1, 36864 / g.rec)), per_cta);
-    if (recs < 1) recs = 1;
-    const size_t xrows = (size_t)std::min(m, 8) * g.k * 2;  // staged activation rows per slot
-    for (;;) {
-        const size_t slot = align_up(std::max((size_t)recs * g.rec, xrows), 16);
-        const size_t avail = di.smem_optin > (int)fixed ? di.smem_optin - fixed : 0;
-        int nslot = (int)std::min<size_t>(8, avail / slot);
-        if (nslot >= 2) {
-            p->slot_recs = recs;
-            p->slot_bytes = (int)slot;
-            p->nslot = nslot;
-            p->smem = fixed + (size_t)nslot * slot;
-            break;
-        }
-        if (recs == 1) return fail(BFP_ESHAPE, "k too large for the activation fragments in shared memory");
-        recs = std::max(1, recs / 2);
+    // grid: the same number of whole row groups per CTA (at most one CTA per SM)
+    const int64_t per = (g.ng + di.sms - 1) / di.sms;
+    p->ncta = (int)((g.ng + per - 1) / per);
+    // parts per row group: every warp gets one when a CTA has fewer row groups than warps
+    p->S = 1;
+    while (per * p->S * 2 <= kLinWarps && p->S * 2 <= g.kc) p->S *= 2;
+    p->scr_bytes = p->S > 1 ? (int)align_up((size_t)kLinWarps * p->ngrp * 128 * 4, 128) : 0;
+    const size_t stage = align_up((size_t)m * g.k * 2, 128);
+    const size_t base = align_up((size_t)p->frag_bytes + p->scr_bytes + sizeof(LinMisc), 16);
+    const int64_t avail = (int64_t)di.smem_optin - (int64_t)base - 128;
+    // chunks of up to 8 records, smaller when two slots per warp would not fit
+    p->nsw = 0;
+    for (int chw : {8, 6, 4, 2, 1}) {
+        p->chw = (int)std::min<int64_t>(chw, g.kc);
+        p->slot_bytes = p->chw * g.rec;
+        p->nsw = (int)std::min<int64_t>(4, avail / ((int64_t)kLinWarps * (p->slot_bytes + 8)));
+        if (p->nsw >= 2) break;
     }
-    p->ws_cnt_off = 0;
-    p->ws_part_off = align_up((size_t)g.ng * 4, 256);
-    p->ws_bytes = p->ws_part_off + (size_t)2 * p->ncta * p->ngrp * 128 * 4;
+    if (p->nsw < 2) return fail(BFP_ESHAPE, "k too large for the activation fragments in shared memory");
+    const size_t ring = (size_t)kLinWarps * p->nsw * p->slot_bytes;
+    if (ring < stage) return fail(BFP_ESHAPE, "activation rows do not fit in shared memory");
+    p->stage_off = (int)(ring - stage);
+    p->smem = align_up(base + 8 * (size_t)kLinWarps * p->nsw, 128) + ring;
+    p->ws_bytes = 0;
     return BFP_OK;
 }
 
@@ -380,14 +366,14 @@ static int launch_linear_t(const LinearArgs &a, const LinearPlan &p, cudaStream_
     auto kern = bfp_linear_kernel<FMT, NGRP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(bfp_linear)");
-    kern<<<p.ncta, kThreads, p.smem, st>>>(a);
+    kern<<<p.ncta, kLinThreads, p.smem, st>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "launch bfp_linear");
     return BFP_OK;
 }
 
 // Shared by bfp_linear and the decode stack's LM head (norm = RMS-normalise x first).
-// status: the workspace status word; body: the kernel's counters and partials.
+// status: the workspace status word; body: the rest of the workspace (unused by this kernel).
 int linear_launch_ex(const bfp_matrix *w, const uint16_t *x, int m, int64_t ldx, float *y, uint16_t *y_bf16,
                      int64_t ldy, uint32_t *status, void *body, size_t body_bytes, cudaStream_t st, int norm) {
     Geometry g;
@@ -397,16 +383,16 @@ int linear_launch_ex(const bfp_matrix *w, const uint16_t *x, int m, int64_t ldx,
     if (!x || (!y && !y_bf16)) return fail(BFP_EINVAL, "null x or no output");
     if (ldx < g.k || ldx % 8 != 0) return fail(BFP_EALIGN, "ldx must be >= k and a multiple of 8");
     if (ldy < g.n) return fail(BFP_EINVAL, "ldy < n");
-    if (!aligned16(x) || (y && !aligned16(y)) || (y_bf16 && !aligned16(y_bf16)) || !aligned16(body))
+    if (!aligned16(x) || (y && !aligned16(y)) || (y_bf16 && !aligned16(y_bf16)))
         return fail(BFP_EALIGN, "device pointers must be 16-byte aligned");
     LinearPlan p;
     rc = plan_linear(g, m, &p);
     if (rc) return rc;
-    if (!body || body_bytes < p.ws_bytes) return fail(BFP_EWORKSPACE, "workspace smaller than bfp_linear_workspace_size");
+    if (body_bytes < p.ws_bytes) return fail(BFP_EWORKSPACE, "workspace smaller than bfp_linear_workspace_size");
     LinearArgs a;
     a.w = static_cast<const uint8_t *>(w->data);
     a.n = g.n;
-    a.ng = g.ng;
+    a.ng = (int)g.ng;
     a.k = (int)g.k;
     a.kc = (int)g.kc;
     a.kbp = (int)(g.kc * g.cb);
@@ -419,22 +405,22 @@ int linear_launch_ex(const bfp_matrix *w, const uint16_t *x, int m, int64_t ldx,
     a.y = y;
     a.yb = y_bf16;
     a.ldy = ldy;
-    uint8_t *wsb = static_cast<uint8_t *>(body);
     a.status = status;
-    a.cnt = reinterpret_cast<uint32_t *>(wsb + p.ws_cnt_off);
-    a.part = reinterpret_cast<float *>(wsb + p.ws_part_off);
     a.ncta = p.ncta;
-    a.nslot = p.nslot;
-    a.slot_recs = p.slot_recs;
+    a.S = p.S;
+    a.chw = p.chw;
+    a.nsw = p.nsw;
     a.slot_bytes = p.slot_bytes;
     a.frag_bytes = p.frag_bytes;
+    a.scr_bytes = p.scr_bytes;
+    a.stage_off = p.stage_off;
     a.wait = WaitCfg{kDefaultWaitIters, kDefaultWaitNanos};  // only this CTA's own copies are waited on
     if (g.fmt == BFP_FMT_BFP4)
         return p.ngrp == 1 ? launch_linear_t<4, 1>(a, p, st) : launch_linear_t<4, 2>(a, p, st);
     return p.ngrp == 1 ? launch_linear_t<8, 1>(a, p, st) : launch_linear_t<8, 2>(a, p, st);
 }
 
-// Bytes of the kernel's counters and partials (the workspace after its header).
+// Bytes of the workspace after its header (the kernel keeps everything in shared memory: none).
 int linear_ws_body_bytes(const bfp_matrix *w, int m, size_t *bytes) {
     Geometry g;
     int rc = check_matrix(w, &g, false);
