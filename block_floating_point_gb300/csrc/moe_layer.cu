@@ -8,26 +8,33 @@
 //     expert  D (silu(G x) * (U x))  combined with the routing weights, plus
 //     sigmoid(g . x) * shared(x).
 //
-// GB300 design: the layer is one persistent cooperative kernel, one CTA per SM
-// (8 consumer warps + 1 producer warp). Nothing waits on the host between the
-// router and the experts. Each CTA walks a fixed list of "units", each a
-// contiguous span of packed weights streamed into a shared-memory ring by
-// cp.async.bulk (TMA, 1D) on mbarriers:
-//   1. its rows of the router (and the shared-gate vector as one extra row):
-//      fp32 logits to the workspace, then a release increment of a counter;
-//   2. its shared-expert gate/up f-tiles (known before routing, so their bytes
-//      stream while the router counter fills);
-//   3. after the router counter reaches the grid size, every CTA redundantly
-//      takes softmax / top-k / renormalisation and deduplicates the union U of
-//      experts selected by any row (so no host sync, no second launch);
-//   4. routed gate/up f-tiles (expert in U, 16 ffn rows): h = silu(a) * b for
-//      every row that chose the expert, fp32 to the workspace, then a release
-//      increment of that expert's counter;
-//   5. down-projection units (expert, 8 row groups of the hidden dimension):
-//      wait for the expert's counter, multiply by the routing weight, split h
-//      into fp16 hi + lo fragments (22 significant bits), write per-(row, slot)
-//      partial outputs; the last of the |U|+1 arrivals for a row group sums
-//      the slots in slot order (deterministic, no float atomics).
+// GB300 design: the layer is one persistent cooperative kernel, one 512-thread
+// CTA (16 warps) per SM. Nothing waits on the host between the router and the
+// experts:
+//   1. thread 0 stages the activation rows and this CTA's router rows (plus
+//      the shared-gate vector as one extra row) in shared memory with 1D bulk
+//      copies (the TMA engine); the warps build fp16 activation fragments and
+//      the CTA's fp32 logits, written to the workspace before a release
+//      increment of a grid counter;
+//   2. once the counter reaches the grid size, every CTA redundantly takes
+//      softmax / top-k / renormalisation and the union U of the experts any row
+//      selected (no host sync, no second launch), and the share of phase-2
+//      units it owns;
+//   3. phase 1: f-tile units (16 ffn rows of an expert's gate and up, or of the
+//      shared expert). Each warp streams whole units through two shared-memory
+//      slots of its own (lane 0 refills a slot with bulk copies as soon as the
+//      warp is done with it; L2 evict-first: the weights are read once) and
+//      writes h = silu(gate) * up for the rows that chose the expert, fp32 to
+//      the workspace, and the per-(row, slot) maxima of |h|. With fewer units
+//      than warps a unit is split over several warps, whose tiles meet in
+//      shared memory;
+//   4. after a grid barrier, phase 2: down-projection units (an expert and 16
+//      row groups of the hidden dimension, one per warp): per expert the CTA
+//      turns the routing-weighted h of its rows into fp16 hi + lo fragments
+//      (22 significant bits) and every warp streams its row group and writes
+//      per-(row, slot) partial outputs;
+//   5. after a second grid barrier, each CTA sums its row groups' slots in slot
+//      order (deterministic, no float atomics) into y (or the bf16 residual).
 // Every expert's weights are read from HBM once per step however many rows
 // chose it. All cross-CTA waits are bounded and report BFP_ETIMEOUT.
 #include <algorithm>
