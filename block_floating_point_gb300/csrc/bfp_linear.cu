@@ -80,7 +80,8 @@ struct LinMisc {
     uint64_t stage_full;                                          // the activation rows landed
     int shift[16];
     float inv[16];
-    int cnt[kLinWarps];  // parts finished per row group of a split
+    float2 red[kLinWarps];  // activation row statistics per (row, segment)
+    int cnt[kLinWarps];     // parts finished per row group of a split
     int flags[4];        // [0] abort
 };
 
@@ -114,15 +115,17 @@ __global__ void __launch_bounds__(kLinThreads, 1) bfp_linear_kernel(const Linear
         mbar_fence_init();
     }
     __syncthreads();
-    if (tid == 0) {  // the activation rows, one copy per row (rows are ldx apart in global memory)
-        mbar_arrive_expect_tx(&lm->stage_full, (uint32_t)a.m * a.k * 2);
-        for (int r = 0; r < a.m; ++r)
-            bulk_g2s(stage + (size_t)r * a.k * 2, a.x + (int64_t)r * a.ldx, (uint32_t)a.k * 2, &lm->stage_full);
+    if (warp == 0) {  // the activation rows, lane r copies row r (rows are ldx apart in global memory)
+        if (lane == 0) mbar_arrive_expect_tx(&lm->stage_full, (uint32_t)a.m * a.k * 2);
+        __syncwarp();
+        if (lane < a.m)
+            bulk_g2s(stage + (size_t)lane * a.k * 2, a.x + (int64_t)lane * a.ldx, (uint32_t)a.k * 2, &lm->stage_full);
     }
     bool bad = !__all_sync(0xffffffffu, mbar_wait(&lm->stage_full, 0u, a.wait, nullptr));
-    build_act_frags<NC>(reinterpret_cast<const uint16_t *>(stage), a.k, 16, 0, a.m, a.k, a.kbp, NGRP, a.norm != 0,
-                        a.eps, frag, lm->shift, lm->inv, tid, warp, lane);
-    // every warp is past its reads of the stage (the barrier ending build_act_frags)
+    uint16_t *const xs = reinterpret_cast<uint16_t *>(stage);
+    act_rows_prepare<NC>(xs, a.k, a.m, a.k, a.norm != 0, a.eps, lm->shift, lm->inv, lm->red, warp, lane);
+    act_rows_frags<NC>(xs, a.k, a.m, a.k, a.kbp, NGRP, lm->shift, frag, tid, warp, lane);
+    // every warp is past its reads of the stage (the barrier ending act_rows_frags)
 
     // ---- this warp's stream: items it = warp, warp + NW, ...; item it = part it % S of row group
     //      rg0 + it / S, i.e. records [part * kc / S, (part + 1) * kc / S) of the group, in chunks

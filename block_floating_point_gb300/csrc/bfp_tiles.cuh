@@ -126,84 +126,141 @@ __device__ __forceinline__ void mma_records(const uint8_t *const recs[NREC], con
 __device__ __forceinline__ int acc_wrow(int lane, int i) { return (lane >> 2) + 8 * (i >> 1); }
 __device__ __forceinline__ int acc_xrow(int lane, int grp, int i) { return 8 * grp + 2 * (lane & 3) + (i & 1); }
 
-// Activation fragments for rows r < m of bf16 x (row stride ldx, k columns, k % 16 == 0):
-// optional RMS normalisation t = bf16(x / sqrt(mean(x^2) + eps)) (fp32), then
-// each row scaled by the power of two shift[r] that puts its max |value| in
-// [2^14, 2^15) and rounded to fp16 (exact for every bf16 value above
-// 2^-14 of the row maximum). Rows >= m and blocks >= k/16 are zero.
-// Row r of x is at x + (r / rpp) * part + (r % rpp) * ldx (elements): x may be one strided array
-// (rpp >= m) or, when staged in shared memory, several slots of rpp rows each.
-// One warp per row: the row's statistics from 16-byte vectors, then lane (bb, t) = (lane >> 2,
-// lane & 3) assembles whole fragments (cols 2t|2t+1 and 2t+8|2t+9 of blocks bb, bb + 8, ...) and
-// stores each with one 8-byte store; the XOR swizzle spreads a warp's stores over the banks.
-// Only the padding (rows >= m, blocks >= k/16) is zeroed. Called by the NC threads of the
-// caller's named barrier 1.
+// Segments per activation row: with few rows, each row is split along k over up to 16 warps (whole
+// 16-value blocks) so that every warp of the CTA has a share of the row statistics and fragments.
 template <int NC>
-__device__ __noinline__ void build_act_frags(const uint16_t *x, int64_t ldx, int rpp, int64_t part, int m, int k,
-                                             int kbp, int ngrp, bool norm, float eps, uint32_t *frag, int *shift,
-                                             float *inv_out, int tid, int warp, int lane) {
-    constexpr int B = 8;  // 16-byte vectors per lane held at once (k <= 8 * 8 * 32 = 2048 in one pass)
+__device__ __forceinline__ int act_segments(int m, int k) {
+    constexpr int NW = NC / kWarp;
+    const int kb = k / 16;
+    int S = 1;
+    while (m * S * 2 <= NW && S * 2 <= 16 && kb % (S * 2) == 0) S *= 2;
+    return S;
+}
+
+// Statistics of the bf16 activation rows r < m staged in shared memory (row stride ldx elements,
+// k columns, k % 16 == 0): shift[r] = the power of two that puts the row's max |value| in
+// [2^14, 2^15) for its fp16 fragments, and with norm the RMS normalisation
+// t = bf16(x / sqrt(mean(x^2) + eps)) (fp32), applied to the rows in place (inv[r] = the factor).
+// The max |t| is bf16(max|x| * inv): rounding is monotonic. red: NC/32 float2 of scratch.
+// Called by the NC threads of the caller's named barrier 1; ends with that barrier.
+template <int NC>
+__device__ __noinline__ void act_rows_prepare(uint16_t *x, int64_t ldx, int m, int k, bool norm, float eps,
+                                              int *shift, float *inv_out, float2 *red, int warp, int lane) {
+    constexpr int NW = NC / kWarp;
+    const int S = act_segments<NC>(m, k);
+    const int nvs = k / 8 / S;  // 16-byte vectors per segment
+    for (int it = warp; it < m * S; it += NW) {
+        const int r = it / S, sg = it - r * S;
+        uint4 *xr = reinterpret_cast<uint4 *>(x + (int64_t)r * ldx) + sg * nvs;
+        float ss = 0.f;
+        uint32_t mx2 = 0u;  // max |x| of the low and high bf16 halves, as bit patterns
+        for (int i = lane; i < nvs; i += kWarp) {
+            const uint4 v = xr[i];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                mx2 = __vmaxu2(mx2, w[h] & 0x7FFF7FFFu);
+                if (norm) {
+                    const float lo = bf16_bits_to_f32(w[h] & 0xFFFFu), hi = bf16_bits_to_f32(w[h] >> 16);
+                    ss = fmaf(lo, lo, ss);
+                    ss = fmaf(hi, hi, ss);
+                }
+            }
+        }
+        float mx = bf16_bits_to_f32(max(mx2 & 0xFFFFu, mx2 >> 16));
+        mx = warp_max(mx);
+        if (norm) ss = warp_sum(ss);
+        if (S > 1) {
+            if (lane == 0) red[it] = make_float2(ss, mx);  // it < NW when S > 1
+        } else {
+            float inv = 1.f;
+            if (norm) {
+                inv = 1.0f / sqrtf(ss / (float)k + eps);
+                for (int i = lane; i < nvs; i += kWarp) {
+                    uint4 v = xr[i];
+                    uint32_t *w = reinterpret_cast<uint32_t *>(&v);
+#pragma unroll
+                    for (int h = 0; h < 4; ++h)
+                        w[h] = (uint32_t)f32_to_bf16_bits(bf16_bits_to_f32(w[h] & 0xFFFFu) * inv) |
+                               ((uint32_t)f32_to_bf16_bits(bf16_bits_to_f32(w[h] >> 16) * inv) << 16);
+                    xr[i] = v;
+                }
+                mx = bf16_bits_to_f32(f32_to_bf16_bits(mx * inv));
+            }
+            if (lane == 0) {
+                shift[r] = frag_shift(mx);
+                if (inv_out) inv_out[r] = inv;
+            }
+        }
+    }
+    if (S > 1) {
+        bar_sync(1, NC);
+        for (int it = warp; it < m * S; it += NW) {
+            const int r = it / S, sg = it - r * S;
+            float ss = 0.f, mx = 0.f;
+            for (int q = 0; q < S; ++q) {  // segments in order: the same sum in every warp
+                const float2 v = red[r * S + q];
+                ss += v.x;
+                mx = fmaxf(mx, v.y);
+            }
+            float inv = 1.f;
+            if (norm) {
+                inv = 1.0f / sqrtf(ss / (float)k + eps);
+                uint4 *xr = reinterpret_cast<uint4 *>(x + (int64_t)r * ldx) + sg * nvs;
+                for (int i = lane; i < nvs; i += kWarp) {
+                    uint4 v = xr[i];
+                    uint32_t *w = reinterpret_cast<uint32_t *>(&v);
+#pragma unroll
+                    for (int h = 0; h < 4; ++h)
+                        w[h] = (uint32_t)f32_to_bf16_bits(bf16_bits_to_f32(w[h] & 0xFFFFu) * inv) |
+                               ((uint32_t)f32_to_bf16_bits(bf16_bits_to_f32(w[h] >> 16) * inv) << 16);
+                    xr[i] = v;
+                }
+                mx = bf16_bits_to_f32(f32_to_bf16_bits(mx * inv));
+            }
+            if (sg == 0 && lane == 0) {
+                shift[r] = frag_shift(mx);
+                if (inv_out) inv_out[r] = inv;
+            }
+        }
+    }
+    bar_sync(1, NC);
+}
+
+// fp16 activation fragments of the prepared rows (act_rows_prepare): row r scaled by 2^shift[r] and
+// rounded to fp16 (exact for every bf16 value above 2^-14 of the row maximum); rows m .. 8 ngrp - 1
+// and blocks k/16 .. kbp - 1 are zero. Item (row, segment) per warp; lane (bb, t) = (lane >> 2,
+// lane & 3) assembles whole fragments (cols 2t|2t+1 and 2t+8|2t+9 of the segment's blocks b with
+// b & 7 = bb) and stores each with one 8-byte store; the XOR swizzle spreads a warp's stores over
+// the banks. Called by the NC threads of the caller's named barrier 1; ends with that barrier.
+template <int NC>
+__device__ __noinline__ void act_rows_frags(const uint16_t *x, int64_t ldx, int m, int k, int kbp, int ngrp,
+                                            const int *shift, uint32_t *frag, int tid, int warp, int lane) {
+    constexpr int NW = NC / kWarp;
     const int kb = k / 16;
     uint2 *f2 = reinterpret_cast<uint2 *>(frag);
     if (m < 8 * ngrp || kb < kbp) {
-        // fragments that no row writes: rows m .. 8 ngrp - 1, blocks kb .. kbp - 1
         for (int i = tid; i < ngrp * kbp * kWarp; i += NC) {
             const int gb = i / kWarp, sl = i % kWarp, b = gb % kbp, grp = gb / kbp;
             const int r = 8 * grp + ((sl ^ frag_swz(b)) >> 2);
             if (r >= m || b >= kb) f2[i] = make_uint2(0u, 0u);
         }
     }
-    const int nv = k / 8;  // uint4 per row
+    const int S = act_segments<NC>(m, k);
+    const int bs = kb / S;  // blocks per segment
     const int bb = lane >> 2, t = lane & 3;
-    for (int r = warp; r < m; r += NC / kWarp) {
-        const uint16_t *xrow = x + (r / rpp) * part + (int64_t)(r % rpp) * ldx;
-        const uint4 *xr = reinterpret_cast<const uint4 *>(xrow);
-        // statistics over the whole row
-        float ss = 0.f, mx = 0.f;
-        for (int base = 0; base < nv; base += B * kWarp) {
-#pragma unroll
-            for (int q = 0; q < B; ++q) {
-                const int i = base + q * kWarp + lane;
-                if (i < nv) {
-                    const uint4 v = xr[i];
-                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        const float lo = bf16_bits_to_f32(w[h] & 0xFFFFu), hi = bf16_bits_to_f32(w[h] >> 16);
-                        ss = fmaf(lo, lo, ss);
-                        ss = fmaf(hi, hi, ss);
-                        mx = fmaxf(mx, fmaxf(fabsf(lo), fabsf(hi)));
-                    }
-                }
-            }
-        }
-        ss = warp_sum(ss);
-        mx = warp_max(mx);
-        float inv = 1.f;
-        if (norm) {
-            inv = 1.0f / sqrtf(ss / (float)k + eps);
-            mx = __bfloat162float(__float2bfloat16_rn(mx * inv));  // rounding is monotonic
-        }
-        const int sh = frag_shift(mx);
-        if (lane == 0) {
-            shift[r] = sh;
-            if (inv_out) inv_out[r] = inv;
-        }
-        const float sc = pow2f(sh);
-        // fragments: lane (bb, t) takes blocks b = bb, bb + 8, ...; fragment word j holds cols
-        // 2t + 8j, 2t + 8j + 1 of the block
+    for (int it = warp; it < m * S; it += NW) {
+        const int r = it / S, sg = it - r * S;
+        const uint16_t *xrow = x + (int64_t)r * ldx;
+        const float sc = pow2f(shift[r]);
         const int grp = r >> 3, g = r & 7;
         uint2 *fr = f2 + (int64_t)grp * kbp * kWarp + ((4 * g + t) ^ (bb << 2));  // (b & 7) == bb
-        for (int b = bb; b < kb; b += 8) {
+        const int b0 = sg * bs, b1 = b0 + bs;
+        for (int b = b0 + ((bb - b0) & 7); b < b1; b += 8) {
             const uint32_t w0 = *reinterpret_cast<const uint32_t *>(xrow + 16 * b + 2 * t);
             const uint32_t w1 = *reinterpret_cast<const uint32_t *>(xrow + 16 * b + 2 * t + 8);
-            float v[4] = {bf16_bits_to_f32(w0 & 0xFFFFu), bf16_bits_to_f32(w0 >> 16), bf16_bits_to_f32(w1 & 0xFFFFu),
-                          bf16_bits_to_f32(w1 >> 16)};
-            if (norm) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) v[e] = __bfloat162float(__float2bfloat16_rn(v[e] * inv));
-            }
-            fr[(int64_t)b * kWarp] = make_uint2(pack_half2(v[0] * sc, v[1] * sc), pack_half2(v[2] * sc, v[3] * sc));
+            fr[(int64_t)b * kWarp] = make_uint2(pack_half2(bf16_bits_to_f32(w0 & 0xFFFFu) * sc, bf16_bits_to_f32(w0 >> 16) * sc),
+                                                pack_half2(bf16_bits_to_f32(w1 & 0xFFFFu) * sc, bf16_bits_to_f32(w1 >> 16) * sc));
         }
     }
     bar_sync(1, NC);

@@ -102,8 +102,8 @@ struct MoeMisc {
     int16_t pos[kMaxExperts];
     int16_t ulist[kMaxExperts + 1];
     int8_t uslot[kMaxExperts + 1][kMaxRows];
-    uint32_t maxbits[2][kMaxRows];  // per-unit max |h| per row (double-buffered like the scratch)
     int8_t colrow[kMaxRows];        // phase 2: fragment column -> row of the current expert
+    float2 red[kMoeWarps];          // activation row statistics per (row, segment)
     int32_t p1cnt[kMoeWarps];         // phase 1, units split over warps: parts finished per unit
     int32_t p2cum[kMaxExperts + 2];  // phase-2 unit cost before each expert of the union (and the total)
     int64_t p2q[2];                  // this CTA's phase-2 units [p2q[0], p2q[1])
@@ -112,6 +112,11 @@ struct MoeMisc {
 };
 
 __host__ __device__ inline int router_row_start(int c, int rows, int ncta) { return (int)((int64_t)c * rows / ncta); }
+// Row stride (floats) of the logits in the workspace: the E expert logits then the shared-gate logit,
+// padded to whole 16-byte vectors.
+__host__ __device__ inline int logit_stride(int E) { return (E + 1 + 3) & ~3; }
+// Row stride (elements) of the activation rows staged in shared memory: 16 bytes of padding per row.
+__host__ __device__ inline int stage_ldx(int H) { return H + 8; }
 
 // Phase-2 unit cost in MMAs per block: an expert used by <= 4 rows carries the hi and lo halves of
 // its rows' h in one 8-column MMA; <= 8 rows need two MMAs (hi, lo); more rows two groups of two.
@@ -212,6 +217,8 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
     const int64_t gb_h = (int64_t)a.kc_h * a.rec;  // bytes of one gate/up row group
     const int ch1 = a.ch1, ch2 = 2 * a.ch1;
 
+    for (int i = tid; i <= kMaxExperts; i += NC) ms->umask[i] = 0u;
+    if (tid < kMaxExperts / 32) ms->bitmap[tid] = 0u;
     if (tid == 0) {
         for (int i = 0; i < NW * a.nsw; ++i) mbar_init(&full[i], 1);
         for (int i = 0; i < 4; ++i) ms->flags[i] = 0;
@@ -222,16 +229,21 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
     }
     __syncthreads();
     STAMP(13);
-    if (tid == 0) {
-        // preamble stage: activation rows, this CTA's router rows and (last CTA) the shared-gate row
+    const int LDXS = stage_ldx(a.H);
+    if (warp == 0) {
+        // preamble stage: the activation rows (row stride LDXS: the padding keeps the router's
+        // fragment loads free of bank conflicts), this CTA's router rows and (the CTA holding row E)
+        // the shared-gate row; lane r < M copies row r, lane M the router rows, lane M + 1 the gate row
         const uint32_t xb = (uint32_t)a.M * a.H * 2;
         const int re = min(rr1, a.E);
         const uint32_t rb = re > rr0 ? (uint32_t)(re - rr0) * a.H * 2 : 0u;
         const uint32_t gsb = rr1 > a.E ? (uint32_t)a.H * 2 : 0u;
-        mbar_arrive_expect_tx(&ms->stage_full, xb + rb + gsb);
-        bulk_g2s(stage, a.x, xb, &ms->stage_full);
-        if (rb) bulk_g2s(stage + a.stage_r, a.router + (int64_t)rr0 * a.H, rb, &ms->stage_full);
-        if (gsb) bulk_g2s(stage + a.stage_r + rb, a.sgate, gsb, &ms->stage_full);
+        if (lane == 0) mbar_arrive_expect_tx(&ms->stage_full, xb + rb + gsb);
+        __syncwarp();
+        if (lane < a.M)
+            bulk_g2s(stage + (size_t)lane * LDXS * 2, a.x + (int64_t)lane * a.H, (uint32_t)a.H * 2, &ms->stage_full);
+        if (lane == a.M && rb) bulk_g2s(stage + a.stage_r, a.router + (int64_t)rr0 * a.H, rb, &ms->stage_full);
+        if (lane == a.M + 1 && gsb) bulk_g2s(stage + a.stage_r + rb, a.sgate, gsb, &ms->stage_full);
     }
     {
         bool bad = false;
@@ -372,20 +384,19 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
             bar_sync(1, NC);
             bool ok = true;
             if (tid == 0) {
-                __threadfence();
+                // the CTA barrier orders every thread's writes before this release (cumulative at gpu scope)
                 red_release_add(counter, 1u);
                 ok = wait_counter(counter, (uint32_t)a.ncta, a.wait);
             }
             return !bar_or(1, NC, !ok || bad);
         };
 
-        // ---- activation fragments (MoE input: x, or bf16(RMSNorm(h)) in stack mode), from the rows
-        //      the producer staged
+        // ---- the MoE input rows (x, or bf16(RMSNorm(h)) in stack mode, normalised in place first)
         if (!__all_sync(0xffffffffu, mbar_wait(&ms->stage_full, 0u, a.wait_data, nullptr))) bad = true;
         STAMP(2);  // stage landed
-        build_act_frags<NC>(reinterpret_cast<const uint16_t *>(stage), a.H, kMaxRows, 0, a.M, a.H, a.kbp_h, NGRP,
-                            a.norm != 0, a.eps, frag, ms->shift_x, ms->inv, tid, warp, lane);
-        STAMP(1);  // activation fragments built
+        uint16_t *const xs = reinterpret_cast<uint16_t *>(stage);
+        if (a.norm)
+            act_rows_prepare<NC>(xs, LDXS, a.M, a.H, true, a.eps, ms->shift_x, ms->inv, ms->red, warp, lane);
 
         // ---- phase-1 unit (run by one warp): f-tile of gate and up over all of k; h = silu(gate) * up
         //      for the rows in the unit's row mask, to the workspace; row maxima of |h| to hmax.
@@ -512,60 +523,65 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
             tacc[10] += BFP_TRACE_NOW() - te0;
         };
 
-        // ---- 1. router rows: logits from the bf16 router rows (shared memory) and the activation
-        //      fragments (shared memory); x' = x * 2^shift exactly, so l = 2^-shift * sum w * x'.
-        //      Work item = (router row i, activation group grp, block segment seg); lane 4g+t reads its
-        //      own fragment words (rows 8grp+g, cols 2t|2t+1 and 2t+8|2t+9 of each block): no bank
-        //      conflicts; the four lanes of a row add up with two shuffles; segments are summed in order.
+        // ---- 1. router rows: fp32 logits of this CTA's router rows (and the shared-gate row) for every
+        //      input row, on the tensor cores: A = the bf16 input rows (m16 x k16 per step, rows >= M
+        //      zero), B = the bf16 router rows (8 per tile, n8), k split over the warps; the warps'
+        //      tiles meet in the fragment area (free until the fragments are built) and are added in
+        //      warp order.
         if (rr1 > rr0) {
             const uint16_t *wr = reinterpret_cast<const uint16_t *>(stage + a.stage_r);
-            const int nrows = rr1 - rr0;
-            const int kb = a.H / 16;
-            const int ngrp = (a.M + 7) / 8;
-            const int nseg = max(1, NW / (nrows * ngrp));
-            float *rpart = scr;  // [nrows][ngrp][nseg][8]
+            const int nrows = rr1 - rr0, nt = (nrows + 7) / 8;
+            const int ksteps = a.H / 16;
+            float *rpart = reinterpret_cast<float *>(frag);  // [nt][NW][32 lanes][4]
             if (!bad) {
                 const int g = lane >> 2, t = lane & 3;
-                for (int it = warp; it < nrows * ngrp * nseg; it += NW) {
-                    const int i = it / (ngrp * nseg), grp = (it / nseg) % ngrp, seg = it % nseg;
-                    const uint16_t *w = wr + (int64_t)i * a.H;
-                    const int b0 = seg * kb / nseg, b1 = (seg + 1) * kb / nseg;
-                    float acc = 0.f;
-                    for (int b = b0; b < b1; ++b) {
-                        const uint2 xf = frag2[frag_idx(grp, b, lane, a.kbp_h)];
-                        const uint32_t w0 = *reinterpret_cast<const uint32_t *>(w + 16 * b + 2 * t);
-                        const uint32_t w1 = *reinterpret_cast<const uint32_t *>(w + 16 * b + 2 * t + 8);
-                        const float2 x0 = __half22float2(*reinterpret_cast<const __half2 *>(&xf.x));
-                        const float2 x1 = __half22float2(*reinterpret_cast<const __half2 *>(&xf.y));
-                        acc = fmaf(bf16_bits_to_f32(w0 & 0xFFFFu), x0.x, acc);
-                        acc = fmaf(bf16_bits_to_f32(w0 >> 16), x0.y, acc);
-                        acc = fmaf(bf16_bits_to_f32(w1 & 0xFFFFu), x1.x, acc);
-                        acc = fmaf(bf16_bits_to_f32(w1 >> 16), x1.y, acc);
+                const int ks0 = warp * ksteps / NW, ks1 = (warp + 1) * ksteps / NW;
+                const bool r0v = g < a.M, r1v = g + 8 < a.M;
+                const uint16_t *xa = xs + (int64_t)g * LDXS + 2 * t;
+                const uint16_t *xb = xa + (int64_t)8 * LDXS;
+                for (int tile = 0; tile < nt; ++tile) {
+                    const int n = 8 * tile + g;  // router row of this lane's B column
+                    const bool nv = n < nrows;
+                    const uint16_t *wb = wr + (int64_t)n * a.H + 2 * t;
+                    float d[4] = {0.f, 0.f, 0.f, 0.f};
+                    for (int ks = ks0; ks < ks1; ++ks) {
+                        const int kk = 16 * ks;
+                        uint32_t af[4];
+                        af[0] = r0v ? *reinterpret_cast<const uint32_t *>(xa + kk) : 0u;
+                        af[1] = r1v ? *reinterpret_cast<const uint32_t *>(xb + kk) : 0u;
+                        af[2] = r0v ? *reinterpret_cast<const uint32_t *>(xa + kk + 8) : 0u;
+                        af[3] = r1v ? *reinterpret_cast<const uint32_t *>(xb + kk + 8) : 0u;
+                        const uint32_t b0 = nv ? *reinterpret_cast<const uint32_t *>(wb + kk) : 0u;
+                        const uint32_t b1 = nv ? *reinterpret_cast<const uint32_t *>(wb + kk + 8) : 0u;
+                        mma16816_bf16(d, af, b0, b1);
                     }
-                    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-                    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-                    if (t == 0) rpart[((i * ngrp + grp) * nseg + seg) * 8 + g] = acc;
+                    *reinterpret_cast<float4 *>(rpart + ((size_t)(tile * NW + warp) * kWarp + lane) * 4) =
+                        make_float4(d[0], d[1], d[2], d[3]);
                 }
             }
             bar_sync(1, NC);
+            const int LS = logit_stride(a.E);
             for (int idx = tid; !bad && idx < nrows * a.M; idx += NC) {
                 const int i = idx / a.M, r = idx % a.M;
+                const int tile = i >> 3, col = i & 7;
+                const int ln = 4 * (r & 7) + (col >> 1), reg = ((r >> 3) << 1) | (col & 1);  // D[r][col]
                 float acc = 0.f;
-                for (int seg = 0; seg < nseg; ++seg) acc += rpart[((i * ngrp + (r >> 3)) * nseg + seg) * 8 + (r & 7)];
+                for (int w = 0; w < NW; ++w) acc += rpart[((size_t)(tile * NW + w) * kWarp + ln) * 4 + reg];
                 const int row = rr0 + i;
-                float l = acc * pow2f(-ms->shift_x[r]);
-                if (row < a.E && a.rbias) l += a.rbias[row];
-                a.logits[(int64_t)r * E1 + row] = l;
+                if (row < a.E && a.rbias) acc += a.rbias[row];
+                a.logits[(int64_t)r * LS + row] = acc;
             }
         }
         if (bar_or(1, NC, bad)) {
             abort_all();
             goto done;
         }
-        if (tid == 0) {
-            __threadfence();
-            red_release_add(&a.ctrl[0], 1u);
-        }
+        if (tid == 0) red_release_add(&a.ctrl[0], 1u);  // after the CTA barrier: publishes every thread's logits
+
+        // ---- activation fragments for phase 1, while the other CTAs' router rows come in
+        if (!a.norm) act_rows_prepare<NC>(xs, LDXS, a.M, a.H, false, a.eps, ms->shift_x, ms->inv, ms->red, warp, lane);
+        act_rows_frags<NC>(xs, LDXS, a.M, a.H, a.kbp_h, NGRP, ms->shift_x, frag, tid, warp, lane);
+        STAMP(1);  // activation fragments built
 
 
         // ---- 3. routing: wait for every CTA's router rows, then top-k and the expert union
@@ -577,79 +593,74 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
                 goto done;
             }
             STAMP(5);  // every CTA's router rows published
-            // the logits of every row, written by every CTA before the router counter (read from L2)
-            const float *lg = a.logits;
-            STAMP(26);
-            // Top-k per row. Warp w takes rows w and w + NW in one loop (two independent chains per
-            // round). Lane l holds experts 8l .. 8l+7 and first sorts them (key descending, index
-            // ascending among equal keys); each round the lanes offer their heads, the largest key wins
-            // and among equal keys the lowest lane, i.e. the lowest expert index (ties go to the lower
-            // index), and the winner records its expert and logit and drops its head.
+            // Top-k per row, one warp per row (warp w: rows w, w + NW, ...), on the logits every CTA
+            // wrote before the router counter (read from L2). Lane l holds experts 8l .. 8l+7 and first
+            // sorts them (key descending, index ascending among equal keys); each round the lanes offer
+            // their heads, the largest key wins and among equal keys the lowest lane, i.e. the lowest
+            // expert index (ties go to the lower index); lane s keeps the slot-s winner.
             // Slot 0 is the row maximum, so p_s = exp(l_s - l_0) and w_s = p_s / sum of p.
-            {
-                constexpr int RPW = (kMaxRows + NW - 1) / NW;
-                uint32_t key[RPW][8];
-                int qi[RPW][8];
+            const int LS = logit_stride(a.E);
+            for (int r = warp; r < a.M; r += NW) {
+                const float *row = a.logits + (int64_t)r * LS;
+                uint32_t key[8];
+                int qi[8];
+                if (8 * lane + 8 <= a.E) {
+                    const float4 v0 = __ldcg(reinterpret_cast<const float4 *>(row + 8 * lane));
+                    const float4 v1 = __ldcg(reinterpret_cast<const float4 *>(row + 8 * lane + 4));
+                    const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
-                for (int j = 0; j < RPW; ++j) {
-                    const int r = warp + NW * j;
+                    for (int q = 0; q < 8; ++q) key[q] = order_key(v[q]);
+                } else {
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
                         const int e = 8 * lane + q;
-                        key[j][q] = r < a.M && e < a.E ? order_key(__ldcg(lg + r * E1 + e)) : 0u;  // 0: below any
-                        qi[j][q] = q;
+                        key[q] = e < a.E ? order_key(__ldcg(row + e)) : 0u;  // 0: below any logit
                     }
-                    sort8_desc(key[j], qi[j]);
                 }
+                const float gate_logit = __ldcg(row + a.E);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) qi[q] = q;
+                sort8_desc(key, qi);
+                int my_e = 0;
+                float my_l = 0.f;
                 for (int s = 0; s < a.K; ++s) {
+                    const uint32_t kmax = __reduce_max_sync(0xffffffffu, key[0]);
+                    const uint32_t bal = __ballot_sync(0xffffffffu, key[0] == kmax);
+                    const int wl = __ffs(bal) - 1;
+                    const int q = __shfl_sync(0xffffffffu, qi[0], wl);
+                    if (lane == s) {
+                        my_e = 8 * wl + q;
+                        my_l = key_value(kmax);
+                    }
+                    const bool win = lane == wl;
 #pragma unroll
-                    for (int j = 0; j < RPW; ++j) {
-                        const uint32_t kmax = __reduce_max_sync(0xffffffffu, key[j][0]);
-                        const uint32_t bal = __ballot_sync(0xffffffffu, kmax != 0u && key[j][0] == kmax);
-                        const bool win = bal != 0u && lane == __ffs(bal) - 1;
-                        if (win) {
-                            const int r = warp + NW * j;
-                            ms->tk_idx[r][s] = 8 * lane + qi[j][0];
-                            ms->tk_w[r][s] = key_value(key[j][0]);  // the logit until the weights below
-                        }
+                    for (int i = 0; i < 7; ++i) {
+                        key[i] = win ? key[i + 1] : key[i];
+                        qi[i] = win ? qi[i + 1] : qi[i];
+                    }
+                    key[7] = win ? 0u : key[7];
+                }
+                const float l0 = __shfl_sync(0xffffffffu, my_l, 0);
+                const float p = lane < a.K ? expf(my_l - l0) : 0.f;
+                float psum = p;
 #pragma unroll
-                        for (int q = 0; q < 7; ++q) {
-                            key[j][q] = win ? key[j][q + 1] : key[j][q];
-                            qi[j][q] = win ? qi[j][q + 1] : qi[j][q];
-                        }
-                        key[j][7] = win ? 0u : key[j][7];
+                for (int o = 1; o < kWarp; o <<= 1) psum += __shfl_xor_sync(0xffffffffu, psum, o);
+                if (lane < a.K) {
+                    const float w = p / psum;
+                    ms->tk_idx[r][lane] = my_e;
+                    ms->tk_w[r][lane] = w;
+                    atomicOr(&ms->bitmap[my_e >> 5], 1u << (my_e & 31));
+                    if (c == 0) {
+                        if (a.topk_idx) a.topk_idx[r * a.K + lane] = my_e;
+                        if (a.topk_w) a.topk_w[r * a.K + lane] = w;
                     }
                 }
-                __syncwarp();
-                const int r = warp + NW * lane;
-                if (lane < RPW && r < a.M) {
-                    const float mx = ms->tk_w[r][0];
-                    float psum = 0.f;
-                    for (int s = 0; s < a.K; ++s) {
-                        const float p = expf(ms->tk_w[r][s] - mx);
-                        ms->tk_w[r][s] = p;
-                        psum += p;
-                    }
-                    for (int s = 0; s < a.K; ++s) ms->tk_w[r][s] = ms->tk_w[r][s] / psum;
-                    ms->gate_w[r] = 1.0f / (1.0f + expf(-__ldcg(lg + r * E1 + a.E)));
-                }
+                if (lane == 0) ms->gate_w[r] = 1.0f / (1.0f + expf(-gate_logit));
             }
             STAMP(27);  // top-k of warp 0's rows done
-            if (tid < kMaxExperts / 32) ms->bitmap[tid] = 0u;
-            for (int i = tid; i <= kMaxExperts; i += NC) ms->umask[i] = 0u;
             bar_sync(1, NC);
-            if (c == 0) {
-                for (int i = tid; i < a.M * a.K; i += NC) {
-                    const int r = i / a.K, s = i % a.K;
-                    if (a.topk_idx) a.topk_idx[i] = ms->tk_idx[r][s];
-                    if (a.topk_w) a.topk_w[i] = ms->tk_w[r][s];
-                }
-            }
-            for (int i = tid; i < a.M * a.K; i += NC) {
-                const int e = ms->tk_idx[i / a.K][i % a.K];
-                atomicOr(&ms->bitmap[e >> 5], 1u << (e & 31));
-            }
-            bar_sync(1, NC);
+            // The union U (ascending expert index, the shared expert last), the rows and slots that
+            // chose each member, and this CTA's phase-2 range: one warp, no CTA barrier in between.
             if (warp == 0) {
                 int base = 0;
                 for (int wd = 0; wd < kMaxExperts / 32; ++wd) {
@@ -662,31 +673,27 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
                     }
                     base += __popc(word);
                 }
+                const int nU = base;
                 if (lane == 0) {
-                    ms->nU = base;
-                    ms->ulist[base] = (int16_t)a.E;
+                    ms->nU = nU;
+                    ms->ulist[nU] = (int16_t)a.E;
+                    ms->umask[nU] = (1u << a.M) - 1u;
+                    ms->umask[kMaxExperts] = (1u << a.M) - 1u;
                 }
-            }
-            bar_sync(1, NC);
-            const int nU = ms->nU;
-            for (int i = tid; i < a.M * a.K; i += NC) {
-                const int r = i / a.K, s = i % a.K;
-                const int j = ms->pos[ms->tk_idx[r][s]];
-                atomicOr(&ms->umask[j], 1u << r);
-                ms->uslot[j][r] = (int8_t)s;
-            }
-            if (tid < a.M) {
-                ms->uslot[nU][tid] = (int8_t)a.K;
-                ms->uslot[kMaxExperts][tid] = (int8_t)a.K;
-            }
-            if (tid == 0) {
-                ms->umask[nU] = (1u << a.M) - 1u;
-                ms->umask[kMaxExperts] = (1u << a.M) - 1u;
-            }
-            bar_sync(1, NC);
-            // phase-2 shares: exclusive prefix of the unit costs over the union (warp scan), then this
-            // CTA's range [first unit starting at >= total*c/ncta, ... >= total*(c+1)/ncta)
-            if (warp == 0) {
+                if (lane < a.M) {
+                    ms->uslot[nU][lane] = (int8_t)a.K;
+                    ms->uslot[kMaxExperts][lane] = (int8_t)a.K;
+                }
+                __syncwarp();
+                for (int i = lane; i < a.M * a.K; i += kWarp) {
+                    const int r = i / a.K, s = i - r * a.K;
+                    const int j = ms->pos[ms->tk_idx[r][s]];
+                    atomicOr(&ms->umask[j], 1u << r);
+                    ms->uslot[j][r] = (int8_t)s;
+                }
+                __syncwarp();
+                // phase-2 shares: exclusive prefix of the unit costs over the union (warp scan), then
+                // this CTA's range [first unit starting at >= total*c/ncta, ... >= total*(c+1)/ncta)
                 int carry = 0;
                 for (int j0 = 0; j0 <= nU; j0 += kWarp) {
                     const int j = j0 + lane;
@@ -1063,11 +1070,11 @@ static int plan_moe(const bfp_moe_layer *L, int m, MoePlan *p) {
     const int64_t worst_units = nft_s + (int64_t)std::min(L->n_experts, m * L->top_k) * nft;
     p->ncta = (int)std::max<int64_t>(1, std::min<int64_t>(di.sms, worst_units));
     const int rows_per_cta = (L->n_experts + 1 + p->ncta - 1) / p->ncta;  // router rows (+ gate row) per CTA
-    // scratch: the router partial sums, then (one activation group) the tiles of phase-1 units
-    // split over warps: one 256-float tile per warp
-    p->scr_bytes = (int)align_up(std::max<size_t>((size_t)std::max(kMoeWarps, 2 * rows_per_cta) * 8 * 4,
-                                                  p->ngrp == 1 ? (size_t)kMoeWarps * 256 * 4 : 0),
-                                 128);
+    // the router's per-warp partial tiles use the fragment area before the fragments are built
+    p->frag_bytes = (int)std::max<int64_t>(p->frag_bytes, (int64_t)(rows_per_cta + 7) / 8 * kMoeWarps * kWarp * 16);
+    // scratch (one activation group): the tiles of phase-1 units split over warps, one 256-float
+    // tile per warp
+    p->scr_bytes = p->ngrp == 1 ? kMoeWarps * 256 * 4 : 0;
     // phase 2: units of up to one row group per consumer warp
     p->r2 = (int)std::min<int64_t>(kMoeWarps, p->dn.ng);
     p->noct = (int)((p->dn.ng + p->r2 - 1) / p->r2);
@@ -1076,7 +1083,7 @@ static int plan_moe(const bfp_moe_layer *L, int m, MoePlan *p) {
     p->ch1 = (int)std::min<int64_t>(4, p->gu.kc);
     p->slot_bytes = 2 * p->ch1 * p->gu.rec;
     // the preamble stage (activation rows, then the CTA's router rows) takes the ring's last bytes
-    p->stage_r = (int)align_up((size_t)m * L->hidden * 2, 16);
+    p->stage_r = (int)align_up((size_t)m * stage_ldx(L->hidden) * 2, 16);
     const size_t stage_bytes = align_up((size_t)p->stage_r + (size_t)rows_per_cta * L->hidden * 2, 128);
     const size_t base = align_up((size_t)p->frag_bytes + p->scr_bytes + sizeof(MoeMisc), 16);
     const int64_t avail = (int64_t)di.smem_optin - (int64_t)base - 128;
@@ -1094,7 +1101,7 @@ static int plan_moe(const bfp_moe_layer *L, int m, MoePlan *p) {
     p->off_hmax = o;
     o = align_up(o + 4 * (size_t)m * (L->top_k + 1), 256);
     p->off_logits = o;
-    o = align_up(o + 4 * (size_t)m * (L->n_experts + 1), 256);
+    o = align_up(o + 4 * (size_t)m * logit_stride(L->n_experts), 256);
     p->off_hbuf = o;
     o = align_up(o + 4 * (size_t)m * (L->top_k + 1) * p->Fmax, 256);
     p->off_part = o;
