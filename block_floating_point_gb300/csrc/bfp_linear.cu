@@ -123,8 +123,8 @@ __global__ void __launch_bounds__(kLinThreads, 1) bfp_linear_kernel(const Linear
     }
     bool bad = !__all_sync(0xffffffffu, mbar_wait(&lm->stage_full, 0u, a.wait, nullptr));
     uint16_t *const xs = reinterpret_cast<uint16_t *>(stage);
-    act_rows_prepare<NC>(xs, a.k, a.m, a.k, a.norm != 0, a.eps, lm->shift, lm->inv, lm->red, warp, lane);
-    act_rows_frags<NC>(xs, a.k, a.m, a.k, a.kbp, NGRP, lm->shift, frag, tid, warp, lane);
+    act_rows_prepare<NC>(xs, a.k, a.m, a.k, a.norm != 0, a.eps, lm->shift, lm->inv, lm->red, 1, warp, lane);
+    act_rows_frags<NC>(xs, a.k, a.m, a.k, a.kbp, NGRP, lm->shift, frag, 1, tid, warp, lane);
     // every warp is past its reads of the stage (the barrier ending act_rows_frags)
 
     // ---- this warp's stream: items it = warp, warp + NW, ...; item it = part it % S of row group

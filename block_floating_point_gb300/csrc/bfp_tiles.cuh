@@ -142,10 +142,11 @@ __device__ __forceinline__ int act_segments(int m, int k) {
 // [2^14, 2^15) for its fp16 fragments, and with norm the RMS normalisation
 // t = bf16(x / sqrt(mean(x^2) + eps)) (fp32), applied to the rows in place (inv[r] = the factor).
 // The max |t| is bf16(max|x| * inv): rounding is monotonic. red: NC/32 float2 of scratch.
-// Called by the NC threads of the caller's named barrier 1; ends with that barrier.
+// Called by the NC threads (warps 0 .. NC/32 - 1 of the call; warp = the caller's warp index among
+// them) that meet at named barrier `bar`; ends with that barrier.
 template <int NC>
 __device__ __noinline__ void act_rows_prepare(uint16_t *x, int64_t ldx, int m, int k, bool norm, float eps,
-                                              int *shift, float *inv_out, float2 *red, int warp, int lane) {
+                                              int *shift, float *inv_out, float2 *red, int bar, int warp, int lane) {
     constexpr int NW = NC / kWarp;
     const int S = act_segments<NC>(m, k);
     const int nvs = k / 8 / S;  // 16-byte vectors per segment
@@ -194,7 +195,7 @@ __device__ __noinline__ void act_rows_prepare(uint16_t *x, int64_t ldx, int m, i
         }
     }
     if (S > 1) {
-        bar_sync(1, NC);
+        bar_sync(bar, NC);
         for (int it = warp; it < m * S; it += NW) {
             const int r = it / S, sg = it - r * S;
             float ss = 0.f, mx = 0.f;
@@ -224,7 +225,7 @@ __device__ __noinline__ void act_rows_prepare(uint16_t *x, int64_t ldx, int m, i
             }
         }
     }
-    bar_sync(1, NC);
+    bar_sync(bar, NC);
 }
 
 // fp16 activation fragments of the prepared rows (act_rows_prepare): row r scaled by 2^shift[r] and
@@ -232,10 +233,10 @@ __device__ __noinline__ void act_rows_prepare(uint16_t *x, int64_t ldx, int m, i
 // and blocks k/16 .. kbp - 1 are zero. Item (row, segment) per warp; lane (bb, t) = (lane >> 2,
 // lane & 3) assembles whole fragments (cols 2t|2t+1 and 2t+8|2t+9 of the segment's blocks b with
 // b & 7 = bb) and stores each with one 8-byte store; the XOR swizzle spreads a warp's stores over
-// the banks. Called by the NC threads of the caller's named barrier 1; ends with that barrier.
+// the banks. Called like act_rows_prepare (tid = the thread's index among the NC threads).
 template <int NC>
 __device__ __noinline__ void act_rows_frags(const uint16_t *x, int64_t ldx, int m, int k, int kbp, int ngrp,
-                                            const int *shift, uint32_t *frag, int tid, int warp, int lane) {
+                                            const int *shift, uint32_t *frag, int bar, int tid, int warp, int lane) {
     constexpr int NW = NC / kWarp;
     const int kb = k / 16;
     uint2 *f2 = reinterpret_cast<uint2 *>(frag);
@@ -263,7 +264,7 @@ __device__ __noinline__ void act_rows_frags(const uint16_t *x, int64_t ldx, int 
                                                 pack_half2(bf16_bits_to_f32(w1 & 0xFFFFu) * sc, bf16_bits_to_f32(w1 >> 16) * sc));
         }
     }
-    bar_sync(1, NC);
+    bar_sync(bar, NC);
 }
 
 }  // namespace dev

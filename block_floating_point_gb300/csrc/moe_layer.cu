@@ -97,11 +97,10 @@ struct MoeMisc {
     float hw[kMaxRows];  // combine weight of the current phase-2 expert per row
     int32_t tk_idx[kMaxRows][kMaxTopK];
     float tk_w[kMaxRows][kMaxTopK];
-    uint32_t bitmap[kMaxExperts / 32];
-    uint32_t umask[kMaxExperts + 1];
-    int16_t pos[kMaxExperts];
+    alignas(16) uint32_t bitmap[kMaxExperts / 32];  // the experts some row chose
+    uint32_t emask[kMaxExperts + 1];  // rows that chose expert e (index kMaxExperts: the shared expert)
     int16_t ulist[kMaxExperts + 1];
-    int8_t uslot[kMaxExperts + 1][kMaxRows];
+    int8_t eslot[kMaxExperts + 1][kMaxRows];  // slot of expert e in row r's top-k (shared: K)
     int8_t colrow[kMaxRows];        // phase 2: fragment column -> row of the current expert
     float2 red[kMoeWarps];          // activation row statistics per (row, segment)
     int32_t p1cnt[kMoeWarps];         // phase 1, units split over warps: parts finished per unit
@@ -126,8 +125,7 @@ __device__ __forceinline__ int p2_cost(uint32_t rowmask) {
 }
 // First phase-2 unit (q = j * noct + o, j = 0..nU) whose cost start cum[j] + o * cost_j is >= X,
 // given cum[j] = the cost of all units of experts before j (cum[0] = 0, cum[nU + 1] = total).
-__device__ __forceinline__ int64_t p2_first_unit(const int32_t *cum, const uint32_t *umask, int nU, int noct,
-                                                 int64_t X) {
+__device__ __forceinline__ int64_t p2_first_unit(const int32_t *cum, int nU, int noct, int64_t X) {
     if (X <= 0) return 0;
     int lo = 0, hi = nU;  // last j with cum[j] < X: cum[0] = 0 < X
     while (lo < hi) {
@@ -137,13 +135,13 @@ __device__ __forceinline__ int64_t p2_first_unit(const int32_t *cum, const uint3
         else
             hi = mid - 1;
     }
-    const int cj = p2_cost(umask[lo]);
+    const int cj = (cum[lo + 1] - cum[lo]) / noct;
     const int64_t o = (X - cum[lo] + cj - 1) / cj;
     return o < noct ? (int64_t)lo * noct + o : (int64_t)(lo + 1) * noct;
 }
 
 // Phase-1 unit g of the list [shared-expert f-tiles, routed f-tiles of union expert 0, 1, ...]:
-// slot-table row (kMaxExperts for the shared expert) and f-tile.
+// position in the union U (kMaxExperts for the shared expert) and f-tile.
 struct P1Tile {
     int jrow, ft;
     bool sh;
@@ -217,7 +215,15 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
     const int64_t gb_h = (int64_t)a.kc_h * a.rec;  // bytes of one gate/up row group
     const int ch1 = a.ch1, ch2 = 2 * a.ch1;
 
-    for (int i = tid; i <= kMaxExperts; i += NC) ms->umask[i] = 0u;
+    // Cross-block counters: the router counter ctrl[0] and the phase barriers ctrl[2], ctrl[3] count to
+    // the grid size. CTA 0 zeroes each once every CTA is past its wait: ctrl[0] after the phase-1
+    // barrier, ctrl[2] (and the row maxima) after the phase-2 barrier, ctrl[3] at the start of the
+    // next launch (no CTA reaches it before CTA 0 has arrived at ctrl[2]). A launch that gave up
+    // (BFP_ETIMEOUT) leaves them set until the workspace is initialised again.
+    if (c == 0 && tid == 0) a.ctrl[3] = 0u;
+    for (int i = tid; i < kMaxExperts; i += NC) ms->emask[i] = 0u;
+    if (tid < a.M) ms->eslot[kMaxExperts][tid] = (int8_t)a.K;
+    if (tid == 0) ms->emask[kMaxExperts] = (1u << a.M) - 1u;
     if (tid < kMaxExperts / 32) ms->bitmap[tid] = 0u;
     if (tid == 0) {
         for (int i = 0; i < NW * a.nsw; ++i) mbar_init(&full[i], 1);
@@ -396,7 +402,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
         STAMP(2);  // stage landed
         uint16_t *const xs = reinterpret_cast<uint16_t *>(stage);
         if (a.norm)
-            act_rows_prepare<NC>(xs, LDXS, a.M, a.H, true, a.eps, ms->shift_x, ms->inv, ms->red, warp, lane);
+            act_rows_prepare<NC>(xs, LDXS, a.M, a.H, true, a.eps, ms->shift_x, ms->inv, ms->red, 1, warp, lane);
 
         // ---- phase-1 unit (run by one warp): f-tile of gate and up over all of k; h = silu(gate) * up
         //      for the rows in the unit's row mask, to the workspace; row maxima of |h| to hmax.
@@ -405,7 +411,8 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
             const int ui = it / p1_S, part = it % p1_S;
             const int r0 = part * p1_nch / p1_S * ch1, r1 = min((part + 1) * p1_nch / p1_S * ch1, a.kc_h);
             const P1Tile pt = p1_tile(c + ui * a.ncta, a.nft_s, a.nft);
-            const uint32_t rowmask = ms->umask[pt.jrow];
+            const int er = pt.sh ? kMaxExperts : ms->ulist[pt.jrow];  // expert row of emask / eslot
+            const uint32_t rowmask = ms->emask[er];
             const uint32_t gm = (((rowmask & 0xFFu) ? 1u : 0u) | ((rowmask & 0xFF00u) ? 2u : 0u)) & ngrp_rows;
             bool both = false;
             if constexpr (NGRP == 2) both = gm == 3u;
@@ -497,7 +504,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
                         const float ga = mul_pow2(va, sh), ub = mul_pow2(vb, sh);
                         const float hv = ga / (1.0f + expf(-ga)) * ub;  // silu(gate) * up
                         const int f = pt.ft * 16 + acc_wrow(lane, i);
-                        a.hbuf[((int64_t)r * (a.K + 1) + ms->uslot[pt.jrow][r]) * a.Fmax + f] = hv;
+                        a.hbuf[((int64_t)r * (a.K + 1) + ms->eslot[er][r]) * a.Fmax + f] = hv;
                         const uint32_t hb = __float_as_uint(fabsf(hv));
                         if (i & 1)
                             mo = max(mo, hb);
@@ -514,9 +521,9 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
                 if (lane < 4) {
                     const int re = 8 * grp + 2 * lane, ro = re + 1;
                     if (re < a.M && ((rowmask >> re) & 1u))
-                        atomicMax(&a.hmax[re * (a.K + 1) + ms->uslot[pt.jrow][re]], me);
+                        atomicMax(&a.hmax[re * (a.K + 1) + ms->eslot[er][re]], me);
                     if (ro < a.M && ((rowmask >> ro) & 1u))
-                        atomicMax(&a.hmax[ro * (a.K + 1) + ms->uslot[pt.jrow][ro]], mo);
+                        atomicMax(&a.hmax[ro * (a.K + 1) + ms->eslot[er][ro]], mo);
                 }
             }
             __syncwarp();
@@ -576,11 +583,17 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
             abort_all();
             goto done;
         }
-        if (tid == 0) red_release_add(&a.ctrl[0], 1u);  // after the CTA barrier: publishes every thread's logits
-
-        // ---- activation fragments for phase 1, while the other CTAs' router rows come in
-        if (!a.norm) act_rows_prepare<NC>(xs, LDXS, a.M, a.H, false, a.eps, ms->shift_x, ms->inv, ms->red, warp, lane);
-        act_rows_frags<NC>(xs, LDXS, a.M, a.H, a.kbp_h, NGRP, ms->shift_x, frag, tid, warp, lane);
+        // ---- warp 0 publishes this CTA's logits (its release waits for them to reach L2); warps
+        //      1 .. NW-1 build the activation fragments for phase 1 meanwhile (named barrier 2)
+        if (warp == 0) {
+            if (tid == 0) red_release_add(&a.ctrl[0], 1u);  // after the CTA barrier: every thread's logits
+        } else {
+            constexpr int NF = NC - kWarp;
+            if (!a.norm)
+                act_rows_prepare<NF>(xs, LDXS, a.M, a.H, false, a.eps, ms->shift_x, ms->inv, ms->red, 2, warp - 1,
+                                     lane);
+            act_rows_frags<NF>(xs, LDXS, a.M, a.H, a.kbp_h, NGRP, ms->shift_x, frag, 2, tid - kWarp, warp - 1, lane);
+        }
         STAMP(1);  // activation fragments built
 
 
@@ -629,7 +642,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
                     const int wl = __ffs(bal) - 1;
                     const int q = __shfl_sync(0xffffffffu, qi[0], wl);
                     if (lane == s) {
-                        my_e = 8 * wl + q;
+                        my_e = min(8 * wl + q, a.E - 1);  // < E: the keys of missing experts are below any logit
                         my_l = key_value(kmax);
                     }
                     const bool win = lane == wl;
@@ -650,6 +663,8 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
                     ms->tk_idx[r][lane] = my_e;
                     ms->tk_w[r][lane] = w;
                     atomicOr(&ms->bitmap[my_e >> 5], 1u << (my_e & 31));
+                    atomicOr(&ms->emask[my_e], 1u << r);
+                    ms->eslot[my_e][r] = (int8_t)lane;
                     if (c == 0) {
                         if (a.topk_idx) a.topk_idx[r * a.K + lane] = my_e;
                         if (a.topk_w) a.topk_w[r * a.K + lane] = w;
@@ -659,59 +674,57 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
             }
             STAMP(27);  // top-k of warp 0's rows done
             bar_sync(1, NC);
-            // The union U (ascending expert index, the shared expert last), the rows and slots that
-            // chose each member, and this CTA's phase-2 range: one warp, no CTA barrier in between.
+            // The union U (ascending expert index, the shared expert last) and this CTA's phase-2 range:
+            // one warp, no CTA barrier in between.
             if (warp == 0) {
+                uint32_t words[kMaxExperts / 32];
+#pragma unroll
+                for (int q = 0; q < kMaxExperts / 128; ++q) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(ms->bitmap + 4 * q);
+                    words[4 * q] = v.x;
+                    words[4 * q + 1] = v.y;
+                    words[4 * q + 2] = v.z;
+                    words[4 * q + 3] = v.w;
+                }
+                const uint32_t below = (1u << lane) - 1u;
                 int base = 0;
+#pragma unroll
                 for (int wd = 0; wd < kMaxExperts / 32; ++wd) {
-                    const uint32_t word = ms->bitmap[wd];
-                    const int pre = __popc(word & ((1u << lane) - 1u));
-                    if ((word >> lane) & 1u) {
-                        const int e = 32 * wd + lane;
-                        ms->pos[e] = (int16_t)(base + pre);
-                        ms->ulist[base + pre] = (int16_t)e;
-                    }
-                    base += __popc(word);
+                    if ((words[wd] >> lane) & 1u) ms->ulist[base + __popc(words[wd] & below)] = (int16_t)(32 * wd + lane);
+                    base += __popc(words[wd]);
                 }
                 const int nU = base;
                 if (lane == 0) {
                     ms->nU = nU;
                     ms->ulist[nU] = (int16_t)a.E;
-                    ms->umask[nU] = (1u << a.M) - 1u;
-                    ms->umask[kMaxExperts] = (1u << a.M) - 1u;
-                }
-                if (lane < a.M) {
-                    ms->uslot[nU][lane] = (int8_t)a.K;
-                    ms->uslot[kMaxExperts][lane] = (int8_t)a.K;
                 }
                 __syncwarp();
-                for (int i = lane; i < a.M * a.K; i += kWarp) {
-                    const int r = i / a.K, s = i - r * a.K;
-                    const int j = ms->pos[ms->tk_idx[r][s]];
-                    atomicOr(&ms->umask[j], 1u << r);
-                    ms->uslot[j][r] = (int8_t)s;
-                }
-                __syncwarp();
-                // phase-2 shares: exclusive prefix of the unit costs over the union (warp scan), then
-                // this CTA's range [first unit starting at >= total*c/ncta, ... >= total*(c+1)/ncta)
-                int carry = 0;
-                for (int j0 = 0; j0 <= nU; j0 += kWarp) {
-                    const int j = j0 + lane;
-                    const int cj = j <= nU ? a.noct * p2_cost(ms->umask[j]) : 0;
-                    int incl = cj;
+                // phase-2 shares: exclusive prefix of the unit costs over U and the shared expert (lane l
+                // sums a run of consecutive members, one warp scan), then this CTA's range [first unit
+                // starting at >= total*c/ncta, ... >= total*(c+1)/ncta)
+                const int n1 = nU + 1, per = (n1 + kWarp - 1) / kWarp;
+                const int j0 = min(lane * per, n1), j1 = min(j0 + per, n1);
+                auto cost = [&](int j) {
+                    return a.noct * p2_cost(ms->emask[j == nU ? kMaxExperts : ms->ulist[j]]);
+                };
+                int local = 0;
+                for (int j = j0; j < j1; ++j) local += cost(j);
+                int incl = local;
 #pragma unroll
-                    for (int o = 1; o < kWarp; o <<= 1) {
-                        const int t = __shfl_up_sync(0xffffffffu, incl, o);
-                        if (lane >= o) incl += t;
-                    }
-                    if (j <= nU) ms->p2cum[j] = carry + incl - cj;
-                    carry += __shfl_sync(0xffffffffu, incl, kWarp - 1);
+                for (int o = 1; o < kWarp; o <<= 1) {
+                    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += t;
                 }
-                if (lane == 0) ms->p2cum[nU + 1] = carry;
+                int run = incl - local;
+                for (int j = j0; j < j1; ++j) {
+                    ms->p2cum[j] = run;
+                    run += cost(j);
+                }
+                if (lane == kWarp - 1) ms->p2cum[n1] = incl;
                 __syncwarp();
                 if (lane < 2) {
-                    const int64_t X = (int64_t)ms->p2cum[nU + 1] * (c + lane) / a.ncta;
-                    ms->p2q[lane] = p2_first_unit(ms->p2cum, ms->umask, nU, a.noct, X);
+                    const int64_t X = (int64_t)ms->p2cum[n1] * (c + lane) / a.ncta;
+                    ms->p2q[lane] = p2_first_unit(ms->p2cum, nU, a.noct, X);
                 }
             }
             bar_sync(1, NC);
@@ -749,6 +762,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
                 goto done;
             }
             STAMP(9);  // phase-1 grid barrier passed
+            if (c == 0 && tid == 0) a.ctrl[0] = 0u;  // every CTA is past the router wait
         }
 
         // ---- 5. down projection + combine. Per expert, the rows that chose it become the
@@ -769,7 +783,8 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
                 const bool sh = j == nU;
                 const int Fe = sh ? a.Fs : a.F;
                 const int kc = sh ? a.kc_fs : a.kc_f, kbp = sh ? a.kbp_fs : a.kbp_f;
-                const uint32_t rowmask = ms->umask[j];
+                const int er = sh ? kMaxExperts : ms->ulist[j];  // expert row of emask / eslot
+                const uint32_t rowmask = ms->emask[er];
                 [[maybe_unused]] const unsigned long long tsu0 = BFP_TRACE_NOW();
                 const bool new_expert = j != cur;
                 if (j != cur) {
@@ -786,9 +801,9 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
                     // phase-1 maximum (weights are positive, so max |w h| = w max |h|, rounding included)
                     if (tid < a.M) {
                         const bool use = (rowmask >> tid) & 1u;
-                        const float w = use ? (sh ? ms->gate_w[tid] : ms->tk_w[tid][ms->uslot[j][tid]]) : 0.f;
+                        const float w = use ? (sh ? ms->gate_w[tid] : ms->tk_w[tid][ms->eslot[er][tid]]) : 0.f;
                         ms->hw[tid] = w;
-                        const uint32_t hm = use ? __ldcg(&a.hmax[tid * (a.K + 1) + ms->uslot[j][tid]]) : 0u;
+                        const uint32_t hm = use ? __ldcg(&a.hmax[tid * (a.K + 1) + ms->eslot[er][tid]]) : 0u;
                         ms->shift_h[tid] = frag_shift(w * __uint_as_float(hm));
                         if (use) ms->colrow[__popc(rowmask & ((1u << tid) - 1u))] = (int8_t)tid;
                     }
@@ -805,7 +820,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
                             const int col = it / (fb * 4), rem = it - col * fb * 4, b = rem >> 2, qq = rem & 3;
                             const int r = ms->colrow[col];
                             const float4 v4 = __ldcg(
-                                reinterpret_cast<const float4 *>(a.hbuf + ((int64_t)r * (a.K + 1) + ms->uslot[j][r]) * a.Fmax) +
+                                reinterpret_cast<const float4 *>(a.hbuf + ((int64_t)r * (a.K + 1) + ms->eslot[er][r]) * a.Fmax) +
                                 rem);
                             const float w = ms->hw[r];
                             const float sc = pow2f(ms->shift_h[r]);
@@ -926,7 +941,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
                             const int col = acc_xrow(lane, g, i);
                             if (col < nr && (!packed || col < 4)) {
                                 const int r = ms->colrow[col];
-                                const int s = ms->uslot[j][r];
+                                const int s = ms->eslot[er][r];
                                 const int n = rg * 16 + acc_wrow(lane, i);
                                 a.part[((int64_t)r * (a.K + 1) + s) * a.H + n] =
                                     mul_pow2(acc[0][g][i], 24 - (MB - 1) - ms->shift_h[r]);
@@ -958,6 +973,10 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
                 goto done;
             }
             STAMP(12);
+            if (c == 0) {  // every CTA is past the phase-1 wait and done reading the row maxima
+                if (tid == 0) a.ctrl[2] = 0u;
+                for (int i = tid; i < a.M * (a.K + 1); i += NC) a.hmax[i] = 0u;
+            }
             // ---- 6. combine: y_r = sum over slots (in slot order) + shared, for this CTA's row groups
             const int g0 = (int)((int64_t)c * a.ng_d / a.ncta), g1 = (int)((int64_t)(c + 1) * a.ng_d / a.ncta);
             for (int i = tid; i < (g1 - g0) * a.M * 16; i += NC) {
@@ -1000,19 +1019,6 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
     __syncthreads();
     STAMP(30);
 #undef STAMP
-    // ---- the last CTA out resets the cross-block counters for the next launch
-    if (tid == 0) {
-        __threadfence();
-        const uint32_t old = atom_add_acq_rel(&a.ctrl[1], 1u);
-        if (old == (uint32_t)(a.ncta - 1)) {
-            for (int i = 0; i < a.M * (a.K + 1); ++i) a.hmax[i] = 0u;
-            a.ctrl[0] = 0u;
-            a.ctrl[2] = 0u;
-            a.ctrl[3] = 0u;
-            __threadfence();
-            atomicExch(&a.ctrl[1], 0u);
-        }
-    }
 }
 
 // ----------------------------------------------------------------------------

@@ -176,7 +176,13 @@ typedef struct {
     const void *shared_down;       /* packed [hidden x shared_ffn] */
 } bfp_moe_layer;
 
-/* Device workspace for moe_decode_layer with m rows (zeroed once, left zeroed). */
+/*
+ * Device workspace for moe_decode_layer / moe_stack_decode with m rows: zeroed
+ * once (bfp_workspace_init) before first use; a successful call leaves it
+ * ready for the next call with any m up to the size it was made for. After a
+ * device-side error (BFP_ETIMEOUT) it must be initialised again. Calls that
+ * share a workspace run in stream order.
+ */
 int moe_workspace_size(const bfp_moe_layer *layer, int m, size_t *bytes);
 
 /* Zeroes a workspace (any of this library's) on the stream; also clears its status word. */
