@@ -59,6 +59,9 @@ constexpr int kMoeWarps = 16;                // warps of the layer kernel (no pr
 constexpr int kMoeThreads = kMoeWarps * 32;
 constexpr int kMaxTopK = 8;
 constexpr int kMaxExperts = 256;
+// Floats of one phase-1 partial tile handed between warps: 2 records (gate, up) x 2 activation
+// groups x 4 accumulators x 32 lanes.
+constexpr int kP1PartFloats = 2 * 2 * 4 * 32;
 
 struct MoeArgs {
     int H, E, F, K, Fs, M, ncta;
@@ -78,6 +81,7 @@ struct MoeArgs {
     uint32_t *status, *ctrl;  // ctrl: [0] router, [1] exit, [2] phase-1, [3] phase-2 barrier counters
     uint32_t *hmax;  // [M][K+1] max |h| bits per (row, slot), raised in phase 1
     float *logits, *hbuf, *part;
+    float *p1part;   // [ncta][NW-1][kP1PartFloats]: phase-1 partial tiles handed between neighbouring warps
     int rec, kc_h, kbp_h, kc_f, kbp_f, kc_fs, kbp_fs;
     int nft, nft_s, ng_d, r2, noct, Fmax;
     int nsw, ch1, slot_bytes, frag_bytes, scr_bytes;  // per-warp slots, phase-1 chunk records, slot bytes
@@ -104,6 +108,7 @@ struct MoeMisc {
     int8_t colrow[kMaxRows];        // phase 2: fragment column -> row of the current expert
     float2 red[kMoeWarps];          // activation row statistics per (row, segment)
     int32_t p1cnt[kMoeWarps];         // phase 1, units split over warps: parts finished per unit
+    int32_t p1flag[kMoeWarps];        // phase 1, contiguous ranges: warp w + 1 has handed over its part
     int32_t p2cum[kMaxExperts + 2];  // phase-2 unit cost before each expert of the union (and the total)
     int64_t p2q[2];                  // this CTA's phase-2 units [p2q[0], p2q[1])
     int nU;
@@ -228,7 +233,10 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
     if (tid == 0) {
         for (int i = 0; i < NW * a.nsw; ++i) mbar_init(&full[i], 1);
         for (int i = 0; i < 4; ++i) ms->flags[i] = 0;
-        for (int i = 0; i < NW; ++i) ms->p1cnt[i] = 0;
+        for (int i = 0; i < NW; ++i) {
+            ms->p1cnt[i] = 0;
+            ms->p1flag[i] = 0;
+        }
         ms->nU = 0;
         mbar_init(&ms->stage_full, 1);
         mbar_fence_init();
@@ -285,11 +293,33 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
         int s_ch = 0;                            // records per chunk
         uint32_t s_b = 0;                        // bytes of a full chunk of one source
         bool s_live = false;
-        // phase 1: this CTA's units are split into p1_S parts each (p1_S > 1 only with one activation
-        // group and fewer units than warps: the parts keep every warp busy); item it = unit it / p1_S,
-        // part it % p1_S (chunks [part * nch / p1_S, (part + 1) * nch / p1_S) of the unit)
-        int p1_S = 1, p1_items = 0, p1_nch = 1;
-        int p1_it = 0;                           // next item this warp issues
+        // phase 1: the CTA's units u = 0 .. nc-1 (list entries c + u * ncta), nch chunks each. With
+        // enough work (nc * nch >= NW * nch) every warp takes a contiguous run of chunks
+        // [C0, C1) = [w * T / NW, (w + 1) * T / NW) of the concatenated list, T = nc * nch (p1_sk): a
+        // unit cut by a run boundary has two parts, the end part as the first item of warp w + 1 and
+        // the start part as the last item of warp w. Otherwise each unit is split into p1_S equal
+        // parts (p1_S > 1 only with one activation group), dealt round-robin: warp w takes parts
+        // w, w + NW, ... of the list of nc * p1_S parts.
+        bool p1_sk = false;
+        int p1_S = 1, p1_items = 0, p1_nch = 1, p1_C0 = 0, p1_C1 = 0;
+        int p1_it = 0;                           // next item (of this warp) to issue
+        struct P1Item {
+            int u, k0c, k1c;  // unit, chunk range [k0c, k1c) of its nch
+        };
+        auto p1_item = [&](int i) -> P1Item {
+            P1Item t;
+            if (p1_sk) {
+                t.u = p1_C0 / p1_nch + i;
+                t.k0c = max(p1_C0 - t.u * p1_nch, 0);
+                t.k1c = min(p1_C1 - t.u * p1_nch, p1_nch);
+            } else {
+                const int it = warp + i * NW, part = it % p1_S;
+                t.u = it / p1_S;
+                t.k0c = part * p1_nch / p1_S;
+                t.k1c = (part + 1) * p1_nch / p1_S;
+            }
+            return t;
+        };
         int q2 = 0, q2end = 0, j2 = 0, oct2 = 0; // phase 2: next unit (and its expert, octet), range end
         int nUl = 0;
         uint8_t *const my_slots = ring + (size_t)warp * a.nsw * a.slot_bytes;
@@ -299,15 +329,15 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
         auto next_segment = [&]() {
             s_live = true;
             if (p1_it < p1_items) {
-                const int i = p1_it / p1_S, part = p1_it % p1_S;
-                const P1Tile pt = p1_tile(c + i * a.ncta, a.nft_s, a.nft);
+                const P1Item t = p1_item(p1_it);
+                const P1Tile pt = p1_tile(c + t.u * a.ncta, a.nft_s, a.nft);
                 const uint8_t *base = pt.sh ? a.sgu : a.gu + (int64_t)ms->ulist[pt.jrow] * a.gu_stride;
-                const int r0 = part * p1_nch / p1_S * ch1, r1 = min((part + 1) * p1_nch / p1_S * ch1, a.kc_h);
+                const int r0 = t.k0c * ch1, r1 = min(t.k1c * ch1, a.kc_h);
                 sa = base + (int64_t)(2 * pt.ft) * gb_h + (int64_t)r0 * a.rec;
                 sb = sa + gb_h;
                 s_left = r1 - r0;
                 s_ch = ch1;
-                p1_it += NW;
+                ++p1_it;
                 return;
             }
             // units whose octet has no row group for this warp are skipped (only an expert's last octet)
@@ -406,11 +436,11 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
 
         // ---- phase-1 unit (run by one warp): f-tile of gate and up over all of k; h = silu(gate) * up
         //      for the rows in the unit's row mask, to the workspace; row maxima of |h| to hmax.
-        auto run_p1_item = [&](int it) {
+        auto run_p1_item = [&](int i) {
             [[maybe_unused]] const unsigned long long tu0 = BFP_TRACE_NOW();
-            const int ui = it / p1_S, part = it % p1_S;
-            const int r0 = part * p1_nch / p1_S * ch1, r1 = min((part + 1) * p1_nch / p1_S * ch1, a.kc_h);
-            const P1Tile pt = p1_tile(c + ui * a.ncta, a.nft_s, a.nft);
+            const P1Item t = p1_item(i);
+            const int r0 = t.k0c * ch1, r1 = min(t.k1c * ch1, a.kc_h);
+            const P1Tile pt = p1_tile(c + t.u * a.ncta, a.nft_s, a.nft);
             const int er = pt.sh ? kMaxExperts : ms->ulist[pt.jrow];  // expert row of emask / eslot
             const uint32_t rowmask = ms->emask[er];
             const uint32_t gm = (((rowmask & 0xFFu) ? 1u : 0u) | ((rowmask & 0xFF00u) ? 2u : 0u)) & ngrp_rows;
@@ -461,15 +491,64 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
                 }
             }
             if (bad) return;
+            if (p1_sk && (t.k0c > 0 || t.k1c < p1_nch)) {
+                // a unit cut by a run boundary: the end part (first item of warp w) goes to the
+                // scratch of boundary w - 1; the start part (last item of warp w) waits for the tile
+                // of boundary w, adds it and writes the unit's results
+                if (t.k0c > 0) {
+                    float *dst = a.p1part + ((size_t)c * (NW - 1) + (warp - 1)) * kP1PartFloats;
+#pragma unroll
+                    for (int r = 0; r < 2; ++r)
+#pragma unroll
+                        for (int gg = 0; gg < NGRP; ++gg)
+#pragma unroll
+                            for (int i4 = 0; i4 < 4; ++i4)
+                                dst[((r * NGRP + gg) * 4 + i4) * kWarp + lane] =
+                                    both ? acc[r][gg][i4] : (gg == 0 ? a1[r][0][i4] : 0.f);
+                    __threadfence();  // the tile reaches L2 before the flag is seen
+                    __syncwarp();
+                    if (lane == 0) reinterpret_cast<volatile int *>(ms->p1flag)[warp - 1] = 1;
+                    return;
+                }
+                bool ok = true;
+                if (lane == 0) {
+                    const volatile int *f = ms->p1flag + warp;
+                    ok = *f != 0;
+                    const uint64_t tw0 = global_ns();
+                    for (int64_t k = 1; !ok && k < a.wait_data.iters; ++k) {
+                        if (vflags[0] || global_ns() - tw0 > a.wait_data.nanos) break;
+                        ok = *f != 0;
+                    }
+                }
+                if (!__shfl_sync(0xffffffffu, (int)ok, 0)) {
+                    abort_warp();
+                    return;
+                }
+                __threadfence_block();
+                const float *src = a.p1part + ((size_t)c * (NW - 1) + warp) * kP1PartFloats;
+#pragma unroll
+                for (int r = 0; r < 2; ++r)
+#pragma unroll
+                    for (int gg = 0; gg < NGRP; ++gg)
+#pragma unroll
+                        for (int i4 = 0; i4 < 4; ++i4) {
+                            const float v = __ldcg(src + ((r * NGRP + gg) * 4 + i4) * kWarp + lane);
+                            if (both)
+                                acc[r][gg][i4] += v;
+                            else if (gg == 0)
+                                a1[r][0][i4] += v;
+                        }
+            }
             if constexpr (NGRP == 1) {
-                if (p1_S > 1) {
+                if (!p1_sk && p1_S > 1) {
+                    const int it = warp + i * NW, ui = t.u;
                     // split unit: store this part's tile; the last part to finish adds the parts in
                     // order (it < NW items, each with its scratch tile) and writes the unit's results
                     float *mine = scr + (size_t)it * 256;
 #pragma unroll
                     for (int r = 0; r < 2; ++r)
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) mine[(r * 4 + i) * kWarp + lane] = a1[r][0][i];
+                        for (int i4 = 0; i4 < 4; ++i4) mine[(r * 4 + i4) * kWarp + lane] = a1[r][0][i4];
                     __syncwarp();
                     int last = 0;
                     if (lane == 0) {
@@ -481,10 +560,10 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
 #pragma unroll
                     for (int r = 0; r < 2; ++r)
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
+                        for (int i4 = 0; i4 < 4; ++i4) {
                             float v = 0.f;
-                            for (int q = 0; q < p1_S; ++q) v += scr[(size_t)(ui * p1_S + q) * 256 + (r * 4 + i) * kWarp + lane];
-                            a1[r][0][i] = v;
+                            for (int q = 0; q < p1_S; ++q) v += scr[(size_t)(ui * p1_S + q) * 256 + (r * 4 + i4) * kWarp + lane];
+                            a1[r][0][i4] = v;
                         }
                 }
             }
@@ -737,11 +816,20 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
             const int p1_total = a.nft_s + nUl * a.nft;
             const int nc = c < p1_total ? (p1_total - c + a.ncta - 1) / a.ncta : 0;  // this CTA's units
             p1_nch = (a.kc_h + ch1 - 1) / ch1;
-            if constexpr (NGRP == 1) {
-                while (nc > 0 && nc * p1_S * 2 <= NW && p1_S * 2 <= p1_nch) p1_S *= 2;
+            // every run at least one unit long (a unit has at most two parts), and room for the tiles
+            p1_sk = a.p1part != nullptr && nc >= NW;
+            if (p1_sk) {
+                const int T = nc * p1_nch;
+                p1_C0 = warp * T / NW;
+                p1_C1 = (warp + 1) * T / NW;
+                p1_items = (p1_C1 - 1) / p1_nch - p1_C0 / p1_nch + 1;
+            } else {
+                if constexpr (NGRP == 1) {
+                    while (nc > 0 && nc * p1_S * 2 <= NW && p1_S * 2 <= p1_nch) p1_S *= 2;
+                }
+                p1_items = warp < nc * p1_S ? (nc * p1_S - warp + NW - 1) / NW : 0;
             }
-            p1_items = nc * p1_S;
-            p1_it = warp;
+            p1_it = 0;
         }
         q2end = (int)ms->p2q[1];
         q2 = (int)ms->p2q[0];
@@ -751,9 +839,9 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
 
         // ---- 4. phase 1: this warp's units of the CTA's list [shared-expert f-tiles, routed f-tiles]
         {
-            for (int it = warp; it < p1_items; it += NW) {
-                if (it == warp + NW) STAMP(21);  // warp 0: second item start
-                run_p1_item(it);
+            for (int i = 0; i < p1_items; ++i) {
+                if (i == 1) STAMP(21);  // warp 0: second item start
+                run_p1_item(i);
             }
             STAMP(8);  // warp 0: phase-1 units done
             tslot = 2;
@@ -1028,7 +1116,9 @@ struct MoePlan {
     Geometry gu, dn, sgu, sdn;
     int ngrp, ncta, nsw, ch1, slot_bytes, frag_bytes, scr_bytes, r2, noct, Fmax, stage_off, stage_r;
     size_t smem;
-    size_t off_ctrl, off_hmax, off_logits, off_hbuf, off_part, ws_bytes;
+    size_t off_ctrl, off_hmax, off_logits, off_hbuf, off_part, off_p1part;
+    size_t ws_core;   // bytes the layer cannot run without
+    size_t ws_bytes;  // plus the phase-1 handoff tiles (moe_workspace_size)
 };
 
 static int validate_layer(const bfp_moe_layer *L, int m) {
@@ -1112,6 +1202,9 @@ static int plan_moe(const bfp_moe_layer *L, int m, MoePlan *p) {
     o = align_up(o + 4 * (size_t)m * (L->top_k + 1) * p->Fmax, 256);
     p->off_part = o;
     o = align_up(o + 4 * (size_t)m * (L->top_k + 1) * L->hidden, 256);
+    p->ws_core = o;
+    p->off_p1part = o;
+    o = align_up(o + 4 * (size_t)p->ncta * (kMoeWarps - 1) * kP1PartFloats, 256);
     p->ws_bytes = o;
     return BFP_OK;
 }
@@ -1152,7 +1245,8 @@ static int moe_launch(const bfp_moe_layer *L, const uint16_t *x, int m, int norm
     if (!aligned16(x) || (y && !aligned16(y)) || (h_out && !aligned16(h_out)) || !aligned16(ws) ||
         (topk_idx && ((uintptr_t)topk_idx & 3u)) || (topk_w && ((uintptr_t)topk_w & 3u)))
         return fail(BFP_EALIGN, "device pointers must be 16-byte aligned");
-    if (!ws || ws_bytes < p.ws_bytes) return fail(BFP_EWORKSPACE, "workspace smaller than moe_workspace_size");
+    // a workspace of ws_core bytes runs the layer without the phase-1 handoff tiles (whole units per warp)
+    if (!ws || ws_bytes < p.ws_core) return fail(BFP_EWORKSPACE, "workspace smaller than moe_workspace_size");
     uint8_t *w = static_cast<uint8_t *>(ws);
     MoeArgs a;
     a.H = L->hidden;
@@ -1184,6 +1278,7 @@ static int moe_launch(const bfp_moe_layer *L, const uint16_t *x, int m, int norm
     a.logits = reinterpret_cast<float *>(w + p.off_logits);
     a.hbuf = reinterpret_cast<float *>(w + p.off_hbuf);
     a.part = reinterpret_cast<float *>(w + p.off_part);
+    a.p1part = ws_bytes >= p.ws_bytes ? reinterpret_cast<float *>(w + p.off_p1part) : nullptr;
     a.rec = p.gu.rec;
     a.kc_h = (int)p.gu.kc;
     a.kbp_h = (int)(p.gu.kc * p.gu.cb);
@@ -1336,8 +1431,8 @@ extern "C" int moe_decode_layer_static(const bfp_moe_layer *layer, const uint16_
     MoePlan p;
     int rc = plan_moe(layer, m, &p);
     if (rc) return rc;
-    if (p.ws_bytes > kStaticScratchBytes)
-        return fail(BFP_EWORKSPACE, "this layer needs " + std::to_string(p.ws_bytes) +
+    if (p.ws_core > kStaticScratchBytes)
+        return fail(BFP_EWORKSPACE, "this layer needs " + std::to_string(p.ws_core) +
                                         " bytes of scratch; the built-in scratch holds " +
                                         std::to_string(kStaticScratchBytes) +
                                         " (use moe_decode_layer with a caller-allocated workspace)");
