@@ -4,14 +4,20 @@
 #pragma once
 
 #ifdef BFP_TRACE
-#define BFP_TRACE_SLOTS 64
+#define BFP_TRACE_SLOTS 128
 // One copy per translation unit, set through that unit's bfp_debug_set_trace
 // (trace builds only); one row of slots per CTA.
 static __device__ unsigned long long *g_bfp_trace = nullptr;
 #define BFP_TRACE_AT(slot)                                                                                  \
     do {                                                                                                    \
-        if (g_bfp_trace != nullptr && (threadIdx.x == 0 || threadIdx.x == 256))                             \
-            g_bfp_trace[(size_t)blockIdx.x * BFP_TRACE_SLOTS + (slot) + (threadIdx.x == 256 ? 48 : 0)] =    \
+        if (g_bfp_trace != nullptr && threadIdx.x == 0)                                                     \
+            g_bfp_trace[(size_t)blockIdx.x * BFP_TRACE_SLOTS + (slot)] = bfp::dev::global_ns();              \
+    } while (0)
+// Lane 0 of every warp stamps slot (base + warp index) of its CTA's row.
+#define BFP_TRACE_WARP(base)                                                                                \
+    do {                                                                                                    \
+        if (g_bfp_trace != nullptr && (threadIdx.x & 31) == 0)                                              \
+            g_bfp_trace[(size_t)blockIdx.x * BFP_TRACE_SLOTS + (base) + (threadIdx.x >> 5)] =               \
                 bfp::dev::global_ns();                                                                      \
     } while (0)
 // Stores a value (a duration accumulated in registers, a count) into a slot of thread 0's row.
@@ -26,6 +32,9 @@ static __device__ unsigned long long *g_bfp_trace = nullptr;
     do {                       \
     } while (0)
 #define BFP_TRACE_NOW() 0ull
+#define BFP_TRACE_WARP(base) \
+    do {                     \
+    } while (0)
 #define BFP_TRACE_AT(slot) \
     do {                   \
     } while (0)

@@ -844,6 +844,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
                 run_p1_item(i);
             }
             STAMP(8);  // warp 0: phase-1 units done
+            BFP_TRACE_WARP(64);  // every warp: phase-1 items done
             tslot = 2;
             if (!grid_barrier(&a.ctrl[2])) {  // every CTA's h and row maxima written
                 abort_all();
@@ -1043,6 +1044,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
                 ++p2n;
             }
             STAMP(11);  // down projections done
+            BFP_TRACE_WARP(80);  // every warp: phase-2 units done
             BFP_TRACE_SET(40, tacc[0]);
             BFP_TRACE_SET(41, tacc[1]);
             BFP_TRACE_SET(42, tacc[2]);
