@@ -13,6 +13,12 @@ static __device__ unsigned long long *g_bfp_trace = nullptr;
         if (g_bfp_trace != nullptr && threadIdx.x == 0)                                                     \
             g_bfp_trace[(size_t)blockIdx.x * BFP_TRACE_SLOTS + (slot)] = bfp::dev::global_ns();              \
     } while (0)
+// Thread t stamps a slot of its CTA's row.
+#define BFP_TRACE_AT_T(slot, t)                                                                             \
+    do {                                                                                                    \
+        if (g_bfp_trace != nullptr && threadIdx.x == (t))                                                   \
+            g_bfp_trace[(size_t)blockIdx.x * BFP_TRACE_SLOTS + (slot)] = bfp::dev::global_ns();              \
+    } while (0)
 // Lane 0 of every warp stamps slot (base + warp index) of its CTA's row.
 #define BFP_TRACE_WARP(base)                                                                                \
     do {                                                                                                    \
@@ -34,6 +40,9 @@ static __device__ unsigned long long *g_bfp_trace = nullptr;
 #define BFP_TRACE_NOW() 0ull
 #define BFP_TRACE_WARP(base) \
     do {                     \
+    } while (0)
+#define BFP_TRACE_AT_T(slot, t) \
+    do {                        \
     } while (0)
 #define BFP_TRACE_AT(slot) \
     do {                   \

@@ -109,7 +109,7 @@ struct MoeMisc {
     float2 red[kMoeWarps];          // activation row statistics per (row, segment)
     int32_t p1cnt[kMoeWarps];         // phase 1, units split over warps: parts finished per unit
     int32_t p1flag[kMoeWarps];        // phase 1, contiguous ranges: warp w + 1 has handed over its part
-    int32_t p2cum[kMaxExperts + 2];  // phase-2 unit cost before each expert of the union (and the total)
+    uint32_t wsum[kMoeWarps];         // routing: per-warp sums of the union scan
     int64_t p2q[2];                  // this CTA's phase-2 units [p2q[0], p2q[1])
     int nU;
     int flags[4];  // [0] abort
@@ -128,23 +128,6 @@ __device__ __forceinline__ int p2_cost(uint32_t rowmask) {
     const int n = __popc(rowmask);
     return n <= 4 ? 1 : (n <= 8 ? 2 : 4);
 }
-// First phase-2 unit (q = j * noct + o, j = 0..nU) whose cost start cum[j] + o * cost_j is >= X,
-// given cum[j] = the cost of all units of experts before j (cum[0] = 0, cum[nU + 1] = total).
-__device__ __forceinline__ int64_t p2_first_unit(const int32_t *cum, int nU, int noct, int64_t X) {
-    if (X <= 0) return 0;
-    int lo = 0, hi = nU;  // last j with cum[j] < X: cum[0] = 0 < X
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (cum[mid] < X)
-            lo = mid;
-        else
-            hi = mid - 1;
-    }
-    const int cj = (cum[lo + 1] - cum[lo]) / noct;
-    const int64_t o = (X - cum[lo] + cj - 1) / cj;
-    return o < noct ? (int64_t)lo * noct + o : (int64_t)(lo + 1) * noct;
-}
-
 // Phase-1 unit g of the list [shared-expert f-tiles, routed f-tiles of union expert 0, 1, ...]:
 // position in the union U (kMaxExperts for the shared expert) and f-tile.
 struct P1Tile {
@@ -230,17 +213,16 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
     if (tid < a.M) ms->eslot[kMaxExperts][tid] = (int8_t)a.K;
     if (tid == 0) ms->emask[kMaxExperts] = (1u << a.M) - 1u;
     if (tid < kMaxExperts / 32) ms->bitmap[tid] = 0u;
-    if (tid == 0) {
-        for (int i = 0; i < NW * a.nsw; ++i) mbar_init(&full[i], 1);
-        for (int i = 0; i < 4; ++i) ms->flags[i] = 0;
-        for (int i = 0; i < NW; ++i) {
-            ms->p1cnt[i] = 0;
-            ms->p1flag[i] = 0;
-        }
-        ms->nU = 0;
-        mbar_init(&ms->stage_full, 1);
+    if (tid <= NW * a.nsw) {  // one barrier per thread
+        mbar_init(tid < NW * a.nsw ? &full[tid] : &ms->stage_full, 1);
         mbar_fence_init();
     }
+    if (tid < NW) {
+        ms->p1cnt[tid] = 0;
+        ms->p1flag[tid] = 0;
+    }
+    if (tid < 4) ms->flags[tid] = 0;
+    if (tid == 0) ms->nU = 0;
     __syncthreads();
     STAMP(13);
     const int LDXS = stage_ldx(a.H);
@@ -645,6 +627,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
                         make_float4(d[0], d[1], d[2], d[3]);
                 }
             }
+            STAMP(96);  // router tiles stored
             bar_sync(1, NC);
             const int LS = logit_stride(a.E);
             for (int idx = tid; !bad && idx < nrows * a.M; idx += NC) {
@@ -662,152 +645,187 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
             abort_all();
             goto done;
         }
-        // ---- warp 0 publishes this CTA's logits (its release waits for them to reach L2); warps
-        //      1 .. NW-1 build the activation fragments for phase 1 meanwhile (named barrier 2)
-        if (warp == 0) {
-            if (tid == 0) red_release_add(&a.ctrl[0], 1u);  // after the CTA barrier: every thread's logits
-        } else {
-            constexpr int NF = NC - kWarp;
-            if (!a.norm)
-                act_rows_prepare<NF>(xs, LDXS, a.M, a.H, false, a.eps, ms->shift_x, ms->inv, ms->red, 2, warp - 1,
-                                     lane);
-            act_rows_frags<NF>(xs, LDXS, a.M, a.H, a.kbp_h, NGRP, ms->shift_x, frag, 2, tid - kWarp, warp - 1, lane);
-        }
-        STAMP(1);  // activation fragments built
-
-
-        // ---- 3. routing: wait for every CTA's router rows, then top-k and the expert union
+        STAMP(97);  // logits written
+        // ---- two groups of warps from here to the end of the routing:
+        //      warps 0 .. NR-1: warp 0 publishes this CTA's logits (its release waits for them to reach
+        //        L2); then every CTA's router rows, top-k and the union (named barrier 3);
+        //      warps NR .. NW-1: the activation fragments for phase 1 (named barrier 2), which nothing
+        //        needs before the first weight chunks land.
         {
-            bool ok = true;
-            if (tid == 0) ok = wait_counter(&a.ctrl[0], (uint32_t)a.ncta, a.wait);
-            if (bar_or(1, NC, !ok)) {
+            constexpr int NR = NW / 2;                     // routing warps
+            constexpr int RPW = (kMaxRows + NR - 1) / NR;  // rows per routing warp
+            if (warp >= NR) {
+                BFP_TRACE_AT_T(110, NR * kWarp);
+                constexpr int NF = NC - NR * kWarp;
+                if (!a.norm)
+                    act_rows_prepare<NF>(xs, LDXS, a.M, a.H, false, a.eps, ms->shift_x, ms->inv, ms->red, 2,
+                                         warp - NR, lane);
+                BFP_TRACE_AT_T(111, NR * kWarp);
+                act_rows_frags<NF>(xs, LDXS, a.M, a.H, a.kbp_h, NGRP, ms->shift_x, frag, 2, tid - NR * kWarp,
+                                   warp - NR, lane);
+                STAMP(1);  // activation fragments built
+                BFP_TRACE_AT_T(112, NR * kWarp);
+            } else {
+                bool ok = true;
+                if (tid == 0) {
+                    red_release_add(&a.ctrl[0], 1u);  // after the CTA barrier: every thread's logits
+                    STAMP(98);
+                    ok = wait_counter(&a.ctrl[0], (uint32_t)a.ncta, a.wait);
+                    STAMP(99);
+                }
+                if (bar_or(3, NR * kWarp, !ok)) bad = true;
+                STAMP(100);
+                STAMP(5);  // every CTA's router rows published
+                // Top-k per row, on the logits every CTA wrote before the router counter (read from
+                // L2); warp w takes rows w and w + NR, as two independent chains. Lane l holds experts
+                // 8l .. 8l+7 and first sorts them (key descending, index ascending among equal keys);
+                // each round the lanes offer their heads, the largest key wins and among equal keys the
+                // lowest lane, i.e. the lowest expert index (ties go to the lower index); lane s keeps
+                // the slot-s winner. Slot 0 is the row maximum, so p_s = exp(l_s - l_0) and
+                // w_s = p_s / sum of p.
+                const int LS = logit_stride(a.E);
+                uint32_t key[RPW][8];
+                int qi[RPW][8];
+                float gate_logit[RPW];
+#pragma unroll
+                for (int j = 0; j < RPW; ++j) {
+                    const int r = warp + NR * j;
+                    const float *row = a.logits + (int64_t)r * LS;
+                    if (bad || r >= a.M) {
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) key[j][q] = 0u;
+                        gate_logit[j] = 0.f;
+                    } else if (8 * lane + 8 <= a.E) {
+                        const float4 v0 = __ldcg(reinterpret_cast<const float4 *>(row + 8 * lane));
+                        const float4 v1 = __ldcg(reinterpret_cast<const float4 *>(row + 8 * lane + 4));
+                        const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) key[j][q] = order_key(v[q]);
+                        gate_logit[j] = __ldcg(row + a.E);
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const int e = 8 * lane + q;
+                            key[j][q] = e < a.E ? order_key(__ldcg(row + e)) : 0u;  // 0: below any logit
+                        }
+                        gate_logit[j] = __ldcg(row + a.E);
+                    }
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) qi[j][q] = q;
+                    sort8_desc(key[j], qi[j]);
+                }
+                STAMP(102);  // logits loaded and sorted
+                int my_e[RPW] = {};
+                float my_l[RPW] = {};
+                for (int s = 0; s < a.K; ++s) {
+#pragma unroll
+                    for (int j = 0; j < RPW; ++j) {
+                        const uint32_t kmax = __reduce_max_sync(0xffffffffu, key[j][0]);
+                        const uint32_t bal = __ballot_sync(0xffffffffu, key[j][0] == kmax);
+                        const int wl = __ffs(bal) - 1;
+                        const int q = __shfl_sync(0xffffffffu, qi[j][0], wl);
+                        if (lane == s) {
+                            my_e[j] = min(8 * wl + q, a.E - 1);  // < E: missing experts' keys are below any logit
+                            my_l[j] = key_value(kmax);
+                        }
+                        const bool win = lane == wl;
+#pragma unroll
+                        for (int i = 0; i < 7; ++i) {
+                            key[j][i] = win ? key[j][i + 1] : key[j][i];
+                            qi[j][i] = win ? qi[j][i + 1] : qi[j][i];
+                        }
+                        key[j][7] = win ? 0u : key[j][7];
+                    }
+                }
+                STAMP(103);  // rounds done
+#pragma unroll
+                for (int j = 0; j < RPW; ++j) {
+                    const int r = warp + NR * j;
+                    const float l0 = __shfl_sync(0xffffffffu, my_l[j], 0);
+                    const float p = lane < a.K ? __expf(my_l[j] - l0) : 0.f;
+                    float psum = p;
+#pragma unroll
+                    for (int o = 1; o < kWarp; o <<= 1) psum += __shfl_xor_sync(0xffffffffu, psum, o);
+                    if (!bad && r < a.M) {
+                        if (lane < a.K) {
+                            const float w = __fdividef(p, psum);
+                            const int e = my_e[j];
+                            ms->tk_idx[r][lane] = e;
+                            ms->tk_w[r][lane] = w;
+                            atomicOr(&ms->bitmap[e >> 5], 1u << (e & 31));
+                            atomicOr(&ms->emask[e], 1u << r);
+                            ms->eslot[e][r] = (int8_t)lane;
+                            if (c == 0) {
+                                if (a.topk_idx) a.topk_idx[r * a.K + lane] = e;
+                                if (a.topk_w) a.topk_w[r * a.K + lane] = w;
+                            }
+                        }
+                        if (lane == 0) ms->gate_w[r] = __fdividef(1.0f, 1.0f + __expf(-gate_logit[j]));
+                    }
+                }
+                STAMP(27);  // top-k of warp 0's rows done
+                bar_sync(3, NR * kWarp);
+                STAMP(105);
+                // The union U (ascending expert index, the shared expert last) and this CTA's phase-2
+                // range, one routing thread per expert: an exclusive scan of (member, cost of its
+                // units) over the experts gives each member its position in U and the cost of the
+                // units before it; the member whose cost interval holds one of the CTA's share
+                // boundaries X = total * c / ncta, total * (c + 1) / ncta writes the first unit that
+                // starts at or after X.
+                {
+                    static_assert(NR * kWarp == kMaxExperts, "one routing thread per expert");
+                    const int e = tid;
+                    const bool in_u = e < a.E && ((ms->bitmap[e >> 5] >> (e & 31)) & 1u);
+                    const int cu = in_u ? p2_cost(ms->emask[e]) : 0;  // cost of one unit of expert e
+                    const uint32_t v = in_u ? (1u << 16) | (uint32_t)(a.noct * cu) : 0u;
+                    uint32_t incl = v;
+#pragma unroll
+                    for (int o = 1; o < kWarp; o <<= 1) {
+                        const uint32_t t2 = __shfl_up_sync(0xffffffffu, incl, o);
+                        if (lane >= o) incl += t2;
+                    }
+                    if (lane == kWarp - 1) ms->wsum[warp] = incl;
+                    bar_sync(3, NR * kWarp);
+                    uint32_t before = 0, total = 0;
+#pragma unroll
+                    for (int w2 = 0; w2 < NR; ++w2) {
+                        const uint32_t ws2 = ms->wsum[w2];
+                        before += w2 < warp ? ws2 : 0u;
+                        total += ws2;
+                    }
+                    const uint32_t ex = before + incl - v;
+                    const int pos = (int)(ex >> 16), cum = (int)(ex & 0xFFFFu);
+                    const int nU = (int)(total >> 16), cost_r = (int)(total & 0xFFFFu);
+                    const int cu_s = p2_cost(ms->emask[kMaxExperts]);
+                    const int tot = cost_r + a.noct * cu_s;
+                    if (in_u) ms->ulist[pos] = (int16_t)e;
+                    if (e == 0) {
+                        ms->nU = nU;
+                        ms->ulist[nU] = (int16_t)a.E;
+                    }
+                    STAMP(106);
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        const int X = tot * (c + i) / a.ncta;
+                        if (in_u && cum <= X && X < cum + a.noct * cu) {
+                            const int o = (X - cum + cu - 1) / cu;
+                            ms->p2q[i] = o < a.noct ? pos * a.noct + o : (pos + 1) * a.noct;
+                        }
+                        if (e == 0 && cost_r <= X && X < tot) {
+                            const int o = (X - cost_r + cu_s - 1) / cu_s;
+                            ms->p2q[i] = o < a.noct ? nU * a.noct + o : (nU + 1) * a.noct;
+                        }
+                        if (e == 0 && X >= tot) ms->p2q[i] = (nU + 1) * a.noct;
+                    }
+                }
+            }
+            // every warp: the fragments, the union and the phase-2 range are in shared memory
+            if (bar_or(1, NC, bad)) {
                 abort_all();
                 goto done;
             }
-            STAMP(5);  // every CTA's router rows published
-            // Top-k per row, one warp per row (warp w: rows w, w + NW, ...), on the logits every CTA
-            // wrote before the router counter (read from L2). Lane l holds experts 8l .. 8l+7 and first
-            // sorts them (key descending, index ascending among equal keys); each round the lanes offer
-            // their heads, the largest key wins and among equal keys the lowest lane, i.e. the lowest
-            // expert index (ties go to the lower index); lane s keeps the slot-s winner.
-            // Slot 0 is the row maximum, so p_s = exp(l_s - l_0) and w_s = p_s / sum of p.
-            const int LS = logit_stride(a.E);
-            for (int r = warp; r < a.M; r += NW) {
-                const float *row = a.logits + (int64_t)r * LS;
-                uint32_t key[8];
-                int qi[8];
-                if (8 * lane + 8 <= a.E) {
-                    const float4 v0 = __ldcg(reinterpret_cast<const float4 *>(row + 8 * lane));
-                    const float4 v1 = __ldcg(reinterpret_cast<const float4 *>(row + 8 * lane + 4));
-                    const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) key[q] = order_key(v[q]);
-                } else {
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const int e = 8 * lane + q;
-                        key[q] = e < a.E ? order_key(__ldcg(row + e)) : 0u;  // 0: below any logit
-                    }
-                }
-                const float gate_logit = __ldcg(row + a.E);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) qi[q] = q;
-                sort8_desc(key, qi);
-                int my_e = 0;
-                float my_l = 0.f;
-                for (int s = 0; s < a.K; ++s) {
-                    const uint32_t kmax = __reduce_max_sync(0xffffffffu, key[0]);
-                    const uint32_t bal = __ballot_sync(0xffffffffu, key[0] == kmax);
-                    const int wl = __ffs(bal) - 1;
-                    const int q = __shfl_sync(0xffffffffu, qi[0], wl);
-                    if (lane == s) {
-                        my_e = min(8 * wl + q, a.E - 1);  // < E: the keys of missing experts are below any logit
-                        my_l = key_value(kmax);
-                    }
-                    const bool win = lane == wl;
-#pragma unroll
-                    for (int i = 0; i < 7; ++i) {
-                        key[i] = win ? key[i + 1] : key[i];
-                        qi[i] = win ? qi[i + 1] : qi[i];
-                    }
-                    key[7] = win ? 0u : key[7];
-                }
-                const float l0 = __shfl_sync(0xffffffffu, my_l, 0);
-                const float p = lane < a.K ? expf(my_l - l0) : 0.f;
-                float psum = p;
-#pragma unroll
-                for (int o = 1; o < kWarp; o <<= 1) psum += __shfl_xor_sync(0xffffffffu, psum, o);
-                if (lane < a.K) {
-                    const float w = p / psum;
-                    ms->tk_idx[r][lane] = my_e;
-                    ms->tk_w[r][lane] = w;
-                    atomicOr(&ms->bitmap[my_e >> 5], 1u << (my_e & 31));
-                    atomicOr(&ms->emask[my_e], 1u << r);
-                    ms->eslot[my_e][r] = (int8_t)lane;
-                    if (c == 0) {
-                        if (a.topk_idx) a.topk_idx[r * a.K + lane] = my_e;
-                        if (a.topk_w) a.topk_w[r * a.K + lane] = w;
-                    }
-                }
-                if (lane == 0) ms->gate_w[r] = 1.0f / (1.0f + expf(-gate_logit));
-            }
-            STAMP(27);  // top-k of warp 0's rows done
-            bar_sync(1, NC);
-            // The union U (ascending expert index, the shared expert last) and this CTA's phase-2 range:
-            // one warp, no CTA barrier in between.
-            if (warp == 0) {
-                uint32_t words[kMaxExperts / 32];
-#pragma unroll
-                for (int q = 0; q < kMaxExperts / 128; ++q) {
-                    const uint4 v = *reinterpret_cast<const uint4 *>(ms->bitmap + 4 * q);
-                    words[4 * q] = v.x;
-                    words[4 * q + 1] = v.y;
-                    words[4 * q + 2] = v.z;
-                    words[4 * q + 3] = v.w;
-                }
-                const uint32_t below = (1u << lane) - 1u;
-                int base = 0;
-#pragma unroll
-                for (int wd = 0; wd < kMaxExperts / 32; ++wd) {
-                    if ((words[wd] >> lane) & 1u) ms->ulist[base + __popc(words[wd] & below)] = (int16_t)(32 * wd + lane);
-                    base += __popc(words[wd]);
-                }
-                const int nU = base;
-                if (lane == 0) {
-                    ms->nU = nU;
-                    ms->ulist[nU] = (int16_t)a.E;
-                }
-                __syncwarp();
-                // phase-2 shares: exclusive prefix of the unit costs over U and the shared expert (lane l
-                // sums a run of consecutive members, one warp scan), then this CTA's range [first unit
-                // starting at >= total*c/ncta, ... >= total*(c+1)/ncta)
-                const int n1 = nU + 1, per = (n1 + kWarp - 1) / kWarp;
-                const int j0 = min(lane * per, n1), j1 = min(j0 + per, n1);
-                auto cost = [&](int j) {
-                    return a.noct * p2_cost(ms->emask[j == nU ? kMaxExperts : ms->ulist[j]]);
-                };
-                int local = 0;
-                for (int j = j0; j < j1; ++j) local += cost(j);
-                int incl = local;
-#pragma unroll
-                for (int o = 1; o < kWarp; o <<= 1) {
-                    const int t = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += t;
-                }
-                int run = incl - local;
-                for (int j = j0; j < j1; ++j) {
-                    ms->p2cum[j] = run;
-                    run += cost(j);
-                }
-                if (lane == kWarp - 1) ms->p2cum[n1] = incl;
-                __syncwarp();
-                if (lane < 2) {
-                    const int64_t X = (int64_t)ms->p2cum[n1] * (c + lane) / a.ncta;
-                    ms->p2q[lane] = p2_first_unit(ms->p2cum, nU, a.noct, X);
-                }
-            }
-            bar_sync(1, NC);
         }
+        STAMP(109);
         STAMP(6);  // top-k + union done
         // this warp's stream: its units and the CTA's phase-2 range are known now; fill its slots
         // (every warp is past its reads of the stage, which the first slots may overlap)
@@ -1176,6 +1194,8 @@ static int plan_moe(const bfp_moe_layer *L, int m, MoePlan *p) {
     // phase 2: units of up to one row group per consumer warp
     p->r2 = (int)std::min<int64_t>(kMoeWarps, p->dn.ng);
     p->noct = (int)((p->dn.ng + p->r2 - 1) / p->r2);
+    // the routing scan packs the phase-2 cost of the union into 16 bits
+    if ((int64_t)p->noct * 4 * (kMaxExperts + 1) >= 65536) return fail(BFP_ESHAPE, "hidden size too large");
     // per-warp slots: a phase-1 chunk is ch1 records of a gate row group and the same of its up row
     // group, a phase-2 chunk 2 * ch1 records of one row group
     p->ch1 = (int)std::min<int64_t>(4, p->gu.kc);
