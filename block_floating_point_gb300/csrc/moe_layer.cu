@@ -62,6 +62,8 @@ constexpr int kMaxExperts = 256;
 // Floats of one phase-1 partial tile handed between warps: 2 records (gate, up) x 2 activation
 // groups x 4 accumulators x 32 lanes.
 constexpr int kP1PartFloats = 2 * 2 * 4 * 32;
+// Experts whose phase-2 fragments one batch sets up together.
+constexpr int kP2Batch = 4;
 
 struct MoeArgs {
     int H, E, F, K, Fs, M, ncta;
@@ -91,25 +93,31 @@ struct MoeArgs {
 };
 
 // Shared-memory bookkeeping of one CTA.
+// Phase 2: one expert of a batch (its units, up to qend, run on fragments set up together).
+struct P2Entry {
+    int j, er, nr, parts, off, qend;  // union position, emask row, rows, fragment parts (1, 2, 4), word offset
+};
+
 struct MoeMisc {
     alignas(16) float esc[kMoeWarps][rec_scale_floats<4, 2>()];  // per-warp block scales (mma_records)
     uint64_t stage_full;  // the preamble stage (activation rows, router rows) landed
     int shift_x[kMaxRows];
     float inv[kMaxRows];
-    int shift_h[kMaxRows];
     float gate_w[kMaxRows];
-    float hw[kMaxRows];  // combine weight of the current phase-2 expert per row
     int32_t tk_idx[kMaxRows][kMaxTopK];
     float tk_w[kMaxRows][kMaxTopK];
     alignas(16) uint32_t bitmap[kMaxExperts / 32];  // the experts some row chose
     uint32_t emask[kMaxExperts + 1];  // rows that chose expert e (index kMaxExperts: the shared expert)
     int16_t ulist[kMaxExperts + 1];
     int8_t eslot[kMaxExperts + 1][kMaxRows];  // slot of expert e in row r's top-k (shared: K)
-    int8_t colrow[kMaxRows];        // phase 2: fragment column -> row of the current expert
     float2 red[kMoeWarps];          // activation row statistics per (row, segment)
     int32_t p1cnt[kMoeWarps];         // phase 1, units split over warps: parts finished per unit
     int32_t p1flag[kMoeWarps];        // phase 1, contiguous ranges: warp w + 1 has handed over its part
     uint32_t wsum[kMoeWarps];         // routing: per-warp sums of the union scan
+    P2Entry p2b[kP2Batch];            // phase 2: the experts of the current batch
+    int8_t p2row[kP2Batch][kMaxRows];  // ... fragment column -> row
+    int p2shift[kP2Batch][kMaxRows];   // ... fragment column -> power-of-two scale of its h
+    int p2nb;
     int64_t p2q[2];                  // this CTA's phase-2 units [p2q[0], p2q[1])
     int nU;
     int flags[4];  // [0] abort
@@ -122,11 +130,13 @@ __host__ __device__ inline int logit_stride(int E) { return (E + 1 + 3) & ~3; }
 // Row stride (elements) of the activation rows staged in shared memory: 16 bytes of padding per row.
 __host__ __device__ inline int stage_ldx(int H) { return H + 8; }
 
-// Phase-2 unit cost in MMAs per block: an expert used by <= 4 rows carries the hi and lo halves of
-// its rows' h in one 8-column MMA; <= 8 rows need two MMAs (hi, lo); more rows two groups of two.
+// Phase-2 unit cost, for sharing the units between CTAs: every unit streams the same bytes and unpacks
+// the same weight tiles (about three MMAs' worth of issue per block); an expert used by <= 4 rows adds
+// one MMA per block (hi and lo halves of its rows' h in one 8-column MMA), <= 8 rows two (hi, lo),
+// more rows four (two column groups of two).
 __device__ __forceinline__ int p2_cost(uint32_t rowmask) {
     const int n = __popc(rowmask);
-    return n <= 4 ? 1 : (n <= 8 ? 2 : 4);
+    return n <= 4 ? 4 : (n <= 8 ? 5 : 7);
 }
 // Phase-1 unit g of the list [shared-expert f-tiles, routed f-tiles of union expert 0, 1, ...]:
 // position in the union U (kMaxExperts for the shared expert) and f-tile.
@@ -872,194 +882,238 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
             if (c == 0 && tid == 0) a.ctrl[0] = 0u;  // every CTA is past the router wait
         }
 
-        // ---- 5. down projection + combine. Per expert, the rows that chose it become the
-        //      columns 0..n-1 of its h fragments (routing weight folded in, fp16 hi + lo parts):
-        //      n <= 4: hi in columns c, lo in columns c + 4 of one 8-column MMA (summed at the end);
-        //      n <= 8: hi and lo fragments, two MMAs; more rows: two column groups.
+        // ---- 5. down projection. Per expert, the rows that chose it become the columns 0..n-1 of
+        //      its h fragments (routing weight folded in, fp16 hi + lo parts): n <= 4: hi in columns
+        //      c, lo in columns c + 4 of one 8-column MMA (summed at the end); n <= 8: hi and lo
+        //      fragments, two MMAs; more rows: two column groups. The CTA takes its units in
+        //      batches: the experts of the next units whose fragments fit in the fragment area
+        //      together (at most kP2Batch) are set up in one pass, then their units run with no
+        //      CTA barrier in between.
         {
             const int nU = ms->nU;
-            const int64_t q0 = ms->p2q[0], q1 = ms->p2q[1];
-            int cur = -1;
+            const int q0 = (int)ms->p2q[0], q1 = (int)ms->p2q[1];
             int p2n = 0;  // phase-2 units done by this CTA (trace stamps)
-            int nr = 0;
-            bool packed = false;
-            uint32_t gm2 = 1;
             uint32_t *hfrag = frag;  // x fragments are dead once phase 1 is done
-            for (int64_t q = q0; q < q1; ++q) {
-                const int j = (int)(q / a.noct), oct = (int)(q % a.noct);
-                const bool sh = j == nU;
-                const int Fe = sh ? a.Fs : a.F;
-                const int kc = sh ? a.kc_fs : a.kc_f, kbp = sh ? a.kbp_fs : a.kbp_f;
-                const int er = sh ? kMaxExperts : ms->ulist[j];  // expert row of emask / eslot
-                const uint32_t rowmask = ms->emask[er];
+            int q = q0;
+            while (q < q1) {
                 [[maybe_unused]] const unsigned long long tsu0 = BFP_TRACE_NOW();
-                const bool new_expert = j != cur;
-                if (j != cur) {
-                    // every warp is done with the previous expert's fragments
-                    if (bar_or(1, NC, bad)) {
-                        abort_all();
-                        goto done;
+                // every warp is done with the previous batch's fragments
+                if (bar_or(1, NC, bad)) {
+                    abort_all();
+                    goto done;
+                }
+                if (tid == 0) {
+                    int nb = 0, qe = q, off = 0;
+                    while (qe < q1 && nb < kP2Batch) {
+                        const int j = qe / a.noct;
+                        const bool sh = j == nU;
+                        const int er = sh ? kMaxExperts : ms->ulist[j];
+                        const int nr = __popc(ms->emask[er]);
+                        const int kbp = sh ? a.kbp_fs : a.kbp_f;
+                        const int parts = nr <= 4 ? 1 : (nr <= 8 ? 2 : 4);
+                        const int words = parts * kbp * 2 * kWarp;
+                        if (nb > 0 && off + words > a.frag_bytes / 4) break;  // the first one always fits
+                        P2Entry &pe = ms->p2b[nb];
+                        pe.j = j;
+                        pe.er = er;
+                        pe.nr = nr;
+                        pe.parts = parts;
+                        pe.off = off;
+                        pe.qend = min((j + 1) * a.noct, q1);
+                        off += words;
+                        qe = pe.qend;
+                        ++nb;
                     }
-                    if (cur < 0) STAMP(14);  // first expert: setup start
-                    nr = __popc(rowmask);
-                    packed = nr <= 4;
-                    gm2 = nr > 8 ? 3u : 1u;
-                    // routing weight folded into h; per-row power-of-two scale into fp16 range from the
-                    // phase-1 maximum (weights are positive, so max |w h| = w max |h|, rounding included)
-                    if (tid < a.M) {
-                        const bool use = (rowmask >> tid) & 1u;
-                        const float w = use ? (sh ? ms->gate_w[tid] : ms->tk_w[tid][ms->eslot[er][tid]]) : 0.f;
-                        ms->hw[tid] = w;
-                        const uint32_t hm = use ? __ldcg(&a.hmax[tid * (a.K + 1) + ms->eslot[er][tid]]) : 0u;
-                        ms->shift_h[tid] = frag_shift(w * __uint_as_float(hm));
-                        if (use) ms->colrow[__popc(rowmask & ((1u << tid) - 1u))] = (int8_t)tid;
+                    ms->p2nb = nb;
+                }
+                bar_sync(1, NC);
+                const int nb = ms->p2nb;
+                // every fragment word of the batch, once: a thread takes 4 consecutive values of one
+                // column in one block and writes their hi and lo words (zeros for padding columns and
+                // blocks), so no separate clearing pass is needed
+                {
+                    int items = 0;
+                    for (int bi = 0; bi < nb; ++bi) {
+                        const P2Entry &pe = ms->p2b[bi];
+                        const int kbp = pe.j == nU ? a.kbp_fs : a.kbp_f;
+                        items += (pe.parts == 1 ? 4 : 8 * (pe.parts / 2)) * kbp * 4;
                     }
-                    const int words = 2 * NGRP * kbp * kWarp * 2;
-                    for (int i = tid; i < words / 4; i += NC) reinterpret_cast<uint4 *>(hfrag)[i] = make_uint4(0, 0, 0, 0);
-                    bar_sync(1, NC);
-                    if (cur < 0) STAMP(15);  // ... fragments zeroed
-                    // one item = 4 consecutive h values (cols 4qq..4qq+3 of block b) of a column, read
-                    // from the workspace (written by every CTA before the phase-1 grid barrier; L2)
-                    {
-                        const int fb = Fe / 16;
-                        const int lo_off = NGRP * kbp * kWarp * 2;  // words
-                        for (int it = tid; it < nr * fb * 4; it += NC) {
-                            const int col = it / (fb * 4), rem = it - col * fb * 4, b = rem >> 2, qq = rem & 3;
-                            const int r = ms->colrow[col];
-                            const float4 v4 = __ldcg(
-                                reinterpret_cast<const float4 *>(a.hbuf + ((int64_t)r * (a.K + 1) + ms->eslot[er][r]) * a.Fmax) +
-                                rem);
-                            const float w = ms->hw[r];
-                            const float sc = pow2f(ms->shift_h[r]);
+                    for (int it = tid; it < items; it += NC) {
+                        int bi = 0, base = 0, cols = 0, kbp = 0;
+                        for (;; ++bi) {
+                            const P2Entry &pe = ms->p2b[bi];
+                            kbp = pe.j == nU ? a.kbp_fs : a.kbp_f;
+                            cols = pe.parts == 1 ? 4 : 8 * (pe.parts / 2);
+                            if (it - base < cols * kbp * 4 || bi == nb - 1) break;
+                            base += cols * kbp * 4;
+                        }
+                        const P2Entry &pe = ms->p2b[bi];
+                        const bool sh = pe.j == nU;
+                        const int rem0 = it - base, col = rem0 / (kbp * 4), rem = rem0 - col * kbp * 4;
+                        const int blk = rem >> 2, qq = rem & 3;
+                        const int Fe = sh ? a.Fs : a.F;
+                        uint32_t *hf = hfrag + pe.off;
+                        const int lo_off = (pe.parts == 4 ? 2 : 1) * kbp * 2 * kWarp;  // words
+                        uint32_t hw2[2] = {0u, 0u}, lw2[2] = {0u, 0u};
+                        if (col < pe.nr && blk < Fe / 16) {
+                            const uint32_t rowmask = ms->emask[pe.er];
+                            const int r = (int)__fns(rowmask, 0, col + 1);
+                            const int slot = ms->eslot[pe.er][r];
+                            const float w = sh ? ms->gate_w[r] : ms->tk_w[r][slot];
+                            const uint32_t hm = __ldcg(&a.hmax[r * (a.K + 1) + slot]);
+                            const float4 v4 = __ldcg(reinterpret_cast<const float4 *>(
+                                                         a.hbuf + ((int64_t)r * (a.K + 1) + slot) * a.Fmax) +
+                                                     rem);
+                            // routing weight folded into h; per-row power-of-two scale into fp16 range
+                            // from the phase-1 maximum (weights are positive, so max |w h| = w max |h|,
+                            // rounding included)
+                            const int shift = frag_shift(w * __uint_as_float(hm));
+                            const float sc = pow2f(shift);
                             const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
                             for (int pr = 0; pr < 2; ++pr) {
                                 const float v0 = vv[2 * pr] * w * sc, v1 = vv[2 * pr + 1] * w * sc;
                                 const __half h0 = __float2half_rn(v0), h1 = __float2half_rn(v1);
-                                const float r0 = v0 - __half2float(h0), r1 = v1 - __half2float(h1);
                                 __half2 hh = __halves2half2(h0, h1);
-                                hfrag[frag_word(col, b, 2 * qq + pr, kbp)] = *reinterpret_cast<uint32_t *>(&hh);
-                                if (packed)
-                                    hfrag[frag_word(col + 4, b, 2 * qq + pr, kbp)] = pack_half2(r0, r1);
-                                else
-                                    hfrag[lo_off + frag_word(col, b, 2 * qq + pr, kbp)] = pack_half2(r0, r1);
+                                hw2[pr] = *reinterpret_cast<uint32_t *>(&hh);
+                                lw2[pr] = pack_half2(v0 - __half2float(h0), v1 - __half2float(h1));
+                            }
+                            if (blk == 0 && qq == 0) {
+                                ms->p2row[bi][col] = (int8_t)r;
+                                ms->p2shift[bi][col] = shift;
                             }
                         }
-                    }
-                    bar_sync(1, NC);
-                    if (cur < 0) STAMP(10);  // first expert's h fragments ready
-                    cur = j;
-                }
-                if (new_expert) {
-                    tacc[7] += BFP_TRACE_NOW() - tsu0;
-                    tacc[9] += 1;
-                }
-                tacc[8] += 1;
-                const int rg0 = oct * a.r2, nrg = min(a.r2, a.ng_d - rg0);
-                const bool mine = warp < nrg;
-                if (p2n == 0) STAMP(16);  // first phase-2 unit: start
-                float acc[1][NGRP][4];
 #pragma unroll
-                for (int g = 0; g < NGRP; ++g)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) acc[0][g][i] = 0.f;
-                if (mine) {
-                    // this warp's row group rg0 + warp of the unit, in chunks of ch2 records
-                    const uint2 *hi2 = reinterpret_cast<const uint2 *>(hfrag);
-                    const uint2 *lo2 = hi2 + NGRP * kbp * kWarp;
-                    bool both = false;
-                    if constexpr (NGRP == 2) both = !packed && gm2 == 3u;
-                    float a1[1][1][4] = {};
-                    // one chunk loop per path (the path is fixed per expert)
-                    if (both) {
-                        for (int k0 = 0; k0 < kc; k0 += ch2) {
-                            const int n = min(ch2, kc - k0);
-                            const uint8_t *rb = take_item();
-                            if (p2n == 0) STAMP(17);  // ... its first data landed (warp 0)
-                            [[maybe_unused]] const unsigned long long tm0 = BFP_TRACE_NOW();
-                            if (!bad)
-                                for (int ch = 0; ch < n; ++ch) {
-                                    const uint8_t *recs[1] = {rb + (size_t)ch * a.rec};
-                                    mma_records<FMT, NGRP, 1, true>(recs, hi2, lo2, kbp, (k0 + ch) * CB, lane,
-                                                                    ms->esc[warp], acc);
-                                }
-                            __syncwarp();
-                            tacc[5] += BFP_TRACE_NOW() - tm0;
-                            [[maybe_unused]] const unsigned long long tg0 = BFP_TRACE_NOW();
-                            give_item();
-                            tacc[6] += BFP_TRACE_NOW() - tg0;
-                        }
-                    } else if (packed) {
-                        // columns of group 0 only: hi in columns c, lo in columns c + 4
-                        for (int k0 = 0; k0 < kc; k0 += ch2) {
-                            const int n = min(ch2, kc - k0);
-                            const uint8_t *rb = take_item();
-                            if (p2n == 0) STAMP(17);
-                            [[maybe_unused]] const unsigned long long tm0 = BFP_TRACE_NOW();
-                            if (!bad)
-                                for (int ch = 0; ch < n; ++ch) {
-                                    const uint8_t *recs[1] = {rb + (size_t)ch * a.rec};
-                                    mma_records<FMT, 1, 1, false>(recs, hi2, nullptr, kbp, (k0 + ch) * CB, lane,
-                                                                  ms->esc[warp], a1);
-                                }
-                            __syncwarp();
-                            tacc[5] += BFP_TRACE_NOW() - tm0;
-                            [[maybe_unused]] const unsigned long long tg0 = BFP_TRACE_NOW();
-                            give_item();
-                            tacc[6] += BFP_TRACE_NOW() - tg0;
-                        }
-                    } else {
-                        for (int k0 = 0; k0 < kc; k0 += ch2) {
-                            const int n = min(ch2, kc - k0);
-                            const uint8_t *rb = take_item();
-                            if (p2n == 0) STAMP(17);
-                            [[maybe_unused]] const unsigned long long tm0 = BFP_TRACE_NOW();
-                            if (!bad)
-                                for (int ch = 0; ch < n; ++ch) {
-                                    const uint8_t *recs[1] = {rb + (size_t)ch * a.rec};
-                                    mma_records<FMT, 1, 1, true>(recs, hi2, lo2, kbp, (k0 + ch) * CB, lane,
-                                                                 ms->esc[warp], a1);
-                                }
-                            __syncwarp();
-                            tacc[5] += BFP_TRACE_NOW() - tm0;
-                            [[maybe_unused]] const unsigned long long tg0 = BFP_TRACE_NOW();
-                            give_item();
-                            tacc[6] += BFP_TRACE_NOW() - tg0;
+                        for (int pr = 0; pr < 2; ++pr) {
+                            hf[frag_word(col, blk, 2 * qq + pr, kbp)] = hw2[pr];
+                            if (pe.parts == 1)
+                                hf[frag_word(col + 4, blk, 2 * qq + pr, kbp)] = lw2[pr];
+                            else
+                                hf[lo_off + frag_word(col, blk, 2 * qq + pr, kbp)] = lw2[pr];
                         }
                     }
-                    if (!both) {
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) acc[0][0][i] = a1[0][0][i];
-                    }
                 }
-                if (p2n == 0) STAMP(18);  // ... warp 0's MMAs done
-                if (p2n == 1) STAMP(29);
-                [[maybe_unused]] const unsigned long long tp0 = BFP_TRACE_NOW();
-                if (!bad && mine) {
-                    const int rg = rg0 + warp;
-                    if (packed) {  // column c + 4 holds the lo half of column c: lanes t and t ^ 2
+                bar_sync(1, NC);
+                if (p2n == 0) STAMP(10);  // first batch's h fragments ready
+                tacc[7] += BFP_TRACE_NOW() - tsu0;
+                tacc[9] += nb;
+                for (int bi = 0; bi < nb; ++bi) {
+                    const P2Entry &pe = ms->p2b[bi];
+                    const int j = pe.j;
+                    const bool sh = j == nU;
+                    const int kc = sh ? a.kc_fs : a.kc_f, kbp = sh ? a.kbp_fs : a.kbp_f;
+                    const int er = pe.er, nr = pe.nr;
+                    const bool packed = pe.parts == 1;
+                    const uint32_t *hfb = hfrag + pe.off;
+                    for (; q < pe.qend; ++q) {
+                        const int oct = q - j * a.noct;
+                        tacc[8] += 1;
+                        const int rg0 = oct * a.r2, nrg = min(a.r2, a.ng_d - rg0);
+                        const bool mine = warp < nrg;
+                        if (p2n == 0) STAMP(16);  // first phase-2 unit: start
+                        float acc[1][NGRP][4];
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) acc[0][0][i] += __shfl_xor_sync(0xffffffffu, acc[0][0][i], 2);
-                    }
+                        for (int g = 0; g < NGRP; ++g)
 #pragma unroll
-                    for (int g = 0; g < NGRP; ++g)
+                            for (int i = 0; i < 4; ++i) acc[0][g][i] = 0.f;
+                        if (mine) {
+                            // this warp's row group rg0 + warp of the unit, in chunks of ch2 records
+                            const uint2 *hi2 = reinterpret_cast<const uint2 *>(hfb);
+                            const uint2 *lo2 = hi2 + (pe.parts == 4 ? 2 : 1) * kbp * kWarp;
+                            const bool both = NGRP == 2 && pe.parts == 4;
+                            float a1[1][1][4] = {};
+                            // one chunk loop per path (the path is fixed per expert)
+                            if (both) {
+                                for (int k0 = 0; k0 < kc; k0 += ch2) {
+                                    const int n = min(ch2, kc - k0);
+                                    const uint8_t *rb = take_item();
+                                    if (p2n == 0) STAMP(17);  // ... its first data landed (warp 0)
+                                    [[maybe_unused]] const unsigned long long tm0 = BFP_TRACE_NOW();
+                                    if (!bad)
+                                        for (int ch = 0; ch < n; ++ch) {
+                                            const uint8_t *recs[1] = {rb + (size_t)ch * a.rec};
+                                            mma_records<FMT, NGRP, 1, true>(recs, hi2, lo2, kbp, (k0 + ch) * CB, lane,
+                                                                            ms->esc[warp], acc);
+                                        }
+                                    __syncwarp();
+                                    tacc[5] += BFP_TRACE_NOW() - tm0;
+                                    [[maybe_unused]] const unsigned long long tg0 = BFP_TRACE_NOW();
+                                    give_item();
+                                    tacc[6] += BFP_TRACE_NOW() - tg0;
+                                }
+                            } else if (packed) {
+                                // columns of group 0 only: hi in columns c, lo in columns c + 4
+                                for (int k0 = 0; k0 < kc; k0 += ch2) {
+                                    const int n = min(ch2, kc - k0);
+                                    const uint8_t *rb = take_item();
+                                    if (p2n == 0) STAMP(17);
+                                    [[maybe_unused]] const unsigned long long tm0 = BFP_TRACE_NOW();
+                                    if (!bad)
+                                        for (int ch = 0; ch < n; ++ch) {
+                                            const uint8_t *recs[1] = {rb + (size_t)ch * a.rec};
+                                            mma_records<FMT, 1, 1, false>(recs, hi2, nullptr, kbp, (k0 + ch) * CB, lane,
+                                                                          ms->esc[warp], a1);
+                                        }
+                                    __syncwarp();
+                                    tacc[5] += BFP_TRACE_NOW() - tm0;
+                                    [[maybe_unused]] const unsigned long long tg0 = BFP_TRACE_NOW();
+                                    give_item();
+                                    tacc[6] += BFP_TRACE_NOW() - tg0;
+                                }
+                            } else {
+                                for (int k0 = 0; k0 < kc; k0 += ch2) {
+                                    const int n = min(ch2, kc - k0);
+                                    const uint8_t *rb = take_item();
+                                    if (p2n == 0) STAMP(17);
+                                    [[maybe_unused]] const unsigned long long tm0 = BFP_TRACE_NOW();
+                                    if (!bad)
+                                        for (int ch = 0; ch < n; ++ch) {
+                                            const uint8_t *recs[1] = {rb + (size_t)ch * a.rec};
+                                            mma_records<FMT, 1, 1, true>(recs, hi2, lo2, kbp, (k0 + ch) * CB, lane,
+                                                                         ms->esc[warp], a1);
+                                        }
+                                    __syncwarp();
+                                    tacc[5] += BFP_TRACE_NOW() - tm0;
+                                    [[maybe_unused]] const unsigned long long tg0 = BFP_TRACE_NOW();
+                                    give_item();
+                                    tacc[6] += BFP_TRACE_NOW() - tg0;
+                                }
+                            }
+                            if (!both) {
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const int col = acc_xrow(lane, g, i);
-                            if (col < nr && (!packed || col < 4)) {
-                                const int r = ms->colrow[col];
-                                const int s = ms->eslot[er][r];
-                                const int n = rg * 16 + acc_wrow(lane, i);
-                                a.part[((int64_t)r * (a.K + 1) + s) * a.H + n] =
-                                    mul_pow2(acc[0][g][i], 24 - (MB - 1) - ms->shift_h[r]);
+                                for (int i = 0; i < 4; ++i) acc[0][0][i] = a1[0][0][i];
                             }
                         }
+                        if (p2n == 0) STAMP(18);  // ... warp 0's MMAs done
+                        if (p2n == 1) STAMP(29);
+                        [[maybe_unused]] const unsigned long long tp0 = BFP_TRACE_NOW();
+                        if (!bad && mine) {
+                            const int rg = rg0 + warp;
+                            if (packed) {  // column c + 4 holds the lo half of column c: lanes t and t ^ 2
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) acc[0][0][i] += __shfl_xor_sync(0xffffffffu, acc[0][0][i], 2);
+                            }
+#pragma unroll
+                            for (int g = 0; g < NGRP; ++g)
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    const int col = acc_xrow(lane, g, i);
+                                    if (col < nr && (!packed || col < 4)) {
+                                        const int r = ms->p2row[bi][col];
+                                        const int s = ms->eslot[er][r];
+                                        const int n = rg * 16 + acc_wrow(lane, i);
+                                        a.part[((int64_t)r * (a.K + 1) + s) * a.H + n] =
+                                            mul_pow2(acc[0][g][i], 24 - (MB - 1) - ms->p2shift[bi][col]);
+                                    }
+                                }
+                        }
+                        __syncwarp();
+                        tacc[12] += BFP_TRACE_NOW() - tp0;
+                        if (p2n == 0) STAMP(19);  // ... partial outputs stored
+                        if (p2n == 1) STAMP(31);
+                        ++p2n;
+                    }
                 }
-                __syncwarp();
-                tacc[12] += BFP_TRACE_NOW() - tp0;
-                if (p2n == 0) STAMP(19);  // ... partial outputs stored
-                if (p2n == 1) STAMP(31);
-                ++p2n;
             }
             STAMP(11);  // down projections done
             BFP_TRACE_WARP(80);  // every warp: phase-2 units done
@@ -1195,7 +1249,7 @@ static int plan_moe(const bfp_moe_layer *L, int m, MoePlan *p) {
     p->r2 = (int)std::min<int64_t>(kMoeWarps, p->dn.ng);
     p->noct = (int)((p->dn.ng + p->r2 - 1) / p->r2);
     // the routing scan packs the phase-2 cost of the union into 16 bits
-    if ((int64_t)p->noct * 4 * (kMaxExperts + 1) >= 65536) return fail(BFP_ESHAPE, "hidden size too large");
+    if ((int64_t)p->noct * 7 * (kMaxExperts + 1) >= 65536) return fail(BFP_ESHAPE, "hidden size too large");
     // per-warp slots: a phase-1 chunk is ch1 records of a gate row group and the same of its up row
     // group, a phase-2 chunk 2 * ch1 records of one row group
     p->ch1 = (int)std::min<int64_t>(4, p->gu.kc);
