@@ -26,6 +26,12 @@ static __device__ unsigned long long *g_bfp_trace = nullptr;
             g_bfp_trace[(size_t)blockIdx.x * BFP_TRACE_SLOTS + (base) + (threadIdx.x >> 5)] =               \
                 bfp::dev::global_ns();                                                                      \
     } while (0)
+// Lane 0 of every warp stores a value into slot (base + warp index) of its CTA's row.
+#define BFP_TRACE_WARP_SET(base, v)                                                                         \
+    do {                                                                                                    \
+        if (g_bfp_trace != nullptr && (threadIdx.x & 31) == 0)                                              \
+            g_bfp_trace[(size_t)blockIdx.x * BFP_TRACE_SLOTS + (base) + (threadIdx.x >> 5)] = (v);          \
+    } while (0)
 // Stores a value (a duration accumulated in registers, a count) into a slot of thread 0's row.
 #define BFP_TRACE_SET(slot, v)                                                                              \
     do {                                                                                                    \
@@ -43,6 +49,9 @@ static __device__ unsigned long long *g_bfp_trace = nullptr;
     } while (0)
 #define BFP_TRACE_AT_T(slot, t) \
     do {                        \
+    } while (0)
+#define BFP_TRACE_WARP_SET(base, v) \
+    do {                            \
     } while (0)
 #define BFP_TRACE_AT(slot) \
     do {                   \

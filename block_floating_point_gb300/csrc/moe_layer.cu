@@ -285,30 +285,30 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
         int s_ch = 0;                            // records per chunk
         uint32_t s_b = 0;                        // bytes of a full chunk of one source
         bool s_live = false;
-        // phase 1: the CTA's units u = 0 .. nc-1 (list entries c + u * ncta), nch chunks each. With
-        // enough work (nc * nch >= NW * nch) every warp takes a contiguous run of chunks
-        // [C0, C1) = [w * T / NW, (w + 1) * T / NW) of the concatenated list, T = nc * nch (p1_sk): a
-        // unit cut by a run boundary has two parts, the end part as the first item of warp w + 1 and
-        // the start part as the last item of warp w. Otherwise each unit is split into p1_S equal
-        // parts (p1_S > 1 only with one activation group), dealt round-robin: warp w takes parts
-        // w, w + NW, ... of the list of nc * p1_S parts.
+        // phase 1: the CTA's units u = 0 .. nc-1 (list entries c + u * ncta), kc_h records of gate and
+        // up each (nch chunks of ch1). With at least NW units (p1_sk) every warp takes a contiguous
+        // run of records [C0, C1) = [w * T / NW, (w + 1) * T / NW) of the concatenated list,
+        // T = nc * kc_h: a unit cut by a run boundary has two parts, the end part as the first item
+        // of warp w + 1 and the start part as the last item of warp w. Otherwise each unit is split
+        // into p1_S equal parts of whole chunks (p1_S > 1 only with one activation group), dealt
+        // round-robin: warp w takes parts w, w + NW, ... of the list of nc * p1_S parts.
         bool p1_sk = false;
         int p1_S = 1, p1_items = 0, p1_nch = 1, p1_C0 = 0, p1_C1 = 0;
         int p1_it = 0;                           // next item (of this warp) to issue
         struct P1Item {
-            int u, k0c, k1c;  // unit, chunk range [k0c, k1c) of its nch
+            int u, k0, k1;  // unit, record range [k0, k1) of its kc_h
         };
         auto p1_item = [&](int i) -> P1Item {
             P1Item t;
             if (p1_sk) {
-                t.u = p1_C0 / p1_nch + i;
-                t.k0c = max(p1_C0 - t.u * p1_nch, 0);
-                t.k1c = min(p1_C1 - t.u * p1_nch, p1_nch);
+                t.u = p1_C0 / a.kc_h + i;
+                t.k0 = max(p1_C0 - t.u * a.kc_h, 0);
+                t.k1 = min(p1_C1 - t.u * a.kc_h, a.kc_h);
             } else {
                 const int it = warp + i * NW, part = it % p1_S;
                 t.u = it / p1_S;
-                t.k0c = part * p1_nch / p1_S;
-                t.k1c = (part + 1) * p1_nch / p1_S;
+                t.k0 = part * p1_nch / p1_S * ch1;
+                t.k1 = min((part + 1) * p1_nch / p1_S * ch1, a.kc_h);
             }
             return t;
         };
@@ -324,7 +324,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
                 const P1Item t = p1_item(p1_it);
                 const P1Tile pt = p1_tile(c + t.u * a.ncta, a.nft_s, a.nft);
                 const uint8_t *base = pt.sh ? a.sgu : a.gu + (int64_t)ms->ulist[pt.jrow] * a.gu_stride;
-                const int r0 = t.k0c * ch1, r1 = min(t.k1c * ch1, a.kc_h);
+                const int r0 = t.k0, r1 = t.k1;
                 sa = base + (int64_t)(2 * pt.ft) * gb_h + (int64_t)r0 * a.rec;
                 sb = sa + gb_h;
                 s_left = r1 - r0;
@@ -381,7 +381,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
         };
         // trace builds: per-phase durations of warp 0 accumulated in registers: [0] phase-1 data waits,
         // [1] phase-1 MMA sections, [2] phase-2 data waits, [3] phase-1 refills, [4] phase-1 chunks
-        unsigned long long tacc[13] = {};  // [10] phase-1 epilogues, [11] phase-1 unit starts, [12] phase-2 epilogues  // [5..9]: phase-2 MMA, refills, setups, units, experts
+        unsigned long long tacc[15] = {};  // [10] phase-1 epilogues, [11] phase-1 unit starts, [12] phase-2 epilogues  // [5..9]: phase-2 MMA, refills, setups, units, experts
         int tslot = 0;
         // Waits for the next item; a warp whose data never came stops issuing and keeps its copies
         // in the drain at exit.
@@ -431,7 +431,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
         auto run_p1_item = [&](int i) {
             [[maybe_unused]] const unsigned long long tu0 = BFP_TRACE_NOW();
             const P1Item t = p1_item(i);
-            const int r0 = t.k0c * ch1, r1 = min(t.k1c * ch1, a.kc_h);
+            const int r0 = t.k0, r1 = t.k1;
             const P1Tile pt = p1_tile(c + t.u * a.ncta, a.nft_s, a.nft);
             const int er = pt.sh ? kMaxExperts : ms->ulist[pt.jrow];  // expert row of emask / eslot
             const uint32_t rowmask = ms->emask[er];
@@ -461,6 +461,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
                             mma_records<FMT, NGRP, 2, false>(recs, frag2, nullptr, a.kbp_h, (k0 + ch) * CB, lane,
                                                              ms->esc[warp], acc);
                         }
+                    tacc[13] += 1;
                     give_item();
                 }
             } else {
@@ -483,11 +484,11 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
                 }
             }
             if (bad) return;
-            if (p1_sk && (t.k0c > 0 || t.k1c < p1_nch)) {
+            if (p1_sk && (t.k0 > 0 || t.k1 < a.kc_h)) {
                 // a unit cut by a run boundary: the end part (first item of warp w) goes to the
                 // scratch of boundary w - 1; the start part (last item of warp w) waits for the tile
                 // of boundary w, adds it and writes the unit's results
-                if (t.k0c > 0) {
+                if (t.k0 > 0) {
                     float *dst = a.p1part + ((size_t)c * (NW - 1) + (warp - 1)) * kP1PartFloats;
 #pragma unroll
                     for (int r = 0; r < 2; ++r)
@@ -847,10 +848,10 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
             // every run at least one unit long (a unit has at most two parts), and room for the tiles
             p1_sk = a.p1part != nullptr && nc >= NW;
             if (p1_sk) {
-                const int T = nc * p1_nch;
+                const int T = nc * a.kc_h;  // records
                 p1_C0 = warp * T / NW;
                 p1_C1 = (warp + 1) * T / NW;
-                p1_items = (p1_C1 - 1) / p1_nch - p1_C0 / p1_nch + 1;
+                p1_items = (p1_C1 - 1) / a.kc_h - p1_C0 / a.kc_h + 1;
             } else {
                 if constexpr (NGRP == 1) {
                     while (nc > 0 && nc * p1_S * 2 <= NW && p1_S * 2 <= p1_nch) p1_S *= 2;
@@ -873,6 +874,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
             }
             STAMP(8);  // warp 0: phase-1 units done
             BFP_TRACE_WARP(64);  // every warp: phase-1 items done
+            BFP_TRACE_WARP_SET(80, tacc[13] * 1000 + tacc[4]);  // ... its two-group and one-group chunks
             tslot = 2;
             if (!grid_barrier(&a.ctrl[2])) {  // every CTA's h and row maxima written
                 abort_all();
@@ -1116,7 +1118,6 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
                 }
             }
             STAMP(11);  // down projections done
-            BFP_TRACE_WARP(80);  // every warp: phase-2 units done
             BFP_TRACE_SET(40, tacc[0]);
             BFP_TRACE_SET(41, tacc[1]);
             BFP_TRACE_SET(42, tacc[2]);
