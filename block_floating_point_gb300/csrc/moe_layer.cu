@@ -848,10 +848,49 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
             // every run at least one unit long (a unit has at most two parts), and room for the tiles
             p1_sk = a.p1part != nullptr && nc >= NW;
             if (p1_sk) {
+                // Runs of equal cost: a record of a unit with rows in both activation groups costs 5
+                // (two MMAs per block), one of a single-group unit 4. Weighted only when every run
+                // still spans at least one unit of the heavier kind (so no unit has three parts).
+                auto unit_wt = [&](int u) {
+                    if (u >= nc) return 0;
+                    if (NGRP == 1) return 4;
+                    const P1Tile pt = p1_tile(c + u * a.ncta, a.nft_s, a.nft);
+                    const uint32_t m = ms->emask[pt.sh ? kMaxExperts : ms->ulist[pt.jrow]];
+                    return ((m & 0xFFu) && (m & 0xFF00u)) ? 5 : 4;
+                };
+                int W = 0;
+                for (int u = lane; u < nc; u += kWarp) W += unit_wt(u);
+                W = __reduce_add_sync(0xffffffffu, W);
                 const int T = nc * a.kc_h;  // records
-                p1_C0 = warp * T / NW;
-                p1_C1 = (warp + 1) * T / NW;
-                p1_items = (p1_C1 - 1) / a.kc_h - p1_C0 / a.kc_h + 1;
+                if (NGRP == 2 && W >= 5 * NW) {
+                    // record position of weight X (in record-weight units, 0 <= X <= W * kc_h): the unit
+                    // holding X and the whole records of it before X
+                    const int X0 = (int)((int64_t)warp * W * a.kc_h / NW);
+                    const int X1 = (int)((int64_t)(warp + 1) * W * a.kc_h / NW);
+                    int P0 = T, P1 = T, carry = 0;
+                    for (int u0 = 0; u0 < nc; u0 += kWarp) {
+                        const int u = u0 + lane, wt = unit_wt(u), span = wt * a.kc_h;
+                        int incl = span;
+#pragma unroll
+                        for (int o = 1; o < kWarp; o <<= 1) {
+                            const int t2 = __shfl_up_sync(0xffffffffu, incl, o);
+                            if (lane >= o) incl += t2;
+                        }
+                        const int beg = carry + incl - span;
+                        const uint32_t b0 = __ballot_sync(0xffffffffu, u < nc && beg <= X0 && X0 < beg + span);
+                        const uint32_t b1 = __ballot_sync(0xffffffffu, u < nc && beg <= X1 && X1 < beg + span);
+                        const int pos0 = u * a.kc_h + (X0 - beg) / max(wt, 1), pos1 = u * a.kc_h + (X1 - beg) / max(wt, 1);
+                        if (b0) P0 = __shfl_sync(0xffffffffu, pos0, __ffs(b0) - 1);
+                        if (b1) P1 = __shfl_sync(0xffffffffu, pos1, __ffs(b1) - 1);
+                        carry += __shfl_sync(0xffffffffu, incl, kWarp - 1);
+                    }
+                    p1_C0 = P0;
+                    p1_C1 = P1;
+                } else {
+                    p1_C0 = warp * T / NW;
+                    p1_C1 = (warp + 1) * T / NW;
+                }
+                p1_items = p1_C1 > p1_C0 ? (p1_C1 - 1) / a.kc_h - p1_C0 / a.kc_h + 1 : 0;
             } else {
                 if constexpr (NGRP == 1) {
                     while (nc > 0 && nc * p1_S * 2 <= NW && p1_S * 2 <= p1_nch) p1_S *= 2;
