@@ -121,6 +121,90 @@ __device__ __forceinline__ void mma_records(const uint8_t *const recs[NREC], con
     }
 }
 
+// acc[grp][i] += sum over NREC consecutive records of one row group (record r covers the CB blocks
+// from kb0 + r * CB) of 2^(E-127) * (A . B_grp): mma_records for records that follow each other
+// along k and share one accumulator (the down projection's row groups). One exponent pass and one
+// set of loads for all NREC records, so the per-record overhead is paid once per call.
+template <int FMT, int NG, int NREC, bool HILO>
+__device__ __forceinline__ void mma_records_k(const uint8_t *recs, int rec_bytes, const uint2 *frag,
+                                              const uint2 *frag_lo, int kbp, int kb0, int lane, float *esc,
+                                              float acc[NG][4]) {
+    constexpr int EB = rec_exp_bytes<FMT>();
+    constexpr int CB = FMT == 4 ? 4 : 2;
+    constexpr int BPL = NREC * EB / kWarp;  // exponent bytes converted per lane
+    static_assert(BPL == 1 || BPL == 2 || BPL == 4, "unsupported record count");
+    const int g = lane >> 2;
+    uint4 wq[NREC];
+#pragma unroll
+    for (int r = 0; r < NREC; ++r) wq[r] = *reinterpret_cast<const uint4 *>(recs + (size_t)r * rec_bytes + 16 * lane);
+    {
+        const int byte0 = lane * BPL;  // byte of the call's exponents, records in order
+        const uint8_t *src = recs + (size_t)(byte0 / EB) * rec_bytes + kRecCodes + byte0 % EB;
+        __syncwarp();  // every lane is done reading the previous call's scales
+        if constexpr (BPL == 4) {
+            const uint32_t w = *reinterpret_cast<const uint32_t *>(src);
+            *reinterpret_cast<float4 *>(esc + byte0) =
+                make_float4(exp_scale(w, 0), exp_scale(w, 1), exp_scale(w, 2), exp_scale(w, 3));
+        } else if constexpr (BPL == 2) {
+            const uint32_t w = *reinterpret_cast<const uint16_t *>(src);
+            *reinterpret_cast<float2 *>(esc + byte0) = make_float2(exp_scale(w, 0), exp_scale(w, 1));
+        } else {
+            esc[byte0] = exp_scale(*src, 0);
+        }
+        __syncwarp();
+    }
+    float sc[NREC][2 * CB];
+#pragma unroll
+    for (int r = 0; r < NREC; ++r) {
+#pragma unroll
+        for (int q = 0; q < CB / 2; ++q) {
+            const float4 f = *reinterpret_cast<const float4 *>(esc + r * EB + 2 * CB * g + 4 * q);
+            sc[r][4 * q] = f.x;
+            sc[r][4 * q + 1] = f.y;
+            sc[r][4 * q + 2] = f.z;
+            sc[r][4 * q + 3] = f.w;
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < NREC; ++r) {
+        const int kr = kb0 + r * CB;  // a multiple of CB: (kr + b) & 7 = (kr & 7) | b
+        const int l0 = lane ^ ((kr & 7) << 2);
+        const uint2 *fh = frag + (int64_t)kr * kWarp;
+        const uint2 *fl = HILO ? frag_lo + (int64_t)kr * kWarp : nullptr;
+#pragma unroll
+        for (int b = 0; b < CB; ++b) {
+            const int li = b * kWarp + (l0 ^ (b << 2));
+            uint2 bx[NG], bl[NG];
+#pragma unroll
+            for (int grp = 0; grp < NG; ++grp) {
+                bx[grp] = fh[(int64_t)grp * kbp * kWarp + li];
+                if constexpr (HILO) bl[grp] = fl[(int64_t)grp * kbp * kWarp + li];
+            }
+            uint32_t a[4];
+            if constexpr (FMT == 4) {
+                const uint32_t wsel = b == 0 ? wq[r].x : b == 1 ? wq[r].y : b == 2 ? wq[r].z : wq[r].w;
+                unpack_bfp4(wsel, a);
+            } else {
+                if (b == 0)
+                    unpack_bfp8(wq[r].x, wq[r].y, a);
+                else
+                    unpack_bfp8(wq[r].z, wq[r].w, a);
+            }
+            const float s0 = sc[r][2 * b], s1 = sc[r][2 * b + 1];
+#pragma unroll
+            for (int grp = 0; grp < NG; ++grp) {
+                float c[4] = {0.f, 0.f, 0.f, 0.f};
+                mma16816(c, a, bx[grp].x, bx[grp].y);
+                if constexpr (HILO) mma16816(c, a, bl[grp].x, bl[grp].y);
+                acc[grp][0] = fmaf(s0, c[0], acc[grp][0]);
+                acc[grp][1] = fmaf(s0, c[1], acc[grp][1]);
+                acc[grp][2] = fmaf(s1, c[2], acc[grp][2]);
+                acc[grp][3] = fmaf(s1, c[3], acc[grp][3]);
+            }
+        }
+    }
+}
+
 // Position of accumulator element (grp, i) of a lane in the 16 x (8*NGRP) output tile:
 //   weight row (within the 16-row group) and activation row.
 __device__ __forceinline__ int acc_wrow(int lane, int i) { return (lane >> 2) + 8 * (i >> 1); }

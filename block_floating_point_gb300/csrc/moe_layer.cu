@@ -1071,10 +1071,13 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
                                     if (p2n == 0) STAMP(17);  // ... its first data landed (warp 0)
                                     [[maybe_unused]] const unsigned long long tm0 = BFP_TRACE_NOW();
                                     if (!bad)
-                                        for (int ch = 0; ch < n; ++ch) {
-                                            const uint8_t *recs[1] = {rb + (size_t)ch * a.rec};
-                                            mma_records<FMT, NGRP, 1, true>(recs, hi2, lo2, kbp, (k0 + ch) * CB, lane,
-                                                                            ms->esc[warp], acc);
+                                        for (int ch = 0; ch < n; ch += 2) {
+                                            if (ch + 1 < n)
+                                                mma_records_k<FMT, NGRP, 2, true>(rb + (size_t)ch * a.rec, a.rec, hi2, lo2, kbp,
+                                                                                  (k0 + ch) * CB, lane, ms->esc[warp], acc[0]);
+                                            else
+                                                mma_records_k<FMT, NGRP, 1, true>(rb + (size_t)ch * a.rec, a.rec, hi2, lo2, kbp,
+                                                                                  (k0 + ch) * CB, lane, ms->esc[warp], acc[0]);
                                         }
                                     __syncwarp();
                                     tacc[5] += BFP_TRACE_NOW() - tm0;
@@ -1090,10 +1093,13 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
                                     if (p2n == 0) STAMP(17);
                                     [[maybe_unused]] const unsigned long long tm0 = BFP_TRACE_NOW();
                                     if (!bad)
-                                        for (int ch = 0; ch < n; ++ch) {
-                                            const uint8_t *recs[1] = {rb + (size_t)ch * a.rec};
-                                            mma_records<FMT, 1, 1, false>(recs, hi2, nullptr, kbp, (k0 + ch) * CB, lane,
-                                                                          ms->esc[warp], a1);
+                                        for (int ch = 0; ch < n; ch += 2) {
+                                            if (ch + 1 < n)
+                                                mma_records_k<FMT, 1, 2, false>(rb + (size_t)ch * a.rec, a.rec, hi2, nullptr, kbp,
+                                                                                (k0 + ch) * CB, lane, ms->esc[warp], a1[0]);
+                                            else
+                                                mma_records_k<FMT, 1, 1, false>(rb + (size_t)ch * a.rec, a.rec, hi2, nullptr, kbp,
+                                                                                (k0 + ch) * CB, lane, ms->esc[warp], a1[0]);
                                         }
                                     __syncwarp();
                                     tacc[5] += BFP_TRACE_NOW() - tm0;
@@ -1108,10 +1114,13 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
                                     if (p2n == 0) STAMP(17);
                                     [[maybe_unused]] const unsigned long long tm0 = BFP_TRACE_NOW();
                                     if (!bad)
-                                        for (int ch = 0; ch < n; ++ch) {
-                                            const uint8_t *recs[1] = {rb + (size_t)ch * a.rec};
-                                            mma_records<FMT, 1, 1, true>(recs, hi2, lo2, kbp, (k0 + ch) * CB, lane,
-                                                                         ms->esc[warp], a1);
+                                        for (int ch = 0; ch < n; ch += 2) {
+                                            if (ch + 1 < n)
+                                                mma_records_k<FMT, 1, 2, true>(rb + (size_t)ch * a.rec, a.rec, hi2, lo2, kbp,
+                                                                               (k0 + ch) * CB, lane, ms->esc[warp], a1[0]);
+                                            else
+                                                mma_records_k<FMT, 1, 1, true>(rb + (size_t)ch * a.rec, a.rec, hi2, lo2, kbp,
+                                                                               (k0 + ch) * CB, lane, ms->esc[warp], a1[0]);
                                         }
                                     __syncwarp();
                                     tacc[5] += BFP_TRACE_NOW() - tm0;
