@@ -115,11 +115,10 @@ __global__ void __launch_bounds__(kLinThreads, 1) bfp_linear_kernel(const Linear
         mbar_fence_init();
     }
     __syncthreads();
-    if (warp == 0) {  // the activation rows, lane r copies row r (rows are ldx apart in global memory)
-        if (lane == 0) mbar_arrive_expect_tx(&lm->stage_full, (uint32_t)a.m * a.k * 2);
-        __syncwarp();
-        if (lane < a.m)
-            bulk_g2s(stage + (size_t)lane * a.k * 2, a.x + (int64_t)lane * a.ldx, (uint32_t)a.k * 2, &lm->stage_full);
+    if (tid == 0) {  // the activation rows, one copy per row (rows are ldx apart in global memory)
+        mbar_arrive_expect_tx(&lm->stage_full, (uint32_t)a.m * a.k * 2);
+        for (int r = 0; r < a.m; ++r)
+            bulk_g2s(stage + (size_t)r * a.k * 2, a.x + (int64_t)r * a.ldx, (uint32_t)a.k * 2, &lm->stage_full);
     }
     bool bad = !__all_sync(0xffffffffu, mbar_wait(&lm->stage_full, 0u, a.wait, nullptr));
     uint16_t *const xs = reinterpret_cast<uint16_t *>(stage);

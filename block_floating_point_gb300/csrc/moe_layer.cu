@@ -236,20 +236,20 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
     __syncthreads();
     STAMP(13);
     const int LDXS = stage_ldx(a.H);
-    if (warp == 0) {
-        // preamble stage: the activation rows (row stride LDXS: the padding keeps the router's
-        // fragment loads free of bank conflicts), this CTA's router rows and (the CTA holding row E)
-        // the shared-gate row; lane r < M copies row r, lane M the router rows, lane M + 1 the gate row
+    if (tid == 0) {
+        // preamble stage: this CTA's router rows and (the CTA holding row E) the shared-gate row,
+        // then the activation rows (row stride LDXS: the padding keeps the router's fragment loads
+        // free of bank conflicts); one thread issues the copies one after another (cheaper than
+        // several lanes issuing at once)
         const uint32_t xb = (uint32_t)a.M * a.H * 2;
         const int re = min(rr1, a.E);
         const uint32_t rb = re > rr0 ? (uint32_t)(re - rr0) * a.H * 2 : 0u;
         const uint32_t gsb = rr1 > a.E ? (uint32_t)a.H * 2 : 0u;
-        if (lane == 0) mbar_arrive_expect_tx(&ms->stage_full, xb + rb + gsb);
-        __syncwarp();
-        if (lane < a.M)
-            bulk_g2s(stage + (size_t)lane * LDXS * 2, a.x + (int64_t)lane * a.H, (uint32_t)a.H * 2, &ms->stage_full);
-        if (lane == a.M && rb) bulk_g2s(stage + a.stage_r, a.router + (int64_t)rr0 * a.H, rb, &ms->stage_full);
-        if (lane == a.M + 1 && gsb) bulk_g2s(stage + a.stage_r + rb, a.sgate, gsb, &ms->stage_full);
+        mbar_arrive_expect_tx(&ms->stage_full, xb + rb + gsb);
+        if (rb) bulk_g2s(stage + a.stage_r, a.router + (int64_t)rr0 * a.H, rb, &ms->stage_full);
+        if (gsb) bulk_g2s(stage + a.stage_r + rb, a.sgate, gsb, &ms->stage_full);
+        for (int r = 0; r < a.M; ++r)
+            bulk_g2s(stage + (size_t)r * LDXS * 2, a.x + (int64_t)r * a.H, (uint32_t)a.H * 2, &ms->stage_full);
     }
     {
         bool bad = false;
