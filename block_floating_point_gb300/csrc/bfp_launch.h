@@ -10,8 +10,6 @@
 
 namespace bfp {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;  // 8 consumer warps + 1 producer warp
 constexpr int64_t kDefaultWaitIters = int64_t(1) << 40;
 constexpr uint64_t kDefaultWaitNanos = 2000000000ull;  // 2 s wall clock per wait
 
