@@ -314,38 +314,38 @@ __device__ __noinline__ void act_rows_prepare(uint16_t *x, int64_t ldx, int m, i
 
 // fp16 activation fragments of the prepared rows (act_rows_prepare): row r scaled by 2^shift[r] and
 // rounded to fp16 (exact for every bf16 value above 2^-14 of the row maximum); rows m .. 8 ngrp - 1
-// and blocks k/16 .. kbp - 1 are zero. Item (row, segment) per warp; lane (bb, t) = (lane >> 2,
-// lane & 3) assembles whole fragments (cols 2t|2t+1 and 2t+8|2t+9 of the segment's blocks b with
-// b & 7 = bb) and stores each with one 8-byte store; the XOR swizzle spreads a warp's stores over
-// the banks. Called like act_rows_prepare (tid = the thread's index among the NC threads).
+// and blocks k/16 .. kbp - 1 are zero. Item (row of the 8 ngrp, segment of the kbp blocks) per warp,
+// padding rows and blocks included, so every fragment word is written once and no clearing pass is
+// needed; lane (bb, t) = (lane >> 2, lane & 3) assembles whole fragments (cols 2t|2t+1 and
+// 2t+8|2t+9 of the segment's blocks b with b & 7 = bb) and stores each with one 8-byte store; the
+// XOR swizzle spreads a warp's stores over the banks. Called like act_rows_prepare (tid unused).
 template <int NC>
 __device__ __noinline__ void act_rows_frags(const uint16_t *x, int64_t ldx, int m, int k, int kbp, int ngrp,
                                             const int *shift, uint32_t *frag, int bar, int tid, int warp, int lane) {
     constexpr int NW = NC / kWarp;
-    const int kb = k / 16;
+    const int kb = k / 16, mp = 8 * ngrp;
     uint2 *f2 = reinterpret_cast<uint2 *>(frag);
-    if (m < 8 * ngrp || kb < kbp) {
-        for (int i = tid; i < ngrp * kbp * kWarp; i += NC) {
-            const int gb = i / kWarp, sl = i % kWarp, b = gb % kbp, grp = gb / kbp;
-            const int r = 8 * grp + ((sl ^ frag_swz(b)) >> 2);
-            if (r >= m || b >= kb) f2[i] = make_uint2(0u, 0u);
-        }
-    }
-    const int S = act_segments<NC>(m, k);
-    const int bs = kb / S;  // blocks per segment
+    int S = 1;  // segments per row: spread the rows over every warp
+    while (mp * S * 2 <= NW && (kbp / 8) % (S * 2) == 0) S *= 2;
+    const int bs = kbp / S;  // blocks per segment (a multiple of 8 when S > 1)
     const int bb = lane >> 2, t = lane & 3;
-    for (int it = warp; it < m * S; it += NW) {
+    for (int it = warp; it < mp * S; it += NW) {
         const int r = it / S, sg = it - r * S;
-        const uint16_t *xrow = x + (int64_t)r * ldx;
-        const float sc = pow2f(shift[r]);
+        const bool real = r < m;
+        const uint16_t *xrow = x + (int64_t)(real ? r : 0) * ldx;
+        const float sc = real ? pow2f(shift[r]) : 0.f;
         const int grp = r >> 3, g = r & 7;
         uint2 *fr = f2 + (int64_t)grp * kbp * kWarp + ((4 * g + t) ^ (bb << 2));  // (b & 7) == bb
         const int b0 = sg * bs, b1 = b0 + bs;
         for (int b = b0 + ((bb - b0) & 7); b < b1; b += 8) {
-            const uint32_t w0 = *reinterpret_cast<const uint32_t *>(xrow + 16 * b + 2 * t);
-            const uint32_t w1 = *reinterpret_cast<const uint32_t *>(xrow + 16 * b + 2 * t + 8);
-            fr[(int64_t)b * kWarp] = make_uint2(pack_half2(bf16_bits_to_f32(w0 & 0xFFFFu) * sc, bf16_bits_to_f32(w0 >> 16) * sc),
-                                                pack_half2(bf16_bits_to_f32(w1 & 0xFFFFu) * sc, bf16_bits_to_f32(w1 >> 16) * sc));
+            uint2 v = make_uint2(0u, 0u);
+            if (real && b < kb) {
+                const uint32_t w0 = *reinterpret_cast<const uint32_t *>(xrow + 16 * b + 2 * t);
+                const uint32_t w1 = *reinterpret_cast<const uint32_t *>(xrow + 16 * b + 2 * t + 8);
+                v = make_uint2(pack_half2(bf16_bits_to_f32(w0 & 0xFFFFu) * sc, bf16_bits_to_f32(w0 >> 16) * sc),
+                               pack_half2(bf16_bits_to_f32(w1 & 0xFFFFu) * sc, bf16_bits_to_f32(w1 >> 16) * sc));
+            }
+            fr[(int64_t)b * kWarp] = v;
         }
     }
     bar_sync(bar, NC);
