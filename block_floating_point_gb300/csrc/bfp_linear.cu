@@ -115,17 +115,7 @@ __global__ void __launch_bounds__(kLinThreads, 1) bfp_linear_kernel(const Linear
         mbar_fence_init();
     }
     __syncthreads();
-    if (tid == 0) {  // the activation rows, one copy per row (rows are ldx apart in global memory)
-        mbar_arrive_expect_tx(&lm->stage_full, (uint32_t)a.m * a.k * 2);
-        for (int r = 0; r < a.m; ++r)
-            bulk_g2s(stage + (size_t)r * a.k * 2, a.x + (int64_t)r * a.ldx, (uint32_t)a.k * 2, &lm->stage_full);
-    }
-    bool bad = !__all_sync(0xffffffffu, mbar_wait(&lm->stage_full, 0u, a.wait, nullptr));
-    uint16_t *const xs = reinterpret_cast<uint16_t *>(stage);
-    act_rows_prepare<NC>(xs, a.k, a.m, a.k, a.norm != 0, a.eps, lm->shift, lm->inv, lm->red, 1, warp, lane);
-    act_rows_frags<NC>(xs, a.k, a.m, a.k, a.kbp, NGRP, lm->shift, frag, 1, tid, warp, lane);
-    // every warp is past its reads of the stage (the barrier ending act_rows_frags)
-
+    bool bad = false;
     // ---- this warp's stream: items it = warp, warp + NW, ...; item it = part it % S of row group
     //      rg0 + it / S, i.e. records [part * kc / S, (part + 1) * kc / S) of the group, in chunks
     //      of chw records through the warp's nsw slots (lane 0 issues, every lane keeps the cursor)
@@ -180,7 +170,24 @@ __global__ void __launch_bounds__(kLinThreads, 1) bfp_linear_kernel(const Linear
             cu_par ^= 1u;
         }
     };
-    for (int i = 0; i < a.nsw; ++i) issue_next();
+    if (tid == 0) {  // the activation rows, one copy per row (rows are ldx apart in global memory)
+        mbar_arrive_expect_tx(&lm->stage_full, (uint32_t)a.m * a.k * 2);
+        for (int r = 0; r < a.m; ++r)
+            bulk_g2s(stage + (size_t)r * a.k * 2, a.x + (int64_t)r * a.ldx, (uint32_t)a.k * 2, &lm->stage_full);
+    }
+    // The weights do not depend on the activations: a warp whose slots lie below the stage starts
+    // its stream before the rows land.
+    const bool early = (size_t)(warp + 1) * a.nsw * a.slot_bytes <= (size_t)a.stage_off;
+    if (early)
+        for (int i = 0; i < a.nsw; ++i) issue_next();
+    if (!__all_sync(0xffffffffu, mbar_wait(&lm->stage_full, 0u, a.wait, nullptr))) bad = true;
+    uint16_t *const xs = reinterpret_cast<uint16_t *>(stage);
+    act_rows_prepare<NC>(xs, a.k, a.m, a.k, a.norm != 0, a.eps, lm->shift, lm->inv, lm->red, 1, warp, lane);
+    act_rows_frags<NC>(xs, a.k, a.m, a.k, a.kbp, NGRP, lm->shift, frag, 1, tid, warp, lane);
+    // every warp is past its reads of the stage (the barrier ending act_rows_frags): the rest
+    // of the streams may start
+    if (!early)
+        for (int i = 0; i < a.nsw; ++i) issue_next();
 
     const uint2 *frag2 = reinterpret_cast<const uint2 *>(frag);
     for (int it = warp; it < items; it += NW) {
