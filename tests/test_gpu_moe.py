@@ -90,6 +90,15 @@ def test_full_layer_m8(full):
     check(case, layer, 8, rms_norm=True, row_seed0=300)
 
 
+def test_contiguous_runs_one_activation_group():
+    """Hidden 2048, 64 experts of width 1024, 8 rows: one activation group with at least 16 f-tile
+    units per CTA, so phase 1 cuts each CTA's unit list into contiguous runs per warp (units split
+    between neighbouring warps), and each down row group spans two chunks."""
+    spec = synth.MoESpec(hidden=2048, n_experts=64, ffn=1024, top_k=8, shared_ffn=1024)
+    case = LayerCase(spec, seed=414)
+    check(case, case.device_layer(), 8, rms_norm=True, row_seed0=700)
+
+
 def test_full_layer_hot_routing_m16():
     case = LayerCase(synth.FULL, seed=303, hot=True)
     layer = case.device_layer()
