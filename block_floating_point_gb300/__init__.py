@@ -67,6 +67,7 @@ SIGNATURES = {
     "moe_stack_decode": [_LP, _I, _MP, _P, _I, _P, _P, _SZ, _P],
     "bfp_workspace_status": [_P, ctypes.POINTER(_I), _P],
     "bfp_set_wait_limit": [_I64],
+    "bfp_set_launch_mode": [_I],
     "bfp_last_error": [],
 }
 
@@ -206,6 +207,14 @@ def workspace_status(ws, stream=None) -> int:
 
 def set_wait_limit(iterations: int):
     _check(load().bfp_set_wait_limit(iterations), "bfp_set_wait_limit")
+
+
+LAUNCH_DEPENDENT, LAUNCH_COOPERATIVE = 0, 1
+
+
+def set_launch_mode(mode: int):
+    """How the MoE layer kernel is launched (include/bfpmoe.h, bfp_set_launch_mode)."""
+    _check(load().bfp_set_launch_mode(mode), "bfp_set_launch_mode")
 
 
 def _alloc_ws(nbytes: int, device, stream=None):

@@ -136,6 +136,15 @@ __device__ __forceinline__ bool wait_counter(const uint32_t *p, uint32_t target,
 // First error wins; the word is cleared only by the host (bfp_workspace_init).
 __device__ __forceinline__ void raise_status(uint32_t *status, uint32_t code) { atomicCAS(status, 0u, code); }
 
+// ------------------------------------------------ programmatic dependent launch
+// Lets the next kernel on the stream be scheduled (its CTAs start as this grid's CTAs leave).
+__device__ __forceinline__ void grid_dep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Waits until the kernels this one depends on have finished and their memory is visible (returns at
+// once when the launch had no such dependency).
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // --------------------------------------------------------- named barriers
 __device__ __forceinline__ void bar_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

@@ -38,4 +38,7 @@ int check_matrix(const bfp_matrix *w, Geometry *g, bool device_ptr);
 // Bounded-wait iteration limit for launches issued from this thread (0 = default).
 int64_t wait_limit();
 
+// How the MoE layer kernel is launched (bfp_set_launch_mode; process-wide).
+int launch_mode();
+
 }  // namespace bfp

@@ -107,13 +107,16 @@ __global__ void __launch_bounds__(kLinThreads, 1) bfp_linear_kernel(const Linear
     const int rg0 = (int)((int64_t)c * a.ng / a.ncta), rg1 = (int)((int64_t)(c + 1) * a.ng / a.ncta);
     const int S = a.S, items = (rg1 - rg0) * S;
 
-    if (tid == 0) {
-        for (int i = 0; i < NW * a.nsw; ++i) mbar_init(&full[i], 1);
-        mbar_init(&lm->stage_full, 1);
-        for (int i = 0; i < NW; ++i) lm->cnt[i] = 0;
-        for (int i = 0; i < 4; ++i) lm->flags[i] = 0;
+    if (tid <= NW * a.nsw) {  // one barrier per thread
+        mbar_init(tid < NW * a.nsw ? &full[tid] : &lm->stage_full, 1);
         mbar_fence_init();
     }
+    if (tid < NW) lm->cnt[tid] = 0;
+    if (tid < 4) lm->flags[tid] = 0;
+    // dependent launch: the next kernel may take the SMs as this grid's CTAs leave; no global memory
+    // is touched before the previous kernel on the stream has finished
+    grid_dep_launch_dependents();
+    grid_dep_wait();
     __syncthreads();
     bool bad = false;
     // ---- this warp's stream: items it = warp, warp + NW, ...; item it = part it % S of row group
@@ -375,8 +378,17 @@ static int launch_linear_t(const LinearArgs &a, const LinearPlan &p, cudaStream_
     auto kern = bfp_linear_kernel<FMT, NGRP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(bfp_linear)");
-    kern<<<p.ncta, kLinThreads, p.smem, st>>>(a);
-    e = cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.ncta);
+    cfg.blockDim = dim3(kLinThreads);
+    cfg.dynamicSmemBytes = p.smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // no waits between CTAs
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, a);
     if (e != cudaSuccess) return cuda_fail(e, "launch bfp_linear");
     return BFP_OK;
 }

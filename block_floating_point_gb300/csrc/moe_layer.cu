@@ -218,7 +218,6 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
     // barrier, ctrl[2] (and the row maxima) after the phase-2 barrier, ctrl[3] at the start of the
     // next launch (no CTA reaches it before CTA 0 has arrived at ctrl[2]). A launch that gave up
     // (BFP_ETIMEOUT) leaves them set until the workspace is initialised again.
-    if (c == 0 && tid == 0) a.ctrl[3] = 0u;
     for (int i = tid; i < kMaxExperts; i += NC) ms->emask[i] = 0u;
     if (tid < a.M) ms->eslot[kMaxExperts][tid] = (int8_t)a.K;
     if (tid == 0) ms->emask[kMaxExperts] = (1u << a.M) - 1u;
@@ -233,6 +232,11 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
     }
     if (tid < 4) ms->flags[tid] = 0;
     if (tid == 0) ms->nU = 0;
+    // dependent launch: the next launch may take the SMs as this one's CTAs leave; nothing here has
+    // touched global memory yet, and nothing below does before the previous launch has finished
+    grid_dep_launch_dependents();
+    grid_dep_wait();
+    if (c == 0 && tid == 0) a.ctrl[3] = 0u;
     __syncthreads();
     STAMP(13);
     const int LDXS = stage_ldx(a.H);
@@ -1345,12 +1349,17 @@ static int launch_moe_t(const MoeArgs &a, const MoePlan &p, cudaStream_t st) {
     cfg.dynamicSmemBytes = p.smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
+    if (launch_mode() == BFP_LAUNCH_COOPERATIVE) {
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+    } else {  // one CTA per SM takes the whole GPU: the CTAs are resident together once it is free
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+    }
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, kern, a);
-    if (e != cudaSuccess) return cuda_fail(e, "launch moe_layer (cooperative)");
+    if (e != cudaSuccess) return cuda_fail(e, "launch moe_layer");
     return BFP_OK;
 }
 

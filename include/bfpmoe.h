@@ -264,6 +264,22 @@ int bfp_workspace_status(const void *ws, int *status, bfp_stream_t stream);
  */
 int bfp_set_wait_limit(int64_t iterations);
 
+/*
+ * How the MoE layer kernel (one CTA on every SM, whose CTAs wait on each
+ * other) is launched, process-wide:
+ *   BFP_LAUNCH_DEPENDENT (default): a programmatic dependent launch on the
+ *     stream; the kernel's CTAs take the SMs as the previous kernel's CTAs
+ *     leave and wait for that kernel to finish before touching memory, so
+ *     back-to-back launches overlap their start-up. The waits between CTAs
+ *     assume the layer has the GPU to itself (nothing else holding SMs); if
+ *     not, they run out and report BFP_ETIMEOUT rather than hang.
+ *   BFP_LAUNCH_COOPERATIVE: a cooperative launch, which the driver starts
+ *     only when every CTA fits; for GPUs shared with other work.
+ * The dense projection (no waits between CTAs) is always a dependent launch.
+ */
+enum { BFP_LAUNCH_DEPENDENT = 0, BFP_LAUNCH_COOPERATIVE = 1 };
+int bfp_set_launch_mode(int mode);
+
 /* Message for the last non-OK status returned on this thread. */
 const char *bfp_last_error(void);
 

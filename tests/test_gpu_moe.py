@@ -70,6 +70,21 @@ def test_tiny_layer(tiny, m):
     check(case, layer, m, rms_norm=False, row_seed0=10 * m)
 
 
+def test_cooperative_launch_mode(tiny):
+    """The layer launched cooperatively (for GPUs shared with other work) gives the same bits as the
+    default dependent launch."""
+    case, layer = tiny
+    x, _ = case.inputs(4, False, 77)
+    y0 = run_layer(layer, x, 4)[0]
+    bfp.set_launch_mode(bfp.LAUNCH_COOPERATIVE)
+    try:
+        y1 = run_layer(layer, x, 4)[0]
+    finally:
+        bfp.set_launch_mode(bfp.LAUNCH_DEPENDENT)
+    assert torch.equal(y0, y1)
+    assert_close(y1.cpu().numpy(), case.oracle_layer(x)[0], "cooperative launch")
+
+
 def test_tiny_layer_bfp8_experts():
     case = LayerCase(synth.TINY, seed=103, fmt=8)
     check(case, case.device_layer(), 3, rms_norm=False)
