@@ -8,31 +8,33 @@
 //     expert  D (silu(G x) * (U x))  combined with the routing weights, plus
 //     sigmoid(g . x) * shared(x).
 //
-// GB300 design: the layer is one persistent cooperative kernel, one 512-thread
-// CTA (16 warps) per SM. Nothing waits on the host between the router and the
-// experts:
+// GB300 design: the layer is one persistent kernel, one 512-thread CTA (16
+// warps) per SM (a dependent launch by default, cooperative on request).
+// Nothing waits on the host between the router and the experts:
 //   1. thread 0 stages the activation rows and this CTA's router rows (plus
 //      the shared-gate vector as one extra row) in shared memory with 1D bulk
-//      copies (the TMA engine); the warps build fp16 activation fragments and
-//      the CTA's fp32 logits, written to the workspace before a release
-//      increment of a grid counter;
-//   2. once the counter reaches the grid size, every CTA redundantly takes
-//      softmax / top-k / renormalisation and the union U of the experts any row
-//      selected (no host sync, no second launch), and the share of phase-2
-//      units it owns;
+//      copies (the TMA engine); the warps compute the CTA's fp32 logits on the
+//      tensor cores and write them to the workspace;
+//   2. warps 0-7 publish them (a release increment of a grid counter), wait for
+//      every CTA's, and redundantly take softmax / top-k / renormalisation, the
+//      union U of the experts any row selected (no host sync, no second launch)
+//      and the share of phase-2 units the CTA owns; warps 8-15 meanwhile build
+//      the fp16 activation fragments;
 //   3. phase 1: f-tile units (16 ffn rows of an expert's gate and up, or of the
-//      shared expert). Each warp streams whole units through two shared-memory
-//      slots of its own (lane 0 refills a slot with bulk copies as soon as the
-//      warp is done with it; L2 evict-first: the weights are read once) and
-//      writes h = silu(gate) * up for the rows that chose the expert, fp32 to
-//      the workspace, and the per-(row, slot) maxima of |h|. With fewer units
-//      than warps a unit is split over several warps, whose tiles meet in
-//      shared memory;
+//      shared expert). Each warp takes a contiguous, cost-balanced run of the
+//      records of the CTA's units (a unit cut by a run boundary is handed from
+//      one warp to its neighbour through the workspace; with few units, units
+//      are split into equal parts that meet in shared memory) and streams them
+//      through two shared-memory slots of its own (lane 0 refills a slot with
+//      bulk copies as soon as the warp is done with it; L2 evict-first: the
+//      weights are read once); it writes h = silu(gate) * up for the rows that
+//      chose the expert, fp32 to the workspace, and the per-(row, slot) maxima
+//      of |h|;
 //   4. after a grid barrier, phase 2: down-projection units (an expert and 16
-//      row groups of the hidden dimension, one per warp): per expert the CTA
-//      turns the routing-weighted h of its rows into fp16 hi + lo fragments
-//      (22 significant bits) and every warp streams its row group and writes
-//      per-(row, slot) partial outputs;
+//      row groups of the hidden dimension, one per warp): the CTA turns the
+//      routing-weighted h of a batch of experts into fp16 hi + lo fragments
+//      (22 significant bits) in one pass, and every warp streams its row group
+//      of each unit and writes per-(row, slot) partial outputs;
 //   5. after a second grid barrier, each CTA sums its row groups' slots in slot
 //      order (deterministic, no float atomics) into y (or the bf16 residual).
 // Every expert's weights are read from HBM once per step however many rows
