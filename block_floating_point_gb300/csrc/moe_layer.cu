@@ -183,13 +183,13 @@ __device__ __forceinline__ void sort8_desc(uint32_t k[8], int q[8]) {
 // Per-warp streams. Warp w has nsw slots of its own in the ring; its k-th item lands in slot
 // k mod nsw, and the warp itself issues item k + nsw (lane 0, one or two bulk copies) as soon as it is
 // done with item k. Its items, in order:
-//   phase 1: the CTA's units i = w, w + NW, ... (unit i is list entry g = c + i * ncta, see p1_tile),
-//            each in chunks of ch1 records of its gate row group followed by the same records of its
-//            up row group;
+//   phase 1: the warp's phase-1 items (parts of the CTA's units, unit u being list entry
+//            g = c + u * ncta, see p1_tile), each in chunks of ch1 records of its gate row group
+//            followed by the same records of its up row group;
 //   phase 2: for each down-projection unit q of the CTA's range that has a row group oct * r2 + w,
 //            that row group in chunks of 2 * ch1 records.
-// No warp waits for another inside a phase: a warp accumulates whole f-tiles (phase 1) or whole row
-// groups (phase 2) over all of k and writes its own results.
+// Within a phase a warp waits for another only where a phase-1 unit is split between warps (the
+// part that finishes first hands its tile over).
 template <int FMT, int NGRP>
 __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
