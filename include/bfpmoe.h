@@ -200,8 +200,9 @@ int bfp_workspace_init(void *ws, size_t ws_bytes, bfp_stream_t stream);
  * (P1 "Fused decode kernels": device top-k routing and batched expert
  * streams). Outputs (device): y fp32 [m x hidden]; topk_idx int32 [m x top_k]
  * and topk_w fp32 [m x top_k] (both nullable) in slot order.
- * One persistent cooperative launch; its cross-block waits are bounded and
- * report BFP_ETIMEOUT through bfp_workspace_status.
+ * One persistent launch (a programmatic dependent launch unless
+ * bfp_set_launch_mode asks for a cooperative one); its cross-block waits are
+ * bounded and report BFP_ETIMEOUT through bfp_workspace_status.
  */
 int moe_decode_layer(const bfp_moe_layer *layer, const uint16_t *x, int m, float *y, int32_t *topk_idx,
                      float *topk_w, void *ws, size_t ws_bytes, bfp_stream_t stream);
@@ -213,13 +214,16 @@ int moe_decode_layer(const bfp_moe_layer *layer, const uint16_t *x, int m, float
  * latency-critical path that must not call cudaMalloc because it can
  * synchronise the device. The block_floating_point pages have no counterpart;
  * this is a convenience of this library.
- *   - Computes exactly what moe_decode_layer computes; x, y, topk_idx, topk_w
- *     as there (caller-owned device memory).
+ *   - Computes what moe_decode_layer computes (same selection; outputs may
+ *     differ in the last fp32 bits: with the smaller scratch the gate/up
+ *     phase deals whole units to warps, which changes the order of some
+ *     sums); x, y, topk_idx, topk_w as there (caller-owned device memory).
  *   - Scratch: one built-in device array of 1.5 MiB (1,572,864 bytes),
  *     allocated when the library is loaded and held by every GPU that loads
- *     it until the process exits. A layer needing more (moe_workspace_size >
- *     1.5 MiB) is rejected with BFP_EWORKSPACE; the full-size layer (hidden
- *     2048, 256 experts, ffn 512, top-8) at 16 rows needs 1,492,224 bytes.
+ *     it until the process exits. A layer whose core state needs more (the
+ *     workspace without its optional phase-1 hand-off area) is rejected with
+ *     BFP_EWORKSPACE; the full-size layer (hidden 2048, 256 experts, ffn 512,
+ *     top-8) at 16 rows needs 1,492,224 bytes.
  *   - The first call on a device looks up the array's device address and
  *     zeroes it, synchronously: make that first call before any stream
  *     capture. Each call then clears the array's counters on its stream.
