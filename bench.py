@@ -496,6 +496,14 @@ def main():
             gd = mat.nbytes / (usd * 1e-6) / 1e9
             sec[f"dense_bfp8_m{m}"] = {"us": usd, "gbs": gd, "pct_of_8tbs": 100 * gd / NOMINAL_HBM_GBS,
                                       "bytes": mat.nbytes}
+        # greedy next token over LM-head logits [16 x 151936] fp32 (read from HBM after a flush)
+        lg = torch.from_numpy(synth.normal(args.seed, 7, (16, 151936), std=3.0)).to(device)
+        wsg = bfp.greedy_workspace(16, 151936, device)
+        tokg = torch.empty(16, dtype=torch.int32, device=device)
+        tot, _ = timed_flushed(lambda i: bfp.greedy_tokens(lg, wsg, tokg), ksec, 5, flush)
+        usg = tot * 1e3 / ksec
+        sec["greedy_m16_v151936"] = {"us": usg, "gbs": lg.numel() * 4 / (usg * 1e-6) / 1e9, "bytes": lg.numel() * 4,
+                                     "launches": 2, "timing": "each call alone after a 256 MB L2 flush"}
         out["secondary"] = sec
         if rank == 0 and world == 1:
             v, s_ = cpu_baseline_sample(args, spec, xs[0])

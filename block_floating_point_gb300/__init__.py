@@ -65,6 +65,8 @@ SIGNATURES = {
     "moe_decode_layer_static": [_LP, _P, _I, _P, _P, _P, _P],
     "moe_stack_workspace_size": [_LP, _I, _MP, _I, ctypes.POINTER(_SZ)],
     "moe_stack_decode": [_LP, _I, _MP, _P, _I, _P, _P, _SZ, _P],
+    "bfp_greedy_workspace_size": [_I, _I64, ctypes.POINTER(_SZ)],
+    "bfp_greedy_tokens": [_P, _I, _I64, _I64, _P, _P, _SZ, _P],
     "bfp_workspace_status": [_P, ctypes.POINTER(_I), _P],
     "bfp_set_wait_limit": [_I64],
     "bfp_set_launch_mode": [_I],
@@ -385,3 +387,25 @@ def moe_stack_decode(layers, lm_head: DeviceMatrix, h, ws, logits=None, stream=N
     _check(load().moe_stack_decode(arr, len(layers), ctypes.byref(c), _ptr(h), m, _ptr(logits), _ptr(ws),
                                    ws.numel(), _stream(stream)), "moe_stack_decode")
     return logits
+
+
+# ----------------------------------------------------------------------------- greedy next token
+def greedy_workspace_size(m: int, n: int) -> int:
+    out = ctypes.c_size_t()
+    _check(load().bfp_greedy_workspace_size(m, n, ctypes.byref(out)), "bfp_greedy_workspace_size")
+    return out.value
+
+
+def greedy_workspace(m: int, n: int, device, stream=None):
+    return _alloc_ws(greedy_workspace_size(m, n), device, stream)
+
+
+def greedy_tokens(logits, ws, tokens=None, stream=None):
+    """Greedy next token per row of fp32 logits [m, n] (CUDA tensor): int32 [m] arg max, ties to the lower index."""
+    import torch
+    m, n = logits.shape
+    if tokens is None:
+        tokens = torch.empty(m, dtype=torch.int32, device=logits.device)
+    _check(load().bfp_greedy_tokens(_ptr(logits), m, n, logits.stride(0), _ptr(tokens), _ptr(ws), ws.numel(),
+                                    _stream(stream)), "bfp_greedy_tokens")
+    return tokens

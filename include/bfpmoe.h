@@ -254,6 +254,21 @@ int moe_stack_decode(const bfp_moe_layer *layers, int n_layers, const bfp_matrix
                      float *logits, void *ws, size_t ws_bytes, bfp_stream_t stream);
 
 /*
+ * Greedy next token for m rows (1..16) of fp32 logits [m x n] (device, row
+ * stride ldl >= n elements), the step after the LM head in greedy decoding
+ * (P1 "Fused decode kernels": the greedy argmax over the logits, up to 16
+ * rows): tokens[r] (int32, device) = the index of the largest logit of row r,
+ * ties to the lower index, -0 equal to +0; NaN is never chosen, and a row
+ * with no other value gives 0. 1 <= n <= 2^31 - 1. The result is exact (no
+ * arithmetic, only comparisons). Two launches on the stream, dependent on
+ * the previous kernel; ws: bfp_greedy_workspace_size bytes of device memory,
+ * no initialisation needed. logits, tokens and ws 16-byte aligned.
+ */
+int bfp_greedy_workspace_size(int m, int64_t n, size_t *bytes);
+int bfp_greedy_tokens(const float *logits, int m, int64_t n, int64_t ldl, int32_t *tokens, void *ws, size_t ws_bytes,
+                      bfp_stream_t stream);
+
+/*
  * Synchronises the stream and reads the workspace's status word: *status =
  * BFP_OK or the first device-side error (BFP_ETIMEOUT). The word stays set
  * until bfp_workspace_init.

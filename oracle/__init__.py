@@ -69,6 +69,8 @@ def _load():
                 fn = getattr(lib, name)
                 fn.argtypes = args
                 fn.restype = ctypes.c_int
+            lib.oracle_greedy_row.argtypes = [_P, _I64]
+            lib.oracle_greedy_row.restype = ctypes.c_int64
             lib.oracle_shared_gate.argtypes = [_P, _P, _I]
             lib.oracle_shared_gate.restype = ctypes.c_double
             _lib = lib
@@ -282,3 +284,17 @@ def lm_head_rows(h_bf16, lm_rows_f32: np.ndarray, fmt: int = BFP8):
     e, c = encode(fmt, lm_rows_f32)
     y, _ = linear(fmt, e, c, t)
     return y
+
+
+def greedy_tokens(logits_f32) -> np.ndarray:
+    """Greedy next token per row of fp32 logits [M, V]: index of the largest value, ties to the lower
+    index, NaN never chosen (a NaN-only row gives 0). The step after the LM head in greedy decoding
+    (Qwen3.6-35B-A3B card, "Fused decode kernels")."""
+    lg = np.ascontiguousarray(logits_f32, dtype=np.float32)
+    if lg.ndim == 1:
+        lg = lg[None, :]
+    lib = _load()
+    out = np.zeros(lg.shape[0], dtype=np.int32)
+    for r in range(lg.shape[0]):
+        out[r] = lib.oracle_greedy_row(lg[r].ctypes.data, lg.shape[1])
+    return out

@@ -203,6 +203,22 @@ int oracle_route_row(const float *logits, int n_experts, int k, int32_t *idx, do
     return ORACLE_OK;
 }
 
+/*
+ * Greedy next token of one row of fp32 logits (the step after the LM head in
+ * greedy decoding; Qwen3.6-35B-A3B card, "Fused decode kernels": the greedy
+ * argmax over the logits for up to 16 rows): the index of the largest value,
+ * ties to the lower index, compared as fp32 numbers (-0 equals +0). NaN is
+ * never chosen; a row of NaN alone gives 0.
+ */
+int64_t oracle_greedy_row(const float *logits, int64_t n) {
+    int64_t best = -1;
+    for (int64_t i = 0; i < n; ++i) {
+        if (isnan(logits[i])) continue;
+        if (best < 0 || logits[i] > logits[best]) best = i; /* strict: ties keep the lower index */
+    }
+    return best < 0 ? 0 : best;
+}
+
 static double sigmoid(double a) { return 1.0 / (1.0 + exp(-a)); }
 
 /*

@@ -148,6 +148,13 @@ def run_stack(case, m, row_seed0, sample_vocab=None):
     got = logits.cpu().numpy()[:, vrows]
     assert_close(got, oracle.lm_head_rows(h_gpu, lm_rows), "LM head on the kernel's final h")
     assert_close(got, oracle.lm_head_rows(h_ref, lm_rows), "end-to-end logits", tol=1e-2)
+    # greedy next token on the stack's logits: a property that holds at any vocabulary size
+    gws = bfp.greedy_workspace(m, case.vocab, logits.device)
+    tok = bfp.greedy_tokens(logits, gws).cpu().numpy()
+    full = logits.cpu().numpy()
+    for r in range(m):
+        t = int(tok[r])
+        assert np.all(full[r] <= full[r, t]) and np.all(full[r, :t] < full[r, t]), f"row {r}: token {t}"
     # a second run from the same h gives the same bits
     h2 = bf16_tensor(h0)
     logits2 = bfp.moe_stack_decode(layers, lm, h2, ws)

@@ -202,3 +202,33 @@ def test_rmsnorm_and_residual():
     assert np.array_equal(t, bf16((hf * inv[:, None]).astype(np.float32)))
     y = np.random.default_rng(82).standard_normal((3, 256)).astype(np.float32)
     assert np.array_equal(oracle.residual_bf16(h, y), bf16((hf + y).astype(np.float32)))
+
+
+def test_greedy_tokens_brute_force_and_special_cases():
+    # Brute force: the first index whose value no other non-NaN value exceeds.
+    rng = np.random.default_rng(91)
+    for trial in range(300):
+        n = int(rng.integers(1, 70))
+        l = rng.standard_normal(n).astype(np.float32)
+        if trial % 3 == 0:  # ties
+            l = np.round(l)
+        if trial % 5 == 0:  # NaNs sprinkled in
+            l[rng.random(n) < 0.3] = np.nan
+        vals = [float(v) for v in l]
+        ok = [i for i in range(n) if vals[i] == vals[i]]
+        want = 0 if not ok else min(i for i in ok if all(vals[i] >= vals[j] for j in ok))
+        assert oracle.greedy_tokens(l)[0] == want
+    # Closed cases: a one-hot row, equal values, signed zeros, infinities, NaN alone.
+    one_hot = np.full(1000, -1.0, np.float32)
+    one_hot[637] = 2.0
+    assert oracle.greedy_tokens(one_hot)[0] == 637
+    assert oracle.greedy_tokens(np.full(9, 3.5, np.float32))[0] == 0
+    assert oracle.greedy_tokens(np.array([-0.0, 0.0, -1.0], np.float32))[0] == 0
+    assert oracle.greedy_tokens(np.array([-1.0, -0.0, 0.0], np.float32))[0] == 1
+    assert oracle.greedy_tokens(np.array([np.nan, -np.inf, 1e30, np.inf, np.inf], np.float32))[0] == 3
+    assert oracle.greedy_tokens(np.array([np.nan, np.nan], np.float32))[0] == 0
+    assert oracle.greedy_tokens(np.array([np.nan, -np.inf], np.float32))[0] == 1
+    # Rows are independent; the last index can win.
+    m = np.zeros((3, 5), np.float32)
+    m[0, 4], m[1, 2], m[2, 0] = 1, 1, 1
+    assert list(oracle.greedy_tokens(m)) == [4, 2, 0]
