@@ -8,9 +8,11 @@ width 512, top-8, shared expert of width 512, BFP4 experts, bf16 router):
 each step streams the union of the experts the 16 rows select (~100) plus the
 shared expert, ~180 MB, more than the 129 MB L2, and steps rotate over
 several independently drawn layer instances. Secondary lines (same run): the
-same layer at M=1, the hot-expert routing variant at M=16, and the dense BFP8
-projection [8192 x 2048] at M=1/16; those steps are smaller than L2, so each
-one is timed alone after a 256 MB L2-flushing write.
+same layer at M=1, the hot-expert routing variant at M=16, the dense BFP8
+projection [8192 x 2048] at M=1/8/16 and the greedy token over [16 x 151936]
+logits (steps smaller than L2, each timed alone after a 256 MB L2-flushing
+write); the BFP8 LM head [151936 x 2048] alone and the 8-row decode stack (40
+layers, LM head, greedy token), both larger than L2, timed back to back.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--quick]
 
@@ -42,16 +44,20 @@ L2_FLUSH_BYTES = 256 << 20
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the M=16 layer kernel, from one ncu
 # capture (profiles/moe_layer_m16.md, "Traffic of the current kernel"), valid while the kernel
 # sources hash to src_sha.
-NCU_TRAFFIC = {"moe_layer_m16": {"bytes_per_launch": 180_546_560, "src_sha": "34a80c9af5fb537d"}}
+NCU_TRAFFIC = {"moe_layer_m16": {"bytes_per_launch": 180_546_560, "src_sha": "78fadbe6d6507594"}}
 
 
 def kernel_src_sha() -> str:
     """Hash of the layer kernel's sources with comments and blank space removed, so
-    that editing a comment keeps a traffic figure taken from the same code."""
+    that editing a comment keeps a traffic figure taken from the same code. Of
+    moe_layer.cu only the part before its public entry points counts (the kernel,
+    its plan and its launch); the entry points after it validate and forward."""
     h = hashlib.sha256()
     for f in ("moe_layer.cu", "bfp_tiles.cuh", "bfp_device.cuh", "bfp_launch.h"):
         with open(os.path.join(ROOT, "block_floating_point_gb300", "csrc", f), encoding="utf-8") as fh:
             src = fh.read()
+        if f == "moe_layer.cu":
+            src = src.split('\nextern "C" {\n', 1)[0]
         src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
         src = re.sub(r"//[^\n]*", "", src)
         h.update(" ".join(src.split()).encode())
@@ -502,21 +508,67 @@ def main():
         tokg = torch.empty(16, dtype=torch.int32, device=device)
         tot, _ = timed_flushed(lambda i: bfp.greedy_tokens(lg, wsg, tokg), ksec, 5, flush)
         usg = tot * 1e3 / ksec
-        # the same calls back to back (logits L2-resident, as right after the LM head that wrote them)
-        for _ in range(5):
-            bfp.greedy_tokens(lg, wsg, tokg)
-        eg0, eg1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        eg0.record()
-        for _ in range(ksec):
-            bfp.greedy_tokens(lg, wsg, tokg)
-        eg1.record()
-        torch.cuda.synchronize()
-        usb = eg0.elapsed_time(eg1) * 1e3 / ksec
+        # the same calls back to back in a CUDA graph (logits L2-resident, as right after the LM head that
+        # wrote them; no host launch overhead between calls)
+        usb = timed_graph(lambda i: bfp.greedy_tokens(lg, wsg, tokg), ksec, 5, True) * 1e3 / ksec
         sec["greedy_m16_v151936"] = {"us": usg, "gbs": lg.numel() * 4 / (usg * 1e-6) / 1e9, "bytes": lg.numel() * 4,
                                      "us_back_to_back": usb, "launches": 2,
                                      "timing": "us: each call alone after a 256 MB L2 flush; us_back_to_back: "
-                                               "consecutive calls on L2-resident logits"}
+                                               "consecutive calls in a CUDA graph on L2-resident logits"}
+        # decode stack, 8 rows: 40 MoE layers (the R weight instances in rotation: an instance comes back after
+        # R - 1 other layers, >= 200 MB of other weights, more than L2) + the BFP8 LM head [151936 x 2048],
+        # then the greedy next token; h is updated in place from step to step, as in decoding.
+        nl, m8, vocab = 40, 8, 151936
+        stack = [layers[l % R] for l in range(nl)]
+        lm = bfp.DeviceMatrix.from_host(8, vocab, spec.hidden, bfp.encode(8, synth.normal(
+            args.seed, synth.stream_id(synth.KIND_LMHEAD), (vocab, spec.hidden), std=synth.W_STD)), device=device)
+        h8 = torch.from_numpy(synth.to_bf16_bits(synth.normal(args.seed, synth.stream_id(synth.KIND_STACK_H),
+                                                              (m8, spec.hidden))).view(np.int16)).to(device)
+        wss = bfp.moe_stack_workspace(stack, lm, m8)
+        lg8 = torch.empty((m8, vocab), dtype=torch.float32, device=device)
+        ws8 = bfp.greedy_workspace(m8, vocab, device)
+        tok8 = torch.empty(m8, dtype=torch.int32, device=device)
+        kst = 10
+        sel = torch.empty((kst, nl, m8, spec.top_k), dtype=torch.int32, device=device)
+        for i in range(3):
+            bfp.moe_stack_decode(stack, lm, h8, wss, logits=lg8, topk_idx=sel[0])
+            bfp.greedy_tokens(lg8, ws8, tok8)
+        es0, es1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        es0.record()
+        for i in range(kst):
+            bfp.moe_stack_decode(stack, lm, h8, wss, logits=lg8, topk_idx=sel[i])
+            bfp.greedy_tokens(lg8, ws8, tok8)
+        es1.record()
+        torch.cuda.synchronize()
+        assert bfp.workspace_status(wss) == bfp.BFP_OK
+        ust = es0.elapsed_time(es1) * 1e3 / kst
+        sa = sel.cpu().numpy()
+        bst = float(np.mean([sum(union_bytes(stack[l], sa[i, l]) for l in range(nl)) for i in range(kst)])) + lm.nbytes
+        nun = float(np.mean([len(np.unique(sa[i, l])) for i in range(kst) for l in range(nl)]))
+        # the LM head alone (330 MB, larger than L2: consecutive calls stream it from HBM)
+        wsl8 = bfp.linear_workspace(lm, m8)
+        x8 = h8.clone()
+        for _ in range(3):
+            bfp.linear(lm, x8, wsl8, y=lg8)
+        el0, el1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        el0.record()
+        for _ in range(20):
+            bfp.linear(lm, x8, wsl8, y=lg8)
+        el1.record()
+        torch.cuda.synchronize()
+        usl = el0.elapsed_time(el1) * 1e3 / 20
+        sec["stack_m8_40layers"] = {
+            "us_per_step": ust, "tokens_per_s": m8 / (ust * 1e-6), "bfp_bytes_per_step": bst,
+            "gbs": bst / (ust * 1e-6) / 1e9, "pct_of_measured_copy": 100 * bst / (ust * 1e-6) / 1e9 / peak,
+            "union_experts_per_layer": nun, "launches_per_step": nl + 3,
+            "timing": f"{kst} consecutive steps (40 layer launches, LM head, 2 greedy launches each), CUDA events",
+            "weights": f"{R} independent layer instances in rotation over the 40 layers; LM head BFP8 "
+                       f"[{vocab} x {spec.hidden}] seeded N(0,0.02)"}
+        sec["lm_head_bfp8_m8"] = {"us": usl, "gbs": lm.nbytes / (usl * 1e-6) / 1e9,
+                                  "pct_of_measured_copy": 100 * lm.nbytes / (usl * 1e-6) / 1e9 / peak,
+                                  "bytes": lm.nbytes, "timing": "20 consecutive calls (330 MB each, > L2)"}
         out["secondary"] = sec
         if rank == 0 and world == 1:
             v, s_ = cpu_baseline_sample(args, spec, xs[0])

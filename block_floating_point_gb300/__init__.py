@@ -64,7 +64,7 @@ SIGNATURES = {
     "moe_decode_layer": [_LP, _P, _I, _P, _P, _P, _P, _SZ, _P],
     "moe_decode_layer_static": [_LP, _P, _I, _P, _P, _P, _P],
     "moe_stack_workspace_size": [_LP, _I, _MP, _I, ctypes.POINTER(_SZ)],
-    "moe_stack_decode": [_LP, _I, _MP, _P, _I, _P, _P, _SZ, _P],
+    "moe_stack_decode": [_LP, _I, _MP, _P, _I, _P, _P, _P, _SZ, _P],
     "bfp_greedy_workspace_size": [_I, _I64, ctypes.POINTER(_SZ)],
     "bfp_greedy_tokens": [_P, _I, _I64, _I64, _P, _P, _SZ, _P],
     "bfp_workspace_status": [_P, ctypes.POINTER(_I), _P],
@@ -376,16 +376,20 @@ def moe_stack_workspace(layers, lm_head: DeviceMatrix, m: int, stream=None):
     return _alloc_ws(moe_stack_workspace_size(layers, lm_head, m), lm_head.data.device, stream)
 
 
-def moe_stack_decode(layers, lm_head: DeviceMatrix, h, ws, logits=None, stream=None):
-    """Decode stack: h (bf16 [m, hidden], updated in place) through every layer, then LM-head logits fp32."""
+def moe_stack_decode(layers, lm_head: DeviceMatrix, h, ws, logits=None, topk_idx=None, stream=None):
+    """Decode stack: h (bf16 [m, hidden], updated in place) through every layer, then LM-head logits fp32.
+    topk_idx (optional int32 CUDA tensor, [n_layers, m, top_k] when the layers share top_k) receives every
+    layer's selection."""
     import torch
     m = h.shape[0]
     if logits is None:
         logits = torch.empty((m, lm_head.n), dtype=torch.float32, device=h.device)
     arr = _layers_array(layers)
     c = lm_head.c()
-    _check(load().moe_stack_decode(arr, len(layers), ctypes.byref(c), _ptr(h), m, _ptr(logits), _ptr(ws),
-                                   ws.numel(), _stream(stream)), "moe_stack_decode")
+    if topk_idx is not None and topk_idx.numel() < m * sum(L.top_k for L in layers):
+        raise ValueError("topk_idx holds fewer than m * sum(top_k) entries")
+    _check(load().moe_stack_decode(arr, len(layers), ctypes.byref(c), _ptr(h), m, _ptr(logits), _ptr(topk_idx),
+                                   _ptr(ws), ws.numel(), _stream(stream)), "moe_stack_decode")
     return logits
 
 

@@ -1498,7 +1498,7 @@ int moe_stack_workspace_size(const bfp_moe_layer *layers, int n_layers, const bf
 }
 
 int moe_stack_decode(const bfp_moe_layer *layers, int n_layers, const bfp_matrix *lm_head, uint16_t *h, int m,
-                     float *logits, void *ws, size_t ws_bytes, bfp_stream_t stream) {
+                     float *logits, int32_t *topk_idx, void *ws, size_t ws_bytes, bfp_stream_t stream) {
     size_t mb, lb, hb;
     int rc = stack_layout(layers, n_layers, lm_head, m, &mb, &lb, &hb);
     if (rc) return rc;
@@ -1509,9 +1509,11 @@ int moe_stack_decode(const bfp_moe_layer *layers, int n_layers, const bfp_matrix
     uint8_t *w = static_cast<uint8_t *>(ws);
     uint16_t *hb2 = reinterpret_cast<uint16_t *>(w + mb + lb);
     uint16_t *cur = h, *nxt = hb2;
+    int32_t *idx = topk_idx;  // layer l's selection follows the layers before it, m * top_k entries each
     for (int l = 0; l < n_layers; ++l) {
-        rc = moe_launch(&layers[l], cur, m, 1, nullptr, nxt, nullptr, nullptr, ws, mb, st);
+        rc = moe_launch(&layers[l], cur, m, 1, nullptr, nxt, idx, nullptr, ws, mb, st);
         if (rc) return rc;
+        if (idx) idx += (int64_t)m * layers[l].top_k;
         std::swap(cur, nxt);
     }
     if (cur != h) {

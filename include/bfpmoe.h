@@ -246,12 +246,15 @@ int moe_decode_layer_static(const bfp_moe_layer *layer, const uint16_t *x, int m
  * (unit weight, fp32), then logits = LMhead( bf16(RMSNorm(h)) ) in fp32
  * [m x lm_head->n] (P1 "Fused decode kernels": one-launch RMSNorm, packed LM
  * head). h: bf16 [m x hidden] device, updated in place. lm_head: BFP matrix
- * [vocab x hidden] in device memory. ws: moe_stack_workspace_size bytes.
+ * [vocab x hidden] in device memory. topk_idx (nullable, device int32): every
+ * layer's selection in slot order, layer after layer, m * layers[l].top_k
+ * entries for layer l (row-major [m x top_k]). ws: moe_stack_workspace_size
+ * bytes.
  */
 int moe_stack_workspace_size(const bfp_moe_layer *layers, int n_layers, const bfp_matrix *lm_head, int m,
                              size_t *bytes);
 int moe_stack_decode(const bfp_moe_layer *layers, int n_layers, const bfp_matrix *lm_head, uint16_t *h, int m,
-                     float *logits, void *ws, size_t ws_bytes, bfp_stream_t stream);
+                     float *logits, int32_t *topk_idx, void *ws, size_t ws_bytes, bfp_stream_t stream);
 
 /*
  * Greedy next token for m rows (1..16) of fp32 logits [m x n] (device, row

@@ -62,7 +62,7 @@ class StackCase:
                     top_k=self.spec.top_k)
 
     def trajectory(self, h_row):
-        """Oracle trajectory of one row: [(h_l, y_l)] per layer and the final h; None if some layer's
+        """Oracle trajectory of one row: [(h_l, y_l, idx_l)] per layer and the final h; None if some layer's
         top-k margin is below MARGIN."""
         h = h_row[None, :].copy()
         steps = []
@@ -70,8 +70,8 @@ class StackCase:
             t = oracle.rmsnorm_bf16(h)
             if oracle.topk_margin(oracle.router_logits(self.routers[l], t)[0], self.spec.top_k) < MARGIN:
                 return None
-            h_next, _, y, _, _ = oracle.stack_layer(h, self.layer_args(l))
-            steps.append((h[0], y[0]))
+            h_next, _, y, idx, _ = oracle.stack_layer(h, self.layer_args(l))
+            steps.append((h[0], y[0], idx[0]))
             h = h_next
         return steps, h[0]
 
@@ -127,9 +127,12 @@ def run_stack(case, m, row_seed0, sample_vocab=None):
         h_in = np.stack([t[0][l][0] for t in trajs])
         y_or = np.stack([t[0][l][1] for t in trajs]).astype(np.float64)
         h = bf16_tensor(h_in)
-        bfp.moe_stack_decode([layers[l]], lm, h, ws1)
+        idx1 = torch.full((m, case.spec.top_k), -1, dtype=torch.int32, device="cuda")
+        bfp.moe_stack_decode([layers[l]], lm, h, ws1, topk_idx=idx1)
         torch.cuda.synchronize()
         assert bfp.workspace_status(ws1) == bfp.BFP_OK
+        idx_or = np.stack([t[0][l][2] for t in trajs])
+        assert np.array_equal(idx1.cpu().numpy(), idx_or), f"layer {l}: selection differs from the oracle's"
         got = synth.bf16_bits_to_f32(h.cpu().numpy().view(np.uint16)).astype(np.float64)
         exact = synth.bf16_bits_to_f32(h_in).astype(np.float64) + y_or
         rms_y = np.sqrt(np.mean(y_or ** 2, axis=1, keepdims=True))
@@ -139,9 +142,16 @@ def run_stack(case, m, row_seed0, sample_vocab=None):
 
     # the whole stack
     h = bf16_tensor(h0)
-    logits = bfp.moe_stack_decode(layers, lm, h, ws)
+    k = case.spec.top_k
+    idx_all = torch.full((case.n_layers, m, k), -1, dtype=torch.int32, device="cuda")
+    logits = bfp.moe_stack_decode(layers, lm, h, ws, topk_idx=idx_all)
     torch.cuda.synchronize()
     assert bfp.workspace_status(ws) == bfp.BFP_OK
+    ia = idx_all.cpu().numpy()
+    # layer 0 sees the same input on both sides; every layer's selection is k distinct experts
+    assert np.array_equal(ia[0], np.stack([t[0][0][2] for t in trajs]))
+    assert ia.min() >= 0 and ia.max() < case.spec.n_experts
+    assert all(len(set(ia[l, r])) == k for l in range(case.n_layers) for r in range(m))
     h_gpu = h.cpu().numpy().view(np.uint16)
     assert_close(synth.bf16_bits_to_f32(h_gpu), synth.bf16_bits_to_f32(h_ref), "final hidden state", tol=1e-2)
     lm_rows = case.lm_rows(vrows)
