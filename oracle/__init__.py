@@ -298,3 +298,89 @@ def greedy_tokens(logits_f32) -> np.ndarray:
     for r in range(lg.shape[0]):
         out[r] = lib.oracle_greedy_row(lg[r].ctypes.data, lg.shape[1])
     return out
+
+
+# ---------------------------------------------------------------------------
+# Error-compensated (GPTQ-style) BFP encoding. The Qwen3.8-27B gptq-ctx2 card,
+# "What changed in this release": BFP4 weights computed by a GPTQ variant for
+# block floating point, with error compensation inside the 16-value blocks,
+# every value exactly representable so that the plain conversion reproduces it.
+# GPTQ itself is the published method of Frantar et al., "GPTQ: Accurate
+# Post-Training Quantization for Generative Pre-trained Transformers" (2022):
+# columns are quantised one at a time and each rounding error is moved onto the
+# columns not yet quantised through the inverse of the layer's Hessian
+# H = X^T X of its calibration inputs X.
+# Readings (the pages give no more): H = X^T X / t plus damp * mean(diag) on the
+# diagonal; columns in their natural order; a block's exponent is taken from its
+# current (already compensated) values when its first column comes up; after its
+# 16 columns the block is brought to canonical form (exponent lowered while every
+# magnitude fits one bit less), which is what plain round-to-nearest would give
+# for the same values.
+# ---------------------------------------------------------------------------
+def gptq_hessian(x_f32, damp: float = 0.01) -> np.ndarray:
+    """H = X^T X / t + damp * mean(diag(X^T X / t)) * I in fp64; x is [t, k] (t calibration inputs)."""
+    x = np.asarray(x_f32, dtype=np.float64)
+    h = x.T @ x / x.shape[0]
+    h[np.diag_indices_from(h)] += damp * float(np.mean(np.diag(h)))
+    return h
+
+
+def gptq_factor(x_f32, damp: float = 0.01) -> np.ndarray:
+    """Upper-triangular U with H^-1 = U^T U (GPTQ's Cholesky form of the inverse Hessian)."""
+    hinv = np.linalg.inv(gptq_hessian(x_f32, damp))
+    return np.linalg.cholesky(hinv).T
+
+
+def _exp_field(v: np.ndarray) -> np.ndarray:
+    """fp32-style biased exponent of fp64 values: floor(log2|v|) + 127, 0 below 2^-126 (and for 0)."""
+    _, p = np.frexp(np.abs(v))
+    e = p.astype(np.int64) + 126
+    return np.where(np.abs(v) < 2.0 ** -126, 0, e)
+
+
+def gptq_quantise_column(v: np.ndarray, E: np.ndarray, mb: int):
+    """Magnitude codes and values of one column on the blocks' grids (ties to even, saturating)."""
+    s = E - 127 - (mb - 1)
+    mag = np.rint(np.ldexp(np.abs(v), -s))
+    mag = np.minimum(mag, 2 ** mb - 1)
+    mag = np.where((E == 0) | (_exp_field(v) == 0), 0, mag).astype(np.int64)
+    q = np.where(mag > 0, np.sign(v) * np.ldexp(mag.astype(np.float64), s), 0.0)
+    return mag, q
+
+
+def gptq_encode(fmt: int, w_f32, u: np.ndarray):
+    """Error-compensated encoding of w [n, k] with the factor u [k, k]: returns (exps [n, k/16] u8,
+    codes [n, k] u8) in the same logical form as ``encode``. Rows are independent; within a row the
+    columns go left to right and column j's error (v - q) / u[j, j] is taken off the later columns
+    in proportion to u[j, j+1:]."""
+    mb = mant_bits(fmt)
+    w = np.array(w_f32, dtype=np.float64)
+    n, k = w.shape
+    if k % 16 or u.shape != (k, k):
+        raise ValueError("k must be a multiple of 16 and u [k, k]")
+    exps = np.zeros((n, k // 16), dtype=np.uint8)
+    mags = np.zeros((n, k), dtype=np.int64)
+    neg = np.zeros((n, k), dtype=bool)
+    for b in range(k // 16):
+        j0 = 16 * b
+        E = _exp_field(w[:, j0:j0 + 16]).max(axis=1)
+        if np.any(E >= 255):
+            raise ValueError("compensated values left the fp32 range")
+        for j in range(j0, j0 + 16):
+            mag, q = gptq_quantise_column(w[:, j], E, mb)
+            mags[:, j], neg[:, j] = mag, (mag > 0) & (w[:, j] < 0)
+            err = (w[:, j] - q) / u[j, j]
+            if j + 1 < k:
+                w[:, j + 1:] -= np.outer(err, u[j, j + 1:])
+        # canonical form: lower the exponent while every magnitude of the block fits mb - 1 bits
+        blk = mags[:, j0:j0 + 16]
+        for r in range(n):
+            if blk[r].max() == 0:
+                E[r] = 0
+                continue
+            while E[r] > 1 and blk[r].max() < 2 ** (mb - 1):
+                E[r] -= 1
+                blk[r] *= 2
+        exps[:, b] = E.astype(np.uint8)
+    codes = (neg.astype(np.int64) << mb) | mags
+    return exps, codes.astype(np.uint8)
