@@ -54,6 +54,9 @@ SIGNATURES = {
     "bfp_packed_size": [_I, _I64, _I64, ctypes.POINTER(_I64)],
     "bfp_encode": [_I, _P, _I64, _I64, _P, _I64, _I],
     "bfp_encode_gate_up": [_I, _P, _P, _I64, _I64, _P, _I64, _I],
+    "bfp_gptq_factor": [_P, _I64, _I64, ctypes.c_double, _P, _I],
+    "bfp_encode_gptq": [_I, _P, _I64, _I64, _P, _P, _I64, _I],
+    "bfp_encode_gate_up_gptq": [_I, _P, _P, _I64, _I64, _P, _P, _I64, _I],
     "bfp_read_fields": [_MP, _P, _P],
     "bfp_decode_host": [_MP, _P],
     "bfp_unpack_device": [_MP, _P, _P],
@@ -146,6 +149,42 @@ def encode_gate_up(fmt: int, gate: np.ndarray, up: np.ndarray, threads: int = 0,
     assert out.nbytes >= size
     _check(load().bfp_encode_gate_up(fmt, gate.ctypes.data, up.ctypes.data, ffn, hidden, out.ctypes.data,
                                      out.nbytes, threads), "bfp_encode_gate_up")
+    return out
+
+
+def gptq_factor(x: np.ndarray, damp: float = 0.01, threads: int = 0) -> np.ndarray:
+    """Upper factor u [k, k] (fp64) with H^-1 = u^T u, H = x^T x / t + damp * mean(diag) * I (x: [t, k] fp32)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    t, k = x.shape
+    u = np.empty((k, k), dtype=np.float64)
+    _check(load().bfp_gptq_factor(x.ctypes.data, t, k, float(damp), u.ctypes.data, threads), "bfp_gptq_factor")
+    return u
+
+
+def encode_gptq(fmt: int, w: np.ndarray, u: np.ndarray, threads: int = 0) -> np.ndarray:
+    """Error-compensated host encoding of fp32 w [n, k] with the factor u [k, k]; packed bytes."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    u = np.ascontiguousarray(u, dtype=np.float64)
+    n, k = w.shape
+    if u.shape != (k, k):
+        raise ValueError("u must be [k, k]")
+    out = np.empty(packed_size(fmt, n, k), dtype=np.uint8)
+    _check(load().bfp_encode_gptq(fmt, w.ctypes.data, n, k, u.ctypes.data, out.ctypes.data, out.nbytes, threads),
+           "bfp_encode_gptq")
+    return out
+
+
+def encode_gate_up_gptq(fmt: int, gate: np.ndarray, up: np.ndarray, u: np.ndarray, threads: int = 0) -> np.ndarray:
+    """bfp_encode_gate_up's layout with both halves error-compensated through the same factor u."""
+    gate = np.ascontiguousarray(gate, dtype=np.float32)
+    up = np.ascontiguousarray(up, dtype=np.float32)
+    u = np.ascontiguousarray(u, dtype=np.float64)
+    ffn, hidden = gate.shape
+    if up.shape != gate.shape or u.shape != (hidden, hidden):
+        raise ValueError("gate and up must match; u must be [hidden, hidden]")
+    out = np.empty(packed_size(fmt, 2 * ffn, hidden), dtype=np.uint8)
+    _check(load().bfp_encode_gate_up_gptq(fmt, gate.ctypes.data, up.ctypes.data, ffn, hidden, u.ctypes.data,
+                                          out.ctypes.data, out.nbytes, threads), "bfp_encode_gate_up_gptq")
     return out
 
 

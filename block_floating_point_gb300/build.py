@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libbfpmoe.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["bfp_host.cpp", "bfp_linear.cu", "moe_layer.cu", "bfp_greedy.cu"]
+SOURCES = ["bfp_host.cpp", "bfp_gptq.cpp", "bfp_linear.cu", "moe_layer.cu", "bfp_greedy.cu"]
 
 
 def nvcc() -> str:
@@ -37,6 +37,10 @@ def _compile(src: str, extra: list[str]) -> str:
     path = os.path.join(CSRC, src)
     obj = os.path.join(OUT_DIR, src + ".o")
     cmd = [nvcc(), "-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-c", path, "-o", obj] + ARCH + extra
+    if src.endswith(".cpp"):
+        # host fp64 arithmetic exactly as written (no fused multiply-add): the error-compensated
+        # encoder's rounding decisions must not depend on the host architecture
+        cmd += ["-Xcompiler", "-ffp-contract=off"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"compile failed: {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")

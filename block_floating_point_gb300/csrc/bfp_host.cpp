@@ -14,6 +14,7 @@
 #include <vector>
 
 #include "bfp_internal.h"
+#include "bfp_pack.h"
 
 namespace bfp {
 
@@ -80,10 +81,7 @@ inline void pattern_codes(uint32_t p, int mb, uint8_t *c0, uint8_t *c1) {
     *c1 = (uint8_t)(((p >> 31) & 1u) << mb | ((p >> 16) & mmask));
 }
 
-// Logical fields of one row group: codes[16][kbp*16] and exps[16][kbp] (zero padded).
-struct GroupFields {
-    std::vector<uint8_t> codes, exps;
-};
+}  // namespace
 
 // Write record (rg, c) from a row group's logical fields.
 void write_record(const Geometry &g, const GroupFields &f, int64_t c, uint8_t *rec) {
@@ -118,6 +116,8 @@ void write_record(const Geometry &g, const GroupFields &f, int64_t c, uint8_t *r
             for (int h = 0; h < 2; ++h)
                 rec[kRecCodeBytes + (gi * g.cb + b) * 2 + h] = f.exps[(size_t)(gi + 8 * h) * kbp + c * g.cb + b];
 }
+
+namespace {
 
 // Read record (rg, c) back into a row group's logical fields.
 void read_record(const Geometry &g, const uint8_t *rec, int64_t c, GroupFields *f) {
@@ -170,33 +170,13 @@ bool encode_group(const Geometry &g, const float *w, int64_t rg, GroupFields *f)
     return true;
 }
 
+}  // namespace
+
 int resolve_threads(int nthreads, int64_t work) {
     if (nthreads <= 0) nthreads = (int)std::max(1u, std::thread::hardware_concurrency());
     nthreads = (int)std::min<int64_t>(nthreads, std::max<int64_t>(1, work));
     return std::min(nthreads, 256);
 }
-
-// Run fn(rg) for rg in [0, ng) over threads; fn returns false on failure.
-template <class F>
-bool parallel_groups(int64_t ng, int nthreads, F fn) {
-    nthreads = resolve_threads(nthreads, ng);
-    std::atomic<int64_t> next{0};
-    std::atomic<bool> good{true};
-    auto worker = [&]() {
-        for (;;) {
-            int64_t rg = next.fetch_add(1);
-            if (rg >= ng || !good.load()) return;
-            if (!fn(rg)) good.store(false);
-        }
-    };
-    std::vector<std::thread> pool;
-    for (int i = 1; i < nthreads; ++i) pool.emplace_back(worker);
-    worker();
-    for (auto &t : pool) t.join();
-    return good.load();
-}
-
-}  // namespace
 
 int fail(int code, const std::string &msg) {
     g_last_error = msg;

@@ -120,6 +120,40 @@ int bfp_encode_gate_up(int fmt, const float *gate, const float *up, int64_t ffn,
                        int64_t out_bytes, int nthreads);
 
 /*
+ * Error-compensated (GPTQ-style) encoding, host only (P5 "What changed in this
+ * release": BFP4 weights from a GPTQ variant for block floating point, error
+ * compensated inside the 16-value blocks, every value exactly representable so
+ * that plain conversion reproduces it; GPTQ: Frantar et al. 2022).
+ *
+ * bfp_gptq_factor: from calibration inputs x [t x k] (host fp32, row-major: t
+ * samples of the k inputs a matrix multiplies) forms
+ *     H = x^T x / t + damp * mean(diag(x^T x / t)) * I      (fp64)
+ * and writes u [k x k] (host fp64, row-major, zero below the diagonal), the
+ * upper-triangular factor with H^-1 = u^T u. damp > 0 (0.01 is usual).
+ * BFP_EINVAL if x is all zero or H is not positive definite, BFP_ENONFINITE
+ * for NaN/Inf in x. k <= 65536.
+ *
+ * bfp_encode_gptq: like bfp_encode (same packed output, same shapes), but each
+ * row's columns are quantised left to right and each rounding error e_j =
+ * (v_j - q_j) / u[j][j] is taken off the later columns, v_l -= e_j * u[j][l],
+ * in fp64. A block's exponent comes from its compensated values when its first
+ * column is reached; values round to nearest (ties to even) on that grid and
+ * saturate; a block whose magnitudes all fit one bit less is then stored with
+ * its exponent lowered, so bfp_encode of the decoded matrix gives the same
+ * bytes. With a diagonal H the result is bfp_encode's. u: a factor for this
+ * k (from bfp_gptq_factor). BFP_ENONFINITE for NaN/Inf in w or a compensated
+ * value beyond the fp32 range.
+ *
+ * bfp_encode_gate_up_gptq: bfp_encode_gate_up's interleaved layout, each half
+ * encoded as bfp_encode_gptq with the same u (gate and up see the same input).
+ */
+int bfp_gptq_factor(const float *x, int64_t t, int64_t k, double damp, double *u, int nthreads);
+int bfp_encode_gptq(int fmt, const float *w, int64_t n, int64_t k, const double *u, void *out, int64_t out_bytes,
+                    int nthreads);
+int bfp_encode_gate_up_gptq(int fmt, const float *gate, const float *up, int64_t ffn, int64_t hidden, const double *u,
+                            void *out, int64_t out_bytes, int nthreads);
+
+/*
  * Host reader of a packed matrix (w->data in host memory): the logical
  * fields, exps [n x k/16] and codes [n x k] (one code per byte, sign << mb |
  * magnitude). Test aid for bit-exact comparisons.
