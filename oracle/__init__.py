@@ -384,3 +384,94 @@ def gptq_encode(fmt: int, w_f32, u: np.ndarray):
         exps[:, b] = E.astype(np.uint8)
     codes = (neg.astype(np.int64) << mb) | mags
     return exps, codes.astype(np.uint8)
+
+
+# ---------------------------------------------------------------------------
+# BFP KV cache and decode attention. The qwen3.6-a3b-blackhole page
+# (QWEN36_KV_DTYPE row): the attention KV cache stored as BFP8, 20.0 -> 10.6
+# KiB per token, decode attention re-reading the whole cache each step. The
+# Qwen3.8-27B s27v6 card ("Changes in s27", bfp8_v4r): K in BFP8 and V
+# Hadamard-rotated, then stored as BFP4 (26,624 instead of 34,816 bytes per
+# token).
+# Readings: the rotation is the Sylvester-ordered Hadamard matrix H_d (entries
+# +-1, d a power of two), applied to each head's V vector before encoding; it
+# is computed in fp32 by the fast transform, stage h = 1, 2, 4, ... pairing
+# (i, i + h) into (a + b, a - b), which is the precision and order in which the
+# encoder decides the codes. Attention undoes it on the weighted sum of the
+# decoded rows: out = H_d (sum_t p_t v'_t) / d (H_d H_d = d I).
+# Attention per query head: s_t = scale * q . k_t, p = softmax(s), out =
+# sum_t p_t v_t, with query head j reading KV head j // (q_heads / kv_heads).
+# ---------------------------------------------------------------------------
+def fwht_f32(x) -> np.ndarray:
+    """Unnormalised fast Walsh-Hadamard transform over the last axis, in fp32, stage by stage."""
+    y = np.array(x, dtype=np.float32)
+    d = y.shape[-1]
+    if d & (d - 1):
+        raise ValueError("length must be a power of two")
+    h = 1
+    while h < d:
+        v = y.reshape(y.shape[:-1] + (d // (2 * h), 2, h))
+        a, b = v[..., 0, :].copy(), v[..., 1, :].copy()
+        v[..., 0, :] = a + b
+        v[..., 1, :] = a - b
+        h *= 2
+    return y
+
+
+def kv_encode(fmt: int, rows_bf16, rotate: bool):
+    """Cache fields of bf16 rows [..., d]: (exps [..., d/16], codes [..., d]) of the rows (Hadamard-
+    rotated in fp32 first when ``rotate``), by the plain round-to-nearest encoder."""
+    r = np.asarray(rows_bf16, dtype=np.uint16)
+    shape = r.shape
+    f = (r.astype(np.uint32) << 16).view(np.float32).reshape(-1, shape[-1])
+    if rotate:
+        f = fwht_f32(f)
+    e, c = encode(fmt, f)
+    return e.reshape(shape[:-1] + (shape[-1] // 16,)), c.reshape(shape)
+
+
+def kv_decode(fmt: int, exps, codes, rotated: bool) -> np.ndarray:
+    """Decoded cache rows in fp64 (rotated back when stored rotated)."""
+    e = np.asarray(exps)
+    c = np.asarray(codes)
+    d = c.shape[-1]
+    v = decode(fmt, e.reshape(-1, d // 16), c.reshape(-1, d)).astype(np.float64)
+    if rotated:
+        v = _hadamard_f64(v) / d
+    return v.reshape(c.shape)
+
+
+def _hadamard_f64(v: np.ndarray) -> np.ndarray:
+    d = v.shape[-1]
+    h = np.ones((1, 1))
+    while h.shape[0] < d:
+        h = np.block([[h, h], [h, -h]])
+    return v @ h  # H is symmetric
+
+
+def attn_decode(q_bf16, k_fields, v_fields, n_ctx: int, scale: float, k_fmt: int, v_fmt: int,
+                v_rotated: bool) -> np.ndarray:
+    """Decode attention of one query token over n_ctx cached tokens, fp64.
+
+    q_bf16 [q_heads, d]; k_fields / v_fields = (exps [kv_heads, n, d/16], codes [kv_heads, n, d]).
+    Returns out [q_heads, d]: softmax(scale * q K^T) V per query head (V rotated back if stored rotated).
+    """
+    q = (np.asarray(q_bf16, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    qh, d = q.shape
+    ke, kc = (np.asarray(a)[:, :n_ctx] for a in k_fields)
+    ve, vc = (np.asarray(a)[:, :n_ctx] for a in v_fields)
+    kvh = kc.shape[0]
+    if qh % kvh:
+        raise ValueError("q_heads must be a multiple of kv_heads")
+    g = qh // kvh
+    kd = kv_decode(k_fmt, ke, kc, False)
+    vd = decode(v_fmt, ve.reshape(-1, d // 16), vc.reshape(-1, d)).astype(np.float64).reshape(kvh, n_ctx, d)
+    out = np.zeros((qh, d))
+    for j in range(qh):
+        h = j // g
+        s = scale * (kd[h] @ q[j])
+        p = np.exp(s - s.max())
+        p /= p.sum()
+        o = p @ vd[h]
+        out[j] = _hadamard_f64(o[None, :])[0] / d if v_rotated else o
+    return out
