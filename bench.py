@@ -569,6 +569,29 @@ def main():
         sec["lm_head_bfp8_m8"] = {"us": usl, "gbs": lm.nbytes / (usl * 1e-6) / 1e9,
                                   "pct_of_measured_copy": 100 * lm.nbytes / (usl * 1e-6) / 1e9 / peak,
                                   "bytes": lm.nbytes, "timing": "20 consecutive calls (330 MB each, > L2)"}
+        # decode attention over a BFP KV cache, one query token: the 35B card's cache (2 KV heads x 256,
+        # BFP8 K and V, 16 query heads) and the 27B card's bfp8_v4r cache (4 KV heads x 256, BFP8 K,
+        # Hadamard-rotated BFP4 V, 24 query heads); caches of 128K tokens (> L2) timed back to back
+        for name, kvh, g, kf, vf, rot in (("attn_bfp8_kv2_q16", 2, 8, 8, 8, False),
+                                          ("attn_v4r_kv4_q24", 4, 6, 8, 4, True)):
+            n_ctx, d = 131072, 256
+            kvc = bfp.KvCache(kvh, d, n_ctx, kf, vf, rot, device=device)
+            for p0 in range(0, n_ctx, 16384):  # fill by appends of seeded bf16 rows
+                kk = torch.from_numpy(synth.to_bf16_bits(synth.normal(args.seed, 40 + kvh, (16384, kvh, d),
+                                                                      offset=p0 * kvh * d)).view(np.int16)).to(device)
+                vv = torch.from_numpy(synth.to_bf16_bits(synth.normal(args.seed, 50 + kvh, (16384, kvh, d),
+                                                                      offset=p0 * kvh * d)).view(np.int16)).to(device)
+                bfp.kv_append(kvc, kk, vv, p0)
+            qa = torch.from_numpy(synth.to_bf16_bits(synth.normal(args.seed, 60, (kvh * g, d))).view(np.int16)).to(device)
+            wsa = bfp.attn_workspace(kvc, kvh * g, n_ctx)
+            oa = torch.empty((kvh * g, d), dtype=torch.float32, device=device)
+            usa = timed_graph(lambda i: bfp.attn_decode(kvc, qa, n_ctx, d ** -0.5, wsa, out=oa), 50, 5, True) * 1e3 / 50
+            assert bfp.workspace_status(wsa) == bfp.BFP_OK
+            nb = n_ctx * kvc.bytes_per_token()
+            sec[name] = {"us": usa, "context": n_ctx, "cache_bytes": nb, "gbs": nb / (usa * 1e-6) / 1e9,
+                         "pct_of_measured_copy": 100 * nb / (usa * 1e-6) / 1e9 / peak, "launches": 2,
+                         "timing": "50 consecutive calls in a CUDA graph (cache larger than L2)"}
+            del kvc
         out["secondary"] = sec
         if rank == 0 and world == 1:
             v, s_ = cpu_baseline_sample(args, spec, xs[0])

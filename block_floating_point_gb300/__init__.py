@@ -46,6 +46,13 @@ class MoeLayerC(ctypes.Structure):
                 ("shared_gate_up", ctypes.c_void_p), ("shared_down", ctypes.c_void_p)]
 
 
+class KvCacheC(ctypes.Structure):
+    _fields_ = [("kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("k_fmt", ctypes.c_int32),
+                ("v_fmt", ctypes.c_int32), ("v_rotated", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("capacity", ctypes.c_int64), ("k_codes", ctypes.c_void_p), ("k_exps", ctypes.c_void_p),
+                ("v_codes", ctypes.c_void_p), ("v_exps", ctypes.c_void_p)]
+
+
 # Every entry point declared in include/bfpmoe.h, with its ctypes signature.
 _P, _I, _I64, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
 _MP = ctypes.POINTER(BfpMatrixC)
@@ -70,6 +77,10 @@ SIGNATURES = {
     "moe_stack_decode": [_LP, _I, _MP, _P, _I, _P, _P, _P, _SZ, _P],
     "bfp_greedy_workspace_size": [_I, _I64, ctypes.POINTER(_SZ)],
     "bfp_greedy_tokens": [_P, _I, _I64, _I64, _P, _P, _SZ, _P],
+    "bfp_kv_cache_size": [_I, _I, _I, _I64, ctypes.POINTER(_SZ), ctypes.POINTER(_SZ)],
+    "bfp_kv_append": [ctypes.POINTER(KvCacheC), _P, _P, _I64, _I, _P],
+    "bfp_attn_workspace_size": [ctypes.POINTER(KvCacheC), _I, _I64, ctypes.POINTER(_SZ)],
+    "bfp_attn_decode": [ctypes.POINTER(KvCacheC), _P, _I, _I64, ctypes.c_float, _P, _P, _SZ, _P],
     "bfp_workspace_status": [_P, ctypes.POINTER(_I), _P],
     "bfp_set_wait_limit": [_I64],
     "bfp_set_launch_mode": [_I],
@@ -452,3 +463,64 @@ def greedy_tokens(logits, ws, tokens=None, stream=None):
     _check(load().bfp_greedy_tokens(_ptr(logits), m, n, logits.stride(0), _ptr(tokens), _ptr(ws), ws.numel(),
                                     _stream(stream)), "bfp_greedy_tokens")
     return tokens
+
+
+# ----------------------------------------------------------------------------- BFP KV cache + decode attention
+class KvCache:
+    """Device arrays of one layer's BFP KV cache (include/bfpmoe.h, bfp_kv_cache)."""
+
+    def __init__(self, kv_heads, head_dim, capacity, k_fmt=BFP8, v_fmt=BFP8, v_rotated=False, device="cuda"):
+        import torch
+        self.kv_heads, self.head_dim, self.capacity = kv_heads, head_dim, capacity
+        self.k_fmt, self.v_fmt, self.v_rotated = k_fmt, v_fmt, bool(v_rotated)
+        self.k_codes, self.k_exps = (torch.zeros(n, dtype=torch.uint8, device=device)
+                                     for n in kv_cache_size(k_fmt, kv_heads, head_dim, capacity))
+        self.v_codes, self.v_exps = (torch.zeros(n, dtype=torch.uint8, device=device)
+                                     for n in kv_cache_size(v_fmt, kv_heads, head_dim, capacity))
+
+    def c(self) -> KvCacheC:
+        return KvCacheC(self.kv_heads, self.head_dim, self.k_fmt, self.v_fmt, int(self.v_rotated), 0, self.capacity,
+                        self.k_codes.data_ptr(), self.k_exps.data_ptr(), self.v_codes.data_ptr(),
+                        self.v_exps.data_ptr())
+
+    def bytes_per_token(self) -> int:
+        d, h = self.head_dim, self.kv_heads
+        code = {BFP8: d, BFP4: d // 2}
+        return h * (code[self.k_fmt] + code[self.v_fmt] + 2 * (d // 16))
+
+
+def kv_cache_size(fmt: int, kv_heads: int, head_dim: int, capacity: int):
+    cb, eb = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(load().bfp_kv_cache_size(fmt, kv_heads, head_dim, capacity, ctypes.byref(cb), ctypes.byref(eb)),
+           "bfp_kv_cache_size")
+    return cb.value, eb.value
+
+
+def kv_append(cache: KvCache, k, v, pos: int, stream=None):
+    """Encode bf16 k, v [n_new, kv_heads, head_dim] (CUDA tensors) into slots pos .. pos + n_new - 1."""
+    c = cache.c()
+    _check(load().bfp_kv_append(ctypes.byref(c), _ptr(k), _ptr(v), pos, k.shape[0], _stream(stream)), "bfp_kv_append")
+
+
+def attn_workspace_size(cache: KvCache, q_heads: int, n_ctx: int) -> int:
+    out = ctypes.c_size_t()
+    c = cache.c()
+    _check(load().bfp_attn_workspace_size(ctypes.byref(c), q_heads, n_ctx, ctypes.byref(out)),
+           "bfp_attn_workspace_size")
+    return out.value
+
+
+def attn_workspace(cache: KvCache, q_heads: int, n_ctx: int, stream=None):
+    return _alloc_ws(attn_workspace_size(cache, q_heads, n_ctx), cache.k_codes.device, stream)
+
+
+def attn_decode(cache: KvCache, q, n_ctx: int, scale: float, ws, out=None, stream=None):
+    """Decode attention of bf16 q [q_heads, head_dim] over the first n_ctx cached tokens; fp32 out."""
+    import torch
+    qh = q.shape[0]
+    if out is None:
+        out = torch.empty((qh, cache.head_dim), dtype=torch.float32, device=q.device)
+    c = cache.c()
+    _check(load().bfp_attn_decode(ctypes.byref(c), _ptr(q), qh, n_ctx, float(scale), _ptr(out), _ptr(ws), ws.numel(),
+                                  _stream(stream)), "bfp_attn_decode")
+    return out

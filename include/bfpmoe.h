@@ -306,6 +306,56 @@ int bfp_greedy_tokens(const float *logits, int m, int64_t n, int64_t ldl, int32_
                       bfp_stream_t stream);
 
 /*
+ * BFP KV cache and decode attention (P3 QWEN36_KV_DTYPE row: the attention KV
+ * cache as BFP8, re-read in full by every decode step; P4 "Changes in s27",
+ * bfp8_v4r: K as BFP8, V Hadamard-rotated and stored as BFP4).
+ * Layout, per KV head h and token slot t < capacity (all device memory):
+ *   K codes at k_codes + (h * capacity + t) * R bytes, R = head_dim for BFP8
+ *     (one byte per value: sign << 7 | magnitude) or head_dim / 2 for BFP4
+ *     (value 2i in the low nibble, 2i + 1 in the high one: sign << 3 | magnitude);
+ *   K exponents at k_exps + (h * capacity + t) * head_dim / 16, one byte per
+ *     16-value block along the head dimension (the BFP rules of bfp_encode);
+ *   V the same in v_codes / v_exps with v_fmt. With v_rotated = 1 a V row is
+ *   stored as H v, H the Sylvester Hadamard matrix of order head_dim (entries
+ *   +-1), computed in fp32 by the fast transform (stages 1, 2, 4, ...).
+ */
+typedef struct {
+    int32_t kv_heads, head_dim;        /* kv_heads 1..64; head_dim 64, 128 or 256 */
+    int32_t k_fmt, v_fmt;              /* BFP_FMT_BFP8 or BFP_FMT_BFP4 each */
+    int32_t v_rotated;                 /* 0 or 1 */
+    int32_t reserved;                  /* must be 0 */
+    int64_t capacity;                  /* token slots: a positive multiple of 64, at most 2^31 */
+    void *k_codes, *k_exps, *v_codes, *v_exps; /* 16-byte aligned; sizes from bfp_kv_cache_size */
+} bfp_kv_cache;
+
+/* Bytes of one codes array and of one exponents array for a format and shape. */
+int bfp_kv_cache_size(int fmt, int kv_heads, int head_dim, int64_t capacity, size_t *code_bytes, size_t *exp_bytes);
+
+/*
+ * Encodes n_new tokens into slots pos .. pos + n_new - 1: k and v are bf16
+ * [n_new x kv_heads x head_dim] (device, contiguous, 16-byte aligned). V is
+ * rotated first when the cache says so. One launch on the stream; finite
+ * inputs assumed (NaN/Inf give unspecified codes).
+ */
+int bfp_kv_append(const bfp_kv_cache *cache, const uint16_t *k, const uint16_t *v, int64_t pos, int n_new,
+                  bfp_stream_t stream);
+
+/*
+ * Decode attention of one query token over the first n_ctx cached tokens
+ * (1 <= n_ctx <= capacity): for query head j (kv head j / (q_heads / kv_heads),
+ * q_heads / kv_heads in 1..8)
+ *     s_t = scale * q_j . k_t,  p = softmax(s),  out_j = sum_t p_t v_t
+ * (for a rotated cache out_j = H (sum_t p_t v'_t) / head_dim), fp32
+ * arithmetic. q: bf16 [q_heads x head_dim]; out: fp32 [q_heads x head_dim]
+ * (device). Two launches on the stream; ws: bfp_attn_workspace_size bytes of
+ * device memory whose status word (first 4 bytes) must be zero
+ * (bfp_workspace_init); a bounded wait that runs out sets BFP_ETIMEOUT there.
+ */
+int bfp_attn_workspace_size(const bfp_kv_cache *cache, int q_heads, int64_t n_ctx, size_t *bytes);
+int bfp_attn_decode(const bfp_kv_cache *cache, const uint16_t *q, int q_heads, int64_t n_ctx, float scale, float *out,
+                    void *ws, size_t ws_bytes, bfp_stream_t stream);
+
+/*
  * Synchronises the stream and reads the workspace's status word: *status =
  * BFP_OK or the first device-side error (BFP_ETIMEOUT). The word stays set
  * until bfp_workspace_init.
