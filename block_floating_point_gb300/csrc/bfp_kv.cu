@@ -64,14 +64,26 @@ struct KvArgs {
     uint8_t *kc, *ke, *vc, *ve;
 };
 
+// fp16 bit pattern whose value is code's magnitude times 2^-24 with its sign (a subnormal: exact).
+__device__ __forceinline__ uint32_t code_pattern(uint32_t code, int mb) {
+    return (code & ((1u << mb) - 1u)) | (((code >> mb) & 1u) << 15);
+}
+
+// Byte offset, inside a 16-token x 16-column tile, of token row r's codes (see include/bfpmoe.h).
+__device__ __forceinline__ int k8_word_off(int r, int j) { return (4 * (r & 7) + j) * 8 + (r >> 3) * 4; }
+__device__ __forceinline__ int k4_half_off(int r, int j) { return (4 * (r & 7) + j) * 4 + (r >> 3) * 2; }
+__device__ __forceinline__ int v8_byte_off(int r, int c) { return (4 * (c & 7) + (r >> 2)) * 8 + (c >> 3) * 4 + (r & 3); }
+__device__ __forceinline__ int v4_byte_off(int r, int c) { return (4 * (c & 7) + (r >> 2)) * 4 + (r & 3); }
+
 // One warp per (token, KV head, K or V) row: load d bf16 values (VPL per lane, contiguous), rotate V
-// if asked (fp32 fast Walsh-Hadamard transform, stages h = 1, 2, 4, ...), encode 16-value blocks.
+// if asked (fp32 fast Walsh-Hadamard transform, stages h = 1, 2, 4, ...), encode 16-value blocks and
+// store them in the tile order of the cache.
 template <int VPL>
 __global__ void __launch_bounds__(128) kv_append_kernel(const KvArgs a, const uint16_t *k, const uint16_t *v,
                                                         int64_t pos, int n_new) {
     grid_dep_launch_dependents();
     grid_dep_wait();
-    constexpr int D = VPL * kWarp;
+    constexpr int D = VPL * kWarp, NB = D / 16;
     const int lane = threadIdx.x & 31;
     const int64_t row = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
     const int64_t nrows = (int64_t)n_new * a.kvh * 2;
@@ -116,20 +128,58 @@ __global__ void __launch_bounds__(128) kv_append_kernel(const KvArgs a, const ui
     constexpr int L = 16 / VPL;  // lanes per block
 #pragma unroll
     for (int o = 1; o < L; o <<= 1) E = max(E, __shfl_xor_sync(0xffffffffu, E, o));
-    const int64_t slot = (int64_t)h * a.cap + pos + tok;
-    uint8_t *codes = (which ? a.vc : a.kc) + slot * row_code_bytes(fmt, D);
-    uint8_t *exps = (which ? a.ve : a.ke) + slot * (D / 16);
-    if ((lane % L) == 0) exps[lane / L] = (uint8_t)E;
-    if (fmt == BFP_FMT_BFP8) {
-        uint8_t c[VPL];
+    uint32_t c[VPL];
 #pragma unroll
-        for (int t = 0; t < VPL; ++t) c[t] = (uint8_t)bfp_code(u[t], E, mb);
+    for (int t = 0; t < VPL; ++t) c[t] = bfp_code(u[t], E, mb);
+    const int64_t slot = pos + tok;            // token slot
+    const int r = (int)(slot & 15);            // row in its 16-token tile group
+    const int b = lane / L;                    // block of this lane's columns
+    const int cb0 = (lane % L) * VPL;          // first column within the block
+    const int tb = fmt == BFP_FMT_BFP8 ? 256 : 128;
+    uint8_t *tile = (which ? a.vc : a.kc) + (((int64_t)h * (a.cap / 16) + (slot >> 4)) * NB + b) * tb;
+    uint8_t *exps = (which ? a.ve : a.ke) + ((int64_t)h * a.cap + slot) * NB;
+    if ((lane % L) == 0) exps[b] = (uint8_t)E;
+    if (!which) {
+        // K: a row's codes of columns 4j..4j+3 are one 32-bit word (BFP8) or one 16-bit half (BFP4)
+        if (fmt == BFP_FMT_BFP8) {
+            uint32_t cc[VPL < 4 ? 4 : VPL];
 #pragma unroll
-        for (int t = 0; t < VPL; ++t) codes[lane * VPL + t] = c[t];
+            for (int t = 0; t < VPL; ++t) cc[t] = c[t];
+            if (VPL == 2) {  // two lanes hold the four codes of a word
+                cc[2] = __shfl_down_sync(0xffffffffu, c[0], 1);
+                cc[3] = __shfl_down_sync(0xffffffffu, c[VPL - 1], 1);
+            }
+            if (VPL >= 4 || (lane & 1) == 0) {
+#pragma unroll
+                for (int j = 0; j < (VPL < 4 ? 1 : VPL / 4); ++j) {
+                    const uint32_t p01 = code_pattern(cc[4 * j], 7) | (code_pattern(cc[4 * j + 1], 7) << 16);
+                    const uint32_t p23 = code_pattern(cc[4 * j + 2], 7) | (code_pattern(cc[4 * j + 3], 7) << 16);
+                    *reinterpret_cast<uint32_t *>(tile + k8_word_off(r, (cb0 >> 2) + j)) = p01 | __funnelshift_l(p23, p23, 8);
+                }
+            }
+        } else {
+            if (VPL >= 4) {
+#pragma unroll
+                for (int j = 0; j < VPL / 4; ++j)
+                    *reinterpret_cast<uint16_t *>(tile + k4_half_off(r, (cb0 >> 2) + j)) =
+                        (uint16_t)(c[4 * j] | (c[4 * j + 1] << 4) | (c[4 * j + 2] << 8) | (c[4 * j + 3] << 12));
+            } else {  // two codes: one byte of the half
+                tile[k4_half_off(r, cb0 >> 2) + ((cb0 & 3) >> 1)] = (uint8_t)(c[0] | (c[VPL - 1] << 4));
+            }
+        }
     } else {
+        // V: a token's code of column c sits in its own byte (BFP8), or shares a byte with column c + 8 (BFP4)
+        if (fmt == BFP_FMT_BFP8) {
 #pragma unroll
-        for (int t = 0; t < VPL; t += 2)
-            codes[(lane * VPL + t) / 2] = (uint8_t)(bfp_code(u[t], E, mb) | (bfp_code(u[t + 1], E, mb) << 4));
+            for (int t = 0; t < VPL; ++t) tile[v8_byte_off(r, cb0 + t)] = (uint8_t)c[t];
+        } else {
+            uint32_t hi[VPL];
+#pragma unroll
+            for (int t = 0; t < VPL; ++t) hi[t] = __shfl_xor_sync(0xffffffffu, c[t], L / 2);
+            if (cb0 < 8)
+#pragma unroll
+                for (int t = 0; t < VPL; ++t) tile[v4_byte_off(r, cb0 + t)] = (uint8_t)(c[t] | (hi[t] << 4));
+        }
     }
 }
 
@@ -144,28 +194,40 @@ struct AttnArgs {
     WaitCfg wait;
 };
 
-// Decoded value of code c (sign << mb | magnitude) times 2^(E - 127 - (mb - 1)).
-template <int MB>
-__device__ __forceinline__ float code_value(uint32_t c, float scale) {
-    const float m = (float)(c & ((1u << MB) - 1u));
-    return ((c >> MB) & 1u) ? -m * scale : m * scale;
+// Two 4-bit codes (low byte of x: first code in the low nibble) -> fp16x2 subnormal patterns.
+__device__ __forceinline__ uint32_t nib2_pattern(uint32_t x) {
+    const uint32_t s = (x & 0xFu) | ((x & 0xF0u) << 12);
+    return (s & 0x00070007u) | ((s & 0x00080008u) << 12);
 }
+// Two 8-bit codes (bytes 0 and 2 of s, other bytes zero) -> fp16x2 subnormal patterns.
+__device__ __forceinline__ uint32_t byte2_pattern(uint32_t s) { return (s & 0x007F007Fu) | ((s & 0x00800080u) << 8); }
 
+// Decode attention, first launch. Per 64-token chunk, with NB = D / 16 blocks per row:
+//   scores: S^T (tokens x heads) = K_tile (16 tokens x 16 dims, BFP codes as fp16 subnormals) x q (16 dims
+//     x 8 heads, fp16 scaled by 2^sq) on mma.sync m16n8k16, zero C, folded into fp32 with each token
+//     row's block scale; warp w takes token slice w / 2 and half the blocks;
+//   softmax: warp g keeps head g's running max m, sum l, and writes the chunk's weights p;
+//   values: O (heads x dims) += P' (8 heads x 16 tokens) x V_tile (16 tokens x 8 dims), where P' carries
+//     each token's block scale relative to the slice's largest (p 2^(E_t - E_ref) <= 1, as fp16 hi + lo),
+//     folded with 2^E_ref; warp w takes blocks w, w + 8, ...
+// The contraction index is permuted the same way in both operands: fragment slots (2t, 2t+1, 2t+8,
+// 2t+9) of lane (g, t) carry dims (tokens) 4t .. 4t+3, which is how the tiles are stored.
 template <int VPL, int KF, int VF>
 __global__ void __launch_bounds__(kAttnThreads) attn_partial_kernel(const AttnArgs a) {
-    constexpr int D = VPL * kWarp;
+    constexpr int D = VPL * kWarp, NB = D / 16;
     constexpr int KMB = KF == BFP_FMT_BFP8 ? 7 : 3, VMB = VF == BFP_FMT_BFP8 ? 7 : 3;
-    constexpr int KROW = row_code_bytes(KF, D), VROW = row_code_bytes(VF, D), EROW = D / 16;
-    constexpr int SK = kChunk * KROW, SKE = kChunk * EROW, SV = kChunk * VROW;
+    constexpr int TBK = KF == BFP_FMT_BFP8 ? 256 : 128, TBV = VF == BFP_FMT_BFP8 ? 256 : 128;
+    constexpr int SK = kChunk / 16 * NB * TBK, SKE = kChunk * NB, SV = kChunk / 16 * NB * TBV;
     constexpr int STAGE = SK + 2 * SKE + SV;
-    constexpr int NTG = kAttnThreads / D;  // token groups of the V pass
+    constexpr int NBA = NB / 2;            // blocks per warp in the scores pass
+    constexpr int NBC = (NB + 7) / 8;      // blocks per warp in the values pass
     extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ __align__(16) float pw[kChunk][kMaxGroup];  // softmax weights of the chunk, [token][head]
-    __shared__ float alpha_s[kMaxGroup], m_s[kMaxGroup], l_s[kMaxGroup];
+    __shared__ float pw[kChunk][kMaxGroup];        // the chunk's softmax weights, [token][head]
+    __shared__ float spart[2][kChunk][kMaxGroup];  // scores, one part per half of the blocks
+    __shared__ float alpha_s[kMaxGroup], m_s[kMaxGroup], l_s[kMaxGroup], qmax_s[kAttnThreads / kWarp];
     __shared__ uint64_t full[2];
     __shared__ int abort_s;
-    __shared__ float red[NTG > 1 ? NTG - 1 : 1][kMaxGroup][NTG > 1 ? D : 1];  // token groups 1.. of the V pass
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g4 = lane >> 2, t4 = lane & 3;
     const int h = blockIdx.y, s = blockIdx.x, G = a.G;
     const int c0 = (int)((int64_t)a.nchunk * s / a.S), c1 = (int)((int64_t)a.nchunk * (s + 1) / a.S);
     if (tid == 0) {
@@ -181,33 +243,49 @@ __global__ void __launch_bounds__(kAttnThreads) attn_partial_kernel(const AttnAr
     grid_dep_launch_dependents();
     grid_dep_wait();
     __syncthreads();
-    const uint8_t *kc = a.kc + (int64_t)h * a.cap * KROW, *ke = a.ke + (int64_t)h * a.cap * EROW;
-    const uint8_t *vc = a.vc + (int64_t)h * a.cap * VROW, *ve = a.ve + (int64_t)h * a.cap * EROW;
+    const uint8_t *kc = a.kc + (int64_t)h * a.cap * (NB * TBK / 16), *ke = a.ke + (int64_t)h * a.cap * NB;
+    const uint8_t *vc = a.vc + (int64_t)h * a.cap * (NB * TBV / 16), *ve = a.ve + (int64_t)h * a.cap * NB;
     auto issue = [&](int ci) {  // thread 0: chunk ci into stage (ci - c0) & 1
         const int st = (ci - c0) & 1;
         uint8_t *dst = smem + st * STAGE;
         const int64_t t0 = (int64_t)ci * kChunk;
         mbar_arrive_expect_tx(&full[st], STAGE);
-        bulk_g2s(dst, kc + t0 * KROW, SK, &full[st]);
-        bulk_g2s(dst + SK, ke + t0 * EROW, SKE, &full[st]);
-        bulk_g2s(dst + SK + SKE, vc + t0 * VROW, SV, &full[st]);
-        bulk_g2s(dst + SK + SKE + SV, ve + t0 * EROW, SKE, &full[st]);
+        bulk_g2s(dst, kc + t0 * (NB * TBK / 16), SK, &full[st]);
+        bulk_g2s(dst + SK, ke + t0 * NB, SKE, &full[st]);
+        bulk_g2s(dst + SK + SKE, vc + t0 * (NB * TBV / 16), SV, &full[st]);
+        bulk_g2s(dst + SK + SKE + SV, ve + t0 * NB, SKE, &full[st]);
     };
     if (tid == 0) {
         if (c0 < c1) issue(c0);
         if (c0 + 1 < c1) issue(c0 + 1);
     }
-    // this lane's slice of the G query vectors (scores pass: lanes split the head dimension)
-    float qr[kMaxGroup][VPL];
+    // q of the group in fp16, scaled by 2^sq so that max |q| lies in [2^14, 2^15)
+    const uint16_t *qg = a.q + (int64_t)h * G * D;
+    float qm = 0.f;
+    for (int i = tid; i < G * D; i += kAttnThreads) qm = fmaxf(qm, fabsf(__uint_as_float((uint32_t)qg[i] << 16)));
+    qm = warp_max(qm);
+    if (lane == 0) qmax_s[warp] = qm;
+    __syncthreads();
+    for (int w = 0; w < kAttnThreads / kWarp; ++w) qm = fmaxf(qm, qmax_s[w]);
+    const int sq = frag_shift(qm);
+    const float sfac = mul_pow2(a.scale, 24 - sq);  // scores = folded MMA sums * 2^24 * 2^-sq * scale
+    const int sl_a = warp >> 1, half = warp & 1;
+    uint32_t bq[NBA][2];
 #pragma unroll
-    for (int g = 0; g < kMaxGroup; ++g)
+    for (int bi = 0; bi < NBA; ++bi) {
+        const int d0 = (half * NBA + bi) * 16 + 4 * t4;
+        float qv[4];
 #pragma unroll
-        for (int t = 0; t < VPL; ++t)
-            qr[g][t] = g < G ? __uint_as_float((uint32_t)a.q[((int64_t)h * G + g) * D + lane * VPL + t] << 16) : 0.f;
-    const int col = tid % D, tg = tid / D;
-    float acc[kMaxGroup];
+        for (int j = 0; j < 4; ++j)
+            qv[j] = g4 < G ? mul_pow2(__uint_as_float((uint32_t)qg[g4 * D + d0 + j] << 16), sq) : 0.f;
+        bq[bi][0] = pack_half2(qv[0], qv[1]);
+        bq[bi][1] = pack_half2(qv[2], qv[3]);
+    }
+    float acc[NBC][2][2];
 #pragma unroll
-    for (int g = 0; g < kMaxGroup; ++g) acc[g] = 0.f;
+    for (int bi = 0; bi < NBC; ++bi)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) acc[bi][hh][0] = acc[bi][hh][1] = 0.f;
 
     for (int ci = c0; ci < c1; ++ci) {
         const int st = (ci - c0) & 1;
@@ -223,69 +301,61 @@ __global__ void __launch_bounds__(kAttnThreads) attn_partial_kernel(const AttnAr
         __syncthreads();
         if (abort_s) return;
         const uint8_t *sk = smem + st * STAGE, *ske = sk + SK, *sv = ske + SKE, *sve = sv + SV;
-        const int64_t tb = (int64_t)ci * kChunk;
-        const int nv = (int)min64((int64_t)kChunk, a.n_ctx - tb);
-        // ---- scores: warp w takes tokens w, w + 8, ...; the G dot products are reduced together
-        for (int i = warp; i < kChunk; i += kAttnThreads / kWarp) {
-            float dot[kMaxGroup];
-            if (i < nv) {
-                const float bs = exact_pow2((int)ske[i * EROW + lane * VPL / 16] - 127 - (KMB - 1));
-                float kv[VPL];
+        const int nv = (int)min64((int64_t)kChunk, a.n_ctx - (int64_t)ci * kChunk);
+        // ---- scores
+        {
+            float cs[4] = {0.f, 0.f, 0.f, 0.f};
+            const int ra = 16 * sl_a + g4;  // token rows ra and ra + 8 of the chunk
+#pragma unroll
+            for (int bi = 0; bi < NBA; ++bi) {
+                const int b = half * NBA + bi;
+                uint32_t A[4];
                 if (KF == BFP_FMT_BFP8) {
-#pragma unroll
-                    for (int t = 0; t < VPL; ++t) kv[t] = code_value<KMB>(sk[i * KROW + lane * VPL + t], bs);
+                    const uint2 w = *reinterpret_cast<const uint2 *>(sk + (sl_a * NB + b) * TBK + lane * 8);
+                    A[0] = w.x & kMaskBfp8;
+                    A[2] = rotr(w.x, 8) & kMaskBfp8;
+                    A[1] = w.y & kMaskBfp8;
+                    A[3] = rotr(w.y, 8) & kMaskBfp8;
                 } else {
-#pragma unroll
-                    for (int t = 0; t < VPL; t += 2) {
-                        const uint32_t b = sk[i * KROW + (lane * VPL + t) / 2];
-                        kv[t] = code_value<KMB>(b & 15u, bs);
-                        kv[t + 1] = code_value<KMB>(b >> 4, bs);
-                    }
+                    const uint32_t w = *reinterpret_cast<const uint32_t *>(sk + (sl_a * NB + b) * TBK + lane * 4);
+                    A[0] = nib2_pattern(w & 0xFFu);
+                    A[2] = nib2_pattern((w >> 8) & 0xFFu);
+                    A[1] = nib2_pattern((w >> 16) & 0xFFu);
+                    A[3] = nib2_pattern(w >> 24);
                 }
-#pragma unroll
-                for (int g = 0; g < kMaxGroup; ++g) {
-                    float sacc = 0.f;
-#pragma unroll
-                    for (int t = 0; t < VPL; ++t) sacc = fmaf(kv[t], qr[g][t], sacc);
-                    dot[g] = sacc;
-                }
-            } else {
-#pragma unroll
-                for (int g = 0; g < kMaxGroup; ++g) dot[g] = 0.f;
+                float c[4] = {0.f, 0.f, 0.f, 0.f};
+                mma16816(c, A, bq[bi][0], bq[bi][1]);
+                const float e0 = exact_pow2((int)ske[ra * NB + b] - 127 - (KMB - 1));
+                const float e1 = exact_pow2((int)ske[(ra + 8) * NB + b] - 127 - (KMB - 1));
+                cs[0] = fmaf(c[0], e0, cs[0]);
+                cs[1] = fmaf(c[1], e0, cs[1]);
+                cs[2] = fmaf(c[2], e1, cs[2]);
+                cs[3] = fmaf(c[3], e1, cs[3]);
             }
-            // 8 values over 32 lanes: halve the set at each of the first three steps
-            float r4[4], r2[2];
-            const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float send = b4 ? dot[j] : dot[j + 4], keep = b4 ? dot[j + 4] : dot[j];
-                r4[j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-            }
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const float send = b3 ? r4[j] : r4[j + 2], keep = b3 ? r4[j + 2] : r4[j];
-                r2[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-            }
-            float r1;
-            {
-                const float send = b2 ? r2[0] : r2[1], keep = b2 ? r2[1] : r2[0];
-                r1 = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-            }
-            r1 += __shfl_xor_sync(0xffffffffu, r1, 2);
-            r1 += __shfl_xor_sync(0xffffffffu, r1, 1);
-            if ((lane & 3) == 0) pw[i][lane >> 2] = i < nv ? r1 * a.scale : -INFINITY;
+            spart[half][ra][2 * t4] = cs[0];
+            spart[half][ra][2 * t4 + 1] = cs[1];
+            spart[half][ra + 8][2 * t4] = cs[2];
+            spart[half][ra + 8][2 * t4 + 1] = cs[3];
         }
         __syncthreads();
         // ---- running softmax: warp g updates head g over the chunk's scores
         if (warp < G) {
             const int g = warp;
+            float sc[kChunk / kWarp];
             float mx = -INFINITY;
-            for (int i = lane; i < kChunk; i += kWarp) mx = fmaxf(mx, pw[i][g]);
+#pragma unroll
+            for (int j = 0; j < kChunk / kWarp; ++j) {
+                const int i = lane + j * kWarp;
+                sc[j] = i < nv ? (spart[0][i][g] + spart[1][i][g]) * sfac : -INFINITY;
+                mx = fmaxf(mx, sc[j]);
+            }
             mx = warp_max(mx);
             const float m_old = m_s[g], m_new = fmaxf(m_old, mx);
             float sum = 0.f;
-            for (int i = lane; i < kChunk; i += kWarp) {
-                const float p = i < nv ? __expf(pw[i][g] - m_new) : 0.f;
+#pragma unroll
+            for (int j = 0; j < kChunk / kWarp; ++j) {
+                const int i = lane + j * kWarp;
+                const float p = i < nv ? __expf(sc[j] - m_new) : 0.f;
                 pw[i][g] = p;
                 sum += p;
             }
@@ -298,28 +368,68 @@ __global__ void __launch_bounds__(kAttnThreads) attn_partial_kernel(const AttnAr
             }
         }
         __syncthreads();
-        // ---- weighted V sum: thread (col, tg) takes column col of tokens tg, tg + NTG, ...
+        // ---- weighted V sum
+        if (warp < NB) {
+            const float al = g4 < G ? alpha_s[g4] : 0.f;
 #pragma unroll
-        for (int g = 0; g < kMaxGroup; ++g) acc[g] *= g < G ? alpha_s[g] : 0.f;
-        for (int i = tg; i < nv; i += NTG) {
-            const float bs = exact_pow2((int)sve[i * EROW + col / 16] - 127 - (VMB - 1));
-            float val;
-            if (VF == BFP_FMT_BFP8) {
-                val = code_value<VMB>(sv[i * VROW + col], bs);
-            } else {
-                const uint32_t b = sv[i * VROW + col / 2];
-                val = code_value<VMB>((col & 1) ? (b >> 4) : (b & 15u), bs);
+            for (int bi = 0; bi < NBC; ++bi)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    acc[bi][hh][0] *= al;
+                    acc[bi][hh][1] *= al;
+                }
+#pragma unroll
+            for (int bi = 0; bi < NBC; ++bi) {
+                const int b = warp + 8 * bi;
+                if (b >= NB) break;
+#pragma unroll
+                for (int sl = 0; sl < kChunk / 16; ++sl) {
+                    if (16 * sl >= nv) break;  // the rest of the chunk is past the context
+                    const int tk = 16 * sl + 4 * t4;
+                    int Ek[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) Ek[j] = tk + j < nv ? (int)sve[(tk + j) * NB + b] : 0;  // slots past the context hold anything
+                    int Er = max(max(Ek[0], Ek[1]), max(Ek[2], Ek[3]));
+                    Er = max(Er, __shfl_xor_sync(0xffffffffu, Er, 1));
+                    Er = max(Er, __shfl_xor_sync(0xffffffffu, Er, 2));
+                    float p[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        p[j] = g4 < G ? pw[tk + j][g4] * exact_pow2(max(Ek[j] - Er, -149)) : 0.f;
+                    const __half2 h01 = __floats2half2_rn(p[0], p[1]), h23 = __floats2half2_rn(p[2], p[3]);
+                    const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+                    const __half2 l01 = __floats2half2_rn(p[0] - f01.x, p[1] - f01.y);
+                    const __half2 l23 = __floats2half2_rn(p[2] - f23.x, p[3] - f23.y);
+                    const uint32_t Ahi[4] = {*reinterpret_cast<const uint32_t *>(&h01), 0u,
+                                             *reinterpret_cast<const uint32_t *>(&h23), 0u};
+                    const uint32_t Alo[4] = {*reinterpret_cast<const uint32_t *>(&l01), 0u,
+                                             *reinterpret_cast<const uint32_t *>(&l23), 0u};
+                    uint32_t Bv[2][2];
+                    if (VF == BFP_FMT_BFP8) {
+                        const uint2 w = *reinterpret_cast<const uint2 *>(sv + (sl * NB + b) * TBV + lane * 8);
+                        Bv[0][0] = byte2_pattern(__byte_perm(w.x, 0u, 0x4140));
+                        Bv[0][1] = byte2_pattern(__byte_perm(w.x, 0u, 0x4342));
+                        Bv[1][0] = byte2_pattern(__byte_perm(w.y, 0u, 0x4140));
+                        Bv[1][1] = byte2_pattern(__byte_perm(w.y, 0u, 0x4342));
+                    } else {
+                        const uint32_t w = *reinterpret_cast<const uint32_t *>(sv + (sl * NB + b) * TBV + lane * 4);
+                        const uint32_t lo = w & 0x0F0F0F0Fu, hi = (w >> 4) & 0x0F0F0F0Fu;
+                        Bv[0][0] = nib2_pattern((lo & 0xFu) | ((lo >> 4) & 0xF0u));
+                        Bv[0][1] = nib2_pattern(((lo >> 16) & 0xFu) | ((lo >> 20) & 0xF0u));
+                        Bv[1][0] = nib2_pattern((hi & 0xFu) | ((hi >> 4) & 0xF0u));
+                        Bv[1][1] = nib2_pattern(((hi >> 16) & 0xFu) | ((hi >> 20) & 0xF0u));
+                    }
+                    const float f = exact_pow2(Er - 127 - (VMB - 1));
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        float c[4] = {0.f, 0.f, 0.f, 0.f};
+                        mma16816(c, Ahi, Bv[hh][0], Bv[hh][1]);
+                        mma16816(c, Alo, Bv[hh][0], Bv[hh][1]);
+                        acc[bi][hh][0] = fmaf(c[0], f, acc[bi][hh][0]);
+                        acc[bi][hh][1] = fmaf(c[1], f, acc[bi][hh][1]);
+                    }
+                }
             }
-            const float4 p0 = *reinterpret_cast<const float4 *>(&pw[i][0]);
-            const float4 p1 = *reinterpret_cast<const float4 *>(&pw[i][4]);
-            acc[0] = fmaf(p0.x, val, acc[0]);
-            acc[1] = fmaf(p0.y, val, acc[1]);
-            acc[2] = fmaf(p0.z, val, acc[2]);
-            acc[3] = fmaf(p0.w, val, acc[3]);
-            acc[4] = fmaf(p1.x, val, acc[4]);
-            acc[5] = fmaf(p1.y, val, acc[5]);
-            acc[6] = fmaf(p1.z, val, acc[6]);
-            acc[7] = fmaf(p1.w, val, acc[7]);
         }
         __syncthreads();  // the stage is free again
         if (tid == 0 && ci + 2 < c1) {
@@ -327,20 +437,21 @@ __global__ void __launch_bounds__(kAttnThreads) attn_partial_kernel(const AttnAr
             issue(ci + 2);
         }
     }
-    // ---- partial results: o for each head (token groups added in order), then m and l
-    if constexpr (NTG > 1) {
-        if (tg > 0)
-#pragma unroll
-            for (int g = 0; g < kMaxGroup; ++g) red[tg - 1][g][col] = acc[g];
-        __syncthreads();
-        if (tg == 0)
-            for (int j = 1; j < NTG; ++j)
-#pragma unroll
-                for (int g = 0; g < kMaxGroup; ++g) acc[g] += red[j - 1][g][col];
-    }
+    // ---- partial results: o = acc * 2^24 (the codes entered as multiples of 2^-24), then m and l
     float *base = a.part + (((int64_t)h * a.S + s) * G) * (D + 2);
-    if (tg == 0)
-        for (int g = 0; g < G; ++g) base[(int64_t)g * (D + 2) + col] = acc[g];
+    if (warp < NB && g4 < G) {
+#pragma unroll
+        for (int bi = 0; bi < NBC; ++bi) {
+            const int b = warp + 8 * bi;
+            if (b >= NB) break;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int col = 16 * b + 8 * hh + 2 * t4;
+                base[(int64_t)g4 * (D + 2) + col] = acc[bi][hh][0] * 16777216.f;
+                base[(int64_t)g4 * (D + 2) + col + 1] = acc[bi][hh][1] * 16777216.f;
+            }
+        }
+    }
     if (tid < G) {
         base[(int64_t)tid * (D + 2) + D] = m_s[tid];
         base[(int64_t)tid * (D + 2) + D + 1] = l_s[tid];

@@ -309,15 +309,26 @@ int bfp_greedy_tokens(const float *logits, int m, int64_t n, int64_t ldl, int32_
  * BFP KV cache and decode attention (P3 QWEN36_KV_DTYPE row: the attention KV
  * cache as BFP8, re-read in full by every decode step; P4 "Changes in s27",
  * bfp8_v4r: K as BFP8, V Hadamard-rotated and stored as BFP4).
- * Layout, per KV head h and token slot t < capacity (all device memory):
- *   K codes at k_codes + (h * capacity + t) * R bytes, R = head_dim for BFP8
- *     (one byte per value: sign << 7 | magnitude) or head_dim / 2 for BFP4
- *     (value 2i in the low nibble, 2i + 1 in the high one: sign << 3 | magnitude);
- *   K exponents at k_exps + (h * capacity + t) * head_dim / 16, one byte per
- *     16-value block along the head dimension (the BFP rules of bfp_encode);
- *   V the same in v_codes / v_exps with v_fmt. With v_rotated = 1 a V row is
- *   stored as H v, H the Sylvester Hadamard matrix of order head_dim (entries
- *   +-1), computed in fp32 by the fast transform (stages 1, 2, 4, ...).
+ * Codes follow the BFP rules of bfp_encode (16-value blocks along the head
+ * dimension, one exponent byte each; code = sign << mb | magnitude). With
+ * v_rotated = 1 a V row is stored as H v, H the Sylvester Hadamard matrix of
+ * order head_dim (entries +-1), computed in fp32 by the fast transform
+ * (stages 1, 2, 4, ...). Layout (device memory), NB = head_dim / 16:
+ *   exponents: k_exps[(h * capacity + t) * NB + b] for KV head h, token slot t,
+ *     block b (v_exps likewise);
+ *   codes: tiles of 16 token slots x 16 values, tile (h, t / 16, b) at byte
+ *     ((h * capacity / 16 + t / 16) * NB + b) * TB, TB = 256 (BFP8) or 128
+ *     (BFP4). In a tile, token row r = t % 16 and column c (0..15):
+ *     K, BFP8: the codes of columns 4j .. 4j+3 of row r form the 32-bit word
+ *       at (4 (r % 8) + j) * 8 + (r / 8) * 4, holding P(c0, c1) | rotl(P(c2, c3), 8)
+ *       with P(x, y) = p(x) | p(y) << 16 and p(code) = magnitude | sign << 15;
+ *     K, BFP4: the same four codes form the 16-bit half at
+ *       (4 (r % 8) + j) * 4 + (r / 8) * 2, column 4j + i in nibble i;
+ *     V, BFP8: byte (4 (c % 8) + r / 4) * 8 + (c / 8) * 4 + r % 4;
+ *     V, BFP4: byte (4 (c % 8) + r / 4) * 4 + r % 4, column c (< 8) in the low
+ *       nibble and column c + 8 in the high one.
+ *   This is the operand order of the tensor-core instruction the attention
+ *   uses; every append writes whole words, halves or bytes of its own token.
  */
 typedef struct {
     int32_t kv_heads, head_dim;        /* kv_heads 1..64; head_dim 64, 128 or 256 */

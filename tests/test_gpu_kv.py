@@ -35,16 +35,44 @@ def bf16_rows(seed, stream, shape, std=1.0):
     return synth.to_bf16_bits(synth.normal(seed, stream, shape, std=std))
 
 
-def cache_bytes(fmt, exps, codes):
-    """The cache layout of oracle fields [kvh, n, ...]: code bytes per row and exponent bytes per row."""
-    c = np.asarray(codes, dtype=np.uint8)
-    if fmt == 4:
-        c = (c[..., 0::2] | (c[..., 1::2] << 4)).astype(np.uint8)
-    return c, np.asarray(exps, dtype=np.uint8)
+def _p(code):
+    return (int(code) & 0x7F) | ((int(code) >> 7) << 15)
 
 
-def device_rows(t, kvh, cap):
-    return t.cpu().numpy().reshape(kvh, cap, -1)
+def tile_bytes(codes16, which, fmt):
+    """One 16-token x 16-column tile of codes in the cache layout (the layout text of include/bfpmoe.h)."""
+    t = np.zeros(256 if fmt == 8 else 128, np.uint8)
+    for r in range(16):
+        for c in range(16):
+            code = int(codes16[r, c])
+            if which == "k" and fmt == 8 and c % 4 == 0:
+                cs = codes16[r, c:c + 4]
+                p01, p23 = _p(cs[0]) | (_p(cs[1]) << 16), _p(cs[2]) | (_p(cs[3]) << 16)
+                w = p01 | (((p23 << 8) | (p23 >> 24)) & 0xFFFFFFFF)
+                off = (4 * (r % 8) + c // 4) * 8 + (r // 8) * 4
+                t[off:off + 4] = np.frombuffer(np.uint32(w).tobytes(), np.uint8)
+            elif which == "k" and fmt == 4:
+                off = (4 * (r % 8) + c // 4) * 4 + (r // 8) * 2 + (c % 4) // 2
+                t[off] |= code << (4 * (c % 2))
+            elif which == "v" and fmt == 8:
+                t[(4 * (c % 8) + r // 4) * 8 + (c // 8) * 4 + r % 4] = code
+            elif which == "v" and fmt == 4:
+                t[(4 * (c % 8) + r // 4) * 4 + r % 4] |= code << (4 * (c // 8))
+    return t
+
+
+def expected_codes(codes, which, fmt, cap):
+    """Cache code bytes [kvh, cap / 16, NB, TB] of oracle codes [kvh, n, d] (slots past n left as zero)."""
+    kvh, n, d = codes.shape
+    nb, tb = d // 16, (256 if fmt == 8 else 128)
+    out = np.zeros((kvh, cap // 16, nb, tb), np.uint8)
+    full = np.zeros((kvh, cap, d), np.uint8)
+    full[:, :n] = codes
+    for h in range(kvh):
+        for g in range((n + 15) // 16):
+            for b in range(nb):
+                out[h, g, b] = tile_bytes(full[h, 16 * g:16 * g + 16, 16 * b:16 * b + 16], which, fmt)
+    return out
 
 
 def build_cache(seed, kvh, d, cap, n, k_fmt, v_fmt, rot, k_std=1.0, chunks=(None,)):
@@ -74,11 +102,22 @@ def test_append_is_bit_exact(kvh, d, k_fmt, v_fmt, rot):
     cache, k, v = build_cache(10 + d + kvh, kvh, d, cap, n, k_fmt, v_fmt, rot, chunks=(100, 1, 1, 48))
     ke, kc = oracle.kv_encode(k_fmt, k.transpose(1, 0, 2), False)
     ve, vc = oracle.kv_encode(v_fmt, v.transpose(1, 0, 2), rot)
-    for fmt, (e, c), (tc, te) in ((k_fmt, (ke, kc), (cache.k_codes, cache.k_exps)),
-                                  (v_fmt, (ve, vc), (cache.v_codes, cache.v_exps))):
-        want_c, want_e = cache_bytes(fmt, e, c)
-        assert np.array_equal(device_rows(tc, kvh, cap)[:, :n], want_c)
-        assert np.array_equal(device_rows(te, kvh, cap)[:, :n], want_e)
+    nb = d // 16
+    for which, fmt, (e, c), (tc, te) in (("k", k_fmt, (ke, kc), (cache.k_codes, cache.k_exps)),
+                                         ("v", v_fmt, (ve, vc), (cache.v_codes, cache.v_exps))):
+        assert np.array_equal(te.cpu().numpy().reshape(kvh, cap, nb)[:, :n], e)
+        got = tc.cpu().numpy().reshape(kvh, cap // 16, nb, -1)
+        want = expected_codes(np.asarray(c, np.uint8), which, fmt, cap)
+        full_groups = n // 16  # whole tiles; the last, partial tile is checked on its written rows below
+        assert np.array_equal(got[:, :full_groups], want[:, :full_groups])
+        if n % 16:
+            # rows past n in the last tile hold the random fill: compare the bytes of written rows only
+            g = full_groups
+            for h in range(kvh):
+                for b in range(nb):
+                    mask = tile_bytes(np.where(np.arange(16)[:, None] < n % 16, 0xFF if fmt == 8 else 0xF, 0)
+                                      * np.ones((16, 16), np.int64), which, fmt)
+                    assert np.array_equal(got[h, g, b] & mask, want[h, g, b] & mask)
 
 
 CASES = [  # kvh, G, d, k_fmt, v_fmt, rot, n_ctx, cap, k_std
