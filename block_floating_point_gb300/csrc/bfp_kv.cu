@@ -458,34 +458,89 @@ __global__ void __launch_bounds__(kAttnThreads) attn_partial_kernel(const AttnAr
     }
 }
 
-// One CTA per query head: merge the S partial results; rotate back (H_d / d) when V is stored rotated.
+constexpr int kMergeThreads = 1024;
+constexpr int kMaxSplits = 1024;
+
+// Deterministic block reductions over kMergeThreads threads (warp butterflies, then warp 0 in order).
+__device__ __forceinline__ float block_max(float v, float *red) {
+    v = warp_max(v);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        const float r = warp_max(red[threadIdx.x]);
+        if (threadIdx.x == 0) red[32] = r;
+    }
+    __syncthreads();
+    const float r = red[32];
+    __syncthreads();
+    return r;
+}
+__device__ __forceinline__ float block_sum(float v, float *red) {
+    v = warp_sum(v);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        const float r = warp_sum(red[threadIdx.x]);
+        if (threadIdx.x == 0) red[32] = r;
+    }
+    __syncthreads();
+    const float r = red[32];
+    __syncthreads();
+    return r;
+}
+
+// One CTA per query head: merge the S partial results (max, weights and normaliser over all threads;
+// the weighted sum with the splits dealt to kMergeThreads / D groups of D threads); then rotate back
+// (H_d / d) when V is stored rotated.
 template <int D>
-__global__ void __launch_bounds__(D) attn_merge_kernel(const float *part, int kvh, int G, int S, int rot, float *out) {
+__global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const float *part, int kvh, int G, int S, int rot,
+                                                                   float *out) {
+    constexpr int NSG = kMergeThreads / D;
+    __shared__ float w_s[kMaxSplits];
+    __shared__ float red[33];
+    __shared__ float osum[NSG][D];
     __shared__ float x[D];
     grid_dep_wait();
-    const int j = blockIdx.x, h = j / G, g = j % G, col = threadIdx.x;
-    float M = -INFINITY;
-    for (int s = 0; s < S; ++s) M = fmaxf(M, part[(((int64_t)h * S + s) * G + g) * (D + 2) + D]);
-    float L = 0.f, o = 0.f;
-    for (int s = 0; s < S; ++s) {
-        const float *p = part + (((int64_t)h * S + s) * G + g) * (D + 2);
-        const float w = p[D] == -INFINITY ? 0.f : __expf(p[D] - M);  // a split with no tokens has m = -inf
-        L = fmaf(p[D + 1], w, L);
-        o = fmaf(p[col], w, o);
+    const int j = blockIdx.x, h = j / G, g = j % G, tid = threadIdx.x;
+    const int64_t sstride = (int64_t)G * (D + 2);
+    const float *pj = part + ((int64_t)h * S * G + g) * (D + 2);  // split s at pj + s * sstride
+    float m = -INFINITY;
+    for (int s = tid; s < S; s += kMergeThreads) m = fmaxf(m, pj[s * sstride + D]);
+    const float M = block_max(m, red);
+    float l = 0.f;
+    for (int s = tid; s < S; s += kMergeThreads) {
+        const float ms = pj[s * sstride + D];
+        const float w = ms == -INFINITY ? 0.f : __expf(ms - M);  // a split with no tokens has m = -inf
+        w_s[s] = w;
+        l = fmaf(pj[s * sstride + D + 1], w, l);
     }
-    float y = o / L;
-    if (rot) {
+    const float L = block_sum(l, red);  // its barriers also publish w_s
+    const int col = tid % D, sg = tid / D;
+    float o = 0.f;
+    for (int s = sg; s < S; s += NSG) o = fmaf(pj[s * sstride + col], w_s[s], o);
+    osum[sg][col] = o;
+    __syncthreads();
+    float y = 0.f;
+    if (sg == 0) {
+        for (int k = 0; k < NSG; ++k) y += osum[k][col];
+        y /= L;
         x[col] = y;
+    }
+    if (rot) {
         __syncthreads();
         for (int hh = 1; hh < D; hh <<= 1) {
-            const float a = x[col & ~hh], b = x[col | hh];
+            float a = 0.f, b = 0.f;
+            if (sg == 0) {
+                a = x[col & ~hh];
+                b = x[col | hh];
+            }
             __syncthreads();
-            x[col] = (col & hh) ? a - b : a + b;
+            if (sg == 0) x[col] = (col & hh) ? a - b : a + b;
             __syncthreads();
         }
-        y = x[col] * (1.0f / D);
+        if (sg == 0) y = x[col] * (1.0f / D);
     }
-    out[(int64_t)j * D + col] = y;
+    if (sg == 0) out[(int64_t)j * D + col] = y;
 }
 
 int check_cache(const bfp_kv_cache *c) {
@@ -513,7 +568,7 @@ int attn_split(const bfp_kv_cache *c, int64_t n_ctx, int *S) {
     // about two CTAs per SM over all KV heads, at least two chunks per CTA
     int64_t s = std::max<int64_t>(1, (int64_t)2 * di.sms / c->kv_heads);
     s = std::min<int64_t>(s, std::max<int64_t>(1, nchunk / 2));
-    *S = (int)s;
+    *S = (int)std::min<int64_t>(s, kMaxSplits);
     return BFP_OK;
 }
 
@@ -645,9 +700,9 @@ int bfp_attn_decode(const bfp_kv_cache *cache, const uint16_t *q, int q_heads, i
     cudaError_t e;
     const float *part = a.part;
     switch (cache->head_dim) {
-        case 64: e = launch_pdl(attn_merge_kernel<64>, dim3(q_heads), dim3(64), 0, st, part, a.kvh, a.G, S, cache->v_rotated, out); break;
-        case 128: e = launch_pdl(attn_merge_kernel<128>, dim3(q_heads), dim3(128), 0, st, part, a.kvh, a.G, S, cache->v_rotated, out); break;
-        default: e = launch_pdl(attn_merge_kernel<256>, dim3(q_heads), dim3(256), 0, st, part, a.kvh, a.G, S, cache->v_rotated, out); break;
+        case 64: e = launch_pdl(attn_merge_kernel<64>, dim3(q_heads), dim3(kMergeThreads), 0, st, part, a.kvh, a.G, S, cache->v_rotated, out); break;
+        case 128: e = launch_pdl(attn_merge_kernel<128>, dim3(q_heads), dim3(kMergeThreads), 0, st, part, a.kvh, a.G, S, cache->v_rotated, out); break;
+        default: e = launch_pdl(attn_merge_kernel<256>, dim3(q_heads), dim3(kMergeThreads), 0, st, part, a.kvh, a.G, S, cache->v_rotated, out); break;
     }
     if (e != cudaSuccess) return cuda_fail(e, "launch attention merge");
     return BFP_OK;
