@@ -11,8 +11,9 @@ several independently drawn layer instances. Secondary lines (same run): the
 same layer at M=1, the hot-expert routing variant at M=16, the dense BFP8
 projection [8192 x 2048] at M=1/8/16 and the greedy token over [16 x 151936]
 logits (steps smaller than L2, each timed alone after a 256 MB L2-flushing
-write); the BFP8 LM head [151936 x 2048] alone and the 8-row decode stack (40
-layers, LM head, greedy token), both larger than L2, timed back to back.
+write); the BFP8 LM head [151936 x 2048] alone, the 8-row decode stack (40
+layers, LM head, greedy token) and decode attention over two BFP KV caches of
+131,072 tokens, all larger than L2, timed back to back.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--quick]
 
