@@ -3,9 +3,11 @@
 Plain CPU reference for the BFP MoE decode path. Only ``tests/``,
 ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg may import it;
 the library (``block_floating_point_gb300``) never does, and the two share no
-code. The arithmetic lives in ``bfp_oracle.c`` (plain C, fp64); this module
-loads it with ctypes and strings its pieces together in the order the decode
-step defines: router -> softmax -> top-k -> renormalise -> experts -> combine.
+code. The arithmetic of the decode step lives in ``bfp_oracle.c`` (plain C,
+fp64); this module loads it with ctypes and strings its pieces together in the
+order the decode step defines: router -> softmax -> top-k -> renormalise ->
+experts -> combine. The error-compensated encoding and the KV-cache attention
+are plain NumPy further down (fp64, except where the method fixes fp32).
 
 Every function cites the passage of the block_floating_point pages it follows
 (page titles abbreviated as in ``bfp_oracle.c``). Readings of points the pages
@@ -13,7 +15,10 @@ leave open are stated in ``bfp_oracle.c``'s header.
 
 Parity status: every function here is pinned by the ``-m "not gpu"`` tests
 (brute-force rational rounding, closed-form sizes, fp64 NumPy matmul,
-brute-force sorting, special-case MoE identities).
+brute-force sorting, special-case MoE identities; for the greedy token brute
+force; for error-compensated encoding the diagonal-Hessian, optimal-brain-
+quantiser, fixed-point and output-error cases; for the KV cache the Hadamard
+matrix, closed forms of attention and a direct softmax).
 """
 from __future__ import annotations
 
