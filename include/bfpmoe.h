@@ -12,7 +12,20 @@
  *     gate/up + down expert program for several rows (P1, "Fused decode kernels");
  *   256 experts, top-8 plus a shared expert (P3, opening paragraph);
  *   several users as the rows of one pass that streams every weight once
- *     (P4, "Multi-user decode").
+ *     (P4, "Multi-user decode");
+ *   the greedy argmax over the LM head's logits (P1, "Fused decode kernels");
+ *   error-compensated (GPTQ-style) BFP4 weights (P5, "What changed in this
+ *     release");
+ *   the KV cache in BFP8, or K BFP8 with Hadamard-rotated BFP4 V (P3,
+ *     QWEN36_KV_DTYPE row; P4, "Changes in s27").
+ *
+ * Entry points: packing (bfp_packed_size, bfp_encode, bfp_encode_gate_up,
+ * bfp_gptq_factor, bfp_encode_gptq, bfp_encode_gate_up_gptq, bfp_read_fields,
+ * bfp_decode_host, bfp_unpack_device); the dense projection (bfp_linear);
+ * the MoE layer and the decode stack (moe_decode_layer, moe_decode_layer_static,
+ * moe_stack_decode); the greedy token (bfp_greedy_tokens); the KV cache and
+ * decode attention (bfp_kv_append, bfp_attn_decode); workspace sizes, status
+ * and launch settings.
  *
  * Conventions for every function:
  *   - returns an int status: BFP_OK (0) or a negative BFP_E* code; never
