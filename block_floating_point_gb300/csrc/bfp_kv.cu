@@ -10,12 +10,18 @@
 // Hadamard matrix H_d applied to V in fp32 by the fast transform before
 // encoding, and undone once on the attention output (H_d H_d = d I).
 //
+// The codes are stored in tiles of 16 tokens x 16 values laid out in the
+// operand order of mma.sync m16n8k16, so that each lane's fragment is one 32-
+// or 64-bit shared-memory load and each appended token writes only its own
+// words, halves or bytes (layout in include/bfpmoe.h).
+//
 // Attention: the context is split into chunks of kChunk tokens; CTA (s, h)
 // takes KV head h and a contiguous range of chunks, streams each chunk's K and
-// V fields into shared memory with bulk copies (two stages), and keeps a
-// running softmax (max, sum, weighted V sum) for the G query heads of the
-// group. A second launch merges the CTAs' partial results per query head and,
-// for rotated V, applies H_d / d.
+// V tiles and exponents into shared memory with bulk copies (two stages), and
+// keeps a running softmax (max, sum, weighted V sum) for the G query heads of
+// the group, with both contractions on the tensor cores. A second launch
+// merges the CTAs' partial results per query head and, for rotated V, applies
+// H_d / d.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -32,7 +38,7 @@ constexpr int kChunk = 64;         // tokens per shared-memory stage
 constexpr int kAttnThreads = 256;  // 8 warps
 constexpr int kMaxGroup = 8;       // query heads per KV head
 
-__host__ __device__ constexpr int row_code_bytes(int fmt, int d) { return fmt == BFP_FMT_BFP8 ? d : d / 2; }
+__host__ __device__ constexpr int code_bytes_per_token(int fmt, int d) { return fmt == BFP_FMT_BFP8 ? d : d / 2; }
 
 // 2^e for e in [-149, 127], exact (subnormal below -126).
 __device__ __forceinline__ float exact_pow2(int e) {
@@ -590,7 +596,7 @@ cudaError_t launch_pdl(K kern, dim3 grid, dim3 block, size_t smem, cudaStream_t 
 template <int VPL, int KF, int VF>
 int launch_partial(const AttnArgs &a, cudaStream_t st) {
     constexpr int D = VPL * kWarp;
-    constexpr int STAGE = kChunk * (row_code_bytes(KF, D) + row_code_bytes(VF, D) + 2 * (D / 16));
+    constexpr int STAGE = kChunk * (code_bytes_per_token(KF, D) + code_bytes_per_token(VF, D) + 2 * (D / 16));
     auto kern = attn_partial_kernel<VPL, KF, VF>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * STAGE);
     if (e != cudaSuccess) return cuda_fail(e, "attention shared memory");
@@ -621,7 +627,7 @@ int bfp_kv_cache_size(int fmt, int kv_heads, int head_dim, int64_t capacity, siz
     if ((head_dim != 64 && head_dim != 128 && head_dim != 256) || kv_heads < 1 || kv_heads > 64 ||
         capacity < kChunk || capacity % kChunk != 0 || capacity > (int64_t(1) << 31))
         return fail(BFP_ESHAPE, "head_dim 64/128/256, kv_heads 1..64, capacity a positive multiple of 64");
-    *code_bytes = (size_t)kv_heads * capacity * row_code_bytes(fmt, head_dim);
+    *code_bytes = (size_t)kv_heads * capacity * code_bytes_per_token(fmt, head_dim);
     *exp_bytes = (size_t)kv_heads * capacity * (head_dim / 16);
     return BFP_OK;
 }
