@@ -107,3 +107,20 @@ def test_gptq_error_codes():
     with pytest.raises(bfp.BFPError) as ei:
         bfp.encode_gptq(4, synth.normal(604, 1, (16, 24)), np.eye(24))
     assert ei.value.code == bfp.BFP_ESHAPE
+
+
+@pytest.mark.parametrize("fmt", [4, 8])
+def test_dead_inputs_and_tiny_calibration_sets(fmt):
+    # inputs that never fire (zero columns of x) leave H singular but for the damping; fewer samples
+    # than inputs (t < k) likewise: both sides must still agree, and the dead columns move no error
+    k = 64
+    x = calibration_inputs(701, 40, k)
+    x[:, [3, 17, 40, 41]] = 0.0
+    w = synth.normal(702, 1, (20, k), std=0.02)
+    packed = bfp.encode_gptq(fmt, w, bfp.gptq_factor(x))
+    e_lib, c_lib = bfp.read_fields(fmt, 20, k, packed)
+    u_or = oracle.gptq_factor(x)
+    e_or, c_or = oracle.gptq_encode(fmt, w, u_or)
+    assert np.array_equal(e_lib, e_or) and np.array_equal(c_lib, c_or)
+    for j in (3, 17, 40, 41):
+        assert np.all(u_or[j, j + 1:] == 0.0)
