@@ -124,23 +124,38 @@ int bfp_gptq_factor(const float *x, int64_t t, int64_t k, double damp, double *u
     if (t < 1 || k < 1 || k > (int64_t(1) << 16)) return fail(BFP_ESHAPE, "need t >= 1 and 1 <= k <= 65536");
     if (!(damp > 0.0) || !std::isfinite(damp)) return fail(BFP_EINVAL, "damp must be positive");
     const size_t kk = (size_t)k;
-    // X^T (k rows of t samples) in fp64, so that every entry of H is one contiguous dot product
-    std::vector<double> xt(kk * (size_t)t);
+    const int64_t k4 = (k + 3) / 4 * 4;
+    // X^T (k rows of t samples, zero rows up to a multiple of 4) in fp64, so that every entry of H is
+    // one contiguous dot product
+    std::vector<double> xt((size_t)k4 * (size_t)t, 0.0);
     for (int64_t s = 0; s < t; ++s)
         for (int64_t a = 0; a < k; ++a) {
             const float v = x[s * k + a];
             if (!std::isfinite(v)) return fail(BFP_ENONFINITE, "calibration inputs hold NaN or Inf");
             xt[(size_t)a * t + s] = v;
         }
-    // H = X^T X / t (upper triangle, then mirrored)
+    // H = X^T X / t: 4 x 4 tiles of the upper triangle, each entry summed over the samples in order
     std::vector<double> h(kk * kk);
-    parallel_groups(k, nthreads, [&](int64_t a) {
-        const double *xa = &xt[(size_t)a * t];
-        for (int64_t b = a; b < k; ++b) {
-            const double *xb = &xt[(size_t)b * t];
-            double acc = 0.0;
-            for (int64_t s = 0; s < t; ++s) acc = acc + xa[s] * xb[s];
-            h[(size_t)a * kk + b] = acc / (double)t;
+    parallel_groups(k4 / 4, nthreads, [&](int64_t ta) {
+        const int64_t a0 = 4 * ta;
+        for (int64_t b0 = a0; b0 < k4; b0 += 4) {
+            double acc[4][4] = {};
+            const double *xa[4], *xb[4];
+            for (int i = 0; i < 4; ++i) {
+                xa[i] = &xt[(size_t)(a0 + i) * t];
+                xb[i] = &xt[(size_t)(b0 + i) * t];
+            }
+            for (int64_t s = 0; s < t; ++s) {
+                const double va[4] = {xa[0][s], xa[1][s], xa[2][s], xa[3][s]};
+                const double vb[4] = {xb[0][s], xb[1][s], xb[2][s], xb[3][s]};
+                for (int i = 0; i < 4; ++i)
+                    for (int j = 0; j < 4; ++j) acc[i][j] = acc[i][j] + va[i] * vb[j];
+            }
+            for (int i = 0; i < 4; ++i)
+                for (int j = 0; j < 4; ++j) {
+                    const int64_t a = a0 + i, b = b0 + j;
+                    if (a < k && b < k && b >= a) h[(size_t)a * kk + b] = acc[i][j] / (double)t;
+                }
         }
         return true;
     });
@@ -152,36 +167,64 @@ int bfp_gptq_factor(const float *x, int64_t t, int64_t k, double damp, double *u
     if (!(mean > 0.0)) return fail(BFP_EINVAL, "calibration inputs are all zero");
     const double lam = damp * mean;
     for (int64_t a = 0; a < k; ++a) h[(size_t)a * kk + a] += lam;
-    // H = R R^T with R upper triangular (a Cholesky factorisation that runs from the last column
-    // to the first); then H^-1 = R^-T R^-1, so U = R^-1 is the upper factor with H^-1 = U^T U.
-    std::vector<double> &r = h;  // factorised in place, upper triangle
-    for (int64_t j = k - 1; j >= 0; --j) {
-        double *rj = &r[(size_t)j * kk];
-        double d = rj[j];
-        for (int64_t l = j + 1; l < k; ++l) d -= rj[l] * rj[l];
-        if (!(d > 0.0)) return fail(BFP_EINVAL, "Hessian not positive definite (raise damp)");
-        const double piv = std::sqrt(d);
-        rj[j] = piv;
-        parallel_groups(j, j >= 256 ? nthreads : 1, [&](int64_t i) {
-            double *ri = &r[(size_t)i * kk];
-            double acc = ri[j];
-            for (int64_t l = j + 1; l < k; ++l) acc -= ri[l] * rj[l];
-            ri[j] = acc / piv;
+    // With J the order reversal, P = J H J = L L^T (lower Cholesky factor L), so H = R R^T with
+    // R = J L J upper triangular, H^-1 = R^-T R^-1, and U = R^-1 = J L^-1 J is the upper factor with
+    // H^-1 = U^T U. L: blocked right-looking factorisation of P in place (lower triangle).
+    std::vector<double> pm(kk * kk);
+    for (int64_t i = 0; i < k; ++i)
+        for (int64_t j = 0; j <= i; ++j) pm[(size_t)i * kk + j] = h[(size_t)(k - 1 - i) * kk + (k - 1 - j)];
+    auto P = [&](int64_t i, int64_t j) -> double & { return pm[(size_t)i * kk + j]; };
+    constexpr int64_t kNb = 64;
+    for (int64_t kb = 0; kb < k; kb += kNb) {
+        const int64_t e = std::min(kb + kNb, k);
+        for (int64_t j = kb; j < e; ++j) {  // the diagonal block
+            double d = P(j, j);
+            for (int64_t l = kb; l < j; ++l) d -= P(j, l) * P(j, l);
+            if (!(d > 0.0)) return fail(BFP_EINVAL, "Hessian not positive definite (raise damp)");
+            const double piv = std::sqrt(d);
+            P(j, j) = piv;
+            for (int64_t i = j + 1; i < e; ++i) {
+                double acc = P(i, j);
+                for (int64_t l = kb; l < j; ++l) acc -= P(i, l) * P(j, l);
+                P(i, j) = acc / piv;
+            }
+        }
+        if (e == k) break;
+        // the panel below it, one row at a time
+        parallel_groups(k - e, nthreads, [&](int64_t ii) {
+            const int64_t i = e + ii;
+            for (int64_t j = kb; j < e; ++j) {
+                double acc = P(i, j);
+                for (int64_t l = kb; l < j; ++l) acc -= P(i, l) * P(j, l);
+                P(i, j) = acc / P(j, j);
+            }
+            return true;
+        });
+        // the trailing matrix, one row at a time
+        parallel_groups(k - e, nthreads, [&](int64_t ii) {
+            const int64_t i = e + ii;
+            const double *pi = &pm[(size_t)i * kk + kb];
+            for (int64_t j = e; j <= i; ++j) {
+                const double *pj = &pm[(size_t)j * kk + kb];
+                double acc = 0.0;
+                for (int64_t l = 0; l < e - kb; ++l) acc = acc + pi[l] * pj[l];
+                P(i, j) -= acc;
+            }
             return true;
         });
     }
-    // U = R^-1, one column at a time: R u_c = e_c by back substitution
+    // L^-1 column by column (forward substitution), written reversed into U
     std::memset(u, 0, kk * kk * sizeof(double));
     parallel_groups(k, nthreads, [&](int64_t c) {
-        std::vector<double> col((size_t)c + 1);
-        col[(size_t)c] = 1.0 / r[(size_t)c * kk + c];
-        for (int64_t i = c - 1; i >= 0; --i) {
-            const double *ri = &r[(size_t)i * kk];
+        std::vector<double> col((size_t)(k - c));
+        col[0] = 1.0 / P(c, c);
+        for (int64_t i = c + 1; i < k; ++i) {
+            const double *pi = &pm[(size_t)i * kk];
             double acc = 0.0;
-            for (int64_t l = i + 1; l <= c; ++l) acc += ri[l] * col[(size_t)l];
-            col[(size_t)i] = -acc / ri[i];
+            for (int64_t l = c; l < i; ++l) acc += pi[l] * col[(size_t)(l - c)];
+            col[(size_t)(i - c)] = -acc / pi[i];
         }
-        for (int64_t i = 0; i <= c; ++i) u[(size_t)i * kk + c] = col[(size_t)i];
+        for (int64_t i = c; i < k; ++i) u[(size_t)(k - 1 - i) * kk + (k - 1 - c)] = col[(size_t)(i - c)];
         return true;
     });
     return BFP_OK;
