@@ -161,3 +161,25 @@ def test_packer_threads_do_not_change_bytes():
     a = bfp.encode(4, w, threads=1)
     b = bfp.encode(4, w, threads=7)
     assert np.array_equal(a, b)
+
+
+def test_kv_cache_sizes_match_the_pages():
+    """bfp_kv_cache_size against the per-token cache sizes the pages print (tests/golden/storage_sizes.json):
+    the 35B bundle's 10 attention layers of 2 KV heads x 256 in BFP8 (20.0 -> 10.6 KiB per token) and the
+    27B card's 16,384 K and 16,384 V values per token (K BFP8 with V BFP4: 26,624 instead of 34,816 B)."""
+    import json
+    g = json.load(open(os.path.join(ROOT, "tests", "golden", "storage_sizes.json")))
+    cap = 64
+
+    def per_token(fmt, heads, d):
+        c, e = bfp.kv_cache_size(fmt, heads, d, cap)
+        return (c + e) / cap
+
+    kv = g["bfp8_kv_cache"]
+    bfp8_35b = 10 * 2 * per_token(8, 2, 256)  # K and V, 10 layers
+    assert 10 * 2 * 2 * 256 * 2 / 1024 == kv["bf16_kib_per_token"]
+    assert round(bfp8_35b / 1024, kv["printed_decimals"]) == kv["bfp8_kib_per_token_printed"]
+    v = g["bfp4_v_cache"]
+    heads = 16384 // 256  # KV heads x layers
+    assert heads * (per_token(8, 1, 256) + per_token(8, 1, 256)) == v["bytes_per_token_k_bfp8_v_bfp8"]
+    assert heads * (per_token(8, 1, 256) + per_token(4, 1, 256)) == v["bytes_per_token_k_bfp8_v_bfp4"]
