@@ -331,30 +331,18 @@ class MoELayer:
     @classmethod
     def from_source(cls, hidden, n_experts, ffn, top_k, shared_ffn, expert_fmt, router_bf16: np.ndarray,
                     shared_gate_bf16: np.ndarray, expert_source, shared_source, router_bias=None, device="cuda",
-                    threads: int = 0):
-        """Pack fp32 weights on the host (bfp_encode / bfp_encode_gate_up) and upload them.
+                    threads: int = 0, gptq_factors=None, shared_gptq_factors=None):
+        """Pack fp32 weights on the host (pack_experts) and upload them.
 
         expert_source(e) -> (gate [ffn, hidden], up [ffn, hidden], down [hidden, ffn]) fp32;
-        shared_source() -> the same for the shared expert.
+        shared_source() -> the same for the shared expert. gptq_factors(e) / shared_gptq_factors()
+        (optional) -> (u_in [hidden, hidden], u_mid [ffn, ffn]) fp64 factors from gptq_factor
+        of the expert's calibration inputs (x for gate/up, h for down): error-compensated encoding.
         """
         import torch
-        gub = packed_size(expert_fmt, 2 * ffn, hidden)
-        dnb = packed_size(expert_fmt, hidden, ffn)
-        host_gu = np.empty(n_experts * gub, dtype=np.uint8)
-        host_dn = np.empty(n_experts * dnb, dtype=np.uint8)
-        def pack(e):
-            g, u, d = expert_source(e)
-            encode_gate_up(expert_fmt, g, u, threads, out=host_gu[e * gub:(e + 1) * gub])
-            encode(expert_fmt, d, threads, out=host_dn[e * dnb:(e + 1) * dnb])
-
-        # experts are independent: pack several at once (the C calls release the GIL)
-        import concurrent.futures as cf
-        workers = max(1, min(8, (os.cpu_count() or 1) // 2))
-        with cf.ThreadPoolExecutor(max_workers=workers) as ex:
-            list(ex.map(pack, range(n_experts)))
-        g, u, d = shared_source()
-        sgu = encode_gate_up(expert_fmt, g, u, threads)
-        sdn = encode(expert_fmt, d, threads)
+        host_gu, host_dn = pack_experts(hidden, n_experts, ffn, expert_fmt, expert_source, threads, gptq_factors)
+        sgu, sdn = pack_experts(hidden, 1, shared_ffn, expert_fmt, lambda e: shared_source(), threads,
+                                None if shared_gptq_factors is None else (lambda e: shared_gptq_factors()))
         dev = torch.device(device)
 
         def up_(a):
@@ -364,6 +352,34 @@ class MoELayer:
                    up_(np.asarray(router_bf16, dtype=np.uint16).view(np.int16)),
                    up_(np.asarray(shared_gate_bf16, dtype=np.uint16).view(np.int16)),
                    up_(host_gu), up_(host_dn), up_(sgu), up_(sdn), router_bias=rb)
+
+
+def pack_experts(hidden, n_experts, ffn, expert_fmt, expert_source, threads: int = 0, gptq_factors=None):
+    """Host packing of a layer's experts: (gate/up bytes of all experts, down bytes of all experts), each
+    expert at a stride of its packed size (the layout moe_decode_layer reads). expert_source(e) -> fp32
+    (gate, up, down); gptq_factors(e) -> (u_in, u_mid) selects error-compensated encoding (bfp_encode_gate_up_gptq
+    with u_in, bfp_encode_gptq of down with u_mid), else round to nearest."""
+    gub = packed_size(expert_fmt, 2 * ffn, hidden)
+    dnb = packed_size(expert_fmt, hidden, ffn)
+    host_gu = np.empty(n_experts * gub, dtype=np.uint8)
+    host_dn = np.empty(n_experts * dnb, dtype=np.uint8)
+
+    def pack(e):
+        g, u, d = expert_source(e)
+        if gptq_factors is None:
+            encode_gate_up(expert_fmt, g, u, threads, out=host_gu[e * gub:(e + 1) * gub])
+            encode(expert_fmt, d, threads, out=host_dn[e * dnb:(e + 1) * dnb])
+        else:
+            u_in, u_mid = gptq_factors(e)
+            host_gu[e * gub:(e + 1) * gub] = encode_gate_up_gptq(expert_fmt, g, u, u_in, threads)
+            host_dn[e * dnb:(e + 1) * dnb] = encode_gptq(expert_fmt, d, u_mid, threads)
+
+    # experts are independent: pack several at once (the C calls release the GIL)
+    import concurrent.futures as cf
+    workers = max(1, min(8, (os.cpu_count() or 1) // 2, n_experts))
+    with cf.ThreadPoolExecutor(max_workers=workers) as ex:
+        list(ex.map(pack, range(n_experts)))
+    return host_gu, host_dn
 
 
 def moe_workspace_size(layer: MoELayer, m: int) -> int:

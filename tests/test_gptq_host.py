@@ -124,3 +124,23 @@ def test_dead_inputs_and_tiny_calibration_sets(fmt):
     assert np.array_equal(e_lib, e_or) and np.array_equal(c_lib, c_or)
     for j in (3, 17, 40, 41):
         assert np.all(u_or[j, j + 1:] == 0.0)
+
+
+def test_layer_packing_with_error_compensated_experts():
+    """pack_experts (the host half of MoELayer.from_source) lays out GPTQ-encoded experts at the same
+    strides as plain ones, each expert's bytes those of its own encode calls."""
+    hidden, ffn, ne = 64, 32, 3
+    src = {e: (synth.normal(801, 3 * e, (ffn, hidden), std=0.02), synth.normal(801, 3 * e + 1, (ffn, hidden), std=0.02),
+               synth.normal(801, 3 * e + 2, (hidden, ffn), std=0.02)) for e in range(ne)}
+    fac = {e: (bfp.gptq_factor(calibration_inputs(810 + e, 200, hidden)),
+               bfp.gptq_factor(calibration_inputs(820 + e, 200, ffn))) for e in range(ne)}
+    gu, dn = bfp.pack_experts(hidden, ne, ffn, 4, lambda e: src[e], gptq_factors=lambda e: fac[e])
+    gu0, dn0 = bfp.pack_experts(hidden, ne, ffn, 4, lambda e: src[e])
+    gub, dnb = bfp.packed_size(4, 2 * ffn, hidden), bfp.packed_size(4, hidden, ffn)
+    assert gu.nbytes == gu0.nbytes == ne * gub and dn.nbytes == dn0.nbytes == ne * dnb
+    for e in range(ne):
+        g, u, d = src[e]
+        assert np.array_equal(gu[e * gub:(e + 1) * gub], bfp.encode_gate_up_gptq(4, g, u, fac[e][0]))
+        assert np.array_equal(dn[e * dnb:(e + 1) * dnb], bfp.encode_gptq(4, d, fac[e][1]))
+        assert np.array_equal(gu0[e * gub:(e + 1) * gub], bfp.encode_gate_up(4, g, u))
+        assert np.array_equal(dn0[e * dnb:(e + 1) * dnb], bfp.encode(4, d))
