@@ -183,3 +183,42 @@ def test_kv_cache_sizes_match_the_pages():
     heads = 16384 // 256  # KV heads x layers
     assert heads * (per_token(8, 1, 256) + per_token(8, 1, 256)) == v["bytes_per_token_k_bfp8_v_bfp8"]
     assert heads * (per_token(8, 1, 256) + per_token(4, 1, 256)) == v["bytes_per_token_k_bfp8_v_bfp4"]
+
+
+def test_greedy_and_kv_argument_checks_on_the_host():
+    """Argument validation of the greedy-token and KV-cache entry points happens before any CUDA call."""
+    import ctypes
+    lib = bfp.load()
+    fake = ctypes.c_void_p(4096)  # never dereferenced: every call below is rejected first
+    sz = ctypes.c_size_t()
+    assert lib.bfp_greedy_tokens(fake, 0, 10, 10, fake, fake, 64, None) == bfp.BFP_ESHAPE
+    assert lib.bfp_greedy_tokens(fake, 17, 10, 10, fake, fake, 64, None) == bfp.BFP_ESHAPE
+    assert lib.bfp_greedy_tokens(fake, 2, 10, 5, fake, fake, 64, None) == bfp.BFP_EINVAL
+    assert lib.bfp_greedy_workspace_size(1, 0, ctypes.byref(sz)) == bfp.BFP_ESHAPE
+    c1, c2 = ctypes.c_size_t(), ctypes.c_size_t()
+    assert lib.bfp_kv_cache_size(5, 2, 256, 64, ctypes.byref(c1), ctypes.byref(c2)) == bfp.BFP_EINVAL
+    assert lib.bfp_kv_cache_size(8, 2, 96, 64, ctypes.byref(c1), ctypes.byref(c2)) == bfp.BFP_ESHAPE
+    assert lib.bfp_kv_cache_size(8, 2, 256, 100, ctypes.byref(c1), ctypes.byref(c2)) == bfp.BFP_ESHAPE
+    assert lib.bfp_kv_cache_size(4, 3, 128, 128, ctypes.byref(c1), ctypes.byref(c2)) == bfp.BFP_OK
+    assert (c1.value, c2.value) == (3 * 128 * 64, 3 * 128 * 8)
+
+    def cache(**kw):
+        f = dict(kv_heads=2, head_dim=128, k_fmt=8, v_fmt=8, v_rotated=0, reserved=0, capacity=128,
+                 k_codes=4096, k_exps=8192, v_codes=12288, v_exps=16384)
+        f.update(kw)
+        return bfp.KvCacheC(*[f[n] for n, _ in bfp.KvCacheC._fields_])
+
+    k = ctypes.c_void_p(4096)
+    for kw, code in ((dict(head_dim=96), bfp.BFP_ESHAPE), (dict(reserved=1), bfp.BFP_EINVAL),
+                     (dict(v_rotated=2), bfp.BFP_EINVAL), (dict(k_fmt=3), bfp.BFP_EINVAL),
+                     (dict(capacity=96), bfp.BFP_ESHAPE), (dict(v_exps=16385), bfp.BFP_EALIGN),
+                     (dict(k_codes=0), bfp.BFP_EINVAL)):
+        c = cache(**kw)
+        assert lib.bfp_kv_append(ctypes.byref(c), k, k, 0, 1, None) == code, kw
+    c = cache()
+    assert lib.bfp_kv_append(ctypes.byref(c), k, k, 120, 9, None) == bfp.BFP_ESHAPE   # past the capacity
+    assert lib.bfp_kv_append(ctypes.byref(c), k, ctypes.c_void_p(4100), 0, 1, None) == bfp.BFP_EALIGN
+    assert lib.bfp_attn_workspace_size(ctypes.byref(c), 18, 10, ctypes.byref(sz)) == bfp.BFP_ESHAPE  # group 9
+    assert lib.bfp_attn_workspace_size(ctypes.byref(c), 3, 10, ctypes.byref(sz)) == bfp.BFP_ESHAPE
+    assert lib.bfp_attn_workspace_size(ctypes.byref(c), 16, 129, ctypes.byref(sz)) == bfp.BFP_ESHAPE
+    assert lib.bfp_attn_decode(ctypes.byref(c), k, 16, 0, ctypes.c_float(0.1), k, k, 1 << 20, None) == bfp.BFP_ESHAPE
