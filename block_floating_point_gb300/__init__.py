@@ -78,6 +78,7 @@ SIGNATURES = {
     "bfp_greedy_workspace_size": [_I, _I64, ctypes.POINTER(_SZ)],
     "bfp_greedy_tokens": [_P, _I, _I64, _I64, _P, _P, _SZ, _P],
     "bfp_kv_cache_size": [_I, _I, _I, _I64, ctypes.POINTER(_SZ), ctypes.POINTER(_SZ)],
+    "bfp_kv_read_fields": [ctypes.POINTER(KvCacheC), _I, _I64, _I64, _P, _P],
     "bfp_kv_append": [ctypes.POINTER(KvCacheC), _P, _P, _I64, _I, _P],
     "bfp_attn_workspace_size": [ctypes.POINTER(KvCacheC), _I, _I64, ctypes.POINTER(_SZ)],
     "bfp_attn_decode": [ctypes.POINTER(KvCacheC), _P, _I, _I64, ctypes.c_float, _P, _P, _SZ, _P],
@@ -510,6 +511,25 @@ def kv_cache_size(fmt: int, kv_heads: int, head_dim: int, capacity: int):
     _check(load().bfp_kv_cache_size(fmt, kv_heads, head_dim, capacity, ctypes.byref(cb), ctypes.byref(eb)),
            "bfp_kv_cache_size")
     return cb.value, eb.value
+
+
+def kv_read_fields(cache: KvCache, which: str, t0: int, n: int):
+    """Logical fields of tokens t0 .. t0 + n - 1 of K ("k") or V ("v"), read from a host copy of the cache:
+    (exps [kv_heads, n, head_dim/16], codes [kv_heads, n, head_dim]) uint8."""
+    arrs = [a.cpu().numpy() for a in (cache.k_codes, cache.k_exps, cache.v_codes, cache.v_exps)]
+    return kv_read_host_fields(cache.kv_heads, cache.head_dim, cache.capacity, cache.k_fmt, cache.v_fmt,
+                               cache.v_rotated, arrs, which, t0, n)
+
+
+def kv_read_host_fields(kv_heads, head_dim, capacity, k_fmt, v_fmt, v_rotated, arrays, which: str, t0: int, n: int):
+    """bfp_kv_read_fields over host arrays (k_codes, k_exps, v_codes, v_exps) of a cache's layout."""
+    arrays = [np.ascontiguousarray(a, dtype=np.uint8) for a in arrays]
+    c = KvCacheC(kv_heads, head_dim, k_fmt, v_fmt, int(v_rotated), 0, capacity, *[a.ctypes.data for a in arrays])
+    exps = np.empty((kv_heads, n, head_dim // 16), np.uint8)
+    codes = np.empty((kv_heads, n, head_dim), np.uint8)
+    _check(load().bfp_kv_read_fields(ctypes.byref(c), {"k": 0, "v": 1}[which], t0, n, exps.ctypes.data,
+                                     codes.ctypes.data), "bfp_kv_read_fields")
+    return exps, codes
 
 
 def kv_append(cache: KvCache, k, v, pos: int, stream=None):

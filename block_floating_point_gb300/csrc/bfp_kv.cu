@@ -25,6 +25,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstring>
 
 #include "bfp_launch.h"
 
@@ -629,6 +630,48 @@ int bfp_kv_cache_size(int fmt, int kv_heads, int head_dim, int64_t capacity, siz
         return fail(BFP_ESHAPE, "head_dim 64/128/256, kv_heads 1..64, capacity a positive multiple of 64");
     *code_bytes = (size_t)kv_heads * capacity * code_bytes_per_token(fmt, head_dim);
     *exp_bytes = (size_t)kv_heads * capacity * (head_dim / 16);
+    return BFP_OK;
+}
+
+int bfp_kv_read_fields(const bfp_kv_cache *cache, int which, int64_t t0, int64_t n, uint8_t *exps, uint8_t *codes) {
+    if (!cache) return fail(BFP_EINVAL, "null cache");
+    if (which != 0 && which != 1) return fail(BFP_EINVAL, "which must be 0 (K) or 1 (V)");
+    int rc = check_cache(cache);
+    if (rc) return rc;
+    if (!exps || !codes) return fail(BFP_EINVAL, "null output");
+    if (t0 < 0 || n < 1 || t0 + n > cache->capacity) return fail(BFP_ESHAPE, "tokens outside the capacity");
+    const int d = cache->head_dim, nb = d / 16, fmt = which ? cache->v_fmt : cache->k_fmt;
+    const int tb = fmt == BFP_FMT_BFP8 ? 256 : 128;
+    const uint8_t *cc = static_cast<const uint8_t *>(which ? cache->v_codes : cache->k_codes);
+    const uint8_t *ce = static_cast<const uint8_t *>(which ? cache->v_exps : cache->k_exps);
+    for (int h = 0; h < cache->kv_heads; ++h)
+        for (int64_t i = 0; i < n; ++i) {
+            const int64_t t = t0 + i, r = t & 15;
+            for (int b = 0; b < nb; ++b) {
+                exps[((int64_t)h * n + i) * nb + b] = ce[((int64_t)h * cache->capacity + t) * nb + b];
+                const uint8_t *tile = cc + (((int64_t)h * (cache->capacity / 16) + (t >> 4)) * nb + b) * tb;
+                uint8_t *out = codes + ((int64_t)h * n + i) * d + 16 * b;
+                for (int c = 0; c < 16; ++c) {
+                    uint32_t code;
+                    if (!which && fmt == BFP_FMT_BFP8) {  // pattern word: P(c0, c1) | rotl(P(c2, c3), 8)
+                        uint32_t w;
+                        std::memcpy(&w, tile + (4 * (r & 7) + c / 4) * 8 + (r >> 3) * 4, 4);
+                        const uint32_t p = (c & 2) ? ((w >> 8) | (w << 24)) : w;  // rotate right by 8 for c2, c3
+                        const uint32_t half = (c & 1) ? (p >> 16) : (p & 0xFFFFu);
+                        code = (half & 0x7Fu) | (((half >> 15) & 1u) << 7);
+                    } else if (!which) {
+                        const uint8_t byte = tile[(4 * (r & 7) + c / 4) * 4 + (r >> 3) * 2 + (c & 3) / 2];
+                        code = (c & 1) ? (byte >> 4) : (byte & 15u);
+                    } else if (fmt == BFP_FMT_BFP8) {
+                        code = tile[(4 * (c & 7) + (r >> 2)) * 8 + (c >> 3) * 4 + (r & 3)];
+                    } else {
+                        const uint8_t byte = tile[(4 * (c & 7) + (r >> 2)) * 4 + (r & 3)];
+                        code = (c >> 3) ? (byte >> 4) : (byte & 15u);
+                    }
+                    out[c] = (uint8_t)code;
+                }
+            }
+        }
     return BFP_OK;
 }
 

@@ -356,6 +356,15 @@ typedef struct {
 int bfp_kv_cache_size(int fmt, int kv_heads, int head_dim, int64_t capacity, size_t *code_bytes, size_t *exp_bytes);
 
 /*
+ * Host reader of a cache (test and inspection aid): with the cache's four
+ * arrays in HOST memory (copies of the device arrays), writes the logical
+ * fields of tokens t0 .. t0 + n - 1 of K (which = 0) or V (which = 1):
+ * exps [kv_heads x n x head_dim/16] and codes [kv_heads x n x head_dim], one
+ * code per byte (sign << mb | magnitude), in the stored (rotated) basis.
+ */
+int bfp_kv_read_fields(const bfp_kv_cache *cache, int which, int64_t t0, int64_t n, uint8_t *exps, uint8_t *codes);
+
+/*
  * Encodes n_new tokens into slots pos .. pos + n_new - 1: k and v are bf16
  * [n_new x kv_heads x head_dim] (device, contiguous, 16-byte aligned). V is
  * rotated first when the cache says so. One launch on the stream; finite

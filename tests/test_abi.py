@@ -222,3 +222,27 @@ def test_greedy_and_kv_argument_checks_on_the_host():
     assert lib.bfp_attn_workspace_size(ctypes.byref(c), 3, 10, ctypes.byref(sz)) == bfp.BFP_ESHAPE
     assert lib.bfp_attn_workspace_size(ctypes.byref(c), 16, 129, ctypes.byref(sz)) == bfp.BFP_ESHAPE
     assert lib.bfp_attn_decode(ctypes.byref(c), k, 16, 0, ctypes.c_float(0.1), k, k, 1 << 20, None) == bfp.BFP_ESHAPE
+
+
+@pytest.mark.parametrize("kvh,d,k_fmt,v_fmt,rot", [(2, 256, 8, 8, False), (4, 256, 8, 4, True), (3, 64, 4, 8, False)])
+def test_kv_read_fields_inverts_the_cache_layout(kvh, d, k_fmt, v_fmt, rot):
+    """bfp_kv_read_fields on host arrays packed by the layout text of include/bfpmoe.h (tests/harness.py)
+    returns the oracle's fields of the same seeded rows."""
+    from harness import expected_codes
+    n, cap = 45, 64
+    k = synth.to_bf16_bits(synth.normal(901 + d, 1, (kvh, n, d)))
+    v = synth.to_bf16_bits(synth.normal(901 + d, 2, (kvh, n, d)))
+    ke, kc = oracle.kv_encode(k_fmt, k, False)
+    ve, vc = oracle.kv_encode(v_fmt, v, rot)
+    nb = d // 16
+    arrays = []
+    for which, fmt, e, c in (("k", k_fmt, ke, kc), ("v", v_fmt, ve, vc)):
+        arrays.append(expected_codes(np.asarray(c, np.uint8), which, fmt, cap).reshape(-1))
+        ex = np.zeros((kvh, cap, nb), np.uint8)
+        ex[:, :n] = e
+        arrays.append(ex.reshape(-1))
+    for which, (e, c) in (("k", (ke, kc)), ("v", (ve, vc))):
+        got_e, got_c = bfp.kv_read_host_fields(kvh, d, cap, k_fmt, v_fmt, rot, arrays, which, 0, n)
+        assert np.array_equal(got_e, e) and np.array_equal(got_c, c)
+        got_e, got_c = bfp.kv_read_host_fields(kvh, d, cap, k_fmt, v_fmt, rot, arrays, which, 17, 20)
+        assert np.array_equal(got_e, e[:, 17:37]) and np.array_equal(got_c, c[:, 17:37])

@@ -14,6 +14,7 @@ import pytest
 
 import oracle
 import synth
+from harness import expected_codes, tile_bytes
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -33,46 +34,6 @@ def _lib():
 
 def bf16_rows(seed, stream, shape, std=1.0):
     return synth.to_bf16_bits(synth.normal(seed, stream, shape, std=std))
-
-
-def _p(code):
-    return (int(code) & 0x7F) | ((int(code) >> 7) << 15)
-
-
-def tile_bytes(codes16, which, fmt):
-    """One 16-token x 16-column tile of codes in the cache layout (the layout text of include/bfpmoe.h)."""
-    t = np.zeros(256 if fmt == 8 else 128, np.uint8)
-    for r in range(16):
-        for c in range(16):
-            code = int(codes16[r, c])
-            if which == "k" and fmt == 8 and c % 4 == 0:
-                cs = codes16[r, c:c + 4]
-                p01, p23 = _p(cs[0]) | (_p(cs[1]) << 16), _p(cs[2]) | (_p(cs[3]) << 16)
-                w = p01 | (((p23 << 8) | (p23 >> 24)) & 0xFFFFFFFF)
-                off = (4 * (r % 8) + c // 4) * 8 + (r // 8) * 4
-                t[off:off + 4] = np.frombuffer(np.uint32(w).tobytes(), np.uint8)
-            elif which == "k" and fmt == 4:
-                off = (4 * (r % 8) + c // 4) * 4 + (r // 8) * 2 + (c % 4) // 2
-                t[off] |= code << (4 * (c % 2))
-            elif which == "v" and fmt == 8:
-                t[(4 * (c % 8) + r // 4) * 8 + (c // 8) * 4 + r % 4] = code
-            elif which == "v" and fmt == 4:
-                t[(4 * (c % 8) + r // 4) * 4 + r % 4] |= code << (4 * (c // 8))
-    return t
-
-
-def expected_codes(codes, which, fmt, cap):
-    """Cache code bytes [kvh, cap / 16, NB, TB] of oracle codes [kvh, n, d] (slots past n left as zero)."""
-    kvh, n, d = codes.shape
-    nb, tb = d // 16, (256 if fmt == 8 else 128)
-    out = np.zeros((kvh, cap // 16, nb, tb), np.uint8)
-    full = np.zeros((kvh, cap, d), np.uint8)
-    full[:, :n] = codes
-    for h in range(kvh):
-        for g in range((n + 15) // 16):
-            for b in range(nb):
-                out[h, g, b] = tile_bytes(full[h, 16 * g:16 * g + 16, 16 * b:16 * b + 16], which, fmt)
-    return out
 
 
 def build_cache(seed, kvh, d, cap, n, k_fmt, v_fmt, rot, k_std=1.0, chunks=(None,)):
