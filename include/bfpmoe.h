@@ -24,8 +24,9 @@
  * bfp_decode_host, bfp_unpack_device); the dense projection (bfp_linear);
  * the MoE layer and the decode stack (moe_decode_layer, moe_decode_layer_static,
  * moe_stack_decode); the greedy token (bfp_greedy_tokens); the KV cache and
- * decode attention (bfp_kv_append, bfp_attn_decode); workspace sizes, status
- * and launch settings.
+ * decode attention (bfp_kv_cache_size, bfp_kv_append, bfp_attn_decode, and
+ * bfp_kv_read_fields on host copies); workspace sizes, status and launch
+ * settings.
  *
  * Conventions for every function:
  *   - returns an int status: BFP_OK (0) or a negative BFP_E* code; never
