@@ -78,6 +78,7 @@ SIGNATURES = {
     "bfp_greedy_workspace_size": [_I, _I64, ctypes.POINTER(_SZ)],
     "bfp_greedy_tokens": [_P, _I, _I64, _I64, _P, _P, _SZ, _P],
     "bfp_kv_cache_size": [_I, _I, _I, _I64, ctypes.POINTER(_SZ), ctypes.POINTER(_SZ)],
+    "bfp_kv_encode_host": [ctypes.POINTER(KvCacheC), _P, _P, _I64, _I, _I],
     "bfp_kv_read_fields": [ctypes.POINTER(KvCacheC), _I, _I64, _I64, _P, _P],
     "bfp_kv_append": [ctypes.POINTER(KvCacheC), _P, _P, _I64, _I, _P],
     "bfp_attn_workspace_size": [ctypes.POINTER(KvCacheC), _I, _I64, ctypes.POINTER(_SZ)],
@@ -519,6 +520,18 @@ def kv_read_fields(cache: KvCache, which: str, t0: int, n: int):
     arrs = [a.cpu().numpy() for a in (cache.k_codes, cache.k_exps, cache.v_codes, cache.v_exps)]
     return kv_read_host_fields(cache.kv_heads, cache.head_dim, cache.capacity, cache.k_fmt, cache.v_fmt,
                                cache.v_rotated, arrs, which, t0, n)
+
+
+def kv_encode_host(kv_heads, head_dim, capacity, k_fmt, v_fmt, v_rotated, arrays, k, v, pos: int, threads: int = 0):
+    """bfp_kv_encode_host into host arrays (k_codes, k_exps, v_codes, v_exps; uint8 numpy, written in place) from
+    bf16 bit patterns k, v [n_new, kv_heads, head_dim] (uint16 numpy)."""
+    for a in arrays:
+        assert a.dtype == np.uint8 and a.flags.c_contiguous
+    k = np.ascontiguousarray(k, dtype=np.uint16)
+    v = np.ascontiguousarray(v, dtype=np.uint16)
+    c = KvCacheC(kv_heads, head_dim, k_fmt, v_fmt, int(v_rotated), 0, capacity, *[a.ctypes.data for a in arrays])
+    _check(load().bfp_kv_encode_host(ctypes.byref(c), k.ctypes.data, v.ctypes.data, pos, k.shape[0], threads),
+           "bfp_kv_encode_host")
 
 
 def kv_read_host_fields(kv_heads, head_dim, capacity, k_fmt, v_fmt, v_rotated, arrays, which: str, t0: int, n: int):

@@ -32,6 +32,8 @@ inline uint32_t f32_to_u32(float f) {
 inline uint32_t rotl32(uint32_t v, int s) { s &= 31; return s ? (v << s) | (v >> (32 - s)) : v; }
 inline uint32_t rotr32(uint32_t v, int s) { s &= 31; return s ? (v >> s) | (v << (32 - s)) : v; }
 
+}  // namespace
+
 // One 16-value block -> exponent byte + 16 codes. Returns false on NaN/Inf.
 // E is the largest exponent field; a value with field e keeps its 24-bit
 // significand shifted right by (24 - mb) + (E - e), rounded to nearest with
@@ -66,6 +68,8 @@ bool encode_block(const float *v, int mb, uint8_t *E_out, uint8_t codes[16]) {
     }
     return true;
 }
+
+namespace {
 
 // fp16-lane pattern of one pair of codes: first value in bits 0-15, second in 16-31,
 // each as (sign << 15 | magnitude).

@@ -26,8 +26,10 @@
 
 #include <algorithm>
 #include <cstring>
+#include <vector>
 
 #include "bfp_launch.h"
+#include "bfp_pack.h"
 
 namespace bfp {
 
@@ -630,6 +632,70 @@ int bfp_kv_cache_size(int fmt, int kv_heads, int head_dim, int64_t capacity, siz
         return fail(BFP_ESHAPE, "head_dim 64/128/256, kv_heads 1..64, capacity a positive multiple of 64");
     *code_bytes = (size_t)kv_heads * capacity * code_bytes_per_token(fmt, head_dim);
     *exp_bytes = (size_t)kv_heads * capacity * (head_dim / 16);
+    return BFP_OK;
+}
+
+int bfp_kv_encode_host(const bfp_kv_cache *cache, const uint16_t *k, const uint16_t *v, int64_t pos, int n_new,
+                       int nthreads) {
+    int rc = check_cache(cache);
+    if (rc) return rc;
+    if (!k || !v) return fail(BFP_EINVAL, "null k or v");
+    if (n_new < 1 || pos < 0 || pos + n_new > cache->capacity) return fail(BFP_ESHAPE, "tokens outside the capacity");
+    const int d = cache->head_dim, nb = d / 16, kvh = cache->kv_heads;
+    const int64_t rows = (int64_t)n_new * kvh * 2;
+    const bool good = parallel_groups(rows, nthreads, [&](int64_t row) {
+        const int which = (int)(row & 1);
+        const int64_t rest = row >> 1, tok = rest / kvh;
+        const int h = (int)(rest % kvh);
+        const uint16_t *src = (which ? v : k) + (tok * kvh + h) * d;
+        std::vector<float> x((size_t)d);
+        for (int i = 0; i < d; ++i) {
+            const uint32_t u = (uint32_t)src[i] << 16;
+            std::memcpy(&x[(size_t)i], &u, 4);
+        }
+        if (which && cache->v_rotated)  // fast Walsh-Hadamard transform in fp32, stages 1, 2, 4, ...
+            for (int hh = 1; hh < d; hh <<= 1)
+                for (int i = 0; i < d; ++i)
+                    if (!(i & hh)) {
+                        const float a = x[(size_t)i], b = x[(size_t)(i + hh)];
+                        x[(size_t)i] = a + b;
+                        x[(size_t)(i + hh)] = a - b;
+                    }
+        const int fmt = which ? cache->v_fmt : cache->k_fmt, mb = fmt == BFP_FMT_BFP8 ? 7 : 3;
+        const int tb = fmt == BFP_FMT_BFP8 ? 256 : 128;
+        const int64_t slot = pos + tok, r = slot & 15;
+        uint8_t *cc = static_cast<uint8_t *>(which ? cache->v_codes : cache->k_codes);
+        uint8_t *ce = static_cast<uint8_t *>(which ? cache->v_exps : cache->k_exps);
+        for (int b = 0; b < nb; ++b) {
+            uint8_t E, c[16];
+            if (!encode_block(&x[(size_t)16 * b], mb, &E, c)) return false;
+            ce[((int64_t)h * cache->capacity + slot) * nb + b] = E;
+            uint8_t *tile = cc + (((int64_t)h * (cache->capacity / 16) + (slot >> 4)) * nb + b) * tb;
+            for (int j = 0; j < 4; ++j) {  // K: a row's 4 codes of columns 4j..4j+3 in its word or half
+                if (which) break;
+                if (fmt == BFP_FMT_BFP8) {
+                    auto pat = [](uint32_t code) { return (code & 0x7Fu) | (((code >> 7) & 1u) << 15); };
+                    const uint32_t p01 = pat(c[4 * j]) | (pat(c[4 * j + 1]) << 16);
+                    const uint32_t p23 = pat(c[4 * j + 2]) | (pat(c[4 * j + 3]) << 16);
+                    const uint32_t w = p01 | ((p23 << 8) | (p23 >> 24));
+                    std::memcpy(tile + (4 * (r & 7) + j) * 8 + (r >> 3) * 4, &w, 4);
+                } else {
+                    const uint16_t hw = (uint16_t)(c[4 * j] | (c[4 * j + 1] << 4) | (c[4 * j + 2] << 8) |
+                                                   (c[4 * j + 3] << 12));
+                    std::memcpy(tile + (4 * (r & 7) + j) * 4 + (r >> 3) * 2, &hw, 2);
+                }
+            }
+            if (which) {  // V: one byte per (token, column), or per (token, column pair c, c + 8)
+                if (fmt == BFP_FMT_BFP8)
+                    for (int col = 0; col < 16; ++col) tile[(4 * (col & 7) + (r >> 2)) * 8 + (col >> 3) * 4 + (r & 3)] = c[col];
+                else
+                    for (int col = 0; col < 8; ++col)
+                        tile[(4 * col + (r >> 2)) * 4 + (r & 3)] = (uint8_t)(c[col] | (c[col + 8] << 4));
+            }
+        }
+        return true;
+    });
+    if (!good) return fail(BFP_ENONFINITE, "k or v holds NaN or Inf");
     return BFP_OK;
 }
 

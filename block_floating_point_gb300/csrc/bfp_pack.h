@@ -15,6 +15,10 @@ struct GroupFields {
     std::vector<uint8_t> codes, exps;
 };
 
+// One 16-value block -> exponent byte + 16 codes (round to nearest, ties to even, saturating; the
+// rules of bfp_encode). Returns false on NaN/Inf.
+bool encode_block(const float *v, int mb, uint8_t *E_out, uint8_t codes[16]);
+
 // Write record (rg, c) of the packed layout from a row group's logical fields.
 void write_record(const Geometry &g, const GroupFields &f, int64_t c, uint8_t *rec);
 

@@ -24,9 +24,9 @@
  * bfp_decode_host, bfp_unpack_device); the dense projection (bfp_linear);
  * the MoE layer and the decode stack (moe_decode_layer, moe_decode_layer_static,
  * moe_stack_decode); the greedy token (bfp_greedy_tokens); the KV cache and
- * decode attention (bfp_kv_cache_size, bfp_kv_append, bfp_attn_decode, and
- * bfp_kv_read_fields on host copies); workspace sizes, status and launch
- * settings.
+ * decode attention (bfp_kv_cache_size, bfp_kv_append, bfp_attn_decode; on
+ * host copies bfp_kv_encode_host and bfp_kv_read_fields); workspace sizes,
+ * status and launch settings.
  *
  * Conventions for every function:
  *   - returns an int status: BFP_OK (0) or a negative BFP_E* code; never
@@ -355,6 +355,17 @@ typedef struct {
 
 /* Bytes of one codes array and of one exponents array for a format and shape. */
 int bfp_kv_cache_size(int fmt, int kv_heads, int head_dim, int64_t capacity, size_t *code_bytes, size_t *exp_bytes);
+
+/*
+ * Host encoder, the counterpart of bfp_kv_append for a cache whose four
+ * arrays are in HOST memory (to pack K/V rows without a GPU, for example a
+ * restored session, then copy the arrays to the device): k, v bf16
+ * [n_new x kv_heads x head_dim] (host); the same codes, bytes and rotation
+ * (fp32, same stage order) as bfp_kv_append. nthreads <= 0: the host's cores.
+ * BFP_ENONFINITE for NaN/Inf.
+ */
+int bfp_kv_encode_host(const bfp_kv_cache *cache, const uint16_t *k, const uint16_t *v, int64_t pos, int n_new,
+                       int nthreads);
 
 /*
  * Host reader of a cache (test and inspection aid): with the cache's four

@@ -246,3 +246,26 @@ def test_kv_read_fields_inverts_the_cache_layout(kvh, d, k_fmt, v_fmt, rot):
         assert np.array_equal(got_e, e) and np.array_equal(got_c, c)
         got_e, got_c = bfp.kv_read_host_fields(kvh, d, cap, k_fmt, v_fmt, rot, arrays, which, 17, 20)
         assert np.array_equal(got_e, e[:, 17:37]) and np.array_equal(got_c, c[:, 17:37])
+
+
+@pytest.mark.parametrize("kvh,d,k_fmt,v_fmt,rot", [(2, 256, 8, 8, False), (4, 256, 8, 4, True), (3, 128, 4, 8, True),
+                                                   (1, 64, 4, 4, True)])
+def test_kv_encode_host_matches_the_oracle(kvh, d, k_fmt, v_fmt, rot):
+    """bfp_kv_encode_host: the cache bytes of the oracle's fields (layout text of include/bfpmoe.h), written
+    in two appends; slots never written keep their bytes."""
+    from harness import expected_codes
+    n, cap = 45, 64
+    k = synth.to_bf16_bits(synth.normal(951 + d, 1, (n, kvh, d)))
+    v = synth.to_bf16_bits(synth.normal(951 + d, 2, (n, kvh, d)))
+    sizes = [bfp.kv_cache_size(f, kvh, d, cap) for f in (k_fmt, v_fmt)]
+    arrays = [np.zeros(sizes[0][0], np.uint8), np.zeros(sizes[0][1], np.uint8),
+              np.zeros(sizes[1][0], np.uint8), np.zeros(sizes[1][1], np.uint8)]
+    bfp.kv_encode_host(kvh, d, cap, k_fmt, v_fmt, rot, arrays, k[:20], v[:20], 0, threads=3)
+    bfp.kv_encode_host(kvh, d, cap, k_fmt, v_fmt, rot, arrays, k[20:], v[20:], 20)
+    nb = d // 16
+    for i, (which, fmt, src, r) in enumerate((("k", k_fmt, k, False), ("v", v_fmt, v, rot))):
+        e, c = oracle.kv_encode(fmt, src.transpose(1, 0, 2), r)
+        assert np.array_equal(arrays[2 * i].reshape(kvh, cap // 16, nb, -1),
+                              expected_codes(np.asarray(c, np.uint8), which, fmt, cap))
+        ex = arrays[2 * i + 1].reshape(kvh, cap, nb)
+        assert np.array_equal(ex[:, :n], e) and not ex[:, n:].any()
