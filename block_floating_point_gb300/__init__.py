@@ -86,6 +86,7 @@ SIGNATURES = {
     "bfp_workspace_status": [_P, ctypes.POINTER(_I), _P],
     "bfp_set_wait_limit": [_I64],
     "bfp_set_launch_mode": [_I],
+    "bfp_set_row_path": [_I],
     "bfp_last_error": [],
 }
 
@@ -269,6 +270,12 @@ LAUNCH_DEPENDENT, LAUNCH_COOPERATIVE = 0, 1
 def set_launch_mode(mode: int):
     """How the MoE layer kernel is launched (include/bfpmoe.h, bfp_set_launch_mode)."""
     _check(load().bfp_set_launch_mode(mode), "bfp_set_launch_mode")
+
+
+def set_row_path(enabled: bool):
+    """Which kernel runs one-row MoE layers: the one-row kernel (True, default) or the general one
+    (include/bfpmoe.h, bfp_set_row_path)."""
+    _check(load().bfp_set_row_path(1 if enabled else 0), "bfp_set_row_path")
 
 
 def _alloc_ws(nbytes: int, device, stream=None):

@@ -89,6 +89,12 @@ __device__ __forceinline__ uint64_t l2_evict_first() {
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
     return pol;
 }
+// L2 policy for small data read by every launch (router rows): last to be evicted.
+__device__ __forceinline__ uint64_t l2_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
 // bulk_g2s with an L2 cache policy.
 __device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
                                               uint64_t policy) {
@@ -128,6 +134,17 @@ __device__ __forceinline__ bool wait_counter(const uint32_t *p, uint32_t target,
     uint64_t t0 = global_ns();
     for (int64_t i = 1; i < w.iters; ++i) {
         __nanosleep(64);
+        if (ld_acquire(p) >= target) return true;
+        if (global_ns() - t0 > w.nanos) return false;
+    }
+    return false;
+}
+// Bounded wait until *p >= target, polling without a pause between loads (each acquire load is an L2 round
+// trip already); false = gave up.
+__device__ __forceinline__ bool poll_counter(const uint32_t *p, uint32_t target, const WaitCfg &w) {
+    if (ld_acquire(p) >= target) return true;
+    const uint64_t t0 = global_ns();
+    for (int64_t i = 1; i < w.iters; ++i) {
         if (ld_acquire(p) >= target) return true;
         if (global_ns() - t0 > w.nanos) return false;
     }

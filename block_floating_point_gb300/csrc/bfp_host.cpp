@@ -22,6 +22,7 @@ namespace {
 thread_local std::string g_last_error = "ok";
 thread_local int64_t g_wait_limit = 0;
 std::atomic<int> g_launch_mode{BFP_LAUNCH_DEPENDENT};
+std::atomic<int> g_row_path{1};
 
 inline uint32_t f32_to_u32(float f) {
     uint32_t u;
@@ -189,6 +190,7 @@ int fail(int code, const std::string &msg) {
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 int64_t wait_limit() { return g_wait_limit; }
 int launch_mode() { return g_launch_mode.load(std::memory_order_relaxed); }
+bool row_path() { return g_row_path.load(std::memory_order_relaxed) != 0; }
 
 int make_geometry(int fmt, int64_t n, int64_t k, Geometry *g) {
     if (fmt != BFP_FMT_BFP4 && fmt != BFP_FMT_BFP8) return fail(BFP_EINVAL, "fmt must be BFP_FMT_BFP4 or BFP_FMT_BFP8");
@@ -321,6 +323,12 @@ int bfp_set_wait_limit(int64_t iterations) {
 int bfp_set_launch_mode(int mode) {
     if (mode != BFP_LAUNCH_DEPENDENT && mode != BFP_LAUNCH_COOPERATIVE) return fail(BFP_EINVAL, "unknown launch mode");
     g_launch_mode.store(mode, std::memory_order_relaxed);
+    return BFP_OK;
+}
+
+int bfp_set_row_path(int enabled) {
+    if (enabled != 0 && enabled != 1) return fail(BFP_EINVAL, "enabled must be 0 or 1");
+    g_row_path.store(enabled, std::memory_order_relaxed);
     return BFP_OK;
 }
 

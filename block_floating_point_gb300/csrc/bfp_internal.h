@@ -41,4 +41,7 @@ int64_t wait_limit();
 // How the MoE layer kernel is launched (bfp_set_launch_mode; process-wide).
 int launch_mode();
 
+// Whether one-row MoE layers run on the one-row kernel (bfp_set_row_path; process-wide).
+bool row_path();
+
 }  // namespace bfp

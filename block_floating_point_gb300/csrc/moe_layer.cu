@@ -47,6 +47,7 @@
 #include "bfp_launch.h"
 #include "bfp_tiles.cuh"
 #include "bfp_trace.h"
+#include "moe_common.cuh"
 
 namespace bfp {
 
@@ -56,11 +57,8 @@ int linear_launch_ex(const bfp_matrix *w, const uint16_t *x, int m, int64_t ldx,
                      int64_t ldy, uint32_t *status, void *body, size_t body_bytes, cudaStream_t st, int norm);
 int linear_ws_body_bytes(const bfp_matrix *w, int m, size_t *bytes);
 
-constexpr int kMaxRows = 16;
 constexpr int kMoeWarps = 16;                // warps of the layer kernel (no producer warp)
 constexpr int kMoeThreads = kMoeWarps * 32;
-constexpr int kMaxTopK = 8;
-constexpr int kMaxExperts = 256;
 // Floats of one phase-1 partial tile handed between warps: 2 records (gate, up) x 2 activation
 // groups x 4 accumulators x 32 lanes.
 constexpr int kP1PartFloats = 2 * 2 * 4 * 32;
@@ -125,10 +123,6 @@ struct MoeMisc {
     int flags[4];  // [0] abort
 };
 
-__host__ __device__ inline int router_row_start(int c, int rows, int ncta) { return (int)((int64_t)c * rows / ncta); }
-// Row stride (floats) of the logits in the workspace: the E expert logits then the shared-gate logit,
-// padded to whole 16-byte vectors.
-__host__ __device__ inline int logit_stride(int E) { return (E + 1 + 3) & ~3; }
 // Row stride (elements) of the activation rows staged in shared memory: 16 bytes of padding per row.
 __host__ __device__ inline int stage_ldx(int H) { return H + 8; }
 
@@ -153,33 +147,6 @@ __device__ __forceinline__ P1Tile p1_tile(int g, int nft_s, int nft) {
     t.ft = t.sh ? g : (g - nft_s) % nft;
     return t;
 }
-// Ordered 32-bit key of a float: larger float <=> larger unsigned key.
-__device__ __forceinline__ uint32_t order_key(float v) {
-    uint32_t u = __float_as_uint(v);
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-// Inverse of order_key.
-__device__ __forceinline__ float key_value(uint32_t k) {
-    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
-}
-// Compare-exchange on (key, index) pairs: larger key first, lower index first among equal keys.
-__device__ __forceinline__ void cmp_xchg(uint32_t &ka, int &qa, uint32_t &kb, int &qb) {
-    const bool sw = kb > ka || (kb == ka && qb < qa);
-    const uint32_t k0 = sw ? kb : ka, k1 = sw ? ka : kb;
-    const int q0 = sw ? qb : qa, q1 = sw ? qa : qb;
-    ka = k0;
-    kb = k1;
-    qa = q0;
-    qb = q1;
-}
-// Sorts 8 (key, index) pairs in registers (Batcher's odd-even merge network, 19 comparators).
-__device__ __forceinline__ void sort8_desc(uint32_t k[8], int q[8]) {
-    constexpr int net[19][2] = {{0, 1}, {2, 3}, {4, 5}, {6, 7}, {0, 2}, {1, 3}, {4, 6}, {5, 7}, {1, 2}, {5, 6},
-                                {0, 4}, {1, 5}, {2, 6}, {3, 7}, {2, 4}, {3, 5}, {1, 2}, {3, 4}, {5, 6}};
-#pragma unroll
-    for (int i = 0; i < 19; ++i) cmp_xchg(k[net[i][0]], q[net[i][0]], k[net[i][1]], q[net[i][1]]);
-}
-
 // Per-warp streams. Warp w has nsw slots of its own in the ring; its k-th item lands in slot
 // k mod nsw, and the warp itself issues item k + nsw (lane 0, one or two bulk copies) as soon as it is
 // done with item k. Its items, in order:
@@ -1243,9 +1210,9 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
 // ----------------------------------------------------------------------------
 struct MoePlan {
     Geometry gu, dn, sgu, sdn;
-    int ngrp, ncta, nsw, ch1, slot_bytes, frag_bytes, scr_bytes, r2, noct, Fmax, stage_off, stage_r;
+    int ngrp, ncta, nsw, ch1, slot_bytes, frag_bytes, scr_bytes, r2, noct, Fmax, stage_off, stage_r, row_boxes;
     size_t smem;
-    size_t off_ctrl, off_hmax, off_logits, off_hbuf, off_part, off_p1part;
+    size_t off_ctrl, off_hmax, off_logits, off_hbuf, off_part, off_row, off_p1part;
     size_t ws_core;   // bytes the layer cannot run without
     size_t ws_bytes;  // plus the phase-1 handoff tiles (moe_workspace_size)
 };
@@ -1324,7 +1291,7 @@ static int plan_moe(const bfp_moe_layer *L, int m, MoePlan *p) {
     // workspace
     size_t o = kWsHeader;
     p->off_ctrl = o;
-    o += 16;
+    o += 32;  // counters: [0..3] this kernel, [4..5] the one-row kernel (moe_row.cu)
     p->off_hmax = o;
     o = align_up(o + 4 * (size_t)m * (L->top_k + 1), 256);
     p->off_logits = o;
@@ -1333,6 +1300,9 @@ static int plan_moe(const bfp_moe_layer *L, int m, MoePlan *p) {
     o = align_up(o + 4 * (size_t)m * (L->top_k + 1) * p->Fmax, 256);
     p->off_part = o;
     o = align_up(o + 4 * (size_t)m * (L->top_k + 1) * L->hidden, 256);
+    p->off_row = o;  // the one-row kernel's exchange area (moe_row.cu): epoch word, tagged logits and h
+    p->row_boxes = row_boxes(di.sms);
+    o = align_up(o + row_ws_bytes(L->n_experts, L->top_k, p->Fmax, p->row_boxes), 256);
     p->ws_core = o;
     p->off_p1part = o;
     o = align_up(o + 4 * (size_t)p->ncta * (kMoeWarps - 1) * kP1PartFloats, 256);
@@ -1437,6 +1407,10 @@ static int moe_launch(const bfp_moe_layer *L, const uint16_t *x, int m, int norm
     a.scr_bytes = p.scr_bytes;
     a.wait = wait_cfg();
     a.wait_data = WaitCfg{kDefaultWaitIters, kDefaultWaitNanos};
+    if (m == 1 && row_path()) {  // one row: the latency path (moe_row.cu), when the layer's shape fits it
+        rc = row_layer_launch(L, x, norm, y, h_out, topk_idx, topk_w, a.status, w + p.off_row, a.Fmax, st);
+        if (rc != kRowNotApplicable) return rc;
+    }
     if (L->expert_fmt == BFP_FMT_BFP4)
         return p.ngrp == 1 ? launch_moe_t<4, 1>(a, p, st) : launch_moe_t<4, 2>(a, p, st);
     return p.ngrp == 1 ? launch_moe_t<8, 1>(a, p, st) : launch_moe_t<8, 2>(a, p, st);
@@ -1533,7 +1507,7 @@ int moe_stack_decode(const bfp_moe_layer *layers, int n_layers, const bfp_matrix
 // ----------------------------------------------------------------------------
 namespace bfp {
 
-constexpr size_t kStaticScratchBytes = size_t(3) << 19;  // 1.5 MiB: a full-size layer at 16 rows needs 1,492,224 B
+constexpr size_t kStaticScratchBytes = size_t(2) << 20;  // 2 MiB: a full-size layer at 16 rows needs about 1.85 MB
 static __device__ __align__(256) uint8_t g_moe_static_scratch[kStaticScratchBytes];
 
 // Device address of the scratch array on the current device. The array's name
@@ -1581,5 +1555,10 @@ extern "C" int moe_decode_layer_static(const bfp_moe_layer *layer, const uint16_
     // The status word and the cross-block counters must start at zero: clear them on the stream.
     cudaError_t e = cudaMemsetAsync(ws, 0, p.off_logits, st);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(static scratch counters)");
+    if (m == 1) {  // the one-row kernel's epoch word and tagged words start over too
+        e = cudaMemsetAsync(static_cast<uint8_t *>(ws) + p.off_row, 0,
+                            row_ws_bytes(layer->n_experts, layer->top_k, p.Fmax, p.row_boxes), st);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(static scratch, one-row area)");
+    }
     return moe_launch(layer, x, m, 0, y, nullptr, topk_idx, topk_w, ws, kStaticScratchBytes, st);
 }

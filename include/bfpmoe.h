@@ -266,15 +266,18 @@ int moe_decode_layer(const bfp_moe_layer *layer, const uint16_t *x, int m, float
  *     differ in the last fp32 bits: with the smaller scratch the gate/up
  *     phase deals whole units to warps, which changes the order of some
  *     sums); x, y, topk_idx, topk_w as there (caller-owned device memory).
- *   - Scratch: one built-in device array of 1.5 MiB (1,572,864 bytes),
- *     allocated when the library is loaded and held by every GPU that loads
- *     it until the process exits. A layer whose core state needs more (the
- *     workspace without its optional phase-1 hand-off area) is rejected with
- *     BFP_EWORKSPACE; the full-size layer (hidden 2048, 256 experts, ffn 512,
- *     top-8) at 16 rows needs 1,492,224 bytes.
+ *   - Scratch: one built-in device array of 2 MiB (2,097,152 bytes). It is
+ *     reserved on a device when the library's MoE module first loads there
+ *     (with CUDA's lazy module loading: the first MoE call on that device)
+ *     and held until the process exits. A layer whose core state needs more
+ *     (the workspace without its optional phase-1 hand-off area) is rejected
+ *     with BFP_EWORKSPACE; the full-size layer (hidden 2048, 256 experts,
+ *     ffn 512, top-8) needs 1,845,760 bytes on a 152-SM GPU (the one-row
+ *     kernel's exchange area grows with the SM count).
  *   - The first call on a device looks up the array's device address and
  *     zeroes it, synchronously: make that first call before any stream
- *     capture. Each call then clears the array's counters on its stream.
+ *     capture. Each call then clears the array's counters (and, with one
+ *     row, the one-row kernel's exchange area) on its stream.
  *   - Each device has its own copy of the array, and every call on that
  *     device shares it; it keeps the last call's contents. Calls on one
  *     device that can overlap on the GPU (on streams with no ordering
@@ -430,6 +433,18 @@ int bfp_set_wait_limit(int64_t iterations);
  */
 enum { BFP_LAUNCH_DEPENDENT = 0, BFP_LAUNCH_COOPERATIVE = 1 };
 int bfp_set_launch_mode(int mode);
+
+/*
+ * Which kernel runs a one-row MoE layer (moe_decode_layer, moe_decode_layer_static
+ * and each layer of moe_stack_decode with m = 1), process-wide: 1 (default) the
+ * one-row kernel, built for the shortest dependent chain of single-sequence
+ * decode (every CTA's share fixed at launch, all of it requested at once, each
+ * CTA summing whole output row groups itself); 0 the general kernel used for
+ * m > 1. Both compute the same layer; layers whose shape does not fit the
+ * one-row kernel's shared-memory plan use the general kernel either way. A
+ * measurement and test hook. BFP_EINVAL for other values.
+ */
+int bfp_set_row_path(int enabled);
 
 /* Message for the last non-OK status returned on this thread. */
 const char *bfp_last_error(void);

@@ -165,3 +165,74 @@ def test_rejects_bad_arguments(tiny):
     with pytest.raises(bfp.BFPError) as ei:
         bfp.moe_decode_layer(layer, x[:1], ws[:256])
     assert ei.value.code == bfp.BFP_EWORKSPACE
+
+
+# ---------------------------------------------------------------- the one-row kernel (m = 1)
+ROW_CASES = {
+    "tiny": (synth.TINY, 121, 4, False),
+    "tiny_bfp8_experts": (synth.TINY, 123, 8, False),
+    "odd_shapes": (synth.MoESpec(hidden=208, n_experts=37, ffn=48, top_k=3, shared_ffn=80), 405, 4, False),
+    "full": (synth.FULL, 222, 4, False),
+    "full_hot_routing": (synth.FULL, 304, 4, True),
+    # 64 experts of width 1024: a CTA's share exceeds shared memory, so the general kernel runs it
+    "wide_experts": (synth.MoESpec(hidden=2048, n_experts=64, ffn=1024, top_k=8, shared_ffn=1024), 415, 4, False),
+}
+
+
+@pytest.mark.parametrize("name", list(ROW_CASES))
+def test_one_row_kernel_against_oracle_and_general_kernel(name):
+    """m = 1 runs on the one-row kernel (every CTA's share fixed at launch, each CTA summing whole output
+    row groups): selection bit-exact and outputs within tolerance of the oracle, and the general kernel
+    (bfp_set_row_path(0)) selects the same experts on the same row."""
+    spec, seed, fmt, hot = ROW_CASES[name]
+    case = LayerCase(spec, seed=seed, hot=hot, fmt=fmt)
+    layer = case.device_layer()
+    full = spec.hidden == 2048
+    for row_seed0 in (0, 40):
+        x = check(case, layer, 1, rms_norm=full, row_seed0=row_seed0)
+        bfp.set_row_path(False)
+        try:
+            y_g, idx_g, w_g, _, _ = run_layer(layer, x, 1)
+        finally:
+            bfp.set_row_path(True)
+        y_ref, idx_ref, w_ref = case.oracle_layer(x)
+        assert np.array_equal(idx_g.cpu().numpy(), idx_ref)
+        assert_close(y_g.cpu().numpy(), y_ref, "general kernel, one row")
+
+
+def test_one_row_and_general_kernels_share_a_workspace(full):
+    """The one-row and the general kernel keep separate counters in the workspace: calls with m = 1 and
+    m = 16 alternating on one workspace stay correct."""
+    case, layer = full
+    x16, _ = case.inputs(16, True, 1300)
+    x1 = x16[:1]
+    ws = bfp.moe_workspace(layer, 16)
+    y16_ref, y1_ref = case.oracle_layer(x16)[0], case.oracle_layer(x1)[0]
+    for _ in range(2):
+        y1 = bfp.moe_decode_layer(layer, bf16_tensor(x1), ws)
+        y16 = bfp.moe_decode_layer(layer, bf16_tensor(x16), ws)
+        torch.cuda.synchronize()
+        assert bfp.workspace_status(ws) == bfp.BFP_OK
+        assert_close(y1.cpu().numpy(), y1_ref, "m = 1 between m = 16 calls")
+        assert_close(y16.cpu().numpy(), y16_ref, "m = 16 between m = 1 calls")
+
+
+def test_one_row_bounded_wait_reports_timeout_and_recovers(tiny):
+    case, layer = tiny
+    x, _ = case.inputs(1, False, 950)
+    ws = bfp.moe_workspace(layer, 1)
+    xt = bf16_tensor(x)
+    bfp.set_wait_limit(1)
+    try:
+        seen = set()
+        for _ in range(5):
+            bfp.moe_decode_layer(layer, xt, ws)
+            seen.add(bfp.workspace_status(ws))
+    finally:
+        bfp.set_wait_limit(0)
+    assert bfp.BFP_ETIMEOUT in seen
+    bfp.workspace_init(ws)
+    y = bfp.moe_decode_layer(layer, xt, ws)
+    torch.cuda.synchronize()
+    assert bfp.workspace_status(ws) == bfp.BFP_OK
+    assert_close(y.cpu().numpy(), case.oracle_layer(x)[0], "one row, after recovery")

@@ -3,7 +3,7 @@
 Some callers cannot call cudaMalloc: code embedded in a host runtime that owns
 all device memory through its own allocator, or a latency-critical path where
 an allocation could synchronise the device. moe_decode_layer_static takes no
-workspace and uses the library's built-in 1.5 MiB device scratch array instead.
+workspace and uses the library's built-in 2 MiB device scratch array instead.
 This test calls it through the C-ABI and checks its outputs against the
 workspace entry point (moe_decode_layer) on two calls in a row, within the
 tolerance the other GPU tests use. It lives in a file that pytest collects
@@ -50,7 +50,7 @@ def test_static_scratch_layer_matches_workspace_layer(spec, m, seed):
 def test_static_scratch_rejects_layers_beyond_its_size():
     import block_floating_point_gb300 as bfp
     lib = bfp.load()
-    # hidden 2048, ffn 1024, 16 rows: fits in shared memory but needs 1,787,136 bytes of scratch (> 1.5 MiB);
+    # hidden 2048, ffn 1024, 16 rows: fits in shared memory but needs about 2.18 MB of scratch (> 2 MiB);
     # the size check comes before anything touches the (placeholder) pointers
     h, f = 2048, 1024
     c = bfp.MoeLayerC(h, 256, f, 8, f, bfp.BFP4, 16, None, 16, 16, 16,
