@@ -346,6 +346,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
                 bulk_g2s_hint(dst, sa, b, fb, pol);
                 if (sb) bulk_g2s_hint(dst + b, sb, b, fb, pol);
             }
+            __syncwarp();
             sa += b;
             if (sb) sb += b;
             s_left -= s_ch;
@@ -363,6 +364,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
             [[maybe_unused]] const unsigned long long tw0 = BFP_TRACE_NOW();
             if (!bad && !__all_sync(0xffffffffu, mbar_wait(my_full + cu_slot, cu_par, a.wait_data, vflags)))
                 abort_warp();
+            __syncwarp();  // lanes leave the wait at different polls: reconverge before the MMAs
             tacc[tslot] += BFP_TRACE_NOW() - tw0;
             return my_slots + (size_t)cu_slot * a.slot_bytes;
         };
@@ -389,11 +391,14 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
                 red_release_add(counter, 1u);
                 ok = wait_counter(counter, (uint32_t)a.ncta, a.wait);
             }
-            return !bar_or(1, NC, !ok || bad);
+            const bool r = !bar_or(1, NC, !ok || bad);
+            __syncwarp();  // thread 0 waited alone: reconverge, or later warp collectives run many times slower
+            return r;
         };
 
         // ---- the MoE input rows (x, or bf16(RMSNorm(h)) in stack mode, normalised in place first)
         if (!__all_sync(0xffffffffu, mbar_wait(&ms->stage_full, 0u, a.wait_data, nullptr))) bad = true;
+        __syncwarp();
         STAMP(2);  // stage landed
         uint16_t *const xs = reinterpret_cast<uint16_t *>(stage);
         if (a.norm)
@@ -490,6 +495,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
                     abort_warp();
                     return;
                 }
+                __syncwarp();
                 __threadfence_block();
                 const float *src = a.p1part + ((size_t)c * (NW - 1) + warp) * kP1PartFloats;
 #pragma unroll
@@ -522,6 +528,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
                         last = atomicAdd(&ms->p1cnt[ui], 1) == p1_S - 1;
                     }
                     if (!__shfl_sync(0xffffffffu, last, 0)) return;
+                    __syncwarp();
                     __threadfence_block();
 #pragma unroll
                     for (int r = 0; r < 2; ++r)
@@ -658,6 +665,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
                     STAMP(99);
                 }
                 if (bar_or(3, NR * kWarp, !ok)) bad = true;
+                __syncwarp();  // thread 0 polled alone
                 STAMP(100);
                 STAMP(5);  // every CTA's router rows published
                 // Top-k per row, on the logits every CTA wrote before the router counter (read from
@@ -941,6 +949,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_layer_kernel(const MoeArgs
                     ms->p2nb = nb;
                 }
                 bar_sync(1, NC);
+                __syncwarp();
                 const int nb = ms->p2nb;
                 // every fragment word of the batch, once: a thread takes 4 consecutive values of one
                 // column in one block and writes their hi and lo words (zeros for padding columns and

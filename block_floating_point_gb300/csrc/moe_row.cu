@@ -507,6 +507,30 @@ __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_co
                     key[7] = win ? 0u : key[7];
                 }
                 CSTAMP(89);
+                // ---- 3. the routed weights of this CTA, at once, one lane per copy: lane jj the f-tile unit jj,
+                //         lane s the down rows of slot s
+                {
+                    const int r = u0 + lane - a.nft_s;
+                    const int su = r >= 0 ? r / a.nft : 0;
+                    const int eu = __shfl_sync(0xffffffffu, my_e, min(su, a.K - 1));
+                    const bool mine = lane < nu && r >= 0;
+                    if (mine) copy_unit(a.gu + (int64_t)eu * a.gu_stride + (int64_t)(2 * (r - su * a.nft)) * a.kc_h * a.rec, lane);
+                    const uint32_t issued = __ballot_sync(0xffffffffu, mine);
+                    if (lane == 0) armed_u |= issued;
+                    if (nrg > 0) {
+                        if (lane == 0) mbar_arrive_expect_tx(&ms->bar_p2rt, (uint32_t)(nrg * a.K * a.kc_f * a.rec));
+                        __syncwarp();
+                        if (lane < a.K)
+                            for (int j = 0; j < nrg; ++j) {
+                                const int rg = c + j * a.ncta;
+                                bulk_g2s_hint(w2 + (int64_t)(j * IPR + lane * a.kc_f) * a.rec,
+                                              a.dn + (int64_t)my_e * a.dn_stride + (int64_t)rg * a.kc_f * a.rec,
+                                              (uint32_t)(a.kc_f * a.rec), &ms->bar_p2rt, pol);
+                            }
+                        armed_p2rt = true;
+                    }
+                    __syncwarp();
+                }
                 const float l0 = __shfl_sync(0xffffffffu, my_l, 0);
                 const float p = lane < a.K ? __expf(my_l - l0) : 0.f;
                 const float psum = warp_sum(p);
@@ -522,26 +546,6 @@ __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_co
                 if (lane == 0) ms->wsl[a.K] = __fdividef(1.0f, 1.0f + __expf(-gate_logit));
                 CSTAMP(90);
                 __syncwarp();
-                // ---- 3. the routed weights of this CTA, at once: its f-tile units, then its down rows
-                if (lane == 0) {
-                    for (int jj = 0; jj < nu; ++jj) {
-                        const int r = u0 + jj - a.nft_s;
-                        if (r < 0) continue;
-                        const int s = r / a.nft, ft = r - s * a.nft;
-                        copy_unit(a.gu + (int64_t)ms->esl[s] * a.gu_stride + (int64_t)(2 * ft) * a.kc_h * a.rec, jj);
-                    }
-                    if (nrg > 0) {
-                        armed_p2rt = true;
-                        mbar_arrive_expect_tx(&ms->bar_p2rt, (uint32_t)(nrg * a.K * a.kc_f * a.rec));
-                        for (int s = 0; s < a.K; ++s)
-                            for (int j = 0; j < nrg; ++j) {
-                                const int rg = c + j * a.ncta;
-                                bulk_g2s_hint(w2 + (int64_t)(j * IPR + s * a.kc_f) * a.rec,
-                                              a.dn + (int64_t)ms->esl[s] * a.dn_stride + (int64_t)rg * a.kc_f * a.rec,
-                                              (uint32_t)(a.kc_f * a.rec), &ms->bar_p2rt, pol);
-                            }
-                    }
-                }
                 STAMP(7);
             }
         } else {
@@ -601,7 +605,6 @@ __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_co
             const int slot = r < 0 ? a.K : r / a.nft;
             const int ft = r < 0 ? i : r - slot * a.nft;
             __stcg(a.hw + (int64_t)slot * a.Fmax + ft * 16 + n, tag_word(T, hv));
-            __threadfence();  // push the store out now
         }
         STAMP(9);
         if (nrg == 0) return;
