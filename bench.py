@@ -43,8 +43,7 @@ FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the M=16 layer kernel, from one ncu
-# capture (profiles/moe_layer_m16.md, "Traffic of the current kernel"), valid while the kernel
-# sources hash to src_sha.
+# capture of the same workload, valid while the kernel sources hash to src_sha (null otherwise).
 NCU_TRAFFIC = {"moe_layer_m16": {"bytes_per_launch": 180_546_560, "src_sha": "78fadbe6d6507594"}}
 
 
@@ -72,6 +71,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--instances", type=int, default=3)
+    ap.add_argument("--stack-layers", type=int, default=40)
     ap.add_argument("--seed", type=int, default=20261202)
     ap.add_argument("--quick", action="store_true", help="headline line only (no secondary workloads, no oracle)")
     ap.add_argument("--no-graph", action="store_true")
@@ -163,13 +163,15 @@ def aggregate_throughput(bytes_per_step: float, steps: int, ms: float, device=No
 
 
 # --------------------------------------------------------------------------- workload
-def build_instances(n, seed, device):
+def build_layers(n, seed, device):
+    """n full-size layers with independent seeded weights (layer l: synth.LayerWeights(FULL, seed, layer=l)),
+    each packed on the host and uploaded before the next is drawn."""
     import block_floating_point_gb300 as bfp
     import synth
     spec = synth.FULL
     layers = []
     for i in range(n):
-        lw = synth.LayerWeights(spec, seed, layer=0, instance=i)
+        lw = synth.LayerWeights(spec, seed, layer=i)
 
         def src(e, lw=lw):
             key = synth.SHARED_EXPERT if e == "shared" else e
@@ -359,7 +361,13 @@ def main():
     bfp.load()
     peak, peak_kind = measured_peak()
 
-    spec, layers = build_instances(args.instances, args.seed + 7919 * rank, device)
+    # every layer of the run has its own seeded weights: the headline rotates over the first `instances`, the
+    # one-row line and the decode stacks run over all `stack_layers` of them (about 18 GB resident)
+    n_all = args.instances if args.quick else max(args.instances, args.stack_layers)
+    t_build = time.perf_counter()
+    spec, all_layers = build_layers(n_all, args.seed + 7919 * rank, device)
+    build_s = time.perf_counter() - t_build
+    layers = all_layers[:args.instances]
     R = len(layers)
     M = 16
     xs, xts, ys, idxs = [], [], [], []
@@ -441,7 +449,8 @@ def main():
                                                  + layers[0].hidden * 2) * args.steps * world / (ms * 1e-3) / 1e9,
                    "l2": "inputs larger than L2: each step streams ~180 MB of experts (> 129 MB L2), "
                          f"rotating over {R} independently drawn layer instances",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "layers_built": n_all, "host_build_s": build_s},
         "roofline": {"bound": "hbm", "achieved": kernel_gbs, "peak": peak, "unit": "GB/s",
                      "frac": kernel_gbs / peak, "traffic": traffic,
                      "kernel": "moe_layer_kernel<4,2> (one launch per step)",
@@ -457,21 +466,32 @@ def main():
         sec = {}
         flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
         ksec = max(20, min(200, args.steps))
-        # M=1 on the same instances, each step alone after an L2 flush
-        ws1 = bfp.moe_workspace(layers[0], 1)
-        x1 = [xt[:1].contiguous() for xt in xts]
+        # M=1: one launch per layer back to back (dependent launches in CUDA graphs) over the run's distinct
+        # layers, each with its own row; the 9 experts one row selects differ from layer to layer, and 40
+        # layers' selections (~640 MB) exceed L2, as in single-sequence decode. Also each step alone after an
+        # L2 flush (launch latency included).
+        NL = len(all_layers)
+        ws1 = bfp.moe_workspace(all_layers[0], 1)
+        x1 = [make_x(spec, args.seed + rank, 1, i, device)[1] for i in range(NL)]
         y1 = torch.empty((1, spec.hidden), dtype=torch.float32, device=device)
         b1 = []
-        for i, L in enumerate(layers):
+        for i, L in enumerate(all_layers):
             idx = torch.empty((1, spec.top_k), dtype=torch.int32, device=device)
             bfp.moe_decode_layer(L, x1[i], ws1, y=y1, topk_idx=idx)
             b1.append(union_bytes(L, idx.cpu().numpy()))
-        tot, _ = timed_flushed(lambda i: bfp.moe_decode_layer(layers[i % R], x1[i % R], ws1, y=y1), ksec, 5, flush)
-        us1 = tot * 1e3 / ksec
-        g1 = float(np.mean([b1[i % R] for i in range(ksec)])) / (us1 * 1e-6) / 1e9
+        k1 = 2 * NL * max(1, (ksec + 2 * NL - 1) // (2 * NL))
+        us1 = timed_graph(lambda i: bfp.moe_decode_layer(all_layers[i % NL], x1[i % NL], ws1, y=y1), k1, 2 * NL,
+                          True, group=2 * NL) * 1e3 / k1
+        g1 = float(np.mean(b1)) / (us1 * 1e-6) / 1e9
+        tot, _ = timed_flushed(lambda i: bfp.moe_decode_layer(all_layers[i % R], x1[i % R], ws1, y=y1), ksec, 5, flush)
+        us1f = tot * 1e3 / ksec
+        assert bfp.workspace_status(ws1) == bfp.BFP_OK
         sec["m1"] = {"us_per_layer": us1, "gbs": g1, "pct_of_8tbs": 100 * g1 / NOMINAL_HBM_GBS,
                      "pct_of_measured_copy": 100 * g1 / peak, "bfp_bytes_per_step": float(np.mean(b1)),
-                     "timing": "each step alone after a 256 MB L2 flush, CUDA events"}
+                     "layers": NL, "kernel": "moe_row_kernel<4> (one launch per layer)",
+                     "timing": f"{k1} launches back to back in CUDA graphs over {NL} distinct layers, CUDA events",
+                     "us_alone_after_flush": us1f,
+                     "alone_timing": "each step alone after a 256 MB L2 flush, CUDA events (includes launch latency)"}
         # hot-expert routing at M=16 (logit bias +2.0 on 8 fixed experts), same weights
         import synth
         bias = torch.from_numpy(synth.hot_bias(spec.n_experts, args.seed)).to(device)
@@ -516,40 +536,70 @@ def main():
                                      "us_back_to_back": usb, "launches": 2,
                                      "timing": "us: each call alone after a 256 MB L2 flush; us_back_to_back: "
                                                "consecutive calls in a CUDA graph on L2-resident logits"}
-        # decode stack, 8 rows: 40 MoE layers (the R weight instances in rotation: an instance comes back after
-        # R - 1 other layers, >= 200 MB of other weights, more than L2) + the BFP8 LM head [151936 x 2048],
-        # then the greedy next token; h is updated in place from step to step, as in decoding.
-        nl, m8, vocab = 40, 8, 151936
-        stack = [layers[l % R] for l in range(nl)]
+        # decode stacks over the run's distinct layers (40 by default, ~18 GB of BFP weights resident) + the BFP8
+        # LM head [151936 x 2048], then the greedy next token; h is updated in place from step to step, as in
+        # decoding. 8 rows (config 5) and 1 row (single-sequence decode).
+        nl, vocab = len(all_layers), 151936
+        stack = all_layers
         lm = bfp.DeviceMatrix.from_host(8, vocab, spec.hidden, bfp.encode(8, synth.normal(
             args.seed, synth.stream_id(synth.KIND_LMHEAD), (vocab, spec.hidden), std=synth.W_STD)), device=device)
-        h8 = torch.from_numpy(synth.to_bf16_bits(synth.normal(args.seed, synth.stream_id(synth.KIND_STACK_H),
-                                                              (m8, spec.hidden))).view(np.int16)).to(device)
-        wss = bfp.moe_stack_workspace(stack, lm, m8)
-        lg8 = torch.empty((m8, vocab), dtype=torch.float32, device=device)
-        ws8 = bfp.greedy_workspace(m8, vocab, device)
-        tok8 = torch.empty(m8, dtype=torch.int32, device=device)
-        kst = 10
-        sel = torch.empty((kst, nl, m8, spec.top_k), dtype=torch.int32, device=device)
-        for i in range(3):
-            bfp.moe_stack_decode(stack, lm, h8, wss, logits=lg8, topk_idx=sel[0])
-            bfp.greedy_tokens(lg8, ws8, tok8)
-        es0, es1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        es0.record()
-        for i in range(kst):
-            bfp.moe_stack_decode(stack, lm, h8, wss, logits=lg8, topk_idx=sel[i])
-            bfp.greedy_tokens(lg8, ws8, tok8)
-        es1.record()
-        torch.cuda.synchronize()
-        assert bfp.workspace_status(wss) == bfp.BFP_OK
-        ust = es0.elapsed_time(es1) * 1e3 / kst
-        sa = sel.cpu().numpy()
-        bst = float(np.mean([sum(union_bytes(stack[l], sa[i, l]) for l in range(nl)) for i in range(kst)])) + lm.nbytes
-        nun = float(np.mean([len(np.unique(sa[i, l])) for i in range(kst) for l in range(nl)]))
+        for mst in (8, 1):
+            hst = torch.from_numpy(synth.to_bf16_bits(synth.normal(args.seed, synth.stream_id(synth.KIND_STACK_H),
+                                                                   (mst, spec.hidden))).view(np.int16)).to(device)
+            wss = bfp.moe_stack_workspace(stack, lm, mst)
+            lgs = torch.empty((mst, vocab), dtype=torch.float32, device=device)
+            wsg = bfp.greedy_workspace(mst, vocab, device)
+            toks = torch.empty(mst, dtype=torch.int32, device=device)
+            kst = 10
+            sel = torch.empty((kst, nl, mst, spec.top_k), dtype=torch.int32, device=device)
+            for i in range(3):
+                bfp.moe_stack_decode(stack, lm, hst, wss, logits=lgs, topk_idx=sel[0])
+                bfp.greedy_tokens(lgs, wsg, toks)
+            es0, es1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            es0.record()
+            for i in range(kst):
+                bfp.moe_stack_decode(stack, lm, hst, wss, logits=lgs, topk_idx=sel[i])
+                bfp.greedy_tokens(lgs, wsg, toks)
+            es1.record()
+            torch.cuda.synchronize()
+            assert bfp.workspace_status(wss) == bfp.BFP_OK
+            ust_eager = es0.elapsed_time(es1) * 1e3 / kst
+            # the same step captured once in a CUDA graph and replayed (no host work between launches)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                bfp.moe_stack_decode(stack, lm, hst, wss, logits=lgs)
+                bfp.greedy_tokens(lgs, wsg, toks)
+            for i in range(3):
+                g.replay()
+            torch.cuda.synchronize()
+            es0.record()
+            for i in range(kst):
+                g.replay()
+            es1.record()
+            torch.cuda.synchronize()
+            assert bfp.workspace_status(wss) == bfp.BFP_OK
+            ust = es0.elapsed_time(es1) * 1e3 / kst
+            sa = sel.cpu().numpy()
+            bst = float(np.mean([sum(union_bytes(stack[l], sa[i, l]) for l in range(nl)) for i in range(kst)])) \
+                + lm.nbytes
+            nun = float(np.mean([len(np.unique(sa[i, l])) for i in range(kst) for l in range(nl)]))
+            sec[f"stack_m{mst}_{nl}layers"] = {
+                "us_per_step": ust, "tokens_per_s": mst / (ust * 1e-6), "bfp_bytes_per_step": bst,
+                "gbs": bst / (ust * 1e-6) / 1e9, "pct_of_measured_copy": 100 * bst / (ust * 1e-6) / 1e9 / peak,
+                "union_experts_per_layer": nun, "launches_per_step": nl + 3,
+                "timing": f"{kst} consecutive replays of the step ({nl} layer launches, LM head, 2 greedy launches) "
+                          "captured in one CUDA graph, CUDA events", "us_per_step_eager": ust_eager,
+                "weights": f"{nl} layers with independent seeded weights (no layer repeats within a step); LM head "
+                           f"BFP8 [{vocab} x {spec.hidden}] seeded N(0,0.02)",
+                "layer_kernel": "moe_row_kernel<4>" if mst == 1 else "moe_layer_kernel<4,1>"}
+            del wss, lgs
         # the LM head alone (330 MB, larger than L2: consecutive calls stream it from HBM)
+        m8 = 8
+        x8 = torch.from_numpy(synth.to_bf16_bits(synth.normal(args.seed, synth.stream_id(synth.KIND_STACK_H),
+                                                              (m8, spec.hidden))).view(np.int16)).to(device)
+        lg8 = torch.empty((m8, vocab), dtype=torch.float32, device=device)
         wsl8 = bfp.linear_workspace(lm, m8)
-        x8 = h8.clone()
         for _ in range(3):
             bfp.linear(lm, x8, wsl8, y=lg8)
         el0, el1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -560,13 +610,6 @@ def main():
         el1.record()
         torch.cuda.synchronize()
         usl = el0.elapsed_time(el1) * 1e3 / 20
-        sec["stack_m8_40layers"] = {
-            "us_per_step": ust, "tokens_per_s": m8 / (ust * 1e-6), "bfp_bytes_per_step": bst,
-            "gbs": bst / (ust * 1e-6) / 1e9, "pct_of_measured_copy": 100 * bst / (ust * 1e-6) / 1e9 / peak,
-            "union_experts_per_layer": nun, "launches_per_step": nl + 3,
-            "timing": f"{kst} consecutive steps (40 layer launches, LM head, 2 greedy launches each), CUDA events",
-            "weights": f"{R} independent layer instances in rotation over the 40 layers; LM head BFP8 "
-                       f"[{vocab} x {spec.hidden}] seeded N(0,0.02)"}
         sec["lm_head_bfp8_m8"] = {"us": usl, "gbs": lm.nbytes / (usl * 1e-6) / 1e9,
                                   "pct_of_measured_copy": 100 * lm.nbytes / (usl * 1e-6) / 1e9 / peak,
                                   "bytes": lm.nbytes, "timing": "20 consecutive calls (330 MB each, > L2)"}

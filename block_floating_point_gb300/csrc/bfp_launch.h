@@ -39,6 +39,10 @@ inline dev::WaitCfg wait_cfg() {
     return w;
 }
 
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per (kernel, device, size): the call costs
+// microseconds of host time, which a one-row layer launch cannot afford every time.
+int set_smem_attr(const void *kernel, int smem, const char *what);
+
 // Workspace header: status word at byte 0 (16 bytes reserved).
 constexpr size_t kWsHeader = 256;
 

@@ -52,6 +52,30 @@ int device_info(DeviceInfo *out) {
 }
 
 
+int set_smem_attr(const void *kernel, int smem, const char *what) {
+    struct Entry {
+        const void *k;
+        int device, smem;
+    };
+    static std::mutex mu;
+    static std::vector<Entry> done;
+    int d = 0;
+    cudaError_t e = cudaGetDevice(&d);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> lk(mu);
+    for (const Entry &x : done)
+        if (x.k == kernel && x.device == d && x.smem >= smem) return BFP_OK;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return cuda_fail(e, what);
+    for (Entry &x : done)
+        if (x.k == kernel && x.device == d) {
+            x.smem = smem;
+            return BFP_OK;
+        }
+    done.push_back(Entry{kernel, d, smem});
+    return BFP_OK;
+}
+
 // ----------------------------------------------------------------------------
 // bfp_linear kernel
 // ----------------------------------------------------------------------------
@@ -376,8 +400,9 @@ static int plan_linear(const Geometry &g, int m, LinearPlan *p) {
 template <int FMT, int NGRP>
 static int launch_linear_t(const LinearArgs &a, const LinearPlan &p, cudaStream_t st) {
     auto kern = bfp_linear_kernel<FMT, NGRP>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(bfp_linear)");
+    int rc = set_smem_attr(reinterpret_cast<const void *>(kern), (int)p.smem, "cudaFuncSetAttribute(bfp_linear)");
+    if (rc) return rc;
+    cudaError_t e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.ncta);
     cfg.blockDim = dim3(kLinThreads);

@@ -1322,8 +1322,9 @@ static int plan_moe(const bfp_moe_layer *L, int m, MoePlan *p) {
 template <int FMT, int NGRP>
 static int launch_moe_t(const MoeArgs &a, const MoePlan &p, cudaStream_t st) {
     auto kern = moe_layer_kernel<FMT, NGRP>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(moe_layer)");
+    int rc = set_smem_attr(reinterpret_cast<const void *>(kern), (int)p.smem, "cudaFuncSetAttribute(moe_layer)");
+    if (rc) return rc;
+    cudaError_t e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.ncta);
     cfg.blockDim = dim3(kMoeThreads);

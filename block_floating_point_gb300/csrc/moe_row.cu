@@ -37,6 +37,7 @@
 // of the activation operand is used (column 4 carries the low half of h in the
 // down projection). All waits are bounded and report BFP_ETIMEOUT.
 #include <algorithm>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -897,8 +898,9 @@ static bool plan_row(const bfp_moe_layer *L, const Geometry &gu, const Geometry 
 template <int FMT>
 static int launch_row_t(const RowArgs &a, size_t smem, cudaStream_t st) {
     auto kern = moe_row_kernel<FMT>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(moe_row)");
+    int rc = set_smem_attr(reinterpret_cast<const void *>(kern), (int)smem, "cudaFuncSetAttribute(moe_row)");
+    if (rc) return rc;
+    cudaError_t e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.ncta);
     cfg.blockDim = dim3(kRowThreads);
@@ -934,8 +936,37 @@ int row_layer_launch(const bfp_moe_layer *L, const uint16_t *x, int norm, float 
     make_geometry(L->expert_fmt, 2 * (int64_t)L->ffn, L->hidden, &gu);
     make_geometry(L->expert_fmt, L->hidden, L->ffn, &dn);
     make_geometry(L->expert_fmt, L->hidden, L->shared_ffn, &sdn);
+    // plans depend on the shape and the device only; a one-row launch cannot afford to recompute one
+    struct Cached {
+        int key[8];
+        bool ok;
+        RowPlan plan;
+    };
+    static std::mutex mu;
+    static std::vector<Cached> cache;
+    const int key[8] = {L->hidden, L->n_experts, L->ffn, L->top_k, L->shared_ffn, L->expert_fmt, di.sms, di.smem_optin};
     RowPlan p;
-    if (!plan_row(L, gu, dn, sdn, di.sms, di.smem_optin, &p)) return kRowNotApplicable;
+    bool ok = false, found = false;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        for (const Cached &x : cache)
+            if (std::equal(key, key + 8, x.key)) {
+                ok = x.ok;
+                if (ok) p = x.plan;
+                found = true;
+                break;
+            }
+    }
+    if (!found) {
+        ok = plan_row(L, gu, dn, sdn, di.sms, di.smem_optin, &p);
+        std::lock_guard<std::mutex> lk(mu);
+        Cached x;
+        std::copy(key, key + 8, x.key);
+        x.ok = ok;
+        x.plan = p;
+        cache.push_back(x);
+    }
+    if (!ok) return kRowNotApplicable;
     RowArgs a;
     a.H = L->hidden;
     a.E = L->n_experts;
