@@ -236,3 +236,75 @@ def test_one_row_bounded_wait_reports_timeout_and_recovers(tiny):
     torch.cuda.synchronize()
     assert bfp.workspace_status(ws) == bfp.BFP_OK
     assert_close(y.cpu().numpy(), case.oracle_layer(x)[0], "one row, after recovery")
+
+
+# ---------------------------------------------------------------- the benchmark's 40-layer decode stack
+STACK_SEED = 20261202  # bench.py's default seed; its layer l is LayerWeights(FULL, STACK_SEED, layer=l)
+
+
+@pytest.mark.parametrize("layer", [0, 17, 39])
+def test_layers_of_the_benchmarked_stack(layer):
+    """Three of the 40 independently seeded full-size layers the benchmark's decode stack runs, each on
+    RMS-normalised bf16 rows (the input the stack feeds a layer), 8 rows (general kernel) and 1 row
+    (one-row kernel): selection bit-exact, outputs within tolerance of the oracle."""
+    case = LayerCase(synth.FULL, seed=STACK_SEED, layer=layer)
+    dl = case.device_layer()
+    check(case, dl, 8, rms_norm=True, row_seed0=3000 + 100 * layer)
+    check(case, dl, 1, rms_norm=True, row_seed0=5000 + 100 * layer)
+
+
+# ---------------------------------------------------------------- error-compensated (GPTQ-style) experts
+def test_gptq_encoded_layer_matches_oracle():
+    """A layer whose experts the library encoded with error compensation (bfp_encode_gate_up_gptq,
+    bfp_encode_gptq) against the oracle's layer on the oracle's own gptq_encode fields of the same fp32
+    weights and calibration inputs: selection bit-exact, outputs within tolerance, 1 and 6 rows."""
+    import oracle
+    spec = synth.MoESpec(hidden=512, n_experts=32, ffn=128, top_k=4, shared_ffn=128)
+    lw = synth.LayerWeights(spec, 515)
+
+    def calib(seed, t, k):  # correlated synthetic calibration inputs (the recipe of the host GPTQ tests)
+        z = synth.normal(seed, 1, (t, k)).astype(np.float64)
+        a = np.eye(k) + 3.0 * synth.normal(seed, 2, (k, k)).astype(np.float64) / np.sqrt(k)
+        return ((z @ a) * np.exp(0.5 * synth.normal(seed, 3, (k,)).astype(np.float64))).astype(np.float32)
+
+    x_cal, h_cal = calib(516, 2048, spec.hidden), calib(517, 1024, spec.ffn)
+    u_in, u_mid = bfp.gptq_factor(x_cal), bfp.gptq_factor(h_cal)
+    uo_in, uo_mid = oracle.gptq_factor(x_cal), oracle.gptq_factor(h_cal)
+
+    def source(e):
+        key = synth.SHARED_EXPERT if e == "shared" else e
+        return lw.gate(key), lw.up(key), lw.down(key)
+
+    class GptqExpert(oracle.EncodedExpert):  # the oracle's expert evaluation on its own GPTQ fields
+        def __init__(self, fmt, g, u, d):
+            self.fmt, (self.ffn, self.hidden) = fmt, g.shape
+            self.g, self.u = oracle.gptq_encode(fmt, g, uo_in), oracle.gptq_encode(fmt, u, uo_in)
+            self.d = oracle.gptq_encode(fmt, d, uo_mid)
+
+    class GptqCache(oracle.ExpertCache):
+        def __call__(self, e):
+            if e not in self._c:
+                self._c[e] = GptqExpert(self.fmt, *self.source(e))
+            return self._c[e]
+
+    router, sgate = lw.router_bf16(), lw.shared_gate_bf16()
+    layer = bfp.MoELayer.from_source(spec.hidden, spec.n_experts, spec.ffn, spec.top_k, spec.shared_ffn, bfp.BFP4,
+                                     router, sgate, source, lambda: source("shared"),
+                                     gptq_factors=lambda e: (u_in, u_mid), shared_gptq_factors=lambda: (u_in, u_mid))
+    plain = bfp.MoELayer.from_source(spec.hidden, spec.n_experts, spec.ffn, spec.top_k, spec.shared_ffn, bfp.BFP4,
+                                     router, sgate, source, lambda: source("shared"))
+    assert not torch.equal(layer.experts_gate_up, plain.experts_gate_up)  # compensation changed the codes
+    experts = GptqCache(bfp.BFP4, source)
+    for m, rs in ((1, 0), (6, 10)):
+        rows = []
+        while len(rows) < m:
+            x = synth.activation_row(515, rs, spec.hidden, True)
+            rs += 1
+            if oracle.topk_margin(oracle.router_logits(router, x[None])[0], spec.top_k) >= 1e-3:
+                rows.append(x)
+        x = np.stack(rows)
+        y, idx, w, _, _ = run_layer(layer, x, m)
+        y_ref, idx_ref, w_ref = oracle.moe_layer(x, router, sgate, experts, spec.top_k)
+        assert np.array_equal(idx.cpu().numpy(), idx_ref)
+        assert_close(w.cpu().numpy(), w_ref, "routing weights")
+        assert_close(y.cpu().numpy(), y_ref, f"GPTQ-encoded layer, {m} rows")

@@ -204,6 +204,24 @@ def test_rmsnorm_and_residual():
     assert np.array_equal(oracle.residual_bf16(h, y), bf16((hf + y).astype(np.float32)))
 
 
+def test_rmsnorm_and_residual_closed_forms():
+    """Values fixed by hand, independent of the formula's code: a constant row normalises to 1; a
+    one-hot row of width 16 gives sqrt(16) = 4 (the mean divides by the width, not width - 1, which
+    would give 3.875); a row of 2^-12 shows eps inside the square root (2^-12 / sqrt(2^-24 + 1e-6)
+    = 0.23717 -> bf16 0.237305; eps outside would give 0.99609, no eps 1.0); the residual rounds
+    h + y to nearest bf16 with ties to even."""
+    h = bf16(np.full((1, 256), 3.0, np.float32))
+    assert np.all(f32_of(oracle.rmsnorm_bf16(h)) == 1.0)
+    h = bf16(np.eye(1, 16, dtype=np.float32))
+    t = f32_of(oracle.rmsnorm_bf16(h))
+    assert t[0, 0] == 4.0 and np.all(t[0, 1:] == 0.0)
+    h = bf16(np.full((1, 64), 2.0 ** -12, np.float32))
+    assert np.all(f32_of(oracle.rmsnorm_bf16(h)) == np.float32(0.2373046875))
+    one = bf16(np.array([[1.0, 1.0078125, 1.0, -1.0]], np.float32))
+    y = np.array([[2.0 ** -8, 2.0 ** -8, 2.0 ** -8 + 2.0 ** -20, 0.5]], np.float32)
+    assert list(f32_of(oracle.residual_bf16(one, y))[0]) == [1.0, 1.015625, 1.0078125, -0.5]
+
+
 def test_greedy_tokens_brute_force_and_special_cases():
     # Brute force: the first index whose value no other non-NaN value exceeds.
     rng = np.random.default_rng(91)

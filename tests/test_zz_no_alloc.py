@@ -5,8 +5,9 @@ all device memory through its own allocator, or a latency-critical path where
 an allocation could synchronise the device. moe_decode_layer_static takes no
 workspace and uses the library's built-in 2 MiB device scratch array instead.
 This test calls it through the C-ABI and checks its outputs against the
-workspace entry point (moe_decode_layer) on two calls in a row, within the
-tolerance the other GPU tests use. It lives in a file that pytest collects
+workspace entry point (moe_decode_layer) and against the oracle, on two calls
+in a row, within the tolerance the other GPU tests use (16 rows and 1 row:
+the general kernel and the one-row kernel). It lives in a file that pytest collects
 last, and it is self-contained so it also passes alone in a fresh process.
 """
 import numpy as np
@@ -19,7 +20,7 @@ torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("spec,m,seed", [(synth.TINY, 3, 611), (synth.FULL, 16, 612)])
+@pytest.mark.parametrize("spec,m,seed", [(synth.TINY, 3, 611), (synth.FULL, 16, 612), (synth.FULL, 1, 613)])
 def test_static_scratch_layer_matches_workspace_layer(spec, m, seed):
     import block_floating_point_gb300 as bfp
     assert torch.cuda.is_available(), "GPU tests need CUDA"
@@ -45,6 +46,10 @@ def test_static_scratch_layer_matches_workspace_layer(spec, m, seed):
         torch.cuda.synchronize()
         assert torch.equal(idx, idx_ref), f"call {call}: expert selection differs"
         assert_close(y.cpu().numpy(), y_ref.cpu().numpy(), f"call {call}: static-scratch layer output")
+        # and directly against the oracle (the tolerance of every other layer test)
+        y_or, idx_or, _ = case.oracle_layer(x)
+        assert np.array_equal(idx.cpu().numpy(), idx_or), f"call {call}: selection differs from the oracle's"
+        assert_close(y.cpu().numpy(), y_or, f"call {call}: static-scratch layer against the oracle")
 
 
 def test_static_scratch_rejects_layers_beyond_its_size():
