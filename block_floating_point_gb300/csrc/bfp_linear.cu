@@ -81,6 +81,7 @@ int set_smem_attr(const void *kernel, int smem, const char *what) {
 // ----------------------------------------------------------------------------
 constexpr int kLinWarps = 16;
 constexpr int kLinThreads = kLinWarps * 32;
+constexpr int kLinInplaceRegs = 8;  // fragment pairs per thread and group when four groups are built in place
 
 struct LinearArgs {
     const uint8_t *w;
@@ -102,8 +103,8 @@ struct LinearArgs {
 struct LinMisc {
     alignas(16) float esc[kLinWarps][rec_scale_floats<4, 1>()];  // per-warp block scales (mma_records)
     uint64_t stage_full;                                          // the activation rows landed
-    int shift[16];
-    float inv[16];
+    int shift[32];
+    float inv[32];
     float2 red[kLinWarps];  // activation row statistics per (row, segment)
     int cnt[kLinWarps];     // parts finished per row group of a split
     int flags[4];        // [0] abort
@@ -118,12 +119,13 @@ __global__ void __launch_bounds__(kLinThreads, 1) bfp_linear_kernel(const Linear
     constexpr int MB = FMT == 4 ? 3 : 7;
     constexpr int CB = FMT == 4 ? 4 : 2;
     uint32_t *frag = reinterpret_cast<uint32_t *>(smem);
-    float *scr = reinterpret_cast<float *>(smem + a.frag_bytes);
     LinMisc *lm = reinterpret_cast<LinMisc *>(smem + a.frag_bytes + a.scr_bytes);
     const size_t bar_off = align_up(a.frag_bytes + a.scr_bytes + sizeof(LinMisc), 16);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + bar_off);  // [NW][nsw]
     uint8_t *ring = smem + align_up(bar_off + 8 * NW * a.nsw, 128);
-    uint8_t *stage = ring + a.stage_off;  // the activation rows, before the streams start
+    // the activation rows, before the streams start: in the ring's tail, or (four activation groups) in the
+    // fragment area itself, turned into fragments in place
+    uint8_t *stage = NGRP == 4 ? smem : ring + a.stage_off;
     volatile int *flags = lm->flags;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -204,13 +206,16 @@ __global__ void __launch_bounds__(kLinThreads, 1) bfp_linear_kernel(const Linear
     }
     // The weights do not depend on the activations: a warp whose slots lie below the stage starts
     // its stream before the rows land.
-    const bool early = (size_t)(warp + 1) * a.nsw * a.slot_bytes <= (size_t)a.stage_off;
+    const bool early = NGRP == 4 || (size_t)(warp + 1) * a.nsw * a.slot_bytes <= (size_t)a.stage_off;
     if (early)
         for (int i = 0; i < a.nsw; ++i) issue_next();
     if (!__all_sync(0xffffffffu, mbar_wait(&lm->stage_full, 0u, a.wait, nullptr))) bad = true;
     uint16_t *const xs = reinterpret_cast<uint16_t *>(stage);
     act_rows_prepare<NC>(xs, a.k, a.m, a.k, a.norm != 0, a.eps, lm->shift, lm->inv, lm->red, 1, warp, lane);
-    act_rows_frags<NC>(xs, a.k, a.m, a.k, a.kbp, NGRP, lm->shift, frag, 1, tid, warp, lane);
+    if constexpr (NGRP == 4)
+        act_rows_frags_inplace<NC>(xs, a.k, a.m, a.k, a.kbp, lm->shift, frag, 1, tid);
+    else
+        act_rows_frags<NC>(xs, a.k, a.m, a.k, a.kbp, NGRP, lm->shift, frag, 1, tid, warp, lane);
     // every warp is past its reads of the stage (the barrier ending act_rows_frags): the rest
     // of the streams may start
     if (!early)
@@ -239,8 +244,12 @@ __global__ void __launch_bounds__(kLinThreads, 1) bfp_linear_kernel(const Linear
         if (bad) continue;
         if (S > 1) {
             // part of a split row group: store the tile; the last part to finish adds the parts in
-            // order (items < NW then: one scratch tile per item) and writes the outputs
-            float *mine = scr + (size_t)it * TILE;
+            // order and writes the outputs. Items < NW then (item it is warp it's only one), so a warp's
+            // own slots are free once its item is done and hold its tile.
+            auto part_tile = [&](int w) {
+                return reinterpret_cast<float *>(ring + (size_t)w * a.nsw * a.slot_bytes);
+            };
+            float *mine = part_tile(it);
 #pragma unroll
             for (int g = 0; g < NGRP; ++g)
 #pragma unroll
@@ -258,7 +267,7 @@ __global__ void __launch_bounds__(kLinThreads, 1) bfp_linear_kernel(const Linear
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     float v = 0.f;
-                    for (int q = 0; q < S; ++q) v += scr[(size_t)((it / S) * S + q) * TILE + (g * 4 + i) * kWarp + lane];
+                    for (int q = 0; q < S; ++q) v += part_tile((it / S) * S + q)[(g * 4 + i) * kWarp + lane];
                     acc[0][g][i] = v;
                 }
         }
@@ -367,17 +376,21 @@ static int plan_linear(const Geometry &g, int m, LinearPlan *p) {
     DeviceInfo di;
     int rc = device_info(&di);
     if (rc) return rc;
-    p->ngrp = m > 8 ? 2 : 1;
+    p->ngrp = m > 16 ? 4 : (m > 8 ? 2 : 1);
     const int kbp = (int)(g.kc * g.cb);
     p->frag_bytes = p->ngrp * kbp * 32 * 8;
+    // four groups: the fragments are built in place from the staged rows, group by group, each thread
+    // holding its share of a group (kLinInplaceRegs fragment pairs) in registers
+    if (p->ngrp == 4 && (int64_t)kbp * 32 > (int64_t)kLinThreads * kLinInplaceRegs)
+        return fail(BFP_ESHAPE, "more than 16 rows needs k <= 2048");
     // grid: the same number of whole row groups per CTA (at most one CTA per SM)
     const int64_t per = (g.ng + di.sms - 1) / di.sms;
     p->ncta = (int)((g.ng + per - 1) / per);
     // parts per row group: every warp gets one when a CTA has fewer row groups than warps
     p->S = 1;
     while (per * p->S * 2 <= kLinWarps && p->S * 2 <= g.kc) p->S *= 2;
-    p->scr_bytes = p->S > 1 ? (int)align_up((size_t)kLinWarps * p->ngrp * 128 * 4, 128) : 0;
-    const size_t stage = align_up((size_t)m * g.k * 2, 128);
+    p->scr_bytes = 0;  // the parts of a split row group meet in their warps' own slots
+    const size_t stage = p->ngrp == 4 ? 0 : align_up((size_t)m * g.k * 2, 128);
     const size_t base = align_up((size_t)p->frag_bytes + p->scr_bytes + sizeof(LinMisc), 16);
     const int64_t avail = (int64_t)di.smem_optin - (int64_t)base - 128;
     // chunks of up to 8 records, smaller when two slots per warp would not fit
@@ -386,7 +399,8 @@ static int plan_linear(const Geometry &g, int m, LinearPlan *p) {
         p->chw = (int)std::min<int64_t>(chw, g.kc);
         p->slot_bytes = p->chw * g.rec;
         p->nsw = (int)std::min<int64_t>(4, avail / ((int64_t)kLinWarps * (p->slot_bytes + 8)));
-        if (p->nsw >= 2) break;
+        if (p->nsw >= 2 && (int64_t)p->nsw * p->slot_bytes >= (int64_t)p->ngrp * 128 * 4) break;
+        p->nsw = 0;
     }
     if (p->nsw < 2) return fail(BFP_ESHAPE, "k too large for the activation fragments in shared memory");
     const size_t ring = (size_t)kLinWarps * p->nsw * p->slot_bytes;
@@ -425,7 +439,7 @@ int linear_launch_ex(const bfp_matrix *w, const uint16_t *x, int m, int64_t ldx,
     Geometry g;
     int rc = check_matrix(w, &g, true);
     if (rc) return rc;
-    if (m < 1 || m > 16) return fail(BFP_ESHAPE, "m must be in [1, 16]");
+    if (m < 1 || m > 32) return fail(BFP_ESHAPE, "m must be in [1, 32]");
     if (!x || (!y && !y_bf16)) return fail(BFP_EINVAL, "null x or no output");
     if (ldx < g.k || ldx % 8 != 0) return fail(BFP_EALIGN, "ldx must be >= k and a multiple of 8");
     if (ldy < g.n) return fail(BFP_EINVAL, "ldy < n");
@@ -462,8 +476,10 @@ int linear_launch_ex(const bfp_matrix *w, const uint16_t *x, int m, int64_t ldx,
     a.stage_off = p.stage_off;
     a.wait = WaitCfg{kDefaultWaitIters, kDefaultWaitNanos};  // only this CTA's own copies are waited on
     if (g.fmt == BFP_FMT_BFP4)
-        return p.ngrp == 1 ? launch_linear_t<4, 1>(a, p, st) : launch_linear_t<4, 2>(a, p, st);
-    return p.ngrp == 1 ? launch_linear_t<8, 1>(a, p, st) : launch_linear_t<8, 2>(a, p, st);
+        return p.ngrp == 1 ? launch_linear_t<4, 1>(a, p, st)
+                           : p.ngrp == 2 ? launch_linear_t<4, 2>(a, p, st) : launch_linear_t<4, 4>(a, p, st);
+    return p.ngrp == 1 ? launch_linear_t<8, 1>(a, p, st)
+                       : p.ngrp == 2 ? launch_linear_t<8, 2>(a, p, st) : launch_linear_t<8, 4>(a, p, st);
 }
 
 // Bytes of the workspace after its header (the kernel keeps everything in shared memory: none).
@@ -471,7 +487,7 @@ int linear_ws_body_bytes(const bfp_matrix *w, int m, size_t *bytes) {
     Geometry g;
     int rc = check_matrix(w, &g, false);
     if (rc) return rc;
-    if (m < 1 || m > 16) return fail(BFP_ESHAPE, "m must be in [1, 16]");
+    if (m < 1 || m > 32) return fail(BFP_ESHAPE, "m must be in [1, 32]");
     LinearPlan p;
     rc = plan_linear(g, m, &p);
     if (rc) return rc;

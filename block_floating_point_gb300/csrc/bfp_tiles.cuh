@@ -351,5 +351,45 @@ __device__ __noinline__ void act_rows_frags(const uint16_t *x, int64_t ldx, int 
     bar_sync(bar, NC);
 }
 
+// act_rows_frags for four activation groups (32 rows) with the rows staged in the fragment area itself
+// (row r at x + r * ldx, bf16; ldx = k). Group g's fragments (kbp blocks) take bytes [g F, (g + 1) F),
+// F = kbp * 256, and its staged rows [g S, (g + 1) S), S = 16 k <= F: going from the last group down,
+// a group's fragments never cover the staged rows of a group still to come. Per group, every thread
+// reads its share (at most 8 fragment pairs: kbp <= 128) into registers, the threads meet at barrier
+// `bar`, and the pairs are written in place. Same values and layout as act_rows_frags with ngrp = 4.
+// Ends with barrier `bar`.
+template <int NC>
+__device__ __noinline__ void act_rows_frags_inplace(const uint16_t *x, int64_t ldx, int m, int k, int kbp,
+                                                    const int *shift, uint32_t *frag, int bar, int tid) {
+    constexpr int KR = 8;
+    const int kb = k / 16, per_group = kbp * kWarp;
+    uint2 *f2 = reinterpret_cast<uint2 *>(frag);
+    for (int grp = 3; grp >= 0; --grp) {
+        uint2 v[KR];
+#pragma unroll
+        for (int j = 0; j < KR; ++j) {
+            const int e = tid + j * NC;  // pair e of the group: block e / 32, position e % 32
+            v[j] = make_uint2(0u, 0u);
+            const int b = e / kWarp, l = (e - b * kWarp) ^ frag_swz(b);  // the lane whose pair sits there
+            const int r = 8 * grp + (l >> 2), t = l & 3;
+            if (e < per_group && r < m && b < kb) {
+                const uint16_t *xr = x + (int64_t)r * ldx + 16 * b + 2 * t;
+                const uint32_t w0 = *reinterpret_cast<const uint32_t *>(xr);
+                const uint32_t w1 = *reinterpret_cast<const uint32_t *>(xr + 8);
+                const float sc = pow2f(shift[r]);
+                v[j] = make_uint2(pack_half2(bf16_bits_to_f32(w0 & 0xFFFFu) * sc, bf16_bits_to_f32(w0 >> 16) * sc),
+                                  pack_half2(bf16_bits_to_f32(w1 & 0xFFFFu) * sc, bf16_bits_to_f32(w1 >> 16) * sc));
+            }
+        }
+        bar_sync(bar, NC);
+#pragma unroll
+        for (int j = 0; j < KR; ++j) {
+            const int e = tid + j * NC;
+            if (e < per_group) f2[(int64_t)grp * per_group + e] = v[j];
+        }
+    }
+    bar_sync(bar, NC);
+}
+
 }  // namespace dev
 }  // namespace bfp

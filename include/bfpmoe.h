@@ -194,13 +194,16 @@ int bfp_linear_workspace_size(const bfp_matrix *w, int m, size_t *bytes);
 
 /*
  * Dense BFP decode projection (P1 "Precision as served": dense projections and
- * LM head in BFP8; P4 "Multi-user decode": all rows in one weight pass):
+ * LM head in BFP8; P4 "Multi-user decode": all rows in one weight pass; P4
+ * "What changed in this release (s27v6)": up to 32 rows in one tile row):
  *     y[r][o] = sum_j x[r][j] * W[o][j],   r < m, o < n,
  * x bf16 [m x k] (device, row stride ldx elements, ldx % 8 == 0), fp32
  * accumulation. y (nullable) receives fp32 [m x n], y_bf16 (nullable) the
  * round-to-nearest-even bf16 of the same fp32 values; both row stride ldy
- * elements. At least one output must be given. 1 <= m <= 16. W in device
- * memory. ws: bfp_linear_workspace_size bytes (device).
+ * elements. At least one output must be given. 1 <= m <= 32 (every weight
+ * is read from HBM once for all m rows); m > 16 needs k <= 2048
+ * (BFP_ESHAPE otherwise). W in device memory. ws: bfp_linear_workspace_size
+ * bytes (device).
  */
 int bfp_linear(const bfp_matrix *w, const uint16_t *x, int m, int64_t ldx, float *y, uint16_t *y_bf16, int64_t ldy,
                void *ws, size_t ws_bytes, bfp_stream_t stream);

@@ -49,6 +49,9 @@ LINEAR_CASES = [
     (8, 8192, 2048, 1), (8, 8192, 2048, 8), (8, 8192, 2048, 16),   # dense BFP8 projection y[M x 8192] = x W^T
     (4, 512, 2048, 1), (4, 512, 2048, 16),
     (8, 37, 96, 3), (4, 37, 96, 9), (8, 130, 2048, 16), (4, 16, 16, 1), (8, 2000, 1024, 5),
+    # up to 32 rows in one weight pass (four activation groups, fragments built in place)
+    (8, 8192, 2048, 17), (8, 8192, 2048, 24), (8, 8192, 2048, 32), (4, 512, 2048, 32), (8, 37, 96, 29),
+    (8, 130, 2048, 32), (4, 2000, 1024, 20),
 ]
 
 
@@ -85,9 +88,14 @@ def test_linear_matches_oracle(fmt, n, k, m):
 def test_linear_rejects_bad_arguments():
     mat = bfp.DeviceMatrix.from_host(8, 64, 64, bfp.encode(8, synth.normal(1, 1, (64, 64), std=0.02)))
     ws = bfp.linear_workspace(mat, 1)
-    x = torch.zeros((17, 64), dtype=torch.int16, device="cuda")
+    x = torch.zeros((33, 64), dtype=torch.int16, device="cuda")
     with pytest.raises(bfp.BFPError) as ei:
         bfp.linear(mat, x, ws)
+    assert ei.value.code == bfp.BFP_ESHAPE
+    # more than 16 rows keeps every fragment in registers while they are built: k <= 2048
+    wide = bfp.DeviceMatrix.from_host(8, 16, 2064, bfp.encode(8, synth.normal(1, 2, (16, 2064), std=0.02)))
+    with pytest.raises(bfp.BFPError) as ei:
+        bfp.linear_workspace(wide, 17)
     assert ei.value.code == bfp.BFP_ESHAPE
     with pytest.raises(bfp.BFPError) as ei:
         bfp.linear(mat, x[:2], ws[:64])
