@@ -547,20 +547,18 @@ def main():
             hst = torch.from_numpy(synth.to_bf16_bits(synth.normal(args.seed, synth.stream_id(synth.KIND_STACK_H),
                                                                    (mst, spec.hidden))).view(np.int16)).to(device)
             wss = bfp.moe_stack_workspace(stack, lm, mst)
-            lgs = torch.empty((mst, vocab), dtype=torch.float32, device=device)
-            wsg = bfp.greedy_workspace(mst, vocab, device)
             toks = torch.empty(mst, dtype=torch.int32, device=device)
             kst = 10
             sel = torch.empty((kst, nl, mst, spec.top_k), dtype=torch.int32, device=device)
+            # one step: the stack, then the greedy next token taken in the LM head's epilogue (the logits are
+            # not written out)
             for i in range(3):
-                bfp.moe_stack_decode(stack, lm, hst, wss, logits=lgs, topk_idx=sel[0])
-                bfp.greedy_tokens(lgs, wsg, toks)
+                bfp.moe_stack_decode_greedy(stack, lm, hst, wss, tokens=toks, topk_idx=sel[0])
             es0, es1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             torch.cuda.synchronize()
             es0.record()
             for i in range(kst):
-                bfp.moe_stack_decode(stack, lm, hst, wss, logits=lgs, topk_idx=sel[i])
-                bfp.greedy_tokens(lgs, wsg, toks)
+                bfp.moe_stack_decode_greedy(stack, lm, hst, wss, tokens=toks, topk_idx=sel[i])
             es1.record()
             torch.cuda.synchronize()
             assert bfp.workspace_status(wss) == bfp.BFP_OK
@@ -568,8 +566,7 @@ def main():
             # the same step captured once in a CUDA graph and replayed (no host work between launches)
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
-                bfp.moe_stack_decode(stack, lm, hst, wss, logits=lgs)
-                bfp.greedy_tokens(lgs, wsg, toks)
+                bfp.moe_stack_decode_greedy(stack, lm, hst, wss, tokens=toks)
             for i in range(3):
                 g.replay()
             torch.cuda.synchronize()
@@ -587,13 +584,14 @@ def main():
             sec[f"stack_m{mst}_{nl}layers"] = {
                 "us_per_step": ust, "tokens_per_s": mst / (ust * 1e-6), "bfp_bytes_per_step": bst,
                 "gbs": bst / (ust * 1e-6) / 1e9, "pct_of_measured_copy": 100 * bst / (ust * 1e-6) / 1e9 / peak,
-                "union_experts_per_layer": nun, "launches_per_step": nl + 3,
-                "timing": f"{kst} consecutive replays of the step ({nl} layer launches, LM head, 2 greedy launches) "
-                          "captured in one CUDA graph, CUDA events", "us_per_step_eager": ust_eager,
+                "union_experts_per_layer": nun, "launches_per_step": nl + 1,
+                "timing": f"{kst} consecutive replays of the step ({nl} layer launches, then the LM head with the "
+                          "greedy token in its epilogue) captured in one CUDA graph, CUDA events",
+                "us_per_step_eager": ust_eager,
                 "weights": f"{nl} layers with independent seeded weights (no layer repeats within a step); LM head "
                            f"BFP8 [{vocab} x {spec.hidden}] seeded N(0,0.02)",
                 "layer_kernel": "moe_row_kernel<4>" if mst == 1 else "moe_layer_kernel<4,1>"}
-            del wss, lgs
+            del wss
         # the LM head alone (330 MB, larger than L2: consecutive calls stream it from HBM)
         m8 = 8
         x8 = torch.from_numpy(synth.to_bf16_bits(synth.normal(args.seed, synth.stream_id(synth.KIND_STACK_H),
@@ -610,9 +608,21 @@ def main():
         el1.record()
         torch.cuda.synchronize()
         usl = el0.elapsed_time(el1) * 1e3 / 20
+        tk8 = torch.empty(m8, dtype=torch.int32, device=device)
+        for _ in range(3):
+            bfp.linear_greedy(lm, x8, wsl8, tokens=tk8)
+        torch.cuda.synchronize()
+        el0.record()
+        for _ in range(20):
+            bfp.linear_greedy(lm, x8, wsl8, tokens=tk8)
+        el1.record()
+        torch.cuda.synchronize()
+        uslg = el0.elapsed_time(el1) * 1e3 / 20
         sec["lm_head_bfp8_m8"] = {"us": usl, "gbs": lm.nbytes / (usl * 1e-6) / 1e9,
                                   "pct_of_measured_copy": 100 * lm.nbytes / (usl * 1e-6) / 1e9 / peak,
-                                  "bytes": lm.nbytes, "timing": "20 consecutive calls (330 MB each, > L2)"}
+                                  "bytes": lm.nbytes, "timing": "20 consecutive calls (330 MB each, > L2)",
+                                  "us_with_greedy_token_no_logits": uslg,
+                                  "gbs_with_greedy_token": lm.nbytes / (uslg * 1e-6) / 1e9}
         # decode attention over a BFP KV cache, one query token: the 35B card's cache (2 KV heads x 256,
         # BFP8 K and V, 16 query heads) and the 27B card's bfp8_v4r cache (4 KV heads x 256, BFP8 K,
         # Hadamard-rotated BFP4 V, 24 query heads); caches of 128K tokens (> L2) timed back to back

@@ -69,12 +69,14 @@ SIGNATURES = {
     "bfp_unpack_device": [_MP, _P, _P],
     "bfp_linear_workspace_size": [_MP, _I, ctypes.POINTER(_SZ)],
     "bfp_linear": [_MP, _P, _I, _I64, _P, _P, _I64, _P, _SZ, _P],
+    "bfp_linear_greedy": [_MP, _P, _I, _I64, _P, _I64, _P, _P, _SZ, _P],
     "moe_workspace_size": [_LP, _I, ctypes.POINTER(_SZ)],
     "bfp_workspace_init": [_P, _SZ, _P],
     "moe_decode_layer": [_LP, _P, _I, _P, _P, _P, _P, _SZ, _P],
     "moe_decode_layer_static": [_LP, _P, _I, _P, _P, _P, _P],
     "moe_stack_workspace_size": [_LP, _I, _MP, _I, ctypes.POINTER(_SZ)],
     "moe_stack_decode": [_LP, _I, _MP, _P, _I, _P, _P, _P, _SZ, _P],
+    "moe_stack_decode_greedy": [_LP, _I, _MP, _P, _I, _P, _P, _P, _P, _SZ, _P],
     "bfp_greedy_workspace_size": [_I, _I64, ctypes.POINTER(_SZ)],
     "bfp_greedy_tokens": [_P, _I, _I64, _I64, _P, _P, _SZ, _P],
     "bfp_kv_cache_size": [_I, _I, _I, _I64, ctypes.POINTER(_SZ), ctypes.POINTER(_SZ)],
@@ -310,6 +312,20 @@ def linear(mat: DeviceMatrix, x, ws, y=None, y_bf16=None, stream=None):
     return y if y is not None else y_bf16
 
 
+def linear_greedy(mat: DeviceMatrix, x, ws, tokens=None, y=None, stream=None):
+    """Greedy next token per row of y = x W^T, taken in the projection's epilogue (bfp_linear_greedy): int32 [m];
+    y (optional fp32 [m, n] CUDA tensor) also receives the outputs."""
+    import torch
+    m = x.shape[0]
+    if tokens is None:
+        tokens = torch.empty(m, dtype=torch.int32, device=x.device)
+    ldy = y.stride(0) if y is not None else mat.n
+    c = mat.c()
+    _check(load().bfp_linear_greedy(ctypes.byref(c), _ptr(x), m, x.stride(0), _ptr(y), ldy, _ptr(tokens), _ptr(ws),
+                                    ws.numel(), _stream(stream)), "bfp_linear_greedy")
+    return tokens
+
+
 # ----------------------------------------------------------------------------- MoE layer
 class MoELayer:
     """Device-resident weights of one MoE decode layer (all BFP experts packed, bf16 router/gate)."""
@@ -466,6 +482,24 @@ def moe_stack_decode(layers, lm_head: DeviceMatrix, h, ws, logits=None, topk_idx
     _check(load().moe_stack_decode(arr, len(layers), ctypes.byref(c), _ptr(h), m, _ptr(logits), _ptr(topk_idx),
                                    _ptr(ws), ws.numel(), _stream(stream)), "moe_stack_decode")
     return logits
+
+
+def moe_stack_decode_greedy(layers, lm_head: DeviceMatrix, h, ws, tokens=None, logits=None, topk_idx=None,
+                            stream=None):
+    """The decode stack with the greedy next token taken in the LM head's epilogue: int32 [m] tokens; logits
+    (optional fp32 [m, vocab] CUDA tensor) are written only when given."""
+    import torch
+    m = h.shape[0]
+    if tokens is None:
+        tokens = torch.empty(m, dtype=torch.int32, device=h.device)
+    arr = _layers_array(layers)
+    c = lm_head.c()
+    if topk_idx is not None and topk_idx.numel() < m * sum(L.top_k for L in layers):
+        raise ValueError("topk_idx holds fewer than m * sum(top_k) entries")
+    _check(load().moe_stack_decode_greedy(arr, len(layers), ctypes.byref(c), _ptr(h), m, _ptr(logits),
+                                          _ptr(tokens), _ptr(topk_idx), _ptr(ws), ws.numel(), _stream(stream)),
+           "moe_stack_decode_greedy")
+    return tokens
 
 
 # ----------------------------------------------------------------------------- greedy next token

@@ -81,6 +81,7 @@ int set_smem_attr(const void *kernel, int smem, const char *what) {
 // ----------------------------------------------------------------------------
 constexpr int kLinWarps = 16;
 constexpr int kLinThreads = kLinWarps * 32;
+constexpr int kLinMaxRows = 32;
 constexpr int kLinInplaceRegs = 8;  // fragment pairs per thread and group when four groups are built in place
 
 struct LinearArgs {
@@ -97,6 +98,11 @@ struct LinearArgs {
     uint32_t *status;
     int ncta, S, chw, nsw, slot_bytes, frag_bytes, scr_bytes, stage_off;
     WaitCfg wait;
+    // greedy next token (nullable): tokens[r] = the index of row r's largest output; gcount and gpart (the
+    // workspace body) take the CTAs' keys, the last CTA to finish reduces them
+    int32_t *tokens;
+    uint32_t *gcount;
+    unsigned long long *gpart;  // [ncta][kLinMaxRows]
 };
 
 // Shared-memory bookkeeping of one CTA.
@@ -107,11 +113,25 @@ struct LinMisc {
     float inv[32];
     float2 red[kLinWarps];  // activation row statistics per (row, segment)
     int cnt[kLinWarps];     // parts finished per row group of a split
-    int flags[4];        // [0] abort
+    int flags[4];        // [0] abort, [1] this CTA reduces the greedy keys
+    unsigned long long gbest[kLinWarps][kLinMaxRows];  // greedy: each warp's best key per row
 };
 
+// Greedy key of output (value v, index i): an order-preserving image of v (with -0 folded into +0) above the
+// complement of i, so the unsigned maximum is the largest value and, among equal values, the lowest index.
+// NaN outputs are given key 0 by the caller (never chosen; a row with nothing else gives index 0).
+__device__ __forceinline__ unsigned long long lin_greedy_key(float v, int64_t i) {
+    v += 0.0f;
+    const uint32_t u = __float_as_uint(v);
+    const uint32_t k = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return ((unsigned long long)k << 32) | (0xFFFFFFFFu - (uint32_t)i);
+}
+__device__ __forceinline__ unsigned long long lin_umax(unsigned long long a, unsigned long long b) {
+    return a > b ? a : b;
+}
+
 template <int FMT, int NGRP>
-__global__ void __launch_bounds__(kLinThreads, 1) bfp_linear_kernel(const LinearArgs a) {
+__global__ void __launch_bounds__(kLinThreads, 1) bfp_linear_kernel(const __grid_constant__ LinearArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int NW = kLinWarps;
     constexpr int NC = NW * kWarp;
@@ -222,6 +242,9 @@ __global__ void __launch_bounds__(kLinThreads, 1) bfp_linear_kernel(const Linear
         for (int i = 0; i < a.nsw; ++i) issue_next();
 
     const uint2 *frag2 = reinterpret_cast<const uint2 *>(frag);
+    unsigned long long gk[NGRP][2];  // greedy: this lane's best keys, rows 8 g + 2 (lane & 3) + j
+#pragma unroll
+    for (int g = 0; g < NGRP; ++g) gk[g][0] = gk[g][1] = 0ull;
     for (int it = warp; it < items; it += NW) {
         const int rg = rg0 + it / S, part = it % S;
         const int r0 = part * a.kc / S, r1 = (part + 1) * a.kc / S;
@@ -281,8 +304,46 @@ __global__ void __launch_bounds__(kLinThreads, 1) bfp_linear_kernel(const Linear
                     const float v = mul_pow2(acc[0][g][i], 24 - (MB - 1) - lm->shift[r]);
                     if (a.y) a.y[(int64_t)r * a.ldy + nrow] = v;
                     if (a.yb) a.yb[(int64_t)r * a.ldy + nrow] = f32_to_bf16_bits(v);
+                    if (v == v) gk[g][i & 1] = lin_umax(gk[g][i & 1], lin_greedy_key(v, nrow));
                 }
             }
+    }
+    // greedy next token: each warp's best key per row (lanes of equal lane & 3 hold the same rows), the
+    // CTA's best per row to the workspace, and the last CTA to finish reduces every CTA's keys
+    if (a.tokens) {
+#pragma unroll
+        for (int g = 0; g < NGRP; ++g)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+#pragma unroll
+                for (int o = 4; o < kWarp; o <<= 1) gk[g][j] = lin_umax(gk[g][j], __shfl_xor_sync(0xffffffffu, gk[g][j], o));
+            }
+        if (lane < 4) {
+#pragma unroll
+            for (int g = 0; g < NGRP; ++g) {
+                lm->gbest[warp][8 * g + 2 * lane] = gk[g][0];
+                lm->gbest[warp][8 * g + 2 * lane + 1] = gk[g][1];
+            }
+        }
+        __syncthreads();
+        if (tid < a.m) {
+            unsigned long long b = 0ull;
+            for (int w = 0; w < NW; ++w) b = lin_umax(b, lm->gbest[w][tid]);
+            __stcg(a.gpart + (int64_t)c * kLinMaxRows + tid, b);
+            __threadfence();  // the key reaches L2 before the count
+        }
+        __syncthreads();
+        if (tid == 0) lm->flags[1] = atomicAdd(a.gcount, 1u) == (uint32_t)(a.ncta - 1);
+        __syncthreads();
+        if (lm->flags[1]) {
+            __threadfence();
+            if (tid < a.m) {
+                unsigned long long b = 0ull;
+                for (int q = 0; q < a.ncta; ++q) b = lin_umax(b, __ldcg(a.gpart + (int64_t)q * kLinMaxRows + tid));
+                a.tokens[tid] = b == 0ull ? 0 : (int32_t)(0xFFFFFFFFu - (uint32_t)(b & 0xFFFFFFFFull));
+            }
+            if (tid == 0) *a.gcount = 0u;  // every CTA has counted: ready for the next call
+        }
     }
     // No copy may still be landing in shared memory when the CTA exits (every path).
     {
@@ -407,7 +468,7 @@ static int plan_linear(const Geometry &g, int m, LinearPlan *p) {
     if (ring < stage) return fail(BFP_ESHAPE, "activation rows do not fit in shared memory");
     p->stage_off = (int)(ring - stage);
     p->smem = align_up(base + 8 * (size_t)kLinWarps * p->nsw, 128) + ring;
-    p->ws_bytes = 0;
+    p->ws_bytes = 256 + (size_t)p->ncta * kLinMaxRows * 8;  // greedy token: count, then one key per (CTA, row)
     return BFP_OK;
 }
 
@@ -435,14 +496,16 @@ static int launch_linear_t(const LinearArgs &a, const LinearPlan &p, cudaStream_
 // Shared by bfp_linear and the decode stack's LM head (norm = RMS-normalise x first).
 // status: the workspace status word; body: the rest of the workspace (unused by this kernel).
 int linear_launch_ex(const bfp_matrix *w, const uint16_t *x, int m, int64_t ldx, float *y, uint16_t *y_bf16,
-                     int64_t ldy, uint32_t *status, void *body, size_t body_bytes, cudaStream_t st, int norm) {
+                     int64_t ldy, uint32_t *status, void *body, size_t body_bytes, cudaStream_t st, int norm,
+                     int32_t *tokens) {
     Geometry g;
     int rc = check_matrix(w, &g, true);
     if (rc) return rc;
     if (m < 1 || m > 32) return fail(BFP_ESHAPE, "m must be in [1, 32]");
-    if (!x || (!y && !y_bf16)) return fail(BFP_EINVAL, "null x or no output");
+    if (!x || (!y && !y_bf16 && !tokens)) return fail(BFP_EINVAL, "null x or no output");
+    if (tokens && ((uintptr_t)tokens & 3u)) return fail(BFP_EALIGN, "tokens must be 4-byte aligned");
     if (ldx < g.k || ldx % 8 != 0) return fail(BFP_EALIGN, "ldx must be >= k and a multiple of 8");
-    if (ldy < g.n) return fail(BFP_EINVAL, "ldy < n");
+    if ((y || y_bf16) && ldy < g.n) return fail(BFP_EINVAL, "ldy < n");
     if (!aligned16(x) || (y && !aligned16(y)) || (y_bf16 && !aligned16(y_bf16)))
         return fail(BFP_EALIGN, "device pointers must be 16-byte aligned");
     LinearPlan p;
@@ -475,6 +538,9 @@ int linear_launch_ex(const bfp_matrix *w, const uint16_t *x, int m, int64_t ldx,
     a.scr_bytes = p.scr_bytes;
     a.stage_off = p.stage_off;
     a.wait = WaitCfg{kDefaultWaitIters, kDefaultWaitNanos};  // only this CTA's own copies are waited on
+    a.tokens = tokens;
+    a.gcount = static_cast<uint32_t *>(body);
+    a.gpart = reinterpret_cast<unsigned long long *>(static_cast<uint8_t *>(body) + 256);
     if (g.fmt == BFP_FMT_BFP4)
         return p.ngrp == 1 ? launch_linear_t<4, 1>(a, p, st)
                            : p.ngrp == 2 ? launch_linear_t<4, 2>(a, p, st) : launch_linear_t<4, 4>(a, p, st);
@@ -536,7 +602,16 @@ int bfp_linear(const bfp_matrix *w, const uint16_t *x, int m, int64_t ldx, float
     if (!ws || ws_bytes < kWsHeader) return fail(BFP_EWORKSPACE, "workspace null or smaller than its header");
     return linear_launch_ex(w, x, m, ldx, y, y_bf16, ldy, static_cast<uint32_t *>(ws),
                             static_cast<uint8_t *>(ws) + kWsHeader, ws_bytes - kWsHeader,
-                            reinterpret_cast<cudaStream_t>(stream), 0);
+                            reinterpret_cast<cudaStream_t>(stream), 0, nullptr);
+}
+
+int bfp_linear_greedy(const bfp_matrix *w, const uint16_t *x, int m, int64_t ldx, float *y, int64_t ldy,
+                      int32_t *tokens, void *ws, size_t ws_bytes, bfp_stream_t stream) {
+    if (!tokens) return fail(BFP_EINVAL, "null tokens");
+    if (!ws || ws_bytes < kWsHeader) return fail(BFP_EWORKSPACE, "workspace null or smaller than its header");
+    return linear_launch_ex(w, x, m, ldx, y, nullptr, ldy, static_cast<uint32_t *>(ws),
+                            static_cast<uint8_t *>(ws) + kWsHeader, ws_bytes - kWsHeader,
+                            reinterpret_cast<cudaStream_t>(stream), 0, tokens);
 }
 
 int bfp_workspace_init(void *ws, size_t ws_bytes, bfp_stream_t stream) {

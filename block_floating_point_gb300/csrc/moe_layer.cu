@@ -54,7 +54,8 @@ namespace bfp {
 using namespace dev;
 
 int linear_launch_ex(const bfp_matrix *w, const uint16_t *x, int m, int64_t ldx, float *y, uint16_t *y_bf16,
-                     int64_t ldy, uint32_t *status, void *body, size_t body_bytes, cudaStream_t st, int norm);
+                     int64_t ldy, uint32_t *status, void *body, size_t body_bytes, cudaStream_t st, int norm,
+                     int32_t *tokens);
 int linear_ws_body_bytes(const bfp_matrix *w, int m, size_t *bytes);
 
 constexpr int kMoeWarps = 16;                // warps of the layer kernel (no producer warp)
@@ -1481,15 +1482,17 @@ int moe_stack_workspace_size(const bfp_moe_layer *layers, int n_layers, const bf
     return BFP_OK;
 }
 
-int moe_stack_decode(const bfp_moe_layer *layers, int n_layers, const bfp_matrix *lm_head, uint16_t *h, int m,
-                     float *logits, int32_t *topk_idx, void *ws, size_t ws_bytes, bfp_stream_t stream) {
+// The stack, then the LM head: fp32 logits (nullable when tokens are asked for) and, with tokens, the greedy
+// next token of every row from the LM head's own epilogue.
+static int stack_run(const bfp_moe_layer *layers, int n_layers, const bfp_matrix *lm_head, uint16_t *h, int m,
+                     float *logits, int32_t *tokens, int32_t *topk_idx, void *ws, size_t ws_bytes, cudaStream_t st) {
     size_t mb, lb, hb;
     int rc = stack_layout(layers, n_layers, lm_head, m, &mb, &lb, &hb);
     if (rc) return rc;
-    if (!h || !logits) return fail(BFP_EINVAL, "null h or logits");
+    if (!h || (!logits && !tokens)) return fail(BFP_EINVAL, "null h, or neither logits nor tokens");
     if (!ws || ws_bytes < mb + lb + hb) return fail(BFP_EWORKSPACE, "workspace smaller than moe_stack_workspace_size");
-    if (!aligned16(h) || !aligned16(logits) || !aligned16(ws)) return fail(BFP_EALIGN, "pointers must be 16-byte aligned");
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (!aligned16(h) || (logits && !aligned16(logits)) || !aligned16(ws))
+        return fail(BFP_EALIGN, "pointers must be 16-byte aligned");
     uint8_t *w = static_cast<uint8_t *>(ws);
     uint16_t *hb2 = reinterpret_cast<uint16_t *>(w + mb + lb);
     uint16_t *cur = h, *nxt = hb2;
@@ -1505,7 +1508,23 @@ int moe_stack_decode(const bfp_moe_layer *layers, int n_layers, const bfp_matrix
         if (e != cudaSuccess) return cuda_fail(e, "copy final h");
     }
     return linear_launch_ex(lm_head, h, m, layers[0].hidden, logits, nullptr, lm_head->n,
-                            reinterpret_cast<uint32_t *>(w), w + mb, lb, st, 1);
+                            reinterpret_cast<uint32_t *>(w), w + mb, lb, st, 1, tokens);
+}
+
+int moe_stack_decode(const bfp_moe_layer *layers, int n_layers, const bfp_matrix *lm_head, uint16_t *h, int m,
+                     float *logits, int32_t *topk_idx, void *ws, size_t ws_bytes, bfp_stream_t stream) {
+    if (!logits) return fail(BFP_EINVAL, "null logits");
+    return stack_run(layers, n_layers, lm_head, h, m, logits, nullptr, topk_idx, ws, ws_bytes,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+int moe_stack_decode_greedy(const bfp_moe_layer *layers, int n_layers, const bfp_matrix *lm_head, uint16_t *h, int m,
+                            float *logits, int32_t *tokens, int32_t *topk_idx, void *ws, size_t ws_bytes,
+                            bfp_stream_t stream) {
+    if (!tokens) return fail(BFP_EINVAL, "null tokens");
+    if ((uintptr_t)tokens & 3u) return fail(BFP_EALIGN, "tokens must be 4-byte aligned");
+    return stack_run(layers, n_layers, lm_head, h, m, logits, tokens, topk_idx, ws, ws_bytes,
+                     reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

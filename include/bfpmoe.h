@@ -21,9 +21,10 @@
  *
  * Entry points: packing (bfp_packed_size, bfp_encode, bfp_encode_gate_up,
  * bfp_gptq_factor, bfp_encode_gptq, bfp_encode_gate_up_gptq, bfp_read_fields,
- * bfp_decode_host, bfp_unpack_device); the dense projection (bfp_linear);
- * the MoE layer and the decode stack (moe_decode_layer, moe_decode_layer_static,
- * moe_stack_decode); the greedy token (bfp_greedy_tokens); the KV cache and
+ * bfp_decode_host, bfp_unpack_device); the dense projection (bfp_linear,
+ * bfp_linear_greedy); the MoE layer and the decode stack (moe_decode_layer,
+ * moe_decode_layer_static, moe_stack_decode, moe_stack_decode_greedy); the
+ * greedy token (bfp_greedy_tokens); the KV cache and
  * decode attention (bfp_kv_cache_size, bfp_kv_append, bfp_attn_decode; on
  * host copies bfp_kv_encode_host and bfp_kv_read_fields); workspace sizes,
  * status and launch settings.
@@ -209,6 +210,22 @@ int bfp_linear(const bfp_matrix *w, const uint16_t *x, int m, int64_t ldx, float
                void *ws, size_t ws_bytes, bfp_stream_t stream);
 
 /*
+ * bfp_linear with the greedy next token folded into its epilogue (P1 "Fused
+ * decode kernels": the greedy arg max taken on the LM head's tiles, without
+ * writing out and re-reading the vocabulary-wide logits): tokens[r] (int32,
+ * device, 4-byte aligned) = the index o of the largest y[r][o], ties to the
+ * lower index, -0 equal to +0, NaN never chosen (a row with nothing else gives
+ * 0): the same rule as bfp_greedy_tokens, on the kernel's own fp32 outputs.
+ * y (nullable) receives those fp32 outputs as bfp_linear does; with y null
+ * no output row is written at all. One launch: every CTA reduces its outputs
+ * to one key per row and the last CTA to finish reduces the CTAs' keys (a
+ * counter in ws, left at zero by every successful call). m, x, ws as for
+ * bfp_linear.
+ */
+int bfp_linear_greedy(const bfp_matrix *w, const uint16_t *x, int m, int64_t ldx, float *y, int64_t ldy,
+                      int32_t *tokens, void *ws, size_t ws_bytes, bfp_stream_t stream);
+
+/*
  * One MoE decode layer's weights (all device memory).
  * Shapes: hidden % 16 == 0, ffn % 16 == 0, shared_ffn % 16 == 0,
  * 1 <= top_k <= 8, top_k <= n_experts <= 256.
@@ -309,6 +326,16 @@ int moe_stack_workspace_size(const bfp_moe_layer *layers, int n_layers, const bf
                              size_t *bytes);
 int moe_stack_decode(const bfp_moe_layer *layers, int n_layers, const bfp_matrix *lm_head, uint16_t *h, int m,
                      float *logits, int32_t *topk_idx, void *ws, size_t ws_bytes, bfp_stream_t stream);
+
+/*
+ * moe_stack_decode whose LM head also gives the greedy next token of every row
+ * (bfp_linear_greedy's rule, folded into the LM head's epilogue: P1 "Fused
+ * decode kernels"): tokens int32 [m] (device). logits is nullable here: with
+ * null logits the vocabulary-wide logits are never written. Same workspace.
+ */
+int moe_stack_decode_greedy(const bfp_moe_layer *layers, int n_layers, const bfp_matrix *lm_head, uint16_t *h, int m,
+                            float *logits, int32_t *tokens, int32_t *topk_idx, void *ws, size_t ws_bytes,
+                            bfp_stream_t stream);
 
 /*
  * Greedy next token for m rows (1..16) of fp32 logits [m x n] (device, row

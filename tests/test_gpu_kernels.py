@@ -100,3 +100,49 @@ def test_linear_rejects_bad_arguments():
     with pytest.raises(bfp.BFPError) as ei:
         bfp.linear(mat, x[:2], ws[:64])
     assert ei.value.code == bfp.BFP_EWORKSPACE
+
+
+def greedy_of(y):
+    """First index of each row's largest non-NaN value (-0 equal to +0), 0 for a row of NaN only."""
+    out = []
+    for row in np.asarray(y, dtype=np.float32):
+        ok = ~np.isnan(row)
+        out.append(int(np.flatnonzero(ok & (row == row[ok].max()))[0]) if ok.any() else 0)
+    return np.array(out, dtype=np.int32)
+
+
+@pytest.mark.parametrize("fmt,n,k,m", [(8, 8192, 2048, 1), (8, 8192, 2048, 16), (8, 8192, 2048, 32),
+                                       (8, 151936, 2048, 8), (4, 37, 96, 9), (8, 2000, 1024, 5), (4, 16, 16, 1)])
+def test_linear_greedy_token_in_the_epilogue(fmt, n, k, m):
+    """bfp_linear_greedy: the projection's outputs are those of bfp_linear, and the tokens are the greedy
+    rule applied to them (exact: comparisons only); away from near-ties (the two largest oracle outputs
+    apart by more than the tolerance) they are also the oracle's arg max. Two rows of W are made equal
+    and largest, so the lower index must win the tie."""
+    w = synth.normal(41, 300 + n + k, (n, k), std=0.02)
+    x = np.stack([synth.activation_row(41, 2000 + r, k, False) for r in range(m)])
+    if n > 40:
+        xf = synth.bf16_bits_to_f32(x[0])
+        w[23] = np.float32(0.05) * np.sign(xf)  # a clear maximum for row 0 ...
+        w[37] = w[23]                           # ... twice: ties go to the lower index
+    mat = bfp.DeviceMatrix.from_host(fmt, n, k, bfp.encode(fmt, w))
+    ws = bfp.linear_workspace(mat, m)
+    xt = bf16_tensor(x)
+    y_plain = bfp.linear(mat, xt, ws)
+    y = torch.empty((m, n), dtype=torch.float32, device="cuda")
+    for call in range(2):  # the counter in the workspace is left at zero: a second call works the same
+        tok = bfp.linear_greedy(mat, xt, ws, y=y)
+        torch.cuda.synchronize()
+        assert bfp.workspace_status(ws) == bfp.BFP_OK
+        assert torch.equal(y, y_plain)
+        assert np.array_equal(tok.cpu().numpy(), greedy_of(y.cpu().numpy())), f"call {call}"
+    tok_only = bfp.linear_greedy(mat, xt, ws)  # no outputs written at all
+    assert torch.equal(tok_only, tok)
+    if n > 40:
+        assert int(tok[0]) == 23
+    e, c = oracle.encode(fmt, w)
+    y_ref, _ = oracle.linear(fmt, e, c, x)
+    for r in range(m):
+        top2 = np.sort(y_ref[r].astype(np.float64))[-2:]
+        rms = np.sqrt(np.mean(y_ref[r].astype(np.float64) ** 2))
+        if top2[1] - top2[0] > 2e-3 * (abs(top2[1]) + rms):
+            assert int(tok[r]) == int(np.argmax(y_ref[r]))

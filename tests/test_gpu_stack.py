@@ -170,6 +170,17 @@ def run_stack(case, m, row_seed0, sample_vocab=None):
     logits2 = bfp.moe_stack_decode(layers, lm, h2, ws)
     torch.cuda.synchronize()
     assert torch.equal(logits, logits2) and torch.equal(h, h2)
+    # the greedy variant: the same logits, and the next tokens taken in the LM head's epilogue are the greedy
+    # rule on them; without logits it still gives the same tokens
+    h3 = bf16_tensor(h0)
+    lg3 = torch.empty_like(logits)
+    tok3 = bfp.moe_stack_decode_greedy(layers, lm, h3, ws, logits=lg3)
+    h4 = bf16_tensor(h0)
+    tok4 = bfp.moe_stack_decode_greedy(layers, lm, h4, ws)
+    torch.cuda.synchronize()
+    assert bfp.workspace_status(ws) == bfp.BFP_OK
+    assert torch.equal(lg3, logits) and torch.equal(h3, h)
+    assert np.array_equal(tok3.cpu().numpy(), tok) and torch.equal(tok4, tok3)
 
 
 def test_tiny_stack_m8():
