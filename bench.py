@@ -64,6 +64,9 @@ def kernel_src_sha() -> str:
     return h.hexdigest()[:16]
 
 
+CASES = ("m1", "m16_hot", "dense_m1", "dense_m16", "dense_m32", "lm_greedy_m8", "attn_32k")
+
+
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -75,6 +78,8 @@ def parse_args():
     ap.add_argument("--seed", type=int, default=20261202)
     ap.add_argument("--quick", action="store_true", help="headline line only (no secondary workloads, no oracle)")
     ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--case", choices=sorted(CASES), default=None,
+                    help="run one kernel's small workload a few times and exit (a short capture for a profiler)")
     return ap.parse_args()
 
 
@@ -342,8 +347,68 @@ def cpu_baseline_sample(args, spec, x_np):
 
 
 # --------------------------------------------------------------------------- our arm
+def run_case(args):
+    """One kernel's workload, launched `--steps` times after `--warmup` (for profiler captures: a few
+    launches, a few GB on the device at most). Prints one line and exits 0."""
+    import torch
+    import block_floating_point_gb300 as bfp
+    import synth
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    bfp.load()
+    case = args.case
+    if case in ("m1", "m16_hot"):
+        spec, layers = build_layers(1, args.seed, device)
+        L = layers[0]
+        m = 1 if case == "m1" else 16
+        if case == "m16_hot":
+            bias = torch.from_numpy(synth.hot_bias(spec.n_experts, args.seed)).to(device)
+            L = bfp.MoELayer(L.hidden, L.n_experts, L.ffn, L.top_k, L.shared_ffn, L.expert_fmt, L.router, L.shared_gate,
+                             L.experts_gate_up, L.experts_down, L.shared_gate_up, L.shared_down, router_bias=bias)
+        x = make_x(spec, args.seed, m, 0, device)[1]
+        ws = bfp.moe_workspace(L, m)
+        y = torch.empty((m, spec.hidden), dtype=torch.float32, device=device)
+        step = lambda: bfp.moe_decode_layer(L, x, ws, y=y)
+    elif case.startswith("dense_m"):
+        m = int(case[len("dense_m"):])
+        w = synth.normal(args.seed, synth.stream_id(synth.KIND_DENSE), (8192, 2048), std=0.02)
+        mat = bfp.DeviceMatrix.from_host(8, 8192, 2048, bfp.encode(8, w), device=device)
+        x = torch.from_numpy(np.stack([synth.activation_row(args.seed, 50000 + r, 2048, False)
+                                       for r in range(m)]).view(np.int16)).to(device)
+        ws = bfp.linear_workspace(mat, m)
+        yl = torch.empty((m, 8192), dtype=torch.int16, device=device)
+        step = lambda: bfp.linear(mat, x, ws, y_bf16=yl)
+    elif case == "lm_greedy_m8":
+        w = synth.normal(args.seed, synth.stream_id(synth.KIND_LMHEAD), (151936, 2048), std=synth.W_STD)
+        mat = bfp.DeviceMatrix.from_host(8, 151936, 2048, bfp.encode(8, w), device=device)
+        del w
+        x = torch.from_numpy(synth.to_bf16_bits(synth.normal(args.seed, synth.stream_id(synth.KIND_STACK_H),
+                                                             (8, 2048))).view(np.int16)).to(device)
+        ws = bfp.linear_workspace(mat, 8)
+        tk = torch.empty(8, dtype=torch.int32, device=device)
+        step = lambda: bfp.linear_greedy(mat, x, ws, tokens=tk)
+    else:  # attn_32k: 2 KV heads x 256, BFP8 K and V, 16 query heads, 32768 cached tokens
+        n_ctx, d, kvh, g = 32768, 256, 2, 8
+        kvc = bfp.KvCache(kvh, d, n_ctx, 8, 8, False, device=device)
+        kk = torch.from_numpy(synth.to_bf16_bits(synth.normal(args.seed, 42, (n_ctx, kvh, d))).view(np.int16)).to(device)
+        vv = torch.from_numpy(synth.to_bf16_bits(synth.normal(args.seed, 52, (n_ctx, kvh, d))).view(np.int16)).to(device)
+        bfp.kv_append(kvc, kk, vv, 0)
+        qa = torch.from_numpy(synth.to_bf16_bits(synth.normal(args.seed, 60, (kvh * g, d))).view(np.int16)).to(device)
+        ws = bfp.attn_workspace(kvc, kvh * g, n_ctx)
+        oa = torch.empty((kvh * g, d), dtype=torch.float32, device=device)
+        step = lambda: bfp.attn_decode(kvc, qa, n_ctx, d ** -0.5, ws, out=oa)
+    for _ in range(args.warmup + args.steps):
+        step()
+    torch.cuda.synchronize()
+    assert bfp.workspace_status(ws) == bfp.BFP_OK
+    print(json.dumps({"case": case, "launches": args.warmup + args.steps}))
+
+
 def main():
     args = parse_args()
+    if args.case:
+        run_case(args)
+        return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
