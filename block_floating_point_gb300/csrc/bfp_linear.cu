@@ -135,7 +135,6 @@ __global__ void __launch_bounds__(kLinThreads, 1) bfp_linear_kernel(const __grid
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int NW = kLinWarps;
     constexpr int NC = NW * kWarp;
-    constexpr int TILE = NGRP * 128;  // accumulator values of one 16-row group
     constexpr int MB = FMT == 4 ? 3 : 7;
     constexpr int CB = FMT == 4 ? 4 : 2;
     uint32_t *frag = reinterpret_cast<uint32_t *>(smem);
@@ -336,12 +335,19 @@ __global__ void __launch_bounds__(kLinThreads, 1) bfp_linear_kernel(const __grid
         if (tid == 0) lm->flags[1] = atomicAdd(a.gcount, 1u) == (uint32_t)(a.ncta - 1);
         __syncthreads();
         if (lm->flags[1]) {
+            // 16 threads per row, each over every 16th CTA's key (independent loads in flight), then a
+            // reduction over the 16 lanes
             __threadfence();
-            if (tid < a.m) {
-                unsigned long long b = 0ull;
-                for (int q = 0; q < a.ncta; ++q) b = lin_umax(b, __ldcg(a.gpart + (int64_t)q * kLinMaxRows + tid));
-                a.tokens[tid] = b == 0ull ? 0 : (int32_t)(0xFFFFFFFFu - (uint32_t)(b & 0xFFFFFFFFull));
+            const int r = tid >> 4, q0 = tid & 15;
+            unsigned long long b = 0ull;
+            if (r < a.m) {
+#pragma unroll 4
+                for (int q = q0; q < a.ncta; q += 16) b = lin_umax(b, __ldcg(a.gpart + (int64_t)q * kLinMaxRows + r));
             }
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) b = lin_umax(b, __shfl_xor_sync(0xffffffffu, b, o));
+            if (r < a.m && q0 == 0)
+                a.tokens[r] = b == 0ull ? 0 : (int32_t)(0xFFFFFFFFu - (uint32_t)(b & 0xFFFFFFFFull));
             if (tid == 0) *a.gcount = 0u;  // every CTA has counted: ready for the next call
         }
     }
