@@ -518,6 +518,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_co
                     if (mine) copy_unit(a.gu + (int64_t)eu * a.gu_stride + (int64_t)(2 * (r - su * a.nft)) * a.kc_h * a.rec, lane);
                     const uint32_t issued = __ballot_sync(0xffffffffu, mine);
                     if (lane == 0) armed_u |= issued;
+                    __syncwarp();  // the gate/up units first: the down rows are needed only after the h exchange
                     if (nrg > 0) {
                         if (lane == 0) mbar_arrive_expect_tx(&ms->bar_p2rt, (uint32_t)(nrg * a.K * a.kc_f * a.rec));
                         __syncwarp();
@@ -850,18 +851,10 @@ static bool plan_row(const bfp_moe_layer *L, const Geometry &gu, const Geometry 
     const int64_t u = 2 * (int64_t)kc_h * rec;
     const int IPR = K * kc_f + kc_fs;
     const int64_t P2 = (int64_t)IPR * rec;
-    // f-tile ranges balanced against the down rows: the list's bytes plus every row group's down bytes, split
-    // evenly; CTA c's cumulative share minus the down bytes of CTAs 0..c-1, in whole units
-    const int q = ng_d / ncta, r = ng_d % ncta;
-    const double tot = (double)n1 * u + (double)ng_d * P2;
+    // f-tile ranges split evenly (whole units): the gate/up bytes of a CTA decide when its h is out, and every
+    // CTA waits for the last h, while the down rows are needed only after that exchange
     p->ub.assign(ncta + 1, 0);
-    for (int c = 1; c < ncta; ++c) {
-        const double C = tot * c / ncta - (double)((int64_t)q * c + std::min(c, r)) * P2;
-        int64_t s = (int64_t)std::floor(C / (double)u + 0.5);
-        s = std::max<int64_t>(s, p->ub[c - 1]);
-        s = std::min<int64_t>(s, n1);
-        p->ub[c] = (int16_t)s;
-    }
+    for (int c = 1; c < ncta; ++c) p->ub[c] = (int16_t)((int64_t)c * n1 / ncta);
     p->ub[ncta] = (int16_t)n1;
     int64_t area = 0;
     for (int c = 0; c < ncta; ++c) {
