@@ -54,6 +54,8 @@ constexpr int kRowThreads = kRowWarps * 32;
 constexpr int kRowPieces = 8;    // most pieces (runs of records of one unit / one down slot) per warp
 constexpr int kRowMaxRg = 4;     // most output row groups per CTA
 constexpr int kRowMaxUnits = 32; // most f-tile units per CTA (one thread per (unit, row) sums their pieces)
+constexpr int kRowMaxRouterRows = 4;  // most router rows (with the shared-gate row) per CTA
+constexpr int kRowRouterRegs = 4;     // 16-byte router vectors held by each thread
 
 struct RowArgs {
     int H, E, F, K, Fs, ncta;
@@ -85,14 +87,15 @@ struct RowArgs {
 };
 
 struct RowMisc {
-    uint64_t bar_x, bar_r, bar_p2sh, bar_p2rt;
+    uint64_t bar_x, bar_p2sh, bar_p2rt;
     uint64_t bar_u[kRowMaxUnits];  // one per f-tile unit of the CTA (its gate and up row groups, one copy)
     int shift_s[kMaxTopK + 1];  // power-of-two scale of each slot's h fragments
     float wsl[kMaxTopK + 1];    // routing weight of each slot; slot K: the shared gate sigmoid(g . x)
     int esl[kMaxTopK];          // expert of each slot
-    int p1u0[kRowWarps];        // first unit (of the CTA's) in each warp's gate/up range
     int p2g0[kRowWarps];        // first (row group, slot) group in each warp's down range
-    float red[kRowWarps][4];    // per-warp partial logits (up to 4 router rows at a time)
+    float red[kRowWarps][4];    // per-warp partial logits (up to 4 router rows)
+    alignas(16) float sst[kRowWarps];     // per-warp partial sums of squares of the row
+    alignas(16) uint32_t smx[kRowWarps];  // per-warp maxima of |x| (bf16 bits)
     float lgv[4];               // the CTA's logits of the current pass
     int flags[4];               // [0] abort
     uint32_t ep;                // the epoch word at the start of the launch
@@ -190,14 +193,17 @@ __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_co
             trp[(i)] = global_ns();                                  \
             trp[64 + (i)] = (unsigned long long)clock64();           \
         }                                                            \
+        __syncwarp();                                                \
     } while (0)
 #define WSTAMP(base)                                                            \
     do {                                                                        \
         if (trp && (threadIdx.x & 31) == 0) trp[(base) + (threadIdx.x >> 5)] = global_ns(); \
+        __syncwarp();                                                           \
     } while (0)
 #define CSTAMP(i)                                                         \
     do {                                                                  \
         if (trp && threadIdx.x == 0) trp[(i)] = (unsigned long long)clock64(); \
+        __syncwarp();                                                     \
     } while (0)
 #else
 #define CSTAMP(i) \
@@ -218,13 +224,13 @@ __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_co
     uint8_t *const w1 = smem;                             // the units, one after another
     uint8_t *const w2 = smem + nu * ubytes;               // then the down items (row group, slot, record)
     uint16_t *const xs = reinterpret_cast<uint16_t *>(smem + a.off_stage);  // activation row [H] bf16
-    uint16_t *const rs = xs + a.H;                                          // router rows [rows][H] bf16
     uint2 *const xc = reinterpret_cast<uint2 *>(smem + a.off_xc);           // [kc_h * CB blocks][kXEnt]
     uint2 *const hc = reinterpret_cast<uint2 *>(smem + a.off_hc);           // [slot][kbf blocks][kHEnt]
     float *const p1p = reinterpret_cast<float *>(smem + a.off_p1);          // [warp][piece][gate, up][16]
     float *const p2p = reinterpret_cast<float *>(smem + a.off_p2);          // [warp][piece][16]
-    const int T1 = nu * a.kc_h;  // chunks (one gate record and the up record of the same k)
-    const int ch0 = warp * T1 / NW, ch1 = (warp + 1) * T1 / NW;
+    // gate/up: every warp takes the same slice [k0w, k1w) of chunks (one gate record and the up record of the
+    // same k) of every unit, so that a unit is computed by all warps at once as soon as it lands
+    const int k0w = warp * a.kc_h / NW, k1w = (warp + 1) * a.kc_h / NW;
     const int nrg = c < a.ng_d ? (a.ng_d - c + a.ncta - 1) / a.ncta : 0;  // row groups c, c + ncta, ...
     const int IPR = a.K * a.kc_f + a.kc_fs;
     const int I2 = nrg * IPR;
@@ -237,7 +243,6 @@ __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_co
 
     if (tid == 0) {
         mbar_init(&ms->bar_x, 1);
-        mbar_init(&ms->bar_r, 1);
         mbar_init(&ms->bar_p2sh, 1);
         mbar_init(&ms->bar_p2rt, 1);
         for (int j = 0; j < nu; ++j) mbar_init(&ms->bar_u[j], 1);
@@ -245,10 +250,8 @@ __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_co
         for (int i = 0; i < 4; ++i) ms->flags[i] = 0;
         for (int i = 0; i <= kMaxTopK; ++i) ms->slot_ready[i] = 0;
     }
-    if (lane == 0) {  // where each warp's ranges start (read by the combines, which avoid divisions)
-        ms->p1u0[warp] = ch0 / a.kc_h;
+    if (lane == 0)  // where each warp's down range starts (read by the combine, which avoids divisions)
         ms->p2g0[warp] = it1 > it0 ? row_p2_group(it0, IPR, a.K, a.kc_f) : 0;
-    }
     __syncthreads();
     // dependent launch: the next kernel may take the SMs as this one's CTAs leave
     grid_dep_launch_dependents();
@@ -256,15 +259,13 @@ __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_co
     bool bad = false;
     uint32_t armed_u = 0u;     // thread 0: units whose copy it issued
     bool armed_p2rt = false;   // thread 0: the routed down rows issued
-    const bool armed_r = rr1 > rr0, armed_p2sh = nrg > 0;
+    bool routed = false;       // warp 0: the top-k is done and the routed f-tile units are requested
+    const bool armed_p2sh = nrg > 0;
     const uint64_t pol = l2_evict_first();  // weights are read once per launch
-    // Pieces of this warp's chunk range: fn(local unit j, first record, end record), in order.
+    // Pieces of this warp: fn(local unit j, first record, end record) for every unit, in order (piece j).
     auto for_pieces = [&](auto fn) {
-        for (int ch = ch0; ch < ch1;) {
-            const int j = ch / a.kc_h, k0 = ch - j * a.kc_h, k1 = min(a.kc_h, ch1 - j * a.kc_h);
-            fn(j, k0, k1);
-            ch = (j + 1) * a.kc_h;
-        }
+        if (k1w > k0w)
+            for (int j = 0; j < nu; ++j) fn(j, k0w, k1w);
     };
     // Copy of unit j (its gate and up row groups are adjacent in the packed matrix) to its place in shared memory.
     auto copy_unit = [&](const uint8_t *src, int j) {
@@ -275,13 +276,19 @@ __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_co
 
     // ---- 0. weights that depend on nothing: router rows (and the shared-gate row), the shared expert's
     //         f-tiles of this CTA, its shared down rows; issued before waiting for the previous kernel
-    if (tid == 0 && armed_r) {
-        const uint32_t rb = re > rr0 ? (uint32_t)(re - rr0) * a.H * 2 : 0u;
-        const uint32_t gsb = rr1 > a.E ? (uint32_t)a.H * 2 : 0u;
-        const uint64_t keep = l2_evict_last();  // router rows are small and read every step: keep them in L2
-        mbar_arrive_expect_tx(&ms->bar_r, rb + gsb);
-        if (rb) bulk_g2s_hint(rs, a.router + (int64_t)rr0 * a.H, rb, &ms->bar_r, keep);
-        if (gsb) bulk_g2s_hint(reinterpret_cast<uint8_t *>(rs) + rb, a.sgate, gsb, &ms->bar_r, keep);
+    // the CTA's router rows (and the shared-gate row) straight into registers: thread t holds 16-byte
+    // vectors t, t + 512, ... of the rows laid end to end
+    const int nvec = a.H / 8, nitems = (rr1 - rr0) * nvec;
+    uint4 rwv[kRowRouterRegs];
+#pragma unroll
+    for (int j = 0; j < kRowRouterRegs; ++j) {
+        const int it = tid + j * kRowThreads;
+        rwv[j] = make_uint4(0u, 0u, 0u, 0u);
+        if (it < nitems) {
+            const int row = it / nvec, v = it - row * nvec;
+            const uint16_t *src = rr0 + row < a.E ? a.router + (int64_t)(rr0 + row) * a.H : a.sgate;
+            rwv[j] = __ldg(reinterpret_cast<const uint4 *>(src) + v);
+        }
     }
     if (tid == 0)
         for (int jj = 0; jj < nu && u0 + jj < a.nft_s; ++jj)
@@ -311,23 +318,24 @@ __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_co
     };
     // Gate/up pieces of one kind (shared or routed), in this warp's order; partial tiles to shared memory.
     auto run_pieces = [&](bool shared_kind) {
-        int pi = 0;
         for_pieces([&](int j, int k0, int k1) {
+            const int pi = j;
             const bool sh = u0 + j < a.nft_s;
             if (sh == shared_kind) {
                 if (!bad && !__all_sync(0xffffffffu, mbar_wait(&ms->bar_u[j], 0u, a.wait_data, vflags))) abort_warp();
                 __syncwarp();  // reconverge before the warp-wide MMAs (lane 0 may have polled alone)
                 float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-                if (!sh && pi == 0) CSTAMP(84);
+                const bool first_routed = !sh && (j == 0 || u0 + j == a.nft_s);
+                if (first_routed) CSTAMP(84);
                 if (!bad) {
                     const uint8_t *un = w1 + j * ubytes;
                     for (int k = k0; k < k1; ++k) {
                         const uint8_t *recs[2] = {un + (int64_t)k * a.rec, un + (int64_t)(a.kc_h + k) * a.rec};
                         row_mma<FMT, 2, kXEnt>(recs, xc + (int64_t)k * CB * kXEnt, xsel, lane, acc);
-                        if (!sh && pi == 0 && k == k0) CSTAMP(85);
+                        if (first_routed && k == k0) CSTAMP(85);
                     }
                 }
-                if (!sh && pi == 0) CSTAMP(86);
+                if (first_routed) CSTAMP(86);
                 if (t4 == 0) {  // column 0: rows g and g + 8
                     float *dst = p1p + (size_t)((warp * kRowPieces + pi) * 2) * 16;
                     dst[g] = acc[0][0];
@@ -336,23 +344,24 @@ __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_co
                     dst[16 + g + 8] = acc[1][1];
                 }
             }
-            ++pi;
         });
     };
 
     [&]() {
-        // ---- 1. the activation row: statistics (every warp, redundantly: no CTA barrier), then this CTA's
-        //         router logits
+        // ---- 1. the activation row: statistics (spread over the CTA, one barrier), then this CTA's router
+        //         logits
         if (!__all_sync(0xffffffffu, mbar_wait(&ms->bar_x, 0u, a.wait_data, nullptr))) abort_warp();
         __syncwarp();  // warps left diverged (lane-0 copy issue above) run warp collectives many times slower
         STAMP(2);
+        // every thread a 16-byte vector (or none), warp partials, then every thread adds the 16 partials in
+        // warp order (the same sum everywhere)
         float inv = 1.f;
         int shift_x = 0;
         {
             const uint4 *xv = reinterpret_cast<const uint4 *>(xs);
             float ss = 0.f;
             uint32_t mx2 = 0u;
-            for (int i = lane; i < a.H / 8; i += kWarp) {
+            for (int i = tid; i < a.H / 8; i += kRowThreads) {
                 const uint4 v = xv[i];
                 const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -363,10 +372,27 @@ __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_co
                     ss = fmaf(hi, hi, ss);
                 }
             }
-            float mx = warp_max(bf16_bits_to_f32(max(mx2 & 0xFFFFu, mx2 >> 16)));
+            uint32_t mxw = max(mx2 & 0xFFFFu, mx2 >> 16);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mxw = max(mxw, __shfl_xor_sync(0xffffffffu, mxw, o));
+            ss = warp_sum(ss);
+            if (lane == 0) {
+                ms->sst[warp] = ss;
+                ms->smx[warp] = mxw;
+            }
+            __syncthreads();
+            float sst = 0.f;
+            uint32_t mxt = 0u;
+#pragma unroll
+            for (int w = 0; w < NW; w += 4) {
+                const float4 s4 = *reinterpret_cast<const float4 *>(ms->sst + w);
+                const uint4 m4 = *reinterpret_cast<const uint4 *>(ms->smx + w);
+                sst = sst + s4.x + s4.y + s4.z + s4.w;
+                mxt = max(max(mxt, max(m4.x, m4.y)), max(m4.z, m4.w));
+            }
+            float mx = bf16_bits_to_f32(mxt);
             if (a.norm) {
-                ss = warp_sum(ss);
-                inv = 1.0f / sqrtf(ss / (float)a.H + a.eps);
+                inv = 1.0f / sqrtf(sst / (float)a.H + a.eps);
                 mx = bf16_bits_to_f32(f32_to_bf16_bits(mx * inv));  // max |bf16(x * inv)|: rounding is monotonic
             }
             shift_x = frag_shift(mx);
@@ -376,58 +402,57 @@ __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_co
             const float v = bf16_bits_to_f32(bits);
             return a.norm ? bf16_bits_to_f32(f32_to_bf16_bits(v * inv)) : v;
         };
-        if (armed_r && !bad && !__all_sync(0xffffffffu, mbar_wait(&ms->bar_r, 0u, a.wait_data, vflags))) abort_warp();
-        __syncwarp();
         STAMP(3);
-        // logits: router row i of the CTA, all threads: each a 16-byte vector of the row, a warp sum, then the
-        // warps' sums in warp order (up to 4 rows per pass)
-        for (int i0 = 0; i0 < rr1 - rr0; i0 += 4) {
-            const int nr = min(4, rr1 - rr0 - i0);
-            __syncwarp();
-            float part[4] = {0.f, 0.f, 0.f, 0.f};
+        // logits of this CTA's router rows: each thread's vectors, warp sums per row, the warps' sums in warp order
+        const int nr = rr1 - rr0;
+        {
+            float part[kRowMaxRouterRows] = {0.f, 0.f, 0.f, 0.f};
             const uint4 *xv = reinterpret_cast<const uint4 *>(xs);
-            for (int v = tid; !bad && v < a.H / 8; v += kRowThreads) {
-                const uint4 xq = xv[v];
-                const uint32_t xw[4] = {xq.x, xq.y, xq.z, xq.w};
-                float xf[8];
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    xf[2 * h] = xval(xw[h] & 0xFFFFu);
-                    xf[2 * h + 1] = xval(xw[h] >> 16);
-                }
+            for (int j = 0; j < kRowRouterRegs; ++j) {
+                const int it = tid + j * kRowThreads;
+                if (!bad && it < nitems) {
+                    const int row = it / nvec, v = it - row * nvec;
+                    const uint4 xq = xv[v];
+                    const uint32_t xw[4] = {xq.x, xq.y, xq.z, xq.w};
+                    const uint32_t ww[4] = {rwv[j].x, rwv[j].y, rwv[j].z, rwv[j].w};
+                    float d = 0.f;
 #pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    if (r < nr) {
-                        const uint4 wq = reinterpret_cast<const uint4 *>(rs + (int64_t)(i0 + r) * a.H)[v];
-                        const uint32_t ww[4] = {wq.x, wq.y, wq.z, wq.w};
-#pragma unroll
-                        for (int h = 0; h < 4; ++h) {
-                            part[r] = fmaf(xf[2 * h], bf16_bits_to_f32(ww[h] & 0xFFFFu), part[r]);
-                            part[r] = fmaf(xf[2 * h + 1], bf16_bits_to_f32(ww[h] >> 16), part[r]);
-                        }
+                    for (int h = 0; h < 4; ++h) {
+                        d = fmaf(xval(xw[h] & 0xFFFFu), bf16_bits_to_f32(ww[h] & 0xFFFFu), d);
+                        d = fmaf(xval(xw[h] >> 16), bf16_bits_to_f32(ww[h] >> 16), d);
                     }
+#pragma unroll
+                    for (int r = 0; r < kRowMaxRouterRows; ++r)
+                        if (r == row) part[r] += d;
                 }
             }
+            CSTAMP(91);
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
+            for (int r = 0; r < kRowMaxRouterRows; ++r) {
                 const float sr = warp_sum(part[r]);
                 if (lane == 0 && r < nr) ms->red[warp][r] = sr;
             }
+            CSTAMP(92);
             __syncthreads();
+            CSTAMP(93);
             if (tid < nr) {
                 float acc = 0.f;
                 for (int w = 0; w < NW; ++w) acc += ms->red[w][tid];
-                const int row = rr0 + i0 + tid;
+                const int row = rr0 + tid;
                 if (row < a.E && a.rbias) acc += a.rbias[row];
                 ms->lgv[tid] = acc;
             }
             __syncthreads();
+            CSTAMP(94);
             // into every CTA's mailbox (a poller reads only its own lines)
             for (int q = tid; q < a.ncta * nr; q += kRowThreads) {
                 const int box = q / nr, r = q - box * nr;
-                __stcg(a.lgw + (int64_t)box * a.lsb + rr0 + i0 + r, tag_word(ms->ep + 1u, ms->lgv[r]));
+                __stcg(a.lgw + (int64_t)box * a.lsb + rr0 + r, tag_word(ms->ep + 1u, ms->lgv[r]));
             }
+            CSTAMP(95);
             __threadfence();  // push the stores out now (nothing waits on this fence but this thread)
+            CSTAMP(96);
         }
         if (__syncthreads_or(bad)) {
             bad = true;
@@ -518,19 +543,8 @@ __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_co
                     if (mine) copy_unit(a.gu + (int64_t)eu * a.gu_stride + (int64_t)(2 * (r - su * a.nft)) * a.kc_h * a.rec, lane);
                     const uint32_t issued = __ballot_sync(0xffffffffu, mine);
                     if (lane == 0) armed_u |= issued;
-                    __syncwarp();  // the gate/up units first: the down rows are needed only after the h exchange
-                    if (nrg > 0) {
-                        if (lane == 0) mbar_arrive_expect_tx(&ms->bar_p2rt, (uint32_t)(nrg * a.K * a.kc_f * a.rec));
-                        __syncwarp();
-                        if (lane < a.K)
-                            for (int j = 0; j < nrg; ++j) {
-                                const int rg = c + j * a.ncta;
-                                bulk_g2s_hint(w2 + (int64_t)(j * IPR + lane * a.kc_f) * a.rec,
-                                              a.dn + (int64_t)my_e * a.dn_stride + (int64_t)rg * a.kc_f * a.rec,
-                                              (uint32_t)(a.kc_f * a.rec), &ms->bar_p2rt, pol);
-                            }
-                        armed_p2rt = true;
-                    }
+                    if (lane < a.K) ms->esl[lane] = my_e;  // the down rows follow once the gate/up bytes are in
+                    routed = true;
                     __syncwarp();
                 }
                 const float l0 = __shfl_sync(0xffffffffu, my_l, 0);
@@ -538,7 +552,6 @@ __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_co
                 const float psum = warp_sum(p);
                 const float my_w = __fdividef(p, psum);
                 if (lane < a.K) {
-                    ms->esl[lane] = my_e;
                     ms->wsl[lane] = my_w;
                     if (c == 0) {
                         if (a.topk_idx) a.topk_idx[lane] = my_e;
@@ -581,6 +594,23 @@ __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_co
             run_pieces(true);
         }
         run_pieces(false);
+        if (warp == 0 && routed && !bad && nrg > 0) {
+            // the routed down rows, one lane per slot: requested only now, so that the gate/up bytes (on the
+            // critical path) have the memory system to themselves; they are needed after the h exchange
+            if (lane == 0) mbar_arrive_expect_tx(&ms->bar_p2rt, (uint32_t)(nrg * a.K * a.kc_f * a.rec));
+            __syncwarp();
+            if (lane < a.K) {
+                const int e = ms->esl[lane];
+                for (int j = 0; j < nrg; ++j) {
+                    const int rg = c + j * a.ncta;
+                    bulk_g2s_hint(w2 + (int64_t)(j * IPR + lane * a.kc_f) * a.rec,
+                                  a.dn + (int64_t)e * a.dn_stride + (int64_t)rg * a.kc_f * a.rec,
+                                  (uint32_t)(a.kc_f * a.rec), &ms->bar_p2rt, pol);
+                }
+            }
+            armed_p2rt = true;
+            __syncwarp();
+        }
         WSTAMP(16);
         if (__syncthreads_or(bad)) {
             bad = true;
@@ -593,9 +623,8 @@ __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_co
             const int j = tid >> 4, n = tid & 15;
             float sg = 0.f, su = 0.f;
             for (int w = 0; w < NW; ++w) {
-                const int c0 = w * T1 / NW, c1 = (w + 1) * T1 / NW;
-                if (c0 >= c1 || c1 <= j * a.kc_h || c0 >= (j + 1) * a.kc_h) continue;
-                const float *src = p1p + (size_t)((w * kRowPieces + (j - ms->p1u0[w])) * 2) * 16;
+                if ((w + 1) * a.kc_h / NW == w * a.kc_h / NW) continue;  // an empty slice
+                const float *src = p1p + (size_t)((w * kRowPieces + j) * 2) * 16;
                 sg += src[n];
                 su += src[16 + n];
             }
@@ -637,6 +666,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_co
                 }
                 if (global_ns() - t0 > a.wait.nanos) break;
             }
+            bool seen = false;
             for (int64_t it = 0; ok && it < a.wait.iters; ++it) {
                 bool mine = true;
 #pragma unroll
@@ -653,10 +683,13 @@ __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_co
                     const ulonglong2 p = ld_words2(hs + 16 * b + 2 * tq), r2 = ld_words2(hs + 16 * b + 2 * tq + 8);
                     mine &= word_tag(p.x) == T && word_tag(p.y) == T && word_tag(r2.x) == T && word_tag(r2.y) == T;
                 }
-                if (__all_sync(0xffffffffu, mine)) break;
-                if (global_ns() - t0 > a.wait.nanos) ok = false;
+                if (__all_sync(0xffffffffu, mine)) {
+                    seen = true;
+                    break;
+                }
+                if (global_ns() - t0 > a.wait.nanos) break;
             }
-            if (!ok) {
+            if (!seen) {
                 abort_warp();
                 break;
             }
@@ -798,7 +831,6 @@ __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_co
         const WaitCfg drain{int64_t(1) << 40, 1000000000ull};
         if (tid == 0) {
             mbar_wait(&ms->bar_x, 0u, drain, nullptr);
-            if (armed_r) mbar_wait(&ms->bar_r, 0u, drain, nullptr);
             for (int j = 0; j < nu; ++j)
                 if ((armed_u >> j) & 1u) mbar_wait(&ms->bar_u[j], 0u, drain, nullptr);
             if (armed_p2rt) mbar_wait(&ms->bar_p2rt, 0u, drain, nullptr);
@@ -862,7 +894,7 @@ static bool plan_row(const bfp_moe_layer *L, const Geometry &gu, const Geometry 
         if (nu * 16 > kRowThreads) return false;  // one thread per (unit, row) sums the pieces
         const int nrg = c < ng_d ? (ng_d - c + ncta - 1) / ncta : 0;
         area = std::max<int64_t>(area, nu * u + nrg * P2);
-        if (max_pieces(nu * kc_h, [&](int ch) { return ch / kc_h; }) > kRowPieces) return false;
+        if (nu > kRowPieces) return false;  // every warp holds one gate/up piece per unit
         if (max_pieces(nrg * IPR, [&](int i) {
                 const int j = i / IPR, rem = i - j * IPR;
                 return j * (K + 1) + (rem < K * kc_f ? rem / kc_f : K);
@@ -870,10 +902,11 @@ static bool plan_row(const bfp_moe_layer *L, const Geometry &gu, const Geometry 
             return false;
     }
     p->rpc = (L->n_experts + 1 + ncta - 1) / ncta;
+    if (p->rpc > kRowMaxRouterRows || (int64_t)p->rpc * (H / 8) > (int64_t)kRowThreads * kRowRouterRegs) return false;
     p->kbf = std::max(kc_f, kc_fs) * CB;
     size_t o = align_up((size_t)area, 128);
     p->off_stage = (int)o;
-    o = align_up(o + (size_t)H * 2 + (size_t)p->rpc * H * 2, 16);
+    o = align_up(o + (size_t)H * 2, 16);
     p->off_xc = (int)o;
     o = align_up(o + (size_t)kc_h * CB * kXEnt * 8, 16);
     p->off_hc = (int)o;
