@@ -51,7 +51,7 @@ using namespace dev;
 
 constexpr int kRowWarps = 16;
 constexpr int kRowThreads = kRowWarps * 32;
-constexpr int kRowPieces = 8;    // most pieces (runs of records of one unit / one down slot) per warp
+constexpr int kRowPieces = 8;    // most partial tiles per warp (one per gate/up unit; one per run of down records)
 constexpr int kRowMaxRg = 4;     // most output row groups per CTA
 constexpr int kRowMaxUnits = 32; // most f-tile units per CTA (one thread per (unit, row) sums their pieces)
 constexpr int kRowMaxRouterRows = 4;  // most router rows (with the shared-gate row) per CTA
@@ -107,9 +107,22 @@ __device__ __forceinline__ unsigned long long tag_word(uint32_t tag, float v) {
 }
 __device__ __forceinline__ uint32_t word_tag(unsigned long long w) { return (uint32_t)(w >> 32); }
 __device__ __forceinline__ float word_value(unsigned long long w) { return __uint_as_float((uint32_t)w); }
-// 64-bit loads and stores at L2 (each 64-bit element is read or written whole)
+// Loads of words another CTA writes, for polling loops: strong (relaxed, gpu scope) loads, so they are
+// served by L2 and never merged with or hoisted out of the loop's earlier iterations; each 64-bit element
+// is read whole.
+__device__ __forceinline__ unsigned long long ld_word(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
 __device__ __forceinline__ ulonglong2 ld_words2(const unsigned long long *p) {
-    return __ldcg(reinterpret_cast<const ulonglong2 *>(p));
+    ulonglong2 v;
+    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(v.x), "=l"(v.y) : "l"(p) : "memory");
+    return v;
+}
+// The matching store (relaxed, gpu scope).
+__device__ __forceinline__ void st_word(unsigned long long *p, unsigned long long v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
 // Compact one-row operands (the B side of m16n8k16, only a few columns used). Per block, the x row has
@@ -448,7 +461,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_co
             // into every CTA's mailbox (a poller reads only its own lines)
             for (int q = tid; q < a.ncta * nr; q += kRowThreads) {
                 const int box = q / nr, r = q - box * nr;
-                __stcg(a.lgw + (int64_t)box * a.lsb + rr0 + r, tag_word(ms->ep + 1u, ms->lgv[r]));
+                st_word(a.lgw + (int64_t)box * a.lsb + rr0 + r, tag_word(ms->ep + 1u, ms->lgv[r]));
             }
             CSTAMP(95);
             __threadfence();  // push the stores out now (nothing waits on this fence but this thread)
@@ -482,9 +495,9 @@ __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_co
                         }
                     } else {
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) wv[q] = 8 * lane + q < a.E ? __ldcg(box + 8 * lane + q) : 0ull;
+                        for (int q = 0; q < 8; ++q) wv[q] = 8 * lane + q < a.E ? ld_word(box + 8 * lane + q) : 0ull;
                     }
-                    wgate = __ldcg(box + a.E);
+                    wgate = ld_word(box + a.E);
 #pragma unroll
                     for (int q = 0; q < 8; ++q) mine &= 8 * lane + q >= a.E || word_tag(wv[q]) == T;
                     mine &= word_tag(wgate) == T;
@@ -515,15 +528,22 @@ __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_co
                 CSTAMP(88);
                 int my_e = 0;
                 float my_l = 0.f;
+                // lane jj < nu holding a routed f-tile unit requests it in the round that decides its slot
+                const int r_l = u0 + lane - a.nft_s;
+                const int su_l = lane < nu && r_l >= 0 ? r_l / a.nft : -1;
                 for (int s = 0; s < a.K; ++s) {
                     const uint32_t kmax = __reduce_max_sync(0xffffffffu, key[0]);
                     const uint32_t bal = __ballot_sync(0xffffffffu, key[0] == kmax);
                     const int wl = __ffs(bal) - 1;
                     const int q = __shfl_sync(0xffffffffu, qi[0], wl);
+                    const int es = min(8 * wl + q, a.E - 1);
                     if (lane == s) {
-                        my_e = min(8 * wl + q, a.E - 1);
+                        my_e = es;
                         my_l = key_value(kmax);
                     }
+                    if (su_l == s)
+                        copy_unit(a.gu + (int64_t)es * a.gu_stride + (int64_t)(2 * (r_l - s * a.nft)) * a.kc_h * a.rec, lane);
+                    __syncwarp();
                     const bool win = lane == wl;
 #pragma unroll
                     for (int i = 0; i < 7; ++i) {
@@ -536,12 +556,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_co
                 // ---- 3. the routed weights of this CTA, at once, one lane per copy: lane jj the f-tile unit jj,
                 //         lane s the down rows of slot s
                 {
-                    const int r = u0 + lane - a.nft_s;
-                    const int su = r >= 0 ? r / a.nft : 0;
-                    const int eu = __shfl_sync(0xffffffffu, my_e, min(su, a.K - 1));
-                    const bool mine = lane < nu && r >= 0;
-                    if (mine) copy_unit(a.gu + (int64_t)eu * a.gu_stride + (int64_t)(2 * (r - su * a.nft)) * a.kc_h * a.rec, lane);
-                    const uint32_t issued = __ballot_sync(0xffffffffu, mine);
+                    const uint32_t issued = __ballot_sync(0xffffffffu, su_l >= 0);
                     if (lane == 0) armed_u |= issued;
                     if (lane < a.K) ms->esl[lane] = my_e;  // the down rows follow once the gate/up bytes are in
                     routed = true;
@@ -635,7 +650,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_co
             const int r = i - a.nft_s;
             const int slot = r < 0 ? a.K : r / a.nft;
             const int ft = r < 0 ? i : r - slot * a.nft;
-            __stcg(a.hw + (int64_t)slot * a.Fmax + ft * 16 + n, tag_word(T, hv));
+            st_word(a.hw + (int64_t)slot * a.Fmax + ft * 16 + n, tag_word(T, hv));
         }
         STAMP(9);
         if (nrg == 0) return;
@@ -659,7 +674,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_co
             const uint64_t t0 = global_ns();
             for (int64_t it = 0; it < a.wait.iters; ++it) {
                 bool mine = true;
-                for (int u = lane; u < nblk; u += kWarp) mine &= word_tag(__ldcg(hs + 16 * u + 15)) == T;
+                for (int u = lane; u < nblk; u += kWarp) mine &= word_tag(ld_word(hs + 16 * u + 15)) == T;
                 if (__all_sync(0xffffffffu, mine)) {
                     ok = true;
                     break;
