@@ -646,16 +646,18 @@ def main():
             bst = float(np.mean([sum(union_bytes(stack[l], sa[i, l]) for l in range(nl)) for i in range(kst)])) \
                 + lm.nbytes
             nun = float(np.mean([len(np.unique(sa[i, l])) for i in range(kst) for l in range(nl)]))
+            # one row: up to 48 layers per launch (the residual row passes between layers inside the launch)
+            layer_launches = -(-nl // 48) if mst == 1 else nl
             sec[f"stack_m{mst}_{nl}layers"] = {
                 "us_per_step": ust, "tokens_per_s": mst / (ust * 1e-6), "bfp_bytes_per_step": bst,
                 "gbs": bst / (ust * 1e-6) / 1e9, "pct_of_measured_copy": 100 * bst / (ust * 1e-6) / 1e9 / peak,
-                "union_experts_per_layer": nun, "launches_per_step": nl + 1,
-                "timing": f"{kst} consecutive replays of the step ({nl} layer launches, then the LM head with the "
-                          "greedy token in its epilogue) captured in one CUDA graph, CUDA events",
+                "union_experts_per_layer": nun, "launches_per_step": layer_launches + 1,
+                "timing": f"{kst} consecutive replays of the step ({nl} layers in {layer_launches} launch(es), then "
+                          "the LM head with the greedy token in its epilogue) captured in one CUDA graph, CUDA events",
                 "us_per_step_eager": ust_eager,
                 "weights": f"{nl} layers with independent seeded weights (no layer repeats within a step); LM head "
                            f"BFP8 [{vocab} x {spec.hidden}] seeded N(0,0.02)",
-                "layer_kernel": "moe_row_kernel<4>" if mst == 1 else "moe_layer_kernel<4,1>"}
+                "layer_kernel": "moe_row_kernel<4, multi-layer>" if mst == 1 else "moe_layer_kernel<4,1>"}
             del wss
         # the LM head alone (330 MB, larger than L2: consecutive calls stream it from HBM)
         m8 = 8

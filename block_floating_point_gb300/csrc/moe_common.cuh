@@ -55,8 +55,8 @@ __device__ __forceinline__ void sort8_desc(uint32_t k[8], int q[8]) {
 // kRowNotApplicable when the layer's shape does not fit the path (the caller then launches the
 // general kernel). row_ws: the workspace's area for this path (row_ws_bytes bytes, 256-byte aligned,
 // zero after bfp_workspace_init): an epoch word; one mailbox of router logits per CTA (every CTA
-// writes its logits into every mailbox, so each CTA polls lines of its own); h of every slot. Values
-// travel as (epoch, value) 64-bit words.
+// writes its logits into every mailbox, so each CTA polls lines of its own); h of every slot; the residual
+// row between layers of one launch. Values travel as (epoch, value) 64-bit words.
 constexpr int kRowNotApplicable = 1;
 constexpr int kRowMaxCta = 256;  // CTAs of the one-row kernel at most (mailboxes in the area)
 __host__ __device__ inline int row_boxes(int sms) { return sms < kRowMaxCta ? sms : kRowMaxCta; }
@@ -64,11 +64,18 @@ __host__ __device__ inline size_t row_ws_logits_off() { return 256; }
 __host__ __device__ inline size_t row_ws_h_off(int E, int boxes) {
     return 256 + (((size_t)boxes * logit_stride(E) * 8 + 255) / 256) * 256;
 }
-__host__ __device__ inline size_t row_ws_bytes(int E, int K, int Fmax, int boxes) {
+__host__ __device__ inline size_t row_ws_x_off(int E, int K, int Fmax, int boxes) {
     return row_ws_h_off(E, boxes) + (size_t)(K + 1) * Fmax * 8;
 }
-int row_layer_launch(const bfp_moe_layer *layer, const uint16_t *x, int norm, float *y, uint16_t *h_out,
-                     int32_t *topk_idx, float *topk_w, uint32_t *status, uint8_t *row_ws, int fmax,
-                     cudaStream_t stream);
+__host__ __device__ inline size_t row_ws_bytes(int E, int K, int Fmax, int H, int boxes) {
+    return row_ws_x_off(E, K, Fmax, boxes) + (size_t)(H / 2) * 8;
+}
+// One launch for nl (1 .. 48) layers of one shape applied in order to one row: layer l + 1 takes layer l's
+// residual row (norm: the stack's bf16(x + y) then RMSNorm); x the first layer's input, y / h_out the last
+// layer's output, topk_idx / topk_w K entries per layer. kRowNotApplicable when the shapes differ or the
+// path does not fit them.
+int row_layers_launch(const bfp_moe_layer *layers, int nl, const uint16_t *x, int norm, float *y, uint16_t *h_out,
+                      int32_t *topk_idx, float *topk_w, uint32_t *status, uint8_t *row_ws, int fmax,
+                      cudaStream_t stream);
 
 }  // namespace bfp

@@ -1312,7 +1312,7 @@ static int plan_moe(const bfp_moe_layer *L, int m, MoePlan *p) {
     o = align_up(o + 4 * (size_t)m * (L->top_k + 1) * L->hidden, 256);
     p->off_row = o;  // the one-row kernel's exchange area (moe_row.cu): epoch word, tagged logits and h
     p->row_boxes = row_boxes(di.sms);
-    o = align_up(o + row_ws_bytes(L->n_experts, L->top_k, p->Fmax, p->row_boxes), 256);
+    o = align_up(o + row_ws_bytes(L->n_experts, L->top_k, p->Fmax, L->hidden, p->row_boxes), 256);
     p->ws_core = o;
     p->off_p1part = o;
     o = align_up(o + 4 * (size_t)p->ncta * (kMoeWarps - 1) * kP1PartFloats, 256);
@@ -1419,7 +1419,7 @@ static int moe_launch(const bfp_moe_layer *L, const uint16_t *x, int m, int norm
     a.wait = wait_cfg();
     a.wait_data = WaitCfg{kDefaultWaitIters, kDefaultWaitNanos};
     if (m == 1 && row_path()) {  // one row: the latency path (moe_row.cu), when the layer's shape fits it
-        rc = row_layer_launch(L, x, norm, y, h_out, topk_idx, topk_w, a.status, w + p.off_row, a.Fmax, st);
+        rc = row_layers_launch(L, 1, x, norm, y, h_out, topk_idx, topk_w, a.status, w + p.off_row, a.Fmax, st);
         if (rc != kRowNotApplicable) return rc;
     }
     if (L->expert_fmt == BFP_FMT_BFP4)
@@ -1497,7 +1497,24 @@ static int stack_run(const bfp_moe_layer *layers, int n_layers, const bfp_matrix
     uint16_t *hb2 = reinterpret_cast<uint16_t *>(w + mb + lb);
     uint16_t *cur = h, *nxt = hb2;
     int32_t *idx = topk_idx;  // layer l's selection follows the layers before it, m * top_k entries each
-    for (int l = 0; l < n_layers; ++l) {
+    int l0 = 0;               // layers done
+    if (m == 1 && row_path()) {
+        // one row: the layers in as few launches as possible (each runs up to 48 layers of one shape, the
+        // residual row passing between them inside the launch), h updated in place
+        MoePlan p;
+        rc = plan_moe(&layers[0], 1, &p);
+        if (rc) return rc;
+        while (l0 < n_layers) {
+            const int nl = std::min(48, n_layers - l0);
+            rc = row_layers_launch(&layers[l0], nl, h, 1, nullptr, h, idx, nullptr, reinterpret_cast<uint32_t *>(w),
+                                   w + p.off_row, p.Fmax, st);
+            if (rc == kRowNotApplicable) break;  // the remaining layers one launch each
+            if (rc) return rc;
+            if (idx) idx += (int64_t)nl * layers[l0].top_k;
+            l0 += nl;
+        }
+    }
+    for (int l = l0; l < n_layers; ++l) {
         rc = moe_launch(&layers[l], cur, m, 1, nullptr, nxt, idx, nullptr, ws, mb, st);
         if (rc) return rc;
         if (idx) idx += (int64_t)m * layers[l].top_k;
@@ -1586,7 +1603,7 @@ extern "C" int moe_decode_layer_static(const bfp_moe_layer *layer, const uint16_
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(static scratch counters)");
     if (m == 1) {  // the one-row kernel's epoch word and tagged words start over too
         e = cudaMemsetAsync(static_cast<uint8_t *>(ws) + p.off_row, 0,
-                            row_ws_bytes(layer->n_experts, layer->top_k, p.Fmax, p.row_boxes), st);
+                            row_ws_bytes(layer->n_experts, layer->top_k, p.Fmax, layer->hidden, p.row_boxes), st);
         if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(static scratch, one-row area)");
     }
     return moe_launch(layer, x, m, 0, y, nullptr, topk_idx, topk_w, ws, kStaticScratchBytes, st);

@@ -1,5 +1,7 @@
-// One-row MoE decode layer: moe_decode_layer (and each layer of moe_stack_decode)
-// with m = 1, the single-sequence decode step.
+// One-row MoE decode layer: moe_decode_layer (and the layers of moe_stack_decode)
+// with m = 1, the single-sequence decode step. One launch runs one layer, or up
+// to 48 layers of one shape in order (the decode stack), the residual row
+// passing from layer to layer inside the launch.
 //
 // What it computes is the layer of moe_layer.cu (Qwen3.6-35B-A3B card, "Fused
 // decode kernels": MoE decode of one row through device top-k routing and
@@ -15,22 +17,21 @@
 //   - every CTA's work is fixed at launch. One row always selects exactly
 //     top_k experts, so the list [shared f-tiles, f-tiles of slot 0, slot 1,
 //     ...] (an f-tile: 16 ffn rows of gate and up over the whole hidden
-//     dimension) and each CTA's range of it are known before the router runs;
-//     only which expert fills a slot is not;
+//     dimension) and each CTA's range of it (whole f-tiles, split evenly) are
+//     known before the router runs; only which expert fills a slot is not;
 //   - each CTA owns whole row groups of the output (16 hidden rows) for the
 //     down projections of every selected expert and sums them itself in slot
-//     order: no combine pass, no third grid-wide wait. The f-tile ranges are
-//     balanced against those row groups (a CTA with down rows takes fewer
-//     f-tiles);
+//     order: no combine pass, no third grid-wide wait;
 //   - what does not depend on the previous kernel or on the routing (the CTA's
 //     router rows, its shared-expert f-tiles and shared down rows) is requested
 //     before the kernel waits for the previous kernel to finish;
 //   - everything a CTA reads (about 115 KB at the full size) fits in its shared
-//     memory, so all of its weight copies (1D bulk copies, the TMA engine) are
-//     issued at once when the routing is known, and the whole step streams at
-//     full memory-level parallelism;
-//   - two grid-wide waits: the router logits (then every warp takes the top-k
-//     itself) and h.
+//     memory: each slot's f-tiles are requested (1D bulk copies, the TMA
+//     engine) in the top-k round that decides the slot, the down rows once the
+//     gate/up bytes are in;
+//   - two grid-wide exchanges per layer: the router logits (then one warp of
+//     every CTA takes the top-k) and h; a third between layers (the residual
+//     row), all through (epoch, value) words, no counters.
 // Contractions run on the tensor cores (mma.sync m16n8k16, BFP codes placed so
 // that a rotate and a mask give exact fp16 values, one BFP block per MMA, its
 // 2^(E-127) folded into the fp32 sum right after); with one row only column 0
@@ -57,17 +58,21 @@ constexpr int kRowMaxUnits = 32; // most f-tile units per CTA (one thread per (u
 constexpr int kRowMaxRouterRows = 4;  // most router rows (with the shared-gate row) per CTA
 constexpr int kRowRouterRegs = 4;     // 16-byte router vectors held by each thread
 
-struct RowArgs {
-    int H, E, F, K, Fs, ncta;
-    const uint16_t *x;
-    int norm;
-    float eps;
+// One layer's weights (every layer of a launch has the same shape).
+struct RowLayer {
     const uint16_t *router;
     const float *rbias;
     const uint16_t *sgate;
-    const uint8_t *gu, *dn;
+    const uint8_t *gu, *dn, *sgu, *sdn;
+};
+constexpr int kRowStackMax = 48;  // layers one launch runs (a longer stack takes several launches)
+
+struct RowArgs {
+    int H, E, F, K, Fs, ncta, nl;
+    const uint16_t *x;
+    int norm;
+    float eps;
     int64_t gu_stride, dn_stride;
-    const uint8_t *sgu, *sdn;
     float *y;
     uint16_t *h_out;
     int32_t *topk_idx;
@@ -80,10 +85,12 @@ struct RowArgs {
     unsigned long long *lgw;  // [CTA][lsb]: every CTA's mailbox of router logits, the shared-gate logit last
     int lsb;                  // words per mailbox
     unsigned long long *hw;   // [K + 1][Fmax] h of each slot (slot K: the shared expert)
+    unsigned long long *xw;   // [H / 2] the residual row after a layer (two bf16 per word), for the next layer
     int rec, kc_h, kc_f, kc_fs, nft, nft_s, ng_d, Fmax, kbf;
     int off_stage, off_xc, off_hc, off_p1, off_p2, off_misc;
     WaitCfg wait, wait_data;
     int16_t ub[kRowMaxCta + 1];  // CTA c takes f-tile units [ub[c], ub[c + 1]) of the list
+    RowLayer layer[kRowStackMax];  // layers 0 .. nl - 1, applied in order (topk_idx: K entries per layer)
 };
 
 struct RowMisc {
@@ -186,7 +193,9 @@ __device__ __forceinline__ void row_mma(const uint8_t *const recs[NREC], const u
     }
 }
 
-template <int FMT>
+// MULTI: several layers per launch (a.nl); otherwise exactly one (the loop and the exchange of the residual row
+// compile away).
+template <int FMT, bool MULTI>
 __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_constant__ RowArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int CB = FMT == 4 ? 4 : 2;
@@ -270,10 +279,11 @@ __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_co
     grid_dep_launch_dependents();
 
     bool bad = false;
-    uint32_t armed_u = 0u;     // thread 0: units whose copy it issued
-    bool armed_p2rt = false;   // thread 0: the routed down rows issued
+    uint32_t armed_u = 0u;     // thread 0: units whose copy it issued (this layer)
+    bool armed_p2rt = false;   // thread 0: the routed down rows issued (this layer)
+    bool armed_p2sh = false;   // thread 32: the shared down rows issued (this layer)
     bool routed = false;       // warp 0: the top-k is done and the routed f-tile units are requested
-    const bool armed_p2sh = nrg > 0;
+    uint32_t par = 0u;         // phase parity of this layer's copies (one phase per layer on each barrier)
     const uint64_t pol = l2_evict_first();  // weights are read once per launch
     // Pieces of this warp: fn(local unit j, first record, end record) for every unit, in order (piece j).
     auto for_pieces = [&](auto fn) {
@@ -286,42 +296,6 @@ __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_co
         bulk_g2s_hint(w1 + j * ubytes, src, (uint32_t)ubytes, &ms->bar_u[j], pol);
         armed_u |= 1u << j;
     };
-
-    // ---- 0. weights that depend on nothing: router rows (and the shared-gate row), the shared expert's
-    //         f-tiles of this CTA, its shared down rows; issued before waiting for the previous kernel
-    // the CTA's router rows (and the shared-gate row) straight into registers: thread t holds 16-byte
-    // vectors t, t + 512, ... of the rows laid end to end
-    const int nvec = a.H / 8, nitems = (rr1 - rr0) * nvec;
-    uint4 rwv[kRowRouterRegs];
-#pragma unroll
-    for (int j = 0; j < kRowRouterRegs; ++j) {
-        const int it = tid + j * kRowThreads;
-        rwv[j] = make_uint4(0u, 0u, 0u, 0u);
-        if (it < nitems) {
-            const int row = it / nvec, v = it - row * nvec;
-            const uint16_t *src = rr0 + row < a.E ? a.router + (int64_t)(rr0 + row) * a.H : a.sgate;
-            rwv[j] = __ldg(reinterpret_cast<const uint4 *>(src) + v);
-        }
-    }
-    if (tid == 0)
-        for (int jj = 0; jj < nu && u0 + jj < a.nft_s; ++jj)
-            copy_unit(a.sgu + (int64_t)(2 * (u0 + jj)) * a.kc_h * a.rec, jj);
-    if (tid == 32 && armed_p2sh) {
-        mbar_arrive_expect_tx(&ms->bar_p2sh, (uint32_t)(nrg * a.kc_fs * a.rec));
-        for (int j = 0; j < nrg; ++j) {
-            const int rg = c + j * a.ncta;
-            bulk_g2s_hint(w2 + (int64_t)(j * IPR + a.K * a.kc_f) * a.rec, a.sdn + (int64_t)rg * a.kc_fs * a.rec,
-                          (uint32_t)(a.kc_fs * a.rec), &ms->bar_p2sh, pol);
-        }
-    }
-    grid_dep_wait();  // the previous kernel (which may have written x) has finished
-    if (tid == 0) ms->ep = *reinterpret_cast<volatile uint32_t *>(a.epoch);  // the previous launch's last word
-    if (tid == 0) {
-        mbar_arrive_expect_tx(&ms->bar_x, (uint32_t)a.H * 2);
-        bulk_g2s(xs, a.x, (uint32_t)a.H * 2, &ms->bar_x);
-    }
-    STAMP(1);
-
     auto abort_warp = [&]() {
         bad = true;
         if (lane == 0) {
@@ -335,7 +309,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_co
             const int pi = j;
             const bool sh = u0 + j < a.nft_s;
             if (sh == shared_kind) {
-                if (!bad && !__all_sync(0xffffffffu, mbar_wait(&ms->bar_u[j], 0u, a.wait_data, vflags))) abort_warp();
+                if (!bad && !__all_sync(0xffffffffu, mbar_wait(&ms->bar_u[j], par, a.wait_data, vflags))) abort_warp();
                 __syncwarp();  // reconverge before the warp-wide MMAs (lane 0 may have polled alone)
                 float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
                 const bool first_routed = !sh && (j == 0 || u0 + j == a.nft_s);
@@ -360,10 +334,87 @@ __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_co
         });
     };
 
+    // ---- the layers, one after another: every CTA takes the same share of each; a layer's input row is the
+    //      residual row the previous layer's CTAs left, exchanged as tagged words like h
+    const int nl = MULTI ? a.nl : 1;
+    for (int l = 0; l < nl; ++l) {
+    const RowLayer &Ly = a.layer[l];
+    par = (uint32_t)l & 1u;
+    if (l > 0) {
+        __syncthreads();  // every reader of the previous layer's shared-memory operands is done
+        if (tid == 0)
+            for (int i = 0; i <= kMaxTopK; ++i) ms->slot_ready[i] = 0;
+        armed_u = 0u;  // the previous layer's copies were all consumed
+        armed_p2rt = false;
+        routed = false;
+    }
+        // ---- 0. weights that depend on nothing: router rows (and the shared-gate row), the shared expert's
+        //         f-tiles of this CTA, its shared down rows; issued before waiting for the previous kernel
+        // the CTA's router rows (and the shared-gate row) straight into registers: thread t holds 16-byte
+        // vectors t, t + 512, ... of the rows laid end to end
+        const int nvec = a.H / 8, nitems = (rr1 - rr0) * nvec;
+        uint4 rwv[kRowRouterRegs];
+    #pragma unroll
+        for (int j = 0; j < kRowRouterRegs; ++j) {
+            const int it = tid + j * kRowThreads;
+            rwv[j] = make_uint4(0u, 0u, 0u, 0u);
+            if (it < nitems) {
+                const int row = it / nvec, v = it - row * nvec;
+                const uint16_t *src = rr0 + row < a.E ? Ly.router + (int64_t)(rr0 + row) * a.H : Ly.sgate;
+                rwv[j] = __ldg(reinterpret_cast<const uint4 *>(src) + v);
+            }
+        }
+        if (tid == 0)
+            for (int jj = 0; jj < nu && u0 + jj < a.nft_s; ++jj)
+                copy_unit(Ly.sgu + (int64_t)(2 * (u0 + jj)) * a.kc_h * a.rec, jj);
+        armed_p2sh = nrg > 0;
+        if (tid == 32 && armed_p2sh) {
+            mbar_arrive_expect_tx(&ms->bar_p2sh, (uint32_t)(nrg * a.kc_fs * a.rec));
+            for (int j = 0; j < nrg; ++j) {
+                const int rg = c + j * a.ncta;
+                bulk_g2s_hint(w2 + (int64_t)(j * IPR + a.K * a.kc_f) * a.rec, Ly.sdn + (int64_t)rg * a.kc_fs * a.rec,
+                              (uint32_t)(a.kc_fs * a.rec), &ms->bar_p2sh, pol);
+            }
+        }
+        if (l == 0) {
+            grid_dep_wait();  // the previous kernel (which may have written x) has finished
+            if (tid == 0) ms->ep = *reinterpret_cast<volatile uint32_t *>(a.epoch);  // the previous launch's last word
+            if (tid == 0) {
+                mbar_arrive_expect_tx(&ms->bar_x, (uint32_t)a.H * 2);
+                bulk_g2s(xs, a.x, (uint32_t)a.H * 2, &ms->bar_x);
+            }
+        }
+        STAMP(1);
+
+
     [&]() {
         // ---- 1. the activation row: statistics (spread over the CTA, one barrier), then this CTA's router
         //         logits
-        if (!__all_sync(0xffffffffu, mbar_wait(&ms->bar_x, 0u, a.wait_data, nullptr))) abort_warp();
+        if (l == 0) {
+            if (!__all_sync(0xffffffffu, mbar_wait(&ms->bar_x, 0u, a.wait_data, nullptr))) abort_warp();
+        } else {
+            // the residual row the previous layer left, tagged with that layer's epoch: each thread the words
+            // of its own 16-byte vectors of the row (the statistics below read exactly those)
+            const uint32_t Tp = ms->ep + (uint32_t)l;
+            bool seen = false;
+            const uint64_t t0 = global_ns();
+            for (int64_t it = 0; !bad && it < a.wait.iters; ++it) {
+                bool mine = true;
+                for (int v = tid; v < a.H / 8; v += kRowThreads) {
+                    const ulonglong2 w0 = ld_words2(a.xw + 4 * v), w1v = ld_words2(a.xw + 4 * v + 2);
+                    mine &= word_tag(w0.x) == Tp && word_tag(w0.y) == Tp && word_tag(w1v.x) == Tp &&
+                            word_tag(w1v.y) == Tp;
+                    reinterpret_cast<uint4 *>(xs)[v] =
+                        make_uint4((uint32_t)w0.x, (uint32_t)w0.y, (uint32_t)w1v.x, (uint32_t)w1v.y);
+                }
+                if (__all_sync(0xffffffffu, mine)) {
+                    seen = true;
+                    break;
+                }
+                if (global_ns() - t0 > a.wait.nanos) break;
+            }
+            if (!seen) abort_warp();
+        }
         __syncwarp();  // warps left diverged (lane-0 copy issue above) run warp collectives many times slower
         STAMP(2);
         // every thread a 16-byte vector (or none), warp partials, then every thread adds the 16 partials in
@@ -453,7 +504,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_co
                 float acc = 0.f;
                 for (int w = 0; w < NW; ++w) acc += ms->red[w][tid];
                 const int row = rr0 + tid;
-                if (row < a.E && a.rbias) acc += a.rbias[row];
+                if (row < a.E && Ly.rbias) acc += Ly.rbias[row];
                 ms->lgv[tid] = acc;
             }
             __syncthreads();
@@ -461,7 +512,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_co
             // into every CTA's mailbox (a poller reads only its own lines)
             for (int q = tid; q < a.ncta * nr; q += kRowThreads) {
                 const int box = q / nr, r = q - box * nr;
-                st_word(a.lgw + (int64_t)box * a.lsb + rr0 + r, tag_word(ms->ep + 1u, ms->lgv[r]));
+                st_word(a.lgw + (int64_t)box * a.lsb + rr0 + r, tag_word(ms->ep + 1u + (uint32_t)l, ms->lgv[r]));
             }
             CSTAMP(95);
             __threadfence();  // push the stores out now (nothing waits on this fence but this thread)
@@ -478,7 +529,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_co
         if (warp == 0) {
             // poll every CTA's logits (lane l: experts 8l .. 8l+7, and the shared-gate logit) until each word
             // carries this launch's epoch
-            const uint32_t T = ms->ep + 1u;
+            const uint32_t T = ms->ep + 1u + (uint32_t)l;
             unsigned long long wv[8], wgate = 0ull;
             bool ok = false;
             {
@@ -542,7 +593,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_co
                         my_l = key_value(kmax);
                     }
                     if (su_l == s)
-                        copy_unit(a.gu + (int64_t)es * a.gu_stride + (int64_t)(2 * (r_l - s * a.nft)) * a.kc_h * a.rec, lane);
+                        copy_unit(Ly.gu + (int64_t)es * a.gu_stride + (int64_t)(2 * (r_l - s * a.nft)) * a.kc_h * a.rec, lane);
                     __syncwarp();
                     const bool win = lane == wl;
 #pragma unroll
@@ -569,8 +620,8 @@ __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_co
                 if (lane < a.K) {
                     ms->wsl[lane] = my_w;
                     if (c == 0) {
-                        if (a.topk_idx) a.topk_idx[lane] = my_e;
-                        if (a.topk_w) a.topk_w[lane] = my_w;
+                        if (a.topk_idx) a.topk_idx[(int64_t)l * a.K + lane] = my_e;
+                        if (a.topk_w) a.topk_w[(int64_t)l * a.K + lane] = my_w;
                     }
                 }
                 if (lane == 0) ms->wsl[a.K] = __fdividef(1.0f, 1.0f + __expf(-gate_logit));
@@ -619,7 +670,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_co
                 for (int j = 0; j < nrg; ++j) {
                     const int rg = c + j * a.ncta;
                     bulk_g2s_hint(w2 + (int64_t)(j * IPR + lane * a.kc_f) * a.rec,
-                                  a.dn + (int64_t)e * a.dn_stride + (int64_t)rg * a.kc_f * a.rec,
+                                  Ly.dn + (int64_t)e * a.dn_stride + (int64_t)rg * a.kc_f * a.rec,
                                   (uint32_t)(a.kc_f * a.rec), &ms->bar_p2rt, pol);
                 }
             }
@@ -633,7 +684,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_co
         }
         STAMP(8);
         // each unit's pieces summed in warp order -> h = silu(gate) * up, out as tagged words
-        const uint32_t T = ms->ep + 1u;
+        const uint32_t T = ms->ep + 1u + (uint32_t)l;
         if (tid < nu * 16) {
             const int j = tid >> 4, n = tid & 15;
             float sg = 0.f, su = 0.f;
@@ -747,8 +798,8 @@ __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_co
             if (lane == 0) reinterpret_cast<volatile int *>(ms->slot_ready)[s] = 1;
             if (s == 0) STAMP(10);
         }
-        if (!bad && !__all_sync(0xffffffffu, mbar_wait(&ms->bar_p2sh, 0u, a.wait_data, vflags) &&
-                                                 mbar_wait(&ms->bar_p2rt, 0u, a.wait_data, vflags)))
+        if (!bad && !__all_sync(0xffffffffu, mbar_wait(&ms->bar_p2sh, par, a.wait_data, vflags) &&
+                                                 mbar_wait(&ms->bar_p2rt, par, a.wait_data, vflags)))
             abort_warp();
         __syncwarp();
         STAMP(11);
@@ -824,22 +875,34 @@ __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_co
             ysl[it] = mul_pow2(ps, 24 - (MB - 1) - ms->shift_s[s]);
         }
         __syncthreads();
-        if (tid < nrg * 16) {
+        if (tid < ((nrg * 16 + kWarp - 1) & ~(kWarp - 1))) {  // whole warps (the pairing shuffle)
             const int j = tid >> 4, n = tid & 15;
-            float yv[kMaxTopK + 1];
-#pragma unroll
-            for (int s = 0; s <= kMaxTopK; ++s) yv[s] = s <= a.K ? ysl[(j * (a.K + 1) + s) * 16 + n] : 0.f;
+            const bool live = tid < nrg * 16;
             float ysum = 0.f;
+            if (live) {
+                float yv[kMaxTopK + 1];
 #pragma unroll
-            for (int s = 0; s <= kMaxTopK; ++s)
-                if (s <= a.K) ysum += yv[s];
+                for (int s = 0; s <= kMaxTopK; ++s) yv[s] = s <= a.K ? ysl[(j * (a.K + 1) + s) * 16 + n] : 0.f;
+#pragma unroll
+                for (int s = 0; s <= kMaxTopK; ++s)
+                    if (s <= a.K) ysum += yv[s];
+            }
             const int o = (c + j * a.ncta) * 16 + n;
-            if (o < a.H) {
-                if (a.y) a.y[o] = ysum;
-                if (a.h_out) a.h_out[o] = f32_to_bf16_bits(bf16_bits_to_f32(a.x[o]) + ysum);
+            const bool inrow = live && o < a.H;
+            const uint32_t hb = inrow ? f32_to_bf16_bits(bf16_bits_to_f32(xs[o]) + ysum) : 0u;  // the residual row
+            if (l == nl - 1) {
+                if (inrow && a.y) a.y[o] = ysum;
+                if (inrow && a.h_out) a.h_out[o] = (uint16_t)hb;
+            } else {
+                // rows 2i, 2i + 1 as word i, tagged with this layer's epoch, for the next layer
+                const uint32_t hb1 = __shfl_down_sync(0xffffffffu, hb, 1);
+                if (inrow && !(n & 1))
+                    st_word(a.xw + o / 2, ((unsigned long long)(ms->ep + 1u + (uint32_t)l) << 32) | hb | (hb1 << 16));
             }
         }
     }();
+    if (bad) break;
+    }
 
     // No copy may still be landing in shared memory when the CTA exits (every path).
     {
@@ -847,10 +910,10 @@ __global__ void __launch_bounds__(kRowThreads, 1) moe_row_kernel(const __grid_co
         if (tid == 0) {
             mbar_wait(&ms->bar_x, 0u, drain, nullptr);
             for (int j = 0; j < nu; ++j)
-                if ((armed_u >> j) & 1u) mbar_wait(&ms->bar_u[j], 0u, drain, nullptr);
-            if (armed_p2rt) mbar_wait(&ms->bar_p2rt, 0u, drain, nullptr);
+                if ((armed_u >> j) & 1u) mbar_wait(&ms->bar_u[j], par, drain, nullptr);
+            if (armed_p2rt) mbar_wait(&ms->bar_p2rt, par, drain, nullptr);
         }
-        if (tid == 32 && armed_p2sh) mbar_wait(&ms->bar_p2sh, 0u, drain, nullptr);
+        if (tid == 32 && armed_p2sh) mbar_wait(&ms->bar_p2sh, par, drain, nullptr);
     }
     WSTAMP(48);
     __syncthreads();
@@ -936,9 +999,9 @@ static bool plan_row(const bfp_moe_layer *L, const Geometry &gu, const Geometry 
     return (int64_t)p->smem <= (int64_t)smem_optin;
 }
 
-template <int FMT>
+template <int FMT, bool MULTI>
 static int launch_row_t(const RowArgs &a, size_t smem, cudaStream_t st) {
-    auto kern = moe_row_kernel<FMT>;
+    auto kern = moe_row_kernel<FMT, MULTI>;
     int rc = set_smem_attr(reinterpret_cast<const void *>(kern), (int)smem, "cudaFuncSetAttribute(moe_row)");
     if (rc) return rc;
     cudaError_t e;
@@ -968,8 +1031,17 @@ extern "C" int bfp_debug_set_trace_row(void *buf) {
 }
 #endif
 
-int row_layer_launch(const bfp_moe_layer *L, const uint16_t *x, int norm, float *y, uint16_t *h_out,
-                     int32_t *topk_idx, float *topk_w, uint32_t *status, uint8_t *row_ws, int fmax, cudaStream_t st) {
+int row_layers_launch(const bfp_moe_layer *Ls, int nl, const uint16_t *x, int norm, float *y, uint16_t *h_out,
+                      int32_t *topk_idx, float *topk_w, uint32_t *status, uint8_t *row_ws, int fmax, cudaStream_t st) {
+    if (nl < 1 || nl > kRowStackMax) return kRowNotApplicable;
+    const bfp_moe_layer *L = Ls;
+    for (int l = 1; l < nl; ++l) {  // one launch runs layers of one shape
+        const bfp_moe_layer &M = Ls[l];
+        if (M.hidden != L->hidden || M.n_experts != L->n_experts || M.ffn != L->ffn || M.top_k != L->top_k ||
+            M.shared_ffn != L->shared_ffn || M.expert_fmt != L->expert_fmt || M.gate_up_stride != L->gate_up_stride ||
+            M.down_stride != L->down_stride)
+            return kRowNotApplicable;
+    }
     DeviceInfo di;
     int rc = device_info(&di);
     if (rc) return rc;
@@ -1015,18 +1087,22 @@ int row_layer_launch(const bfp_moe_layer *L, const uint16_t *x, int norm, float 
     a.K = L->top_k;
     a.Fs = L->shared_ffn;
     a.ncta = p.ncta;
+    a.nl = nl;
     a.x = x;
     a.norm = norm;
     a.eps = 1e-6f;
-    a.router = L->router;
-    a.rbias = L->router_bias;
-    a.sgate = L->shared_gate;
-    a.gu = static_cast<const uint8_t *>(L->experts_gate_up);
-    a.dn = static_cast<const uint8_t *>(L->experts_down);
     a.gu_stride = L->gate_up_stride;
     a.dn_stride = L->down_stride;
-    a.sgu = static_cast<const uint8_t *>(L->shared_gate_up);
-    a.sdn = static_cast<const uint8_t *>(L->shared_down);
+    for (int l = 0; l < nl; ++l) {
+        RowLayer &w = a.layer[l];
+        w.router = Ls[l].router;
+        w.rbias = Ls[l].router_bias;
+        w.sgate = Ls[l].shared_gate;
+        w.gu = static_cast<const uint8_t *>(Ls[l].experts_gate_up);
+        w.dn = static_cast<const uint8_t *>(Ls[l].experts_down);
+        w.sgu = static_cast<const uint8_t *>(Ls[l].shared_gate_up);
+        w.sdn = static_cast<const uint8_t *>(Ls[l].shared_down);
+    }
     a.y = y;
     a.h_out = h_out;
     a.topk_idx = topk_idx;
@@ -1036,6 +1112,8 @@ int row_layer_launch(const bfp_moe_layer *L, const uint16_t *x, int norm, float 
     a.lgw = reinterpret_cast<unsigned long long *>(row_ws + row_ws_logits_off());
     a.lsb = logit_stride(L->n_experts);
     a.hw = reinterpret_cast<unsigned long long *>(row_ws + row_ws_h_off(L->n_experts, row_boxes(di.sms)));
+    a.xw = reinterpret_cast<unsigned long long *>(row_ws +
+                                                  row_ws_x_off(L->n_experts, L->top_k, fmax, row_boxes(di.sms)));
     a.rec = gu.rec;
     a.kc_h = (int)gu.kc;
     a.kc_f = (int)dn.kc;
@@ -1054,7 +1132,9 @@ int row_layer_launch(const bfp_moe_layer *L, const uint16_t *x, int norm, float 
     a.wait = wait_cfg();
     a.wait_data = WaitCfg{kDefaultWaitIters, kDefaultWaitNanos};
     for (int c = 0; c <= kRowMaxCta; ++c) a.ub[c] = c <= p.ncta ? p.ub[c] : p.ub[p.ncta];
-    return L->expert_fmt == BFP_FMT_BFP4 ? launch_row_t<4>(a, p.smem, st) : launch_row_t<8>(a, p.smem, st);
+    if (nl > 1)
+        return L->expert_fmt == BFP_FMT_BFP4 ? launch_row_t<4, true>(a, p.smem, st) : launch_row_t<8, true>(a, p.smem, st);
+    return L->expert_fmt == BFP_FMT_BFP4 ? launch_row_t<4, false>(a, p.smem, st) : launch_row_t<8, false>(a, p.smem, st);
 }
 
 }  // namespace bfp

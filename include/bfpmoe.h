@@ -292,7 +292,7 @@ int moe_decode_layer(const bfp_moe_layer *layer, const uint16_t *x, int m, float
  *     and held until the process exits. A layer whose core state needs more
  *     (the workspace without its optional phase-1 hand-off area) is rejected
  *     with BFP_EWORKSPACE; the full-size layer (hidden 2048, 256 experts,
- *     ffn 512, top-8) needs 1,845,760 bytes on a 152-SM GPU (the one-row
+ *     ffn 512, top-8) needs 1,853,952 bytes on a 152-SM GPU (the one-row
  *     kernel's exchange area grows with the SM count).
  *   - The first call on a device looks up the array's device address and
  *     zeroes it, synchronously: make that first call before any stream
@@ -320,7 +320,12 @@ int moe_decode_layer_static(const bfp_moe_layer *layer, const uint16_t *x, int m
  * [vocab x hidden] in device memory. topk_idx (nullable, device int32): every
  * layer's selection in slot order, layer after layer, m * layers[l].top_k
  * entries for layer l (row-major [m x top_k]). ws: moe_stack_workspace_size
- * bytes.
+ * bytes. Launches: with m = 1 (and the one-row kernel, bfp_set_row_path) the
+ * layers run up to 48 per launch when consecutive layers share a shape (P1
+ * "Fused decode kernels": fewer, larger device programs): every CTA takes
+ * the same share of each layer and the residual row passes from layer to
+ * layer inside the launch; otherwise one launch per layer. Then one launch
+ * for the LM head.
  */
 int moe_stack_workspace_size(const bfp_moe_layer *layers, int n_layers, const bfp_matrix *lm_head, int m,
                              size_t *bytes);

@@ -200,3 +200,37 @@ def test_full_size_stack_sampled_logits():
     case = StackCase(synth.FULL, n_layers=3, vocab=151936, seed=803)
     rng = np.random.default_rng(5)
     run_stack(case, 8, 0, sample_vocab=np.sort(rng.choice(151936, 512, replace=False)))
+
+
+@pytest.mark.parametrize("spec,n_layers,seed", [(synth.TINY, 50, 811), (synth.FULL, 3, 812)], ids=["tiny_50", "full_3"])
+def test_one_row_stack_in_one_launch_matches_layer_by_layer(spec, n_layers, seed):
+    """With one row the stack runs up to 48 layers in one launch, the residual row passing from layer to layer
+    inside it (50 layers: two launches); one-layer stacks chained through global memory give the same bits:
+    the final h, every layer's selection and the logits."""
+    case = StackCase(spec, n_layers=n_layers, vocab=1000, seed=seed)
+    layers, lm = case.device()
+    h0 = synth.to_bf16_bits(synth.normal(seed, synth.stream_id(synth.KIND_STACK_H, 0, 0, 0, 0), (spec.hidden,),
+                                         std=1.0))[None, :]
+    k = spec.top_k
+    ws = bfp.moe_stack_workspace(layers, lm, 1)
+    h_a = bf16_tensor(h0)
+    idx_a = torch.full((n_layers, 1, k), -1, dtype=torch.int32, device="cuda")
+    lg_a = bfp.moe_stack_decode(layers, lm, h_a, ws, topk_idx=idx_a)
+    torch.cuda.synchronize()
+    assert bfp.workspace_status(ws) == bfp.BFP_OK
+    h_b = bf16_tensor(h0)
+    idx_b = torch.full((n_layers, 1, k), -1, dtype=torch.int32, device="cuda")
+    ws1 = bfp.moe_stack_workspace([layers[0]], lm, 1)
+    for l in range(n_layers):
+        lg_b = bfp.moe_stack_decode([layers[l]], lm, h_b, ws1, topk_idx=idx_b[l])
+    torch.cuda.synchronize()
+    assert bfp.workspace_status(ws1) == bfp.BFP_OK
+    assert torch.equal(idx_a, idx_b)
+    assert torch.equal(h_a, h_b)
+    assert torch.equal(lg_a, lg_b)
+    # the same stack again on the same workspace (the exchange words carry the next launch's epochs)
+    h_c = bf16_tensor(h0)
+    lg_c = bfp.moe_stack_decode(layers, lm, h_c, ws)
+    torch.cuda.synchronize()
+    assert bfp.workspace_status(ws) == bfp.BFP_OK
+    assert torch.equal(h_c, h_a) and torch.equal(lg_c, lg_a)
