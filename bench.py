@@ -64,7 +64,7 @@ def kernel_src_sha() -> str:
     return h.hexdigest()[:16]
 
 
-CASES = ("m1", "m16_hot", "dense_m1", "dense_m16", "dense_m32", "lm_greedy_m8", "attn_32k")
+CASES = ("m1", "m16_hot", "dense_m1", "dense_m16", "dense_m32", "dense_m32_tc", "lm_greedy_m8", "attn_32k")
 
 
 def parse_args():
@@ -370,7 +370,9 @@ def run_case(args):
         y = torch.empty((m, spec.hidden), dtype=torch.float32, device=device)
         step = lambda: bfp.moe_decode_layer(L, x, ws, y=y)
     elif case.startswith("dense_m"):
-        m = int(case[len("dense_m"):])
+        m = int(case[len("dense_m"):].split("_")[0])
+        if case.endswith("_tc"):
+            bfp.set_linear_path(2)  # the tcgen05 kernel
         w = synth.normal(args.seed, synth.stream_id(synth.KIND_DENSE), (8192, 2048), std=0.02)
         mat = bfp.DeviceMatrix.from_host(8, 8192, 2048, bfp.encode(8, w), device=device)
         x = torch.from_numpy(np.stack([synth.activation_row(args.seed, 50000 + r, 2048, False)
@@ -575,19 +577,37 @@ def main():
         gh = float(np.mean([bh[i % R] for i in range(ksec)])) / (ush * 1e-6) / 1e9
         sec["m16_hot"] = {"us_per_layer": ush, "gbs": gh, "pct_of_8tbs": 100 * gh / NOMINAL_HBM_GBS,
                           "union_experts_per_step": nh, "timing": "each step alone after a 256 MB L2 flush"}
-        # dense BFP8 projection [8192 x 2048], M = 1 / 8 / 16
+        # dense BFP8 projection [8192 x 2048], M = 1 / 8 / 16 / 32: alone after a flush (launch latency included)
+        # and back to back (a CUDA graph over 12 distinct matrices, 214 MB > L2, as inside a decode step); at 16
+        # and 32 rows also the tcgen05 kernel (bfp_set_linear_path(2))
         w = synth.normal(args.seed, synth.stream_id(synth.KIND_DENSE), (8192, 2048), std=0.02)
-        mat = bfp.DeviceMatrix.from_host(8, 8192, 2048, bfp.encode(8, w), device=device)
-        for m in (1, 8, 16):
+        mats = [bfp.DeviceMatrix.from_host(8, 8192, 2048, bfp.encode(8, w), device=device)]
+        for i in range(1, 12):
+            mats.append(bfp.DeviceMatrix.from_host(8, 8192, 2048, bfp.encode(8, synth.normal(
+                args.seed, synth.stream_id(synth.KIND_DENSE, i), (8192, 2048), std=0.02)), device=device))
+        mat = mats[0]
+        for m, path in ((1, 0), (8, 0), (16, 0), (32, 0), (16, 2), (32, 2)):
             xd_ = torch.from_numpy(np.stack([synth.activation_row(args.seed, 50000 + r, 2048, False)
                                              for r in range(m)]).view(np.int16)).to(device)
             wsl = bfp.linear_workspace(mat, m)
             yl = torch.empty((m, 8192), dtype=torch.int16, device=device)
-            tot, _ = timed_flushed(lambda i: bfp.linear(mat, xd_, wsl, y_bf16=yl), ksec, 5, flush)
+            bfp.set_linear_path(path)
+            try:
+                tot, _ = timed_flushed(lambda i: bfp.linear(mat, xd_, wsl, y_bf16=yl), ksec, 5, flush)
+                usb = timed_graph(lambda i: bfp.linear(mats[i % 12], xd_, wsl, y_bf16=yl), 198, 10, True) * 1e3 / 198
+            finally:
+                bfp.set_linear_path(0)
+            assert bfp.workspace_status(wsl) == bfp.BFP_OK
             usd = tot * 1e3 / ksec
             gd = mat.nbytes / (usd * 1e-6) / 1e9
-            sec[f"dense_bfp8_m{m}"] = {"us": usd, "gbs": gd, "pct_of_8tbs": 100 * gd / NOMINAL_HBM_GBS,
-                                      "bytes": mat.nbytes}
+            key = f"dense_bfp8_m{m}" + ("_tcgen05" if path == 2 else "")
+            sec[key] = {"us": usd, "gbs": gd, "pct_of_8tbs": 100 * gd / NOMINAL_HBM_GBS, "bytes": mat.nbytes,
+                        "us_back_to_back": usb,
+                        "gbs_back_to_back": mat.nbytes / (usb * 1e-6) / 1e9,
+                        "kernel": "bfp_linear_tc_kernel (tcgen05)" if path == 2 else "bfp_linear_kernel (mma.sync)",
+                        "timing": "us: each call alone after a 256 MB L2 flush; us_back_to_back: CUDA graph over "
+                                  "12 distinct matrices"}
+        del mats
         # greedy next token over LM-head logits [16 x 151936] fp32 (read from HBM after a flush)
         lg = torch.from_numpy(synth.normal(args.seed, 7, (16, 151936), std=3.0)).to(device)
         wsg = bfp.greedy_workspace(16, 151936, device)

@@ -89,6 +89,7 @@ SIGNATURES = {
     "bfp_set_wait_limit": [_I64],
     "bfp_set_launch_mode": [_I],
     "bfp_set_row_path": [_I],
+    "bfp_set_linear_path": [_I],
     "bfp_last_error": [],
 }
 
@@ -278,6 +279,12 @@ def set_row_path(enabled: bool):
     """Which kernel runs one-row MoE layers: the one-row kernel (True, default) or the general one
     (include/bfpmoe.h, bfp_set_row_path)."""
     _check(load().bfp_set_row_path(1 if enabled else 0), "bfp_set_row_path")
+
+
+def set_linear_path(mode: int):
+    """Which kernel bfp_linear runs: 0 (default) or 1 the mma.sync kernel, 2 the tcgen05 kernel wherever the
+    shape fits it (include/bfpmoe.h, bfp_set_linear_path)."""
+    _check(load().bfp_set_linear_path(int(mode)), "bfp_set_linear_path")
 
 
 def _alloc_ws(nbytes: int, device, stream=None):

@@ -16,7 +16,8 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libbfpmoe.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["bfp_host.cpp", "bfp_gptq.cpp", "bfp_linear.cu", "moe_layer.cu", "moe_row.cu", "bfp_greedy.cu", "bfp_kv.cu"]
+SOURCES = ["bfp_host.cpp", "bfp_gptq.cpp", "bfp_linear.cu", "bfp_linear_tc.cu", "moe_layer.cu", "moe_row.cu", "bfp_greedy.cu",
+           "bfp_kv.cu"]
 
 
 def nvcc() -> str:

@@ -21,6 +21,7 @@
 #include <vector>
 
 #include "bfp_launch.h"
+#include "bfp_tc.h"
 #include "bfp_tiles.cuh"
 
 namespace bfp {
@@ -518,6 +519,11 @@ int linear_launch_ex(const bfp_matrix *w, const uint16_t *x, int m, int64_t ldx,
     rc = plan_linear(g, m, &p);
     if (rc) return rc;
     if (body_bytes < p.ws_bytes) return fail(BFP_EWORKSPACE, "workspace smaller than bfp_linear_workspace_size");
+    // the tcgen05 kernel when asked for (bfp_set_linear_path(2)) and the shape fits it
+    if (!tokens && !norm && linear_path() == 2) {
+        rc = linear_tc_launch(g, static_cast<const uint8_t *>(w->data), x, m, ldx, y, y_bf16, ldy, status, st);
+        if (rc != kTcNotApplicable) return rc;
+    }
     LinearArgs a;
     a.w = static_cast<const uint8_t *>(w->data);
     a.n = g.n;

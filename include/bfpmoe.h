@@ -481,6 +481,22 @@ int bfp_set_launch_mode(int mode);
  */
 int bfp_set_row_path(int enabled);
 
+/*
+ * Which kernel runs bfp_linear (not the greedy variant, which keeps the
+ * mma.sync kernel), process-wide: 0 (default) and 1 the mma.sync kernel; 2
+ * the tcgen05 kernel wherever it fits (k a multiple of 128, m <= 32, half of
+ * each activation row in shared memory as fp16: k <= 2048 at 32 rows), the
+ * mma.sync kernel otherwise. The tcgen05 kernel (P4, "What changed in this
+ * release": up to 32 rows in one tile row) folds each block's exponent into
+ * its fp16 operand relative to the largest exponent of the row's 64 inputs of
+ * a chunk (exact for blocks within 2^15 of it; within 2^-16 of that chunk's
+ * largest value otherwise) and accumulates in tensor memory; on GB300 it is
+ * slower than the mma.sync kernel at every row count measured (1 to 32), so
+ * it is not the default. A measurement and test hook. BFP_EINVAL for other
+ * values.
+ */
+int bfp_set_linear_path(int mode);
+
 /* Message for the last non-OK status returned on this thread. */
 const char *bfp_last_error(void);
 

@@ -146,3 +146,41 @@ def test_linear_greedy_token_in_the_epilogue(fmt, n, k, m):
         rms = np.sqrt(np.mean(y_ref[r].astype(np.float64) ** 2))
         if top2[1] - top2[0] > 2e-3 * (abs(top2[1]) + rms):
             assert int(tok[r]) == int(np.argmax(y_ref[r]))
+
+
+@pytest.mark.parametrize("path,fmt,n,k,m", [
+    (2, 8, 8192, 2048, 1), (2, 8, 8192, 2048, 8), (2, 8, 8192, 2048, 16), (2, 4, 512, 2048, 8),
+    (2, 8, 130, 2048, 5), (2, 4, 2000, 1024, 16), (2, 8, 8192, 2048, 17), (2, 8, 8192, 2048, 24),
+    (2, 8, 8192, 2048, 32), (2, 4, 512, 2048, 32), (2, 8, 130, 2048, 32), (2, 4, 2000, 1024, 20),
+    (1, 8, 8192, 2048, 24), (1, 8, 8192, 2048, 32), (1, 4, 512, 2048, 32),
+])
+def test_linear_each_kernel_matches_oracle(path, fmt, n, k, m):
+    """Both kernels behind bfp_linear against the oracle: the tcgen05 one (path 2, asked for) and the mma.sync
+    one (path 1, the default's)."""
+    bfp.set_linear_path(path)
+    try:
+        test_linear_matches_oracle(fmt, n, k, m)
+    finally:
+        bfp.set_linear_path(0)
+
+
+def test_linear_tcgen05_block_exponent_spread():
+    """The tcgen05 kernel scales each 16-value block relative to the largest exponent among a row's 64 inputs
+    of a chunk: blocks 2^14 apart within a chunk stay exact, blocks 2^40 apart lose only what lies below 2^-16
+    of the chunk's largest value; checked against the oracle within the stated tolerance."""
+    fmt, n, k, m = 8, 256, 2048, 32
+    w = synth.normal(41, 7, (n, k), std=0.02)
+    w[:, 0:16] *= np.float32(2.0 ** 14)   # block 0 of every chunk-0 row far above its neighbours
+    w[:128, 64:80] *= np.float32(2.0 ** -40)  # a tiny block in chunk 1 of the first half of the rows
+    x = np.stack([synth.activation_row(41, 2000 + r, k, False) for r in range(m)])
+    e, c = oracle.encode(fmt, w)
+    y_ref, _ = oracle.linear(fmt, e, c, x)
+    mat = bfp.DeviceMatrix.from_host(fmt, n, k, bfp.encode(fmt, w))
+    ws = bfp.linear_workspace(mat, m)
+    bfp.set_linear_path(2)
+    try:
+        y = bfp.linear(mat, bf16_tensor(x), ws)
+    finally:
+        bfp.set_linear_path(0)
+    assert bfp.workspace_status(ws) == bfp.BFP_OK
+    assert_close(y.cpu().numpy(), y_ref, "tcgen05 linear, spread block exponents")
