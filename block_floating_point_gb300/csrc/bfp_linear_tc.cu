@@ -147,6 +147,19 @@ __device__ __forceinline__ void st_cluster_f32x4(uint32_t addr, float a, float b
     asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
                  : "memory");
 }
+// Bounded wait for an mbarrier phase that pauses between polls (warps that wait leave the issue slots to
+// the unpack warps); false = gave up (or *abort was raised).
+__device__ __forceinline__ bool tc_wait(uint64_t *bar, uint32_t parity, const WaitCfg &w, const volatile int *abort) {
+    if (mbar_test(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (int64_t i = 1; i < w.iters; ++i) {
+        __nanosleep(64);
+        if (mbar_test(bar, parity)) return true;
+        if (abort && *abort) return false;
+        if (global_ns() - t0 > w.nanos) return false;
+    }
+    return false;
+}
 __device__ __forceinline__ uint32_t hmul2_bits(uint32_t a, uint32_t s) {
     __half2 r = __hmul2(*reinterpret_cast<const __half2 *>(&a), *reinterpret_cast<const __half2 *>(&s));
     return *reinterpret_cast<uint32_t *>(&r);
@@ -228,21 +241,33 @@ __global__ void __launch_bounds__(kTcThreads, 1) bfp_linear_tc_kernel(const __gr
     //      K-major core matrices. All loads in flight at once; each row's maximum over both halves (the two
     //      CTAs exchange theirs), so both scale a row alike.
     uint4 xv[kTcXLoads];
+    // piece j of this thread: warp item wi = (tid >> 5) + j * kTcWarps covers rows 8 (wi % nb) + (lane & 7) and
+    // 16-byte pieces 4 (wi / nb) + (lane >> 3) (nb = nm / 8 row bands): full sectors on the loads, 128 contiguous
+    // bytes per 8 lanes on the stores into the core matrices
+    const int nb = a.nm / 8;
+    auto piece = [&](int j, int &r, int &kq) {
+        const int wi = warp + j * kTcWarps;
+        r = 8 * (wi % nb) + (lane & 7);
+        kq = 4 * (wi / nb) + (lane >> 3);
+    };
 #pragma unroll
     for (int j = 0; j < kTcXLoads; ++j) {
-        const int it = tid + j * kTcThreads, kq = it / a.nm, r = it - kq * a.nm;  // rows fastest
+        int r, kq;
+        piece(j, r, kq);
         xv[j] = make_uint4(0u, 0u, 0u, 0u);
-        if (it < a.nm * kg8 && r < a.m)
+        if (kq < kg8 && r < a.m)
             xv[j] = *reinterpret_cast<const uint4 *>(a.x + (int64_t)r * a.ldx + half * kh + 8 * kq);
     }
-    {
-        // every item of a thread is of row tid % nm (the thread count is a multiple of 32): one atomic each
-        uint32_t m2 = 0u;
 #pragma unroll
-        for (int j = 0; j < kTcXLoads; ++j)
-            m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(xv[j].x & 0x7FFF7FFFu, xv[j].y & 0x7FFF7FFFu),
-                                       __vmaxu2(xv[j].z & 0x7FFF7FFFu, xv[j].w & 0x7FFF7FFFu)));
-        if (tid % a.nm < a.m) atomicMax(&ms->rmax[tid % a.nm], max(m2 & 0xFFFFu, m2 >> 16));
+    for (int j = 0; j < kTcXLoads; ++j) {
+        int r, kq;
+        piece(j, r, kq);
+        uint32_t m2 = __vmaxu2(__vmaxu2(xv[j].x & 0x7FFF7FFFu, xv[j].y & 0x7FFF7FFFu),
+                               __vmaxu2(xv[j].z & 0x7FFF7FFFu, xv[j].w & 0x7FFF7FFFu));
+        uint32_t mr = max(m2 & 0xFFFFu, m2 >> 16);
+        mr = max(mr, __shfl_xor_sync(0xffffffffu, mr, 8));  // the 4 lanes of one row
+        mr = max(mr, __shfl_xor_sync(0xffffffffu, mr, 16));
+        if (lane < 8 && kq < kg8 && r < a.m) atomicMax(&ms->rmax[r], mr);
     }
     __syncthreads();
     if (tid < a.m) st_cluster_u32(map_rank(smem_addr(&ms->pmax[tid]), (uint32_t)(1 - half)), ms->rmax[tid]);
@@ -251,8 +276,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) bfp_linear_tc_kernel(const __gr
     __syncthreads();
 #pragma unroll
     for (int j = 0; j < kTcXLoads; ++j) {
-        const int it = tid + j * kTcThreads, kq = it / a.nm, r = it - kq * a.nm;
-        if (it < a.nm * kg8) {
+        int r, kq;
+        piece(j, r, kq);
+        if (kq < kg8) {
             uint4 o = make_uint4(0u, 0u, 0u, 0u);
             if (r < a.m) {
                 const float sc = pow2f(ms->shift[r]);
@@ -276,7 +302,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) bfp_linear_tc_kernel(const __gr
         // ---- producer: the remaining chunks, each into the stage the unpack warps have released
         for (; issued < nch && !vflags[0]; ++issued) {
             const int st = issued % NR;
-            if (!__all_sync(0xffffffffu, mbar_wait(&ms->raw_empty[st], (uint32_t)(issued / NR - 1) & 1u, a.wait,
+            if (!__all_sync(0xffffffffu, tc_wait(&ms->raw_empty[st], (uint32_t)(issued / NR - 1) & 1u, a.wait,
                                                    vflags))) {
                 fail_wait();
                 break;
@@ -292,8 +318,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) bfp_linear_tc_kernel(const __gr
         if (lane == 0) {
             for (int q = 0; q < nch && !vflags[0]; ++q) {
                 const int sa = q % kTcA, d = q % kTcD;
-                if (!mbar_wait(&ms->a_full[sa], (uint32_t)(q / kTcA) & 1u, a.wait, vflags) ||
-                    (q >= kTcD && !mbar_wait(&ms->d_free[d], (uint32_t)(q / kTcD - 1) & 1u, a.wait, vflags))) {
+                if (!tc_wait(&ms->a_full[sa], (uint32_t)(q / kTcA) & 1u, a.wait, vflags) ||
+                    (q >= kTcD && !tc_wait(&ms->d_free[d], (uint32_t)(q / kTcD - 1) & 1u, a.wait, vflags))) {
                     fail_wait();
                     break;
                 }
@@ -410,7 +436,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) bfp_linear_tc_kernel(const __gr
         const int row = 32 * e + lane;
         for (int q = 0; q < nch; ++q) {
             const int d = q % kTcD;
-            if (!__all_sync(0xffffffffu, mbar_wait(&ms->mma_done[d], (uint32_t)(q / kTcD) & 1u, a.wait, vflags))) {
+            if (!__all_sync(0xffffffffu, tc_wait(&ms->mma_done[d], (uint32_t)(q / kTcD) & 1u, a.wait, vflags))) {
                 fail_wait();
                 break;
             }
@@ -497,7 +523,11 @@ static int launch_tc_t(const TcArgs &a, int ncta, size_t smem, cudaStream_t st) 
 int linear_tc_launch(const Geometry &g, const uint8_t *w, const uint16_t *x, int m, int64_t ldx, float *y,
                      uint16_t *y_bf16, int64_t ldy, uint32_t *status, cudaStream_t st) {
     if (m < 1 || m > 32 || g.k % (2 * kTcK) != 0) return kTcNotApplicable;
-    if ((m > 16 ? 32 : 16) * (g.k / 2) / 8 > (int64_t)kTcXLoads * kTcThreads) return kTcNotApplicable;
+    {
+        // the activation pieces: (nm / 8) row bands x (k / 2 / 32) groups of four 16-byte pieces, one per warp item
+        const int64_t items = (int64_t)((m > 16 ? 32 : 16) / 8) * ((g.k / 2) / 32);
+        if (items > (int64_t)kTcXLoads * kTcWarps) return kTcNotApplicable;
+    }
     DeviceInfo di;
     int rc = device_info(&di);
     if (rc) return rc;
