@@ -7,19 +7,19 @@
 // goes. The mma.sync path multiplies each 16-value block on its own and folds
 // 2^(E-127) into the fp32 sum right after, which costs 4 FMAs per activation
 // group and block (16 at 32 rows). Here a cluster of two CTAs owns 128 weight
-// rows (the MMA's M), each CTA half of k, streamed in chunks of 64:
+// rows (the MMA's M), each CTA half of k, streamed in chunks of 128:
 //   - a producer warp requests every chunk's records (1D bulk copies, the TMA
 //     engine; the first stages before the previous kernel has finished), as
 //     many stages ahead as shared memory holds;
 //   - eight unpack warps, one per 16-row group, place the BFP codes as fp16
 //     values with the exponent folded in: per row and chunk a reference
-//     exponent Er = the largest of the chunk's block exponents, each block
+//     exponent Er = the largest of the chunk's 8 block exponents, each block
 //     scaled by 2^(E - Er) (one packed fp16 multiply per pair; exact for blocks
 //     within 2^15 of the row's largest in the chunk, and within 2^-16 of the
 //     chunk's largest value otherwise), into the K-major core-matrix layout
 //     the MMA reads from shared memory;
 //   - one thread issues tcgen05.mma (kind::f16, fp32 accumulators in tensor
-//     memory, M = 128, N = 16 or 32 activation rows, 4 MMAs of k16 per chunk)
+//     memory, M = 128, N = 16 or 32 activation rows, 8 MMAs of k16 per chunk)
 //     against the activation rows, converted once per CTA to fp16 scaled by a
 //     power of two per row (as in bfp_linear), and commits to an mbarrier;
 //   - four epilogue warps read each chunk's accumulator tile from tensor
@@ -44,7 +44,7 @@ using namespace dev;
 namespace {
 
 constexpr int kTcRows = 128;    // weight rows per CTA (the MMA's M)
-constexpr int kTcK = 64;        // k per chunk
+constexpr int kTcK = 128;       // k per chunk
 constexpr int kTcGroups = 8;    // 16-row groups per CTA, one unpack warp each
 constexpr int kTcEpi0 = 8;      // warps 8-11 read the accumulators back (tensor-memory lanes 32 (w % 4) ..)
 constexpr int kTcMmaWarp = 12;  // lane 0 issues the MMAs; the warp owns the tensor-memory allocation
@@ -52,7 +52,7 @@ constexpr int kTcProdWarp = 13; // lanes request the record copies
 constexpr int kTcWarps = 14;
 constexpr int kTcThreads = kTcWarps * 32;
 constexpr int kTcRawMax = 16;   // record stages at most (as many as shared memory holds)
-constexpr int kTcA = 4;         // operand stages (a stage is free again once its chunk's MMAs are done)
+constexpr int kTcA = 2;         // operand stages (a stage is free again once its chunk's MMAs are done)
 constexpr int kTcD = 8;         // accumulator tiles in tensor memory (the read-back may lag this many chunks)
 constexpr int kTcCols = 256;    // tensor-memory columns: kTcD tiles of up to 32
 constexpr int kTcXLoads = 10;   // 16-byte activation loads per thread (32 rows x 1024 of k at most)
@@ -311,7 +311,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) bfp_linear_tc_kernel(const __gr
             produce(issued);
         }
     } else if (warp == kTcMmaWarp) {
-        // ---- one thread issues each chunk's 4 MMAs (k16 each): operands from stage q % kTcA, accumulators in
+        // ---- one thread issues each chunk's 8 MMAs (k16 each): operands from stage q % kTcA, accumulators in
         //      tile q % kTcD
         const uint32_t idesc = (1u << 4) | ((uint32_t)(a.nm >> 3) << 17) | ((uint32_t)(kTcRows >> 4) << 24);
         int done = 0;  // chunks committed
@@ -361,10 +361,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) bfp_linear_tc_kernel(const __gr
             if (live) {
                 const uint8_t *rp = sRaw + (size_t)(st * kTcGroups + warp) * raw_bytes;
                 // this lane's rows' exponents: per record, blocks in order, (row g, row g + 8) byte pairs
-                uint32_t ew[2][2];
-                uint4 wq[2];
+                constexpr int RPCM = kTcK / 32;  // most records of a row group per chunk (BFP8)
+                uint32_t ew[RPCM][2];
+                uint4 wq[RPCM];
 #pragma unroll
-                for (int r = 0; r < 2; ++r) {
+                for (int r = 0; r < RPCM; ++r) {
                     if (r < a.rpc) {
                         wq[r] = *reinterpret_cast<const uint4 *>(rp + (size_t)r * a.rec + 16 * lane);
                         if constexpr (CB == 4) {
@@ -387,12 +388,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) bfp_linear_tc_kernel(const __gr
                 };
                 int er0 = 0, er1 = 0;
 #pragma unroll
-                for (int kb = 0; kb < 4; ++kb) {
+                for (int kb = 0; kb < kTcK / 16; ++kb) {
                     er0 = max(er0, ex(kb, 0));
                     er1 = max(er1, ex(kb, 1));
                 }
 #pragma unroll
-                for (int kb = 0; kb < 4; ++kb) {
+                for (int kb = 0; kb < kTcK / 16; ++kb) {
                     const int r = kb / CB, bb = kb % CB;
                     uint32_t av[4];
                     if constexpr (FMT == 4) {

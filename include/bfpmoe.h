@@ -488,7 +488,7 @@ int bfp_set_row_path(int enabled);
  * each activation row in shared memory as fp16: k <= 2048 at 32 rows), the
  * mma.sync kernel otherwise. The tcgen05 kernel (P4, "What changed in this
  * release": up to 32 rows in one tile row) folds each block's exponent into
- * its fp16 operand relative to the largest exponent of the row's 64 inputs of
+ * its fp16 operand relative to the largest exponent of the row's 128 inputs of
  * a chunk (exact for blocks within 2^15 of it; within 2^-16 of that chunk's
  * largest value otherwise) and accumulates in tensor memory; on GB300 it is
  * slower than the mma.sync kernel at every row count measured (1 to 32), so
