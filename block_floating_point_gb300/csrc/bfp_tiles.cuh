@@ -352,19 +352,20 @@ __device__ __noinline__ void act_rows_frags(const uint16_t *x, int64_t ldx, int 
 }
 
 // act_rows_frags for four activation groups (32 rows) with the rows staged in the fragment area itself
-// (row r at x + r * ldx, bf16; ldx = k). Group g's fragments (kbp blocks) take bytes [g F, (g + 1) F),
-// F = kbp * 256, and its staged rows [g S, (g + 1) S), S = 16 k <= F: going from the last group down,
-// a group's fragments never cover the staged rows of a group still to come. Per group, every thread
-// reads its share (at most 8 fragment pairs: kbp <= 128) into registers, the threads meet at barrier
-// `bar`, and the pairs are written in place. Same values and layout as act_rows_frags with ngrp = 4.
-// Ends with barrier `bar`.
+// (row r at x + r * ldx, bf16). Group g's fragments (kbp blocks) take bytes [g F, (g + 1) F),
+// F = kbp * 256, and its staged rows [g R, (g + 1) R), R = 16 ldx bytes; with ldx >= 16 kbp (R >= F),
+// going from the first group up, a group's fragments never cover the staged rows of a group still to
+// come. Per group, every thread reads its share (at most 8 fragment pairs: kbp <= 128) into registers,
+// the threads meet at barrier `bar`, and the pairs are written in place. A warp reads one block of the
+// group's 8 rows at once: with ldx = 8 mod 64 (rows 4 banks apart) those reads are free of bank
+// conflicts. Same values and layout as act_rows_frags with ngrp = 4. Ends with barrier `bar`.
 template <int NC>
 __device__ __noinline__ void act_rows_frags_inplace(const uint16_t *x, int64_t ldx, int m, int k, int kbp,
                                                     const int *shift, uint32_t *frag, int bar, int tid) {
     constexpr int KR = 8;
     const int kb = k / 16, per_group = kbp * kWarp;
     uint2 *f2 = reinterpret_cast<uint2 *>(frag);
-    for (int grp = 3; grp >= 0; --grp) {
+    for (int grp = 0; grp < 4; ++grp) {
         uint2 v[KR];
 #pragma unroll
         for (int j = 0; j < KR; ++j) {
