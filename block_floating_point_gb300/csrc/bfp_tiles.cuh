@@ -229,7 +229,7 @@ __device__ __forceinline__ int act_segments(int m, int k) {
 // Called by the NC threads (warps 0 .. NC/32 - 1 of the call; warp = the caller's warp index among
 // them) that meet at named barrier `bar`; ends with that barrier.
 template <int NC>
-__device__ __noinline__ void act_rows_prepare(uint16_t *x, int64_t ldx, int m, int k, bool norm, float eps,
+__device__ __forceinline__ void act_rows_prepare_body(uint16_t *x, int64_t ldx, int m, int k, bool norm, float eps,
                                               int *shift, float *inv_out, float2 *red, int bar, int warp, int lane) {
     constexpr int NW = NC / kWarp;
     const int S = act_segments<NC>(m, k);
@@ -311,6 +311,12 @@ __device__ __noinline__ void act_rows_prepare(uint16_t *x, int64_t ldx, int m, i
     }
     bar_sync(bar, NC);
 }
+// The same, as a call: one copy of the code for kernels that reach it from more than one place.
+template <int NC>
+__device__ __noinline__ void act_rows_prepare(uint16_t *x, int64_t ldx, int m, int k, bool norm, float eps,
+                                              int *shift, float *inv_out, float2 *red, int bar, int warp, int lane) {
+    act_rows_prepare_body<NC>(x, ldx, m, k, norm, eps, shift, inv_out, red, bar, warp, lane);
+}
 
 // fp16 activation fragments of the prepared rows (act_rows_prepare): row r scaled by 2^shift[r] and
 // rounded to fp16 (exact for every bf16 value above 2^-14 of the row maximum); rows m .. 8 ngrp - 1
@@ -320,7 +326,7 @@ __device__ __noinline__ void act_rows_prepare(uint16_t *x, int64_t ldx, int m, i
 // 2t+8|2t+9 of the segment's blocks b with b & 7 = bb) and stores each with one 8-byte store; the
 // XOR swizzle spreads a warp's stores over the banks. Called like act_rows_prepare (tid unused).
 template <int NC>
-__device__ __noinline__ void act_rows_frags(const uint16_t *x, int64_t ldx, int m, int k, int kbp, int ngrp,
+__device__ __forceinline__ void act_rows_frags_body(const uint16_t *x, int64_t ldx, int m, int k, int kbp, int ngrp,
                                             const int *shift, uint32_t *frag, int bar, int tid, int warp, int lane) {
     constexpr int NW = NC / kWarp;
     const int kb = k / 16, mp = 8 * ngrp;
@@ -350,6 +356,12 @@ __device__ __noinline__ void act_rows_frags(const uint16_t *x, int64_t ldx, int 
     }
     bar_sync(bar, NC);
 }
+// The same, as a call: one copy of the code for kernels that reach it from more than one place.
+template <int NC>
+__device__ __noinline__ void act_rows_frags(const uint16_t *x, int64_t ldx, int m, int k, int kbp, int ngrp,
+                                            const int *shift, uint32_t *frag, int bar, int tid, int warp, int lane) {
+    act_rows_frags_body<NC>(x, ldx, m, k, kbp, ngrp, shift, frag, bar, tid, warp, lane);
+}
 
 // act_rows_frags for four activation groups (32 rows) with the rows staged in the fragment area itself
 // (row r at x + r * ldx, bf16). Group g's fragments (kbp blocks) take bytes [g F, (g + 1) F),
@@ -360,7 +372,7 @@ __device__ __noinline__ void act_rows_frags(const uint16_t *x, int64_t ldx, int 
 // group's 8 rows at once: with ldx = 8 mod 64 (rows 4 banks apart) those reads are free of bank
 // conflicts. Same values and layout as act_rows_frags with ngrp = 4. Ends with barrier `bar`.
 template <int NC>
-__device__ __noinline__ void act_rows_frags_inplace(const uint16_t *x, int64_t ldx, int m, int k, int kbp,
+__device__ __forceinline__ void act_rows_frags_inplace_body(const uint16_t *x, int64_t ldx, int m, int k, int kbp,
                                                     const int *shift, uint32_t *frag, int bar, int tid) {
     constexpr int KR = 8;
     const int kb = k / 16, per_group = kbp * kWarp;
@@ -390,6 +402,12 @@ __device__ __noinline__ void act_rows_frags_inplace(const uint16_t *x, int64_t l
         }
     }
     bar_sync(bar, NC);
+}
+// The same, as a call: one copy of the code for kernels that reach it from more than one place.
+template <int NC>
+__device__ __noinline__ void act_rows_frags_inplace(const uint16_t *x, int64_t ldx, int m, int k, int kbp,
+                                                    const int *shift, uint32_t *frag, int bar, int tid) {
+    act_rows_frags_inplace_body<NC>(x, ldx, m, k, kbp, shift, frag, bar, tid);
 }
 
 }  // namespace dev

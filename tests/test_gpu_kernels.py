@@ -52,6 +52,8 @@ LINEAR_CASES = [
     # up to 32 rows in one weight pass (four activation groups, fragments built in place)
     (8, 8192, 2048, 17), (8, 8192, 2048, 24), (8, 8192, 2048, 32), (4, 512, 2048, 32), (8, 37, 96, 29),
     (8, 130, 2048, 32), (4, 2000, 1024, 20),
+    # k below the records' padded width (staged rows then take the padded width plus 8 elements)
+    (8, 2000, 2000, 32), (4, 96, 1008, 31),
 ]
 
 
