@@ -236,11 +236,14 @@ __global__ void __launch_bounds__(kLinThreads, 1) bfp_linear_kernel(const __grid
     if (!__all_sync(0xffffffffu, mbar_wait(&lm->stage_full, 0u, a.wait, nullptr))) bad = true;
     uint16_t *const xs = reinterpret_cast<uint16_t *>(stage);
     // (inlined: 0.3-0.5 us less than the calls at 1 and 16 rows)
-    act_rows_prepare_body<NC>(xs, a.ldxs, a.m, a.k, a.norm != 0, a.eps, lm->shift, lm->inv, lm->red, 1, warp, lane);
-    if constexpr (NGRP == 4)
+    if constexpr (NGRP == 4) {
+        act_rows_prepare_body<NC>(xs, a.ldxs, a.m, a.k, a.norm != 0, a.eps, lm->shift, lm->inv, lm->red, 1, warp,
+                                  lane);
         act_rows_frags_inplace_body<NC>(xs, a.ldxs, a.m, a.k, a.kbp, lm->shift, frag, 1, tid);
-    else
-        act_rows_frags_body<NC>(xs, a.ldxs, a.m, a.k, a.kbp, NGRP, lm->shift, frag, 1, tid, warp, lane);
+    } else {
+        act_rows_stats_frags_body<NC>(xs, a.ldxs, a.m, a.k, a.kbp, NGRP, a.norm != 0, a.eps, lm->shift, frag, 1,
+                                      warp, lane);
+    }
     // every warp is past its reads of the stage (the barrier ending act_rows_frags): the rest
     // of the streams may start
     if (!early)

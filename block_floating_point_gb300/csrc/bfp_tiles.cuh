@@ -363,6 +363,78 @@ __device__ __noinline__ void act_rows_frags(const uint16_t *x, int64_t ldx, int 
     act_rows_frags_body<NC>(x, ldx, m, k, kbp, ngrp, shift, frag, bar, tid, warp, lane);
 }
 
+// act_rows_prepare and act_rows_frags in one pass, for rows staged apart from the fragment area (up to
+// 16 rows): the warp that converts a segment of row r first takes row r's statistics itself, over the
+// whole row (every warp with a segment of the row computes the same values in the same order), so no
+// CTA barrier separates the statistics from the fragments and no partial sums cross warps. The same
+// fragment values and layout as act_rows_prepare followed by act_rows_frags (with norm, t =
+// bf16(x * inv) is formed on the fly and the staged rows are left as they are); shift[r] is written by
+// the warp of row r's first segment. Ends with barrier `bar`.
+template <int NC>
+__device__ __forceinline__ void act_rows_stats_frags_body(const uint16_t *x, int64_t ldx, int m, int k, int kbp,
+                                                          int ngrp, bool norm, float eps, int *shift, uint32_t *frag,
+                                                          int bar, int warp, int lane) {
+    constexpr int NW = NC / kWarp;
+    const int kb = k / 16, mp = 8 * ngrp, nv = k / 8;
+    uint2 *f2 = reinterpret_cast<uint2 *>(frag);
+    int S = 1;  // segments per row: spread the rows over every warp
+    while (mp * S * 2 <= NW && (kbp / 8) % (S * 2) == 0) S *= 2;
+    const int bs = kbp / S;  // blocks per segment (a multiple of 8 when S > 1)
+    const int bb = lane >> 2, t = lane & 3;
+    for (int it = warp; it < mp * S; it += NW) {
+        const int r = it / S, sg = it - r * S;
+        const bool real = r < m;
+        const uint16_t *xrow = x + (int64_t)(real ? r : 0) * ldx;
+        float sc = 0.f, inv = 1.f;
+        if (real) {
+            const uint4 *xr = reinterpret_cast<const uint4 *>(xrow);
+            float ss = 0.f;
+            uint32_t mx2 = 0u;  // max |x| of the low and high bf16 halves, as bit patterns
+            for (int i = lane; i < nv; i += kWarp) {
+                const uint4 v = xr[i];
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    mx2 = __vmaxu2(mx2, w[h] & 0x7FFF7FFFu);
+                    if (norm) {
+                        const float lo = bf16_bits_to_f32(w[h] & 0xFFFFu), hi = bf16_bits_to_f32(w[h] >> 16);
+                        ss = fmaf(lo, lo, ss);
+                        ss = fmaf(hi, hi, ss);
+                    }
+                }
+            }
+            // bit patterns of non-negative bf16 values order as the values do
+            float mx = bf16_bits_to_f32(__reduce_max_sync(0xffffffffu, max(mx2 & 0xFFFFu, mx2 >> 16)));
+            if (norm) {
+                inv = 1.0f / sqrtf(warp_sum(ss) / (float)k + eps);
+                mx = bf16_bits_to_f32(f32_to_bf16_bits(mx * inv));
+            }
+            const int sh = frag_shift(mx);
+            sc = pow2f(sh);
+            if (sg == 0 && lane == 0) shift[r] = sh;
+        }
+        const int grp = r >> 3, g = r & 7;
+        uint2 *fr = f2 + (int64_t)grp * kbp * kWarp + ((4 * g + t) ^ (bb << 2));  // (b & 7) == bb
+        const int b0 = sg * bs, b1 = b0 + bs;
+        for (int b = b0 + ((bb - b0) & 7); b < b1; b += 8) {
+            uint2 v = make_uint2(0u, 0u);
+            if (real && b < kb) {
+                const uint32_t w0 = *reinterpret_cast<const uint32_t *>(xrow + 16 * b + 2 * t);
+                const uint32_t w1 = *reinterpret_cast<const uint32_t *>(xrow + 16 * b + 2 * t + 8);
+                float f[4] = {bf16_bits_to_f32(w0 & 0xFFFFu), bf16_bits_to_f32(w0 >> 16),
+                              bf16_bits_to_f32(w1 & 0xFFFFu), bf16_bits_to_f32(w1 >> 16)};
+                if (norm) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) f[q] = bf16_bits_to_f32(f32_to_bf16_bits(f[q] * inv));
+                }
+                v = make_uint2(pack_half2(f[0] * sc, f[1] * sc), pack_half2(f[2] * sc, f[3] * sc));
+            }
+            fr[(int64_t)b * kWarp] = v;
+        }
+    }
+    bar_sync(bar, NC);
+}
+
 // act_rows_frags for four activation groups (32 rows) with the rows staged in the fragment area itself
 // (row r at x + r * ldx, bf16). Group g's fragments (kbp blocks) take bytes [g F, (g + 1) F),
 // F = kbp * 256, and its staged rows [g R, (g + 1) R), R = 16 ldx bytes; with ldx >= 16 kbp (R >= F),
